@@ -1,0 +1,486 @@
+#!/usr/bin/env python
+"""Benchmark of the staged halo exchange: coordinates (Z->Y->X) + forces
+(X->Y->Z) on fixed maps, one GPU per rank.
+
+One step = hx_exchange_coords + hx_exchange_forces on the device-resident
+layout. Metric: microseconds per step (lower is better) and effective GB/s of
+algorithmic bytes (28 B per map entry for coordinates, 40 B for forces)
+against the measured HBM copy peak.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload C5]
+  python bench.py --impl reference ...   (the CPU oracle, timed on host cores)
+
+For N > 1 (torchrun) every rank runs an independent replica of the workload
+on its own GPU (the exchange is single-GPU by construction); timing is the
+max over ranks. Prints one JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from domain_decomposition_halo_gb300 import workloads as W  # noqa: E402
+
+BYTES_COORD = 28   # map 4 + gather 12 + store 12
+BYTES_FORCE = 40   # map 4 + halo-slot read 12 + target read 12 + target write 12
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 2 ** 20
+METRIC = "halo exchange μs/step (coords+forces) and effective GB/s vs GB300 HBM peak"
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="C5", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--no-extras", action="store_true", help="skip the secondary measurements")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU baseline budget")
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def workload_label(w):
+    return f"{w.name}: " + w.describe()
+
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            v = float(json.load(fh)["hbm_gbs"])
+        return v, "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_digest():
+    h = hashlib.sha256()
+    for name in ("hx_kernels.cu", "hx_internal.h"):
+        with open(os.path.join(ROOT, "domain_decomposition_halo_gb300", "csrc", name), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary of this kernel,
+    if it was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    s = re.search(r"kernel_source_digest:\s*([0-9a-f]+)", text)
+    if not m or not s or s.group(1) != kernel_source_digest():
+        return None
+    return float(m.group(1))
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons while it runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        sel = self._selector(device_index)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", sel], stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    @staticmethod
+    def _selector(idx: int) -> str:
+        try:
+            import torch
+            u = str(torch.cuda.get_device_properties(idx).uuid)
+            return u if u.startswith("GPU-") else "GPU-" + u
+        except Exception:  # noqa: BLE001 - any failure: fall back to the visible index
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+            if vis:
+                return vis.split(",")[idx]
+            return str(idx)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.flush()
+        self.out.seek(0)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.out.read().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.out.name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    from domain_decomposition_halo_gb300 import HaloExchange
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    w = W.WORKLOADS[args.workload]
+    pos = W.positions(w)
+    hx = HaloExchange(w.box, w.dims, w.cutoff, device=local)
+    pos_t = torch.from_numpy(pos).to(dev)
+    slots = hx.build_maps(pos_t)
+    coords = torch.empty((slots, 3), device=dev)
+    hx.build_maps(pos_t, coords)
+    torch.cuda.synchronize()
+    # map build time (size + fill call), reported apart from the step
+    t_build = []
+    for _ in range(3):
+        t0 = time.perf_counter()
+        hx.build_maps(pos_t, coords)
+        torch.cuda.synchronize()
+        t_build.append((time.perf_counter() - t0) * 1e6)
+    n_dom, n_pulses, _, entries = hx.counts()
+    forces = torch.from_numpy(W.forces(w, slots)).to(dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        hx.exchange_coords(coords)
+        hx.exchange_forces(forces)
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks = Clocks(local) if rank == 0 else None
+    start.record(stream)
+    for k in range(K):
+        a, b, c = ev[k]
+        a.record(stream)
+        hx.exchange_coords(coords)
+        b.record(stream)
+        hx.exchange_forces(forces)
+        c.record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop() if clocks else None
+    total_ms = start.elapsed_time(end)
+    coord_ms = statistics.fmean(e[0].elapsed_time(e[1]) for e in ev)
+    force_ms = statistics.fmean(e[1].elapsed_time(e[2]) for e in ev)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+        torch.distributed.barrier()
+    rc, detail = hx.status()
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} (detail {detail}) after the timed region")
+    us_step = total_ms * 1e3 / K
+
+    # end to end through the public API: host buffers in, results out, every step
+    coords_h = coords.cpu().pin_memory()
+    forces_h = forces.cpu().pin_memory()
+    coords_o = torch.empty_like(coords_h).pin_memory()
+    forces_o = torch.empty_like(forces_h).pin_memory()
+    n_e2e = max(3, min(K, 30))
+    for i in range(2 + n_e2e):
+        if i == 2:
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record(stream)
+        coords.copy_(coords_h, non_blocking=True)
+        forces.copy_(forces_h, non_blocking=True)
+        hx.exchange_coords(coords)
+        hx.exchange_forces(forces)
+        coords_o.copy_(coords, non_blocking=True)
+        forces_o.copy_(forces, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_us = e0.elapsed_time(e1) * 1e3 / n_e2e
+    bytes_h2d = 2 * slots * 12
+    bytes_d2h = 2 * slots * 12
+
+    peak, peak_kind = measured_hbm_peak()
+    dominant = "hx_forces_fused" if force_ms >= coord_ms else "hx_coords_fused"
+    dom_bytes = (BYTES_FORCE if dominant == "hx_forces_fused" else BYTES_COORD) * entries
+    dom_ms = max(force_ms, coord_ms)
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    step_gbs = (BYTES_COORD + BYTES_FORCE) * entries / (us_step * 1e-6) / 1e9
+    out = {
+        "metric": METRIC,
+        "value": round(us_step, 3),
+        "unit": "us/step",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(total_ms / K, 6),
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded uniform positions, N(0,1) forces; stands in for the pages' water-ethanol systems)",
+        "config": {
+            "workload": workload_label(w),
+            "domains": n_dom, "pulses": n_pulses, "map_entries": entries, "slots": slots,
+            "l2": f"inputs larger than L2: coords+forces {2 * slots * 12 / 2**20:.0f} MiB vs L2 129 MiB; no flush",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "launch": "one CUDA-graph launch per direction per step",
+        },
+        "effective_gbs": round(step_gbs, 1),
+        "roofline": {
+            "bound": "hbm", "kernel": dominant, "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
+            "algorithmic_bytes_per_launch": dom_bytes,
+            "traffic": profiled_traffic(dominant, w.name),
+        },
+        "kernels_ms": {"hx_coords_fused": round(coord_ms, 5), "hx_forces_fused": round(force_ms, 5)},
+        "clocks": clk,
+        "e2e": {"value": round(e2e_us, 2), "unit": "us/step", "h2d_bytes_per_step": bytes_h2d,
+                "d2h_bytes_per_step": bytes_d2h,
+                "what": "pinned host coords+forces -> device, both exchanges, coords+forces -> host, every step"},
+        "gpu_launches": 2 * K,
+        "build_maps_us": round(statistics.median(t_build), 1),
+    }
+    if rank == 0 and not args.no_extras:
+        out["secondary"] = secondary(hx, coords, forces, w, dev, peak)
+    del hx
+    if rank == 0:
+        out["cpu_baseline"] = cpu_baseline(w, pos, args.cpu_seconds)
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def _flush(buf):
+    buf.add_(1.0)
+
+
+def secondary(hx_main, coords, forces, w_main, dev, peak):
+    """Cold-L2 numbers of the headline workload, the 1M-atom configuration,
+    and the small configurations' step latency against the launch floor."""
+    import torch
+
+    from domain_decomposition_halo_gb300 import HaloExchange
+
+    flush_buf = torch.zeros(2 * L2_BYTES // 4, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def timed(hx, x, f, reps, flush):
+        ts = []
+        for _ in range(reps):
+            if flush:
+                _flush(flush_buf)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            hx.exchange_coords(x)
+            hx.exchange_forces(f)
+            b.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b) * 1e3)
+        return statistics.median(ts)
+
+    def floor(hx, reps=300):
+        ts = []
+        for _ in range(reps):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            hx.noop()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b) * 1e3)
+        return statistics.median(ts)
+
+    res = {}
+    entries = hx_main.counts()[3]
+    cold = timed(hx_main, coords, forces, 30, True)
+    res[w_main.name + "_cold_l2"] = {"us_step": round(cold, 2),
+                                     "frac_of_peak": round(68 * entries / (cold * 1e-6) / 1e9 / peak, 4)}
+    for name in ("C1", "C2", "C3", "C4"):
+        if name == w_main.name:
+            continue
+        w = W.WORKLOADS[name]
+        hx = HaloExchange(w.box, w.dims, w.cutoff, device=dev.index)
+        pos = torch.from_numpy(W.positions(w)).to(dev)
+        slots = hx.build_maps(pos)
+        x = torch.empty((slots, 3), device=dev)
+        hx.build_maps(pos, x)
+        f = torch.from_numpy(W.forces(w, slots)).to(dev)
+        ent = hx.counts()[3]
+        for _ in range(20):
+            hx.exchange_coords(x)
+            hx.exchange_forces(f)
+        n = 2000
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(n):
+            hx.exchange_coords(x)
+            hx.exchange_forces(f)
+        b.record(stream)
+        torch.cuda.synchronize()
+        back_to_back = a.elapsed_time(b) * 1e3 / n
+        single = timed(hx, x, f, 300, name == "C4")
+        fl = floor(hx)
+        entry = {"us_step_back_to_back": round(back_to_back, 2), "us_step_single": round(single, 2),
+                 "launch_floor_us": round(fl, 2), "single_over_floor": round(single / fl, 2),
+                 "map_entries": ent,
+                 "frac_of_peak_back_to_back": round(68 * ent / (back_to_back * 1e-6) / 1e9 / peak, 4)}
+        if name == "C4":
+            entry["cold_l2"] = True
+        res[name] = entry
+        del hx
+    return res
+
+
+def cpu_baseline(w, pos, budget_s):
+    """The oracle as it stands, single-threaded, on the full workload:
+    coordinate + force exchange steps until the budget is spent."""
+    from oracle.oracle import Oracle
+
+    o = Oracle(w.box, w.dims, w.cutoff)
+    o.build(pos)
+    x = o.coords()
+    f = W.forces(w, o.total_slots)
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        o.exchange_coords(x)
+        o.exchange_forces(f)
+        n += 1
+        el = time.perf_counter() - t0
+        if (el >= budget_s and n >= 3) or n >= 1000:
+            break
+    return {"value": round(el / n * 1e6, 1), "unit": "us/step", "cores": 1, "kind": "oracle",
+            "sample": f"{n} full steps of {w.name} (coords + forces), one host thread, C oracle gcc -O2",
+            "host_cpus": os.cpu_count()}
+
+
+# ---------------------------------------------------------------- reference arm
+
+def sample_workload(w, halvings):
+    """The same per-domain geometry (slab widths, atoms per domain, cutoff,
+    in-domain order) on a decomposition with 2**halvings fewer domains."""
+    dims = list(w.dims)
+    for _ in range(halvings):
+        d = max(range(3), key=lambda i: (dims[i], i))
+        if dims[d] <= 2:
+            break
+        dims[d] //= 2
+    box = tuple(w.box[i] / w.dims[i] * dims[i] for i in range(3))
+    n_dom = dims[0] * dims[1] * dims[2]
+    per = w.n_atoms // (w.dims[0] * w.dims[1] * w.dims[2])
+    return W.custom(f"{w.name}-sample", per * n_dom, box, tuple(dims), w.cutoff, w.seed, w.forces, w.order)
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from oracle.oracle import Oracle
+
+    w = W.WORKLOADS[args.workload]
+    full = Oracle(w.box, w.dims, w.cutoff)
+    full.build(W.positions(w))
+    full_entries = full.total_entries
+    x = full.coords()
+    f = W.forces(w, full.total_slots)
+    t0 = time.perf_counter()
+    full.exchange_coords(x)
+    full.exchange_forces(f)
+    t_full = time.perf_counter() - t0
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    sw, o = w, full
+    halvings = 0
+    while t_full / (2 ** halvings) > budget and halvings < 12:
+        halvings += 1
+    if halvings:
+        sw = sample_workload(w, halvings)
+        o = Oracle(sw.box, sw.dims, sw.cutoff)
+        o.build(W.positions(sw))
+        x = o.coords()
+        f = W.forces(sw, o.total_slots)
+    scale = full_entries / max(1, o.total_entries)
+    for _ in range(args.warmup):
+        o.exchange_coords(x)
+        o.exchange_forces(f)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        o.exchange_coords(x)
+        o.exchange_forces(f)
+    el = time.perf_counter() - t0
+    us_step = el / args.steps * 1e6 * scale
+    sample = (f"full {w.name} each step" if sw is w else
+              f"{sw.describe()} each step ({o.total_entries} of {full_entries} map entries, same per-domain "
+              f"geometry), scaled by the entry ratio {scale:.3f}")
+    out = {
+        "metric": METRIC, "value": round(us_step, 1), "unit": "us/step", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(us_step / 1e3, 4), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": workload_label(w), "map_entries": full_entries},
+        "impl": "reference",
+        "cpu_baseline": {"value": round(us_step, 1), "unit": "us/step", "kind": "oracle", "cores": 1,
+                         "sample": sample},
+        "e2e": {"value": round(us_step, 1), "unit": "us/step", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,834 @@
+// Host runtime and C-ABI of libhx: decomposition plan, map-build driver,
+// work tables of the fused kernels, CUDA-graph launch cache, status.
+//
+// The plan follows "A Practical Guide to GPU-Initiated Communication for
+// Molecular Dynamics at Scale": pulses numbered globally Z -> Y -> X
+// (section "Dependency-aware packing"); a dependent tail that waits for every
+// earlier pulse into its sender; forces in reverse pulse order (section
+// "Force halo exchange: Reversing the dependency chain").
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "../../include/hx.h"
+#include "hx_internal.h"
+
+using namespace hx;
+
+namespace {
+
+constexpr int kGraphCache = 16;
+
+struct GraphEntry {
+  int kind;        // 0 coords, 1 forces, 2 noop
+  void* ptr;
+  cudaGraphExec_t exec;
+};
+
+template <class T>
+cudaError_t dev_alloc(T** p, size_t count) {
+  *p = nullptr;
+  if (count == 0) count = 1;
+  return cudaMalloc(reinterpret_cast<void**>(p), sizeof(T) * count);
+}
+
+template <class T>
+void dev_free(T*& p) {
+  if (p) cudaFree(p);
+  p = nullptr;
+}
+
+struct Plan {
+  double box[3];
+  int dims[3];
+  double cutoff;
+  float boxf[3];
+  float rcf;
+  int np[3];
+  int n_pulses;
+  int pulse_dim[HX_MAX_PULSES];
+  int pulse_k[HX_MAX_PULSES];
+  int ndom;
+  std::vector<float> lo[3];
+};
+
+int make_plan(const double box[3], const int dims[3], double cutoff, Plan* pl) {
+  if (!box || !dims || !(cutoff > 0.0) || !std::isfinite(cutoff)) return HX_ERR_ARG;
+  int64_t ndom = 1;
+  for (int d = 0; d < 3; ++d) {
+    if (dims[d] < 1 || !(box[d] > 0.0) || !std::isfinite(box[d])) return HX_ERR_ARG;
+    ndom *= dims[d];
+  }
+  if (ndom > HX_MAX_DOMAINS) return HX_ERR_ARG;
+  pl->cutoff = cutoff;
+  pl->rcf = static_cast<float>(cutoff);
+  pl->ndom = static_cast<int>(ndom);
+  for (int d = 0; d < 3; ++d) {
+    pl->box[d] = box[d];
+    pl->dims[d] = dims[d];
+    pl->boxf[d] = static_cast<float>(box[d]);
+    if (dims[d] > 1) {
+      const double w = box[d] / dims[d];
+      const double np = std::ceil(cutoff / w);
+      if (np >= dims[d]) return HX_ERR_PULSES;
+      pl->np[d] = static_cast<int>(np);
+    } else {
+      pl->np[d] = 0;
+    }
+    pl->lo[d].resize(dims[d]);
+    for (int c = 0; c < dims[d]; ++c) pl->lo[d][c] = static_cast<float>(static_cast<double>(c) * box[d] / dims[d]);
+  }
+  int p = 0;
+  for (int d = 2; d >= 0; --d) {
+    for (int k = 0; k < pl->np[d]; ++k) {
+      if (p >= HX_MAX_PULSES) return HX_ERR_PULSES;
+      pl->pulse_dim[p] = d;
+      pl->pulse_k[p] = k;
+      ++p;
+    }
+  }
+  pl->n_pulses = p;
+  return HX_OK;
+}
+
+void cell_of(const Plan& pl, int r, int c[3]) {
+  c[0] = r % pl.dims[0];
+  c[1] = (r / pl.dims[0]) % pl.dims[1];
+  c[2] = r / (pl.dims[0] * pl.dims[1]);
+}
+
+int domain_of(const Plan& pl, const int c[3]) { return c[0] + pl.dims[0] * (c[1] + pl.dims[1] * c[2]); }
+
+int neighbour(const Plan& pl, int r, int d, int step) {
+  int c[3];
+  cell_of(pl, r, c);
+  c[d] = ((c[d] + step) % pl.dims[d] + pl.dims[d]) % pl.dims[d];
+  return domain_of(pl, c);
+}
+
+}  // namespace
+
+struct hx_ctx {
+  Plan pl;
+  int device = 0;
+  unsigned flags = 0;
+  unsigned long long timeout_ns = 0;
+  int sm_count = 0;
+
+  bool built = false;
+  int64_t n_atoms = 0;
+  int64_t total_slots = 0;
+  int64_t total_entries = 0;
+  std::vector<int64_t> dom_offset;
+  std::vector<int32_t> home, halo;
+  // per (pulse p, sender r), index p * ndom + r
+  std::vector<int64_t> t_map_off;
+  std::vector<int32_t> t_size, t_recv, t_off, t_shift, t_split;
+
+  int32_t* d_maps = nullptr;
+  int32_t* d_home_ids = nullptr;
+  Item* d_items = nullptr;
+  Chunk* d_chunks[2] = {nullptr, nullptr};   // fused coordinate / force chunk lists
+  Wait* d_waits[2] = {nullptr, nullptr};
+  Chunk* d_uchunks = nullptr;                // unfused per-pulse chunk list
+  unsigned long long* d_flags = nullptr;     // [2][n_items]
+  unsigned int* d_blk = nullptr;             // [2][n_items]
+  Ctrl* d_ctrl = nullptr;                    // [2]
+  int n_chunks[2] = {0, 0};
+  int grid[2] = {0, 0};
+  std::vector<int> u_begin;                  // per pulse, first unfused chunk (P + 1 entries)
+  std::vector<GraphEntry> graphs;
+};
+
+namespace {
+
+void drop_graphs(hx_ctx* h) {
+  for (auto& g : h->graphs) cudaGraphExecDestroy(g.exec);
+  h->graphs.clear();
+}
+
+void free_tables(hx_ctx* h) {
+  drop_graphs(h);
+  dev_free(h->d_maps);
+  dev_free(h->d_home_ids);
+  dev_free(h->d_items);
+  for (int k = 0; k < 2; ++k) {
+    dev_free(h->d_chunks[k]);
+    dev_free(h->d_waits[k]);
+  }
+  dev_free(h->d_uchunks);
+  dev_free(h->d_flags);
+  dev_free(h->d_blk);
+  dev_free(h->d_ctrl);
+  h->built = false;
+}
+
+#define HX_CUDA(call)                       \
+  do {                                      \
+    cudaError_t e_ = (call);                \
+    if (e_ != cudaSuccess) return HX_ERR_CUDA; \
+  } while (0)
+
+int to_err(cudaError_t e) {
+  if (e == cudaSuccess) return HX_OK;
+  if (e == cudaErrorMemoryAllocation) return HX_ERR_NOMEM;
+  return HX_ERR_CUDA;
+}
+
+DirParams dir_params(hx_ctx* h, int dir) {
+  DirParams P;
+  const int n_items = h->pl.n_pulses * h->pl.ndom;
+  P.items = h->d_items;
+  P.chunks = h->d_chunks[dir];
+  P.waits = h->d_waits[dir];
+  P.maps = h->d_maps;
+  P.flags = h->d_flags + static_cast<size_t>(dir) * n_items;
+  P.blk_count = h->d_blk + static_cast<size_t>(dir) * n_items;
+  P.ctrl = h->d_ctrl + dir;
+  P.n_chunks = h->n_chunks[dir];
+  P.direction = dir;
+  P.timeout_ns = h->timeout_ns;
+  return P;
+}
+
+const void* kernel_for(hx_ctx* h, int kind) {
+  const int mode = (h->flags & HX_FLAG_COUNTER_SIGNAL) ? kCounter : kLastBlock;
+  if (kind == 0) return coords_kernel(mode);
+  if (kind == 1) return forces_kernel(mode, !(h->flags & HX_FLAG_UNORDERED_FORCES));
+  return noop_kernel();
+}
+
+// Launch a fused exchange (kind 0/1) or the no-op (kind 2): directly, or via
+// a cached single-node graph keyed by (kind, buffer pointer).
+int launch(hx_ctx* h, int kind, float* buf, cudaStream_t s) {
+  DirParams P;
+  void* args2[2];
+  void** args = nullptr;
+  dim3 grid(1), block(kind == 2 ? 1 : kThreads);
+  if (kind != 2) {
+    P = dir_params(h, kind);
+    args2[0] = &buf;
+    args2[1] = &P;
+    args = args2;
+    grid = dim3(static_cast<unsigned>(h->grid[kind]));
+  }
+  const void* fn = kernel_for(h, kind);
+  if (h->flags & HX_FLAG_NO_GRAPH) return to_err(cudaLaunchKernel(fn, grid, block, args, 0, s));
+  for (auto& g : h->graphs)
+    if (g.kind == kind && g.ptr == buf) return to_err(cudaGraphLaunch(g.exec, s));
+  cudaGraph_t graph;
+  HX_CUDA(cudaGraphCreate(&graph, 0));
+  cudaKernelNodeParams kp;
+  std::memset(&kp, 0, sizeof(kp));
+  kp.func = const_cast<void*>(fn);
+  kp.gridDim = grid;
+  kp.blockDim = block;
+  kp.sharedMemBytes = 0;
+  kp.kernelParams = args;
+  cudaGraphNode_t node;
+  cudaError_t e = cudaGraphAddKernelNode(&node, graph, nullptr, 0, &kp);
+  cudaGraphExec_t exec = nullptr;
+  if (e == cudaSuccess) e = cudaGraphInstantiate(&exec, graph, 0);
+  cudaGraphDestroy(graph);
+  if (e != cudaSuccess) return to_err(e);
+  if (static_cast<int>(h->graphs.size()) >= kGraphCache) {
+    cudaGraphExecDestroy(h->graphs.front().exec);
+    h->graphs.erase(h->graphs.begin());
+  }
+  h->graphs.push_back({kind, buf, exec});
+  return to_err(cudaGraphLaunch(exec, s));
+}
+
+int reset_signals(hx_ctx* h, cudaStream_t s) {
+  const size_t n_items = static_cast<size_t>(h->pl.n_pulses) * h->pl.ndom;
+  HX_CUDA(cudaMemsetAsync(h->d_flags, 0, sizeof(unsigned long long) * 2 * std::max<size_t>(n_items, 1), s));
+  HX_CUDA(cudaMemsetAsync(h->d_blk, 0, sizeof(unsigned int) * 2 * std::max<size_t>(n_items, 1), s));
+  Ctrl c[2];
+  std::memset(c, 0, sizeof(c));
+  c[0].drop_item = c[1].drop_item = -1;
+  HX_CUDA(cudaMemcpyAsync(h->d_ctrl, c, sizeof(c), cudaMemcpyHostToDevice, s));
+  HX_CUDA(cudaStreamSynchronize(s));
+  return HX_OK;
+}
+
+int64_t chunk_entries(int64_t total_entries) {
+  // Large exchanges: two block passes per chunk; small ones: one, so that the
+  // chain of dependent pulses is spread over as many blocks as possible.
+  return total_entries > (int64_t{4} << 20) ? 2 * kPass : kPass;
+}
+
+// Work tables of the fused and unfused kernels from the host copy of the plan.
+int build_tables(hx_ctx* h, cudaStream_t s) {
+  const Plan& pl = h->pl;
+  const int P = pl.n_pulses, nd = pl.ndom;
+  const int n_items = P * nd;
+  const int64_t CH = chunk_entries(h->total_entries);
+  std::vector<Item> items(std::max(n_items, 1));
+  std::vector<Chunk> cch, fch, uch;
+  std::vector<Wait> cw, fw;
+  for (int p = 0; p < P; ++p) {
+    for (int r = 0; r < nd; ++r) {
+      const int t = p * nd + r;
+      Item& it = items[t];
+      std::memset(&it, 0, sizeof(it));
+      it.src_base = h->dom_offset[r];
+      it.dst_base = h->dom_offset[h->t_recv[t]] + h->t_off[t];
+      it.map_off = h->t_map_off[t];
+      it.size = h->t_size[t];
+      it.split = h->t_split[t];
+      it.dim = pl.pulse_dim[p];
+      it.do_shift = h->t_shift[t];
+      it.shift = pl.boxf[it.dim];
+    }
+  }
+  auto add_chunks = [&](std::vector<Chunk>& out, int t, int begin, int end, int halo_src, int woff, int wcnt,
+                        bool always_one) {
+    int made = 0;
+    for (int64_t b = begin; b < end; b += CH) {
+      out.push_back({t, static_cast<int32_t>(b), static_cast<int32_t>(std::min<int64_t>(end, b + CH)), woff, wcnt,
+                     halo_src});
+      ++made;
+    }
+    if (made == 0 && always_one) {
+      out.push_back({t, begin, begin, woff, wcnt, halo_src});
+      ++made;
+    }
+    return made;
+  };
+  // Coordinates: all independent parts (pulse order), then the dependent
+  // tails (pulse order). A dependent tail of (r, p) waits for the pulses
+  // p' < p into r, i.e. for items (upper_{p'}(r), p').
+  for (int p = 0; p < P; ++p)
+    for (int r = 0; r < nd; ++r) {
+      const int t = p * nd + r;
+      items[t].coord_chunks = add_chunks(cch, t, 0, items[t].split, 0, 0, 0, items[t].size == 0);
+    }
+  for (int p = 0; p < P; ++p)
+    for (int r = 0; r < nd; ++r) {
+      const int t = p * nd + r;
+      if (items[t].split >= items[t].size) continue;
+      const int woff = static_cast<int>(cw.size());
+      for (int q = 0; q < p; ++q) cw.push_back({q * nd + neighbour(pl, r, pl.pulse_dim[q], +1), 0});
+      const int wcnt = static_cast<int>(cw.size()) - woff;
+      items[t].coord_chunks += add_chunks(cch, t, items[t].split, items[t].size, 1, woff, wcnt, false);
+    }
+  for (auto& w : cw) w.chunks = items[w.item].coord_chunks;
+  // Forces: pulses last to first. (r, p) waits for (r, p') and for its
+  // receiver's (q, p'), p' > p; unordered mode keeps only the receiver's.
+  const bool ordered = !(h->flags & HX_FLAG_UNORDERED_FORCES);
+  for (int p = P - 1; p >= 0; --p)
+    for (int r = 0; r < nd; ++r) {
+      const int t = p * nd + r;
+      const int q = h->t_recv[t];
+      const int woff = static_cast<int>(fw.size());
+      for (int pp = p + 1; pp < P; ++pp) {
+        fw.push_back({pp * nd + q, 0});
+        if (ordered && r != q) fw.push_back({pp * nd + r, 0});
+      }
+      const int wcnt = static_cast<int>(fw.size()) - woff;
+      items[t].force_chunks = add_chunks(fch, t, 0, items[t].size, 1, woff, wcnt, true);
+    }
+  for (auto& w : fw) w.chunks = items[w.item].force_chunks;
+  // Unfused: per pulse, every item's entries, no waits.
+  h->u_begin.assign(P + 1, 0);
+  for (int p = 0; p < P; ++p) {
+    h->u_begin[p] = static_cast<int>(uch.size());
+    for (int r = 0; r < nd; ++r) add_chunks(uch, p * nd + r, 0, h->t_size[p * nd + r], 1, 0, 0, false);
+  }
+  h->u_begin[P] = static_cast<int>(uch.size());
+
+  h->n_chunks[0] = static_cast<int>(cch.size());
+  h->n_chunks[1] = static_cast<int>(fch.size());
+  HX_CUDA(dev_alloc(&h->d_items, items.size()));
+  HX_CUDA(dev_alloc(&h->d_chunks[0], cch.size()));
+  HX_CUDA(dev_alloc(&h->d_chunks[1], fch.size()));
+  HX_CUDA(dev_alloc(&h->d_waits[0], cw.size()));
+  HX_CUDA(dev_alloc(&h->d_waits[1], fw.size()));
+  HX_CUDA(dev_alloc(&h->d_uchunks, uch.size()));
+  HX_CUDA(dev_alloc(&h->d_flags, 2 * static_cast<size_t>(std::max(n_items, 1))));
+  HX_CUDA(dev_alloc(&h->d_blk, 2 * static_cast<size_t>(std::max(n_items, 1))));
+  HX_CUDA(dev_alloc(&h->d_ctrl, 2));
+  HX_CUDA(cudaMemcpyAsync(h->d_items, items.data(), sizeof(Item) * items.size(), cudaMemcpyHostToDevice, s));
+  if (!cch.empty())
+    HX_CUDA(cudaMemcpyAsync(h->d_chunks[0], cch.data(), sizeof(Chunk) * cch.size(), cudaMemcpyHostToDevice, s));
+  if (!fch.empty())
+    HX_CUDA(cudaMemcpyAsync(h->d_chunks[1], fch.data(), sizeof(Chunk) * fch.size(), cudaMemcpyHostToDevice, s));
+  if (!cw.empty())
+    HX_CUDA(cudaMemcpyAsync(h->d_waits[0], cw.data(), sizeof(Wait) * cw.size(), cudaMemcpyHostToDevice, s));
+  if (!fw.empty())
+    HX_CUDA(cudaMemcpyAsync(h->d_waits[1], fw.data(), sizeof(Wait) * fw.size(), cudaMemcpyHostToDevice, s));
+  if (!uch.empty())
+    HX_CUDA(cudaMemcpyAsync(h->d_uchunks, uch.data(), sizeof(Chunk) * uch.size(), cudaMemcpyHostToDevice, s));
+  // Persistent grid: every block co-resident.
+  for (int k = 0; k < 2; ++k) {
+    const int per_sm = std::max(1, max_blocks_per_sm(kernel_for(h, k)));
+    h->grid[k] = std::max(1, std::min(h->n_chunks[k], per_sm * h->sm_count));
+  }
+  return reset_signals(h, s);   // synchronises: the host vectors above may go
+}
+
+struct BuildScratch {
+  int32_t* dom_id = nullptr;
+  int32_t* hist = nullptr;
+  int32_t* hist_scan = nullptr;
+  int* err = nullptr;
+  float* home_xyz = nullptr;
+  int32_t* home_dom = nullptr;
+  int64_t* home_start = nullptr;
+  int64_t* dom_off = nullptr;
+  BuildTile* tiles = nullptr;
+  int32_t* tile_cnt = nullptr;
+  int32_t* tile_off = nullptr;
+  const float** bufs = nullptr;
+  std::vector<float*> recv;     // per pulse: received coordinates, sender-major
+  std::vector<int32_t*> maps;   // per pulse: maps, sender-major
+  ~BuildScratch() {
+    dev_free(dom_id); dev_free(hist); dev_free(hist_scan); dev_free(err); dev_free(home_xyz);
+    dev_free(home_dom); dev_free(home_start); dev_free(dom_off); dev_free(tiles); dev_free(tile_cnt);
+    dev_free(tile_off); dev_free(bufs);
+    for (auto* p : recv) dev_free(p);
+    for (auto* p : maps) dev_free(p);
+  }
+};
+
+int build(hx_ctx* h, const float* pos, int64_t n, float* coords, int64_t capacity, cudaStream_t s) {
+  const Plan& pl = h->pl;
+  const int nd = pl.ndom, P = pl.n_pulses;
+  BuildScratch b;
+  // 1. home cells and stable partition
+  const int ntiles = static_cast<int>((n + kPartTile - 1) / kPartTile);
+  HX_CUDA(dev_alloc(&b.dom_id, n));
+  HX_CUDA(dev_alloc(&b.hist, static_cast<size_t>(nd) * std::max(ntiles, 1)));
+  HX_CUDA(dev_alloc(&b.hist_scan, static_cast<size_t>(nd) * std::max(ntiles, 1)));
+  HX_CUDA(dev_alloc(&b.err, 1));
+  HX_CUDA(dev_alloc(&b.home_xyz, 3 * static_cast<size_t>(n)));
+  HX_CUDA(dev_alloc(&b.home_dom, n));
+  HX_CUDA(dev_alloc(&h->d_home_ids, n));
+  HX_CUDA(cudaMemsetAsync(b.err, 0, sizeof(int), s));
+  HX_CUDA(launch_cells(pos, n, pl.dims, pl.box, nd, b.dom_id, b.hist, ntiles, b.err, s));
+  HX_CUDA(scan_exclusive(b.hist, b.hist_scan, static_cast<int64_t>(nd) * ntiles, s));
+  std::vector<int32_t> first(nd, 0);
+  if (ntiles > 0)
+    HX_CUDA(cudaMemcpy2DAsync(first.data(), sizeof(int32_t), b.hist_scan, sizeof(int32_t) * ntiles,
+                              sizeof(int32_t), nd, cudaMemcpyDeviceToHost, s));
+  int err_host = 0;
+  HX_CUDA(cudaMemcpyAsync(&err_host, b.err, sizeof(int), cudaMemcpyDeviceToHost, s));
+  HX_CUDA(cudaStreamSynchronize(s));
+  if (err_host) return HX_ERR_RANGE;
+  std::vector<int64_t> home_start(nd);
+  h->home.assign(nd, 0);
+  for (int r = 0; r < nd; ++r) {
+    home_start[r] = first[r];
+    const int64_t next = (r + 1 < nd) ? first[r + 1] : n;
+    h->home[r] = static_cast<int32_t>(next - first[r]);
+  }
+  HX_CUDA(launch_scatter_home(pos, n, nd, b.dom_id, b.hist_scan, ntiles, h->d_home_ids, b.home_xyz, b.home_dom,
+                              s));
+
+  // 2. pulses in global order
+  std::vector<int64_t> len(nd);
+  for (int r = 0; r < nd; ++r) len[r] = h->home[r];
+  std::vector<int64_t> off(static_cast<size_t>(nd) * std::max(P, 1), 0), rcv(off.size(), 0);
+  std::vector<int64_t> sender_prefix(off.size(), 0);   // [p * nd + r] position of r's map in pulse p
+  std::vector<int64_t> pulse_total(std::max(P, 1), 0);
+  h->t_map_off.assign(static_cast<size_t>(nd) * P, 0);
+  h->t_size.assign(static_cast<size_t>(nd) * P, 0);
+  h->t_recv.assign(static_cast<size_t>(nd) * P, 0);
+  h->t_off.assign(static_cast<size_t>(nd) * P, 0);
+  h->t_shift.assign(static_cast<size_t>(nd) * P, 0);
+  h->t_split.assign(static_cast<size_t>(nd) * P, 0);
+  HX_CUDA(dev_alloc(&b.bufs, 1 + P));
+  std::vector<const float*> bufs_host(1 + P, nullptr);
+  bufs_host[0] = b.home_xyz;
+  b.recv.assign(P, nullptr);
+  b.maps.assign(P, nullptr);
+  for (int p = 0; p < P; ++p) {
+    const int d = pl.pulse_dim[p];
+    const int k = pl.pulse_k[p];
+    std::vector<BuildTile> tiles;
+    std::vector<int> tile_home(0);   // 1 when the tile lies in the sender's home range
+    std::vector<int> first_tile(nd + 1, 0);
+    for (int r = 0; r < nd; ++r) {
+      first_tile[r] = static_cast<int>(tiles.size());
+      int c[3];
+      cell_of(pl, r, c);
+      auto add_segment = [&](int buf, int64_t elem_begin, int64_t local_begin, int64_t count, int is_home) {
+        for (int64_t e = 0; e < count; e += kSelTile) {
+          BuildTile t;
+          std::memset(&t, 0, sizeof(t));
+          t.sender = r;
+          t.local_begin = static_cast<int32_t>(local_begin + e);
+          t.n = static_cast<int32_t>(std::min<int64_t>(kSelTile, count - e));
+          t.buf = buf;
+          t.elem_begin = elem_begin + e;
+          t.lo = pl.lo[d][c[d]];
+          t.shift = pl.boxf[d];
+          t.do_shift = (c[d] == 0);
+          tiles.push_back(t);
+          tile_home.push_back(is_home);
+        }
+      };
+      if (k == 0) {
+        add_segment(0, home_start[r], 0, h->home[r], 1);
+        for (int q = 0; q < p; ++q) {
+          const int up = neighbour(pl, r, pl.pulse_dim[q], +1);   // the domain that sent into r in pulse q
+          add_segment(1 + q, sender_prefix[static_cast<size_t>(q) * nd + up], off[static_cast<size_t>(r) * P + q],
+                      rcv[static_cast<size_t>(r) * P + q], 0);
+        }
+      } else {
+        const int q = p - 1;
+        const int up = neighbour(pl, r, pl.pulse_dim[q], +1);
+        add_segment(1 + q, sender_prefix[static_cast<size_t>(q) * nd + up], off[static_cast<size_t>(r) * P + q],
+                    rcv[static_cast<size_t>(r) * P + q], 0);
+      }
+    }
+    first_tile[nd] = static_cast<int>(tiles.size());
+    const int nt = static_cast<int>(tiles.size());
+    dev_free(b.tiles);
+    dev_free(b.tile_cnt);
+    dev_free(b.tile_off);
+    HX_CUDA(dev_alloc(&b.tiles, nt));
+    HX_CUDA(dev_alloc(&b.tile_cnt, nt));
+    HX_CUDA(dev_alloc(&b.tile_off, nt));
+    if (nt > 0)
+      HX_CUDA(cudaMemcpyAsync(b.tiles, tiles.data(), sizeof(BuildTile) * nt, cudaMemcpyHostToDevice, s));
+    HX_CUDA(cudaMemcpyAsync(b.bufs, bufs_host.data(), sizeof(float*) * bufs_host.size(), cudaMemcpyHostToDevice, s));
+    HX_CUDA(launch_select_count(b.tiles, nt, b.bufs, d, pl.rcf, b.tile_cnt, s));
+    HX_CUDA(scan_exclusive(b.tile_cnt, b.tile_off, nt, s));
+    std::vector<int32_t> cnt(std::max(nt, 1)), toff(std::max(nt, 1));
+    if (nt > 0) {
+      HX_CUDA(cudaMemcpyAsync(cnt.data(), b.tile_cnt, sizeof(int32_t) * nt, cudaMemcpyDeviceToHost, s));
+      HX_CUDA(cudaMemcpyAsync(toff.data(), b.tile_off, sizeof(int32_t) * nt, cudaMemcpyDeviceToHost, s));
+    }
+    HX_CUDA(cudaStreamSynchronize(s));
+    int64_t total = 0;
+    for (int r = 0; r < nd; ++r) {
+      int64_t S = 0, split = 0;
+      for (int t = first_tile[r]; t < first_tile[r + 1]; ++t) {
+        S += cnt[t];
+        if (tile_home[t]) split += cnt[t];
+      }
+      const size_t idx = static_cast<size_t>(p) * nd + r;
+      sender_prefix[idx] = total;
+      if (first_tile[r] < first_tile[r + 1] && toff[first_tile[r]] != total) return HX_ERR_CUDA;
+      h->t_size[idx] = static_cast<int32_t>(S);
+      h->t_split[idx] = static_cast<int32_t>(split);
+      int c[3];
+      cell_of(pl, r, c);
+      h->t_shift[idx] = (c[d] == 0);
+      total += S;
+    }
+    pulse_total[p] = total;
+    HX_CUDA(dev_alloc(&b.recv[p], 3 * static_cast<size_t>(total)));
+    HX_CUDA(dev_alloc(&b.maps[p], static_cast<size_t>(total)));
+    bufs_host[1 + p] = b.recv[p];
+    HX_CUDA(launch_select_write(b.tiles, nt, b.bufs, d, pl.rcf, b.tile_off, b.maps[p], b.recv[p], s));
+    // receivers: each domain receives exactly one range per pulse
+    std::vector<int64_t> len_before = len;
+    for (int r = 0; r < nd; ++r) {
+      const size_t idx = static_cast<size_t>(p) * nd + r;
+      const int q = neighbour(pl, r, d, -1);
+      h->t_recv[idx] = q;
+      h->t_off[idx] = static_cast<int32_t>(len_before[q]);
+      off[static_cast<size_t>(q) * P + p] = len_before[q];
+      rcv[static_cast<size_t>(q) * P + p] = h->t_size[idx];
+      len[q] += h->t_size[idx];
+    }
+    for (int r = 0; r < nd; ++r)
+      if (len[r] > INT32_MAX) return HX_ERR_CAPACITY;
+  }
+
+  // 3. layout and concatenated maps (pulse-major, sender-minor)
+  h->dom_offset.assign(nd, 0);
+  h->halo.assign(nd, 0);
+  int64_t slots = 0;
+  for (int r = 0; r < nd; ++r) {
+    h->dom_offset[r] = slots;
+    h->halo[r] = static_cast<int32_t>(len[r] - h->home[r]);
+    slots += len[r];
+  }
+  h->total_slots = slots;
+  int64_t entries = 0;
+  for (int p = 0; p < P; ++p) entries += pulse_total[p];
+  h->total_entries = entries;
+  HX_CUDA(dev_alloc(&h->d_maps, entries));
+  int64_t base = 0;
+  for (int p = 0; p < P; ++p) {
+    if (pulse_total[p] > 0)
+      HX_CUDA(cudaMemcpyAsync(h->d_maps + base, b.maps[p], sizeof(int32_t) * pulse_total[p],
+                              cudaMemcpyDeviceToDevice, s));
+    for (int r = 0; r < nd; ++r) {
+      const size_t idx = static_cast<size_t>(p) * nd + r;
+      h->t_map_off[idx] = base + sender_prefix[idx];
+    }
+    base += pulse_total[p];
+  }
+  // keep what placing the home coordinates needs
+  HX_CUDA(dev_alloc(&b.home_start, nd));
+  HX_CUDA(dev_alloc(&b.dom_off, nd));
+  HX_CUDA(cudaMemcpyAsync(b.home_start, home_start.data(), sizeof(int64_t) * nd, cudaMemcpyHostToDevice, s));
+  HX_CUDA(cudaMemcpyAsync(b.dom_off, h->dom_offset.data(), sizeof(int64_t) * nd, cudaMemcpyHostToDevice, s));
+  int rc = build_tables(h, s);
+  if (rc != HX_OK) return rc;
+  h->n_atoms = n;
+  h->built = true;
+  if (!coords) return HX_OK;
+  if (capacity < h->total_slots) return HX_ERR_CAPACITY;
+  // 4. fill the caller's array: home coordinates, then one coordinate exchange
+  HX_CUDA(launch_place_home(b.home_xyz, b.home_dom, b.home_start, b.dom_off, n, coords, s));
+  if (P > 0 && h->n_chunks[0] > 0) {
+    rc = launch(h, 0, coords, s);
+    if (rc != HX_OK) return rc;
+  }
+  HX_CUDA(cudaStreamSynchronize(s));
+  return HX_OK;
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ C ABI
+
+extern "C" {
+
+const char* hx_error_string(int code) {
+  switch (code) {
+    case HX_OK: return "ok";
+    case HX_ERR_ARG: return "invalid argument";
+    case HX_ERR_PULSES: return "too many pulses: the cutoff spans the whole periodic dimension";
+    case HX_ERR_RANGE: return "position outside [0, L)";
+    case HX_ERR_CAPACITY: return "buffer smaller than the layout";
+    case HX_ERR_CUDA: return "CUDA error";
+    case HX_ERR_TIMEOUT: return "device wait for a pulse signal timed out";
+    case HX_ERR_STATE: return "exchange before a successful build";
+    case HX_ERR_NOMEM: return "out of memory";
+    default: return "unknown error";
+  }
+}
+
+int hx_query_plan(const double box[3], const int dims[3], double cutoff, int* n_pulses, int32_t* pulse_dim,
+                  int32_t* pulse_k) {
+  Plan pl;
+  const int rc = make_plan(box, dims, cutoff, &pl);
+  if (rc != HX_OK) return rc;
+  if (n_pulses) *n_pulses = pl.n_pulses;
+  for (int p = 0; p < pl.n_pulses; ++p) {
+    if (pulse_dim) pulse_dim[p] = pl.pulse_dim[p];
+    if (pulse_k) pulse_k[p] = pl.pulse_k[p];
+  }
+  return HX_OK;
+}
+
+int hx_init(hx_handle* out, const double box[3], const int dims[3], double cutoff, int device, unsigned flags,
+            unsigned timeout_us) {
+  if (!out) return HX_ERR_ARG;
+  *out = nullptr;
+  Plan pl;
+  int rc = make_plan(box, dims, cutoff, &pl);
+  if (rc != HX_OK) return rc;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) return HX_ERR_CUDA;
+  if (cudaSetDevice(device) != cudaSuccess) return HX_ERR_CUDA;
+  hx_ctx* h = new (std::nothrow) hx_ctx();
+  if (!h) return HX_ERR_NOMEM;
+  h->pl = pl;
+  h->device = device;
+  h->flags = flags;
+  h->timeout_ns = 1000ull * (timeout_us ? timeout_us : 1000000u);
+  if (cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
+    delete h;
+    return HX_ERR_CUDA;
+  }
+  *out = h;
+  return HX_OK;
+}
+
+int hx_build_maps(hx_handle h, const float* pos_in, int64_t n_atoms, float* coords, int64_t capacity,
+                  int64_t* needed, void* stream) {
+  if (!h || n_atoms < 0 || n_atoms > INT32_MAX || (n_atoms > 0 && !pos_in)) return HX_ERR_ARG;
+  if (cudaSetDevice(h->device) != cudaSuccess) return HX_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  free_tables(h);
+  const int rc = build(h, pos_in, n_atoms, coords, capacity, s);
+  if (rc == HX_OK || rc == HX_ERR_CAPACITY) {
+    if (needed) *needed = h->total_slots;
+    return rc;
+  }
+  free_tables(h);
+  return rc;
+}
+
+namespace {
+
+int ensure_device(hx_ctx* h) {
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) return HX_ERR_CUDA;
+  if (cur != h->device && cudaSetDevice(h->device) != cudaSuccess) return HX_ERR_CUDA;
+  return HX_OK;
+}
+
+int exchange(hx_handle h, float* buf, void* stream, int kind) {
+  if (!h) return HX_ERR_ARG;
+  if (!h->built) return HX_ERR_STATE;
+  if (!buf && h->total_slots > 0) return HX_ERR_ARG;   // an empty layout touches no memory
+  if (h->pl.n_pulses == 0) return HX_OK;
+  const int rc = ensure_device(h);
+  if (rc != HX_OK) return rc;
+  return launch(h, kind, buf, static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+
+int hx_exchange_coords(hx_handle h, float* coords, void* stream) { return exchange(h, coords, stream, 0); }
+
+int hx_exchange_forces(hx_handle h, float* forces, void* stream) { return exchange(h, forces, stream, 1); }
+
+int hx_exchange_coords_unfused(hx_handle h, float* coords, void* stream) {
+  if (!h) return HX_ERR_ARG;
+  if (!h->built) return HX_ERR_STATE;
+  if (!coords && h->total_slots > 0) return HX_ERR_ARG;
+  int rc = ensure_device(h);
+  if (rc != HX_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  for (int p = 0; p < h->pl.n_pulses; ++p) {
+    PulseParams pp{h->d_items, h->d_uchunks, h->d_maps, h->u_begin[p]};
+    rc = to_err(launch_pack_pulse(coords, pp, h->u_begin[p + 1] - h->u_begin[p], s));
+    if (rc != HX_OK) return rc;
+  }
+  return HX_OK;
+}
+
+int hx_exchange_forces_unfused(hx_handle h, float* forces, void* stream) {
+  if (!h) return HX_ERR_ARG;
+  if (!h->built) return HX_ERR_STATE;
+  if (!forces && h->total_slots > 0) return HX_ERR_ARG;
+  int rc = ensure_device(h);
+  if (rc != HX_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  for (int p = h->pl.n_pulses - 1; p >= 0; --p) {
+    PulseParams pp{h->d_items, h->d_uchunks, h->d_maps, h->u_begin[p]};
+    rc = to_err(launch_unpack_pulse(forces, pp, h->u_begin[p + 1] - h->u_begin[p], s));
+    if (rc != HX_OK) return rc;
+  }
+  return HX_OK;
+}
+
+int hx_noop(hx_handle h, void* stream) {
+  if (!h) return HX_ERR_ARG;
+  const int rc = ensure_device(h);
+  if (rc != HX_OK) return rc;
+  return launch(h, 2, nullptr, static_cast<cudaStream_t>(stream));
+}
+
+int hx_get_counts(hx_handle h, int* n_domains, int* n_pulses, int64_t* total_slots, int64_t* total_entries) {
+  if (!h) return HX_ERR_ARG;
+  if (n_domains) *n_domains = h->pl.ndom;
+  if (n_pulses) *n_pulses = h->pl.n_pulses;
+  if (!h->built) return HX_ERR_STATE;
+  if (total_slots) *total_slots = h->total_slots;
+  if (total_entries) *total_entries = h->total_entries;
+  return HX_OK;
+}
+
+int hx_get_layout(hx_handle h, int64_t* dom_offset, int32_t* home_count, int32_t* halo_count) {
+  if (!h) return HX_ERR_ARG;
+  if (!h->built) return HX_ERR_STATE;
+  for (int r = 0; r < h->pl.ndom; ++r) {
+    if (dom_offset) dom_offset[r] = h->dom_offset[r];
+    if (home_count) home_count[r] = h->home[r];
+    if (halo_count) halo_count[r] = h->halo[r];
+  }
+  return HX_OK;
+}
+
+int hx_get_home_ids(hx_handle h, int32_t* home_ids, void* stream) {
+  if (!h || (!home_ids && h->n_atoms > 0)) return HX_ERR_ARG;
+  if (!h->built) return HX_ERR_STATE;
+  if (h->n_atoms == 0) return HX_OK;
+  int rc = ensure_device(h);
+  if (rc != HX_OK) return rc;
+  return to_err(cudaMemcpyAsync(home_ids, h->d_home_ids, sizeof(int32_t) * h->n_atoms, cudaMemcpyDeviceToDevice,
+                                static_cast<cudaStream_t>(stream)));
+}
+
+int hx_get_maps(hx_handle h, int32_t* maps_host, int64_t cap, int64_t* table_host) {
+  if (!h) return HX_ERR_ARG;
+  if (!h->built) return HX_ERR_STATE;
+  int rc = ensure_device(h);
+  if (rc != HX_OK) return rc;
+  if (maps_host) {
+    if (cap < h->total_entries) return HX_ERR_CAPACITY;
+    if (h->total_entries > 0 &&
+        cudaMemcpy(maps_host, h->d_maps, sizeof(int32_t) * h->total_entries, cudaMemcpyDeviceToHost) != cudaSuccess)
+      return HX_ERR_CUDA;
+  }
+  if (table_host) {
+    const size_t n = static_cast<size_t>(h->pl.n_pulses) * h->pl.ndom;
+    for (size_t t = 0; t < n; ++t) {
+      table_host[6 * t + 0] = h->t_map_off[t];
+      table_host[6 * t + 1] = h->t_size[t];
+      table_host[6 * t + 2] = h->t_recv[t];
+      table_host[6 * t + 3] = h->t_off[t];
+      table_host[6 * t + 4] = h->t_shift[t];
+      table_host[6 * t + 5] = h->t_split[t];
+    }
+  }
+  return HX_OK;
+}
+
+int hx_status(hx_handle h, void* stream, int* detail) {
+  if (detail) *detail = -1;
+  if (!h) return HX_ERR_ARG;
+  if (!h->built) return HX_OK;
+  int rc = ensure_device(h);
+  if (rc != HX_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return HX_ERR_CUDA;
+  Ctrl c[2];
+  if (cudaMemcpy(c, h->d_ctrl, sizeof(c), cudaMemcpyDeviceToHost) != cudaSuccess) return HX_ERR_CUDA;
+  for (int k = 0; k < 2; ++k) {
+    if (c[k].status != 0) {
+      if (detail) *detail = c[k].detail;
+      return c[k].status;
+    }
+  }
+  return HX_OK;
+}
+
+int hx_clear_status(hx_handle h, void* stream) {
+  if (!h) return HX_ERR_ARG;
+  if (!h->built) return HX_OK;
+  int rc = ensure_device(h);
+  if (rc != HX_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return HX_ERR_CUDA;
+  return reset_signals(h, s);
+}
+
+int hx_debug_drop_signal(hx_handle h, int direction, int domain, int pulse) {
+  if (!h || direction < 0 || direction > 1) return HX_ERR_ARG;
+  if (!h->built) return HX_ERR_STATE;
+  int item = -1;
+  if (domain >= 0) {
+    if (domain >= h->pl.ndom || pulse < 0 || pulse >= h->pl.n_pulses) return HX_ERR_ARG;
+    item = pulse * h->pl.ndom + domain;
+  }
+  int rc = ensure_device(h);
+  if (rc != HX_OK) return rc;
+  if (cudaDeviceSynchronize() != cudaSuccess) return HX_ERR_CUDA;
+  Ctrl* c = h->d_ctrl + direction;
+  if (cudaMemcpy(&c->drop_item, &item, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return HX_ERR_CUDA;
+  return HX_OK;
+}
+
+void hx_destroy(hx_handle h) {
+  if (!h) return;
+  if (ensure_device(h) == HX_OK) cudaDeviceSynchronize();
+  free_tables(h);
+  delete h;
+}
+
+}  // extern "C"

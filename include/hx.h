@@ -1,0 +1,197 @@
+/*
+ * hx.h - staged-forwarding halo exchange of a 3D domain decomposition, with
+ * every domain held as a simulated rank in one GPU's memory (sm_103a).
+ *
+ * The operation is the GROMACS halo exchange described in "A Practical Guide
+ * to GPU-Initiated Communication for Molecular Dynamics at Scale" (NVIDIA
+ * technical blog):
+ *   - coordinates: per pulse, the atoms listed by an index map are gathered
+ *     from the sender's coordinate array and stored directly into the
+ *     receiver's array at that pulse's receive offset; pulses run Z -> Y -> X
+ *     and later pulses forward atoms received in earlier ones (intro; section
+ *     "From MPI baseline to optimized GPU-native halo exchange"; section
+ *     "Optimizing for efficient transfers across NVIDIA NVLink-connected
+ *     GPUs" for the direct store into the peer's array);
+ *   - forces: the same maps in reverse pulse order, accumulating received halo
+ *     forces into the sender's force array (unpackRecvBufKernel<accumulate> in
+ *     the MPI-baseline section; section "Force halo exchange: Reversing the
+ *     dependency chain");
+ *   - one fused launch per direction for all pulses, with per-pulse signals
+ *     and a dependent tail that waits only for earlier pulses (sections
+ *     "Enabling parallelism across pulses through kernel fusion" and
+ *     "Dependency-aware packing"; signalPeerOnLastBlock for the last-block
+ *     notification).
+ *
+ * Geometry (the pages leave it open; these readings fix it):
+ *   orthorhombic periodic box L, n_d uniform slabs per dimension, domain id
+ *   r = cx + nx*(cy + ny*cz); home cell c_d = min(n_d-1, floor(x_d*n_d/L_d))
+ *   in fp64 on the fp32 input, home atoms in input order; only dimensions
+ *   with n_d > 1 communicate, np_d = ceil(cutoff / (L_d/n_d)) pulses each,
+ *   np_d < n_d required; in each pulse a domain sends to its lower neighbour
+ *   (c_d - 1 mod n_d) the candidates x with (float)(x_d - lo_d) < (float)cutoff,
+ *   lo_d = (float)(c_d*L_d/n_d) of the sender; candidates of pulse (d,0) are
+ *   all local atoms, of pulse (d,k>0) the atoms received in (d,k-1); maps
+ *   list local indices in ascending order; a sender in cell 0 adds (float)L_d
+ *   to component d; forces are never shifted.
+ *
+ * Layout in the caller's flat float3 (AoS, 12 bytes per atom) buffers:
+ *   domain r occupies slots [dom_offset[r], dom_offset[r] + home[r] + halo[r]):
+ *   its home atoms, then the slots received in pulse 0, pulse 1, ... in the
+ *   global pulse order. Coordinates and forces use the same layout.
+ *
+ * Conventions: every pointer argument is a device pointer unless marked
+ * "host". `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ * stream). Calls are asynchronous on `stream` unless marked "synchronises".
+ * Return value: HX_OK (0) or a negative HX_ERR_* code; no call throws, and
+ * there is no CPU fallback: a handle exists only on a working CUDA device.
+ * The library owns the maps, tables, flags and graphs of a handle until
+ * hx_destroy; the caller owns every buffer it passes in.
+ */
+#ifndef HX_H
+#define HX_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct hx_ctx* hx_handle;
+
+#define HX_OK 0
+#define HX_ERR_ARG (-1)       /* null pointer, cutoff <= 0, dims < 1, box <= 0, bad index */
+#define HX_ERR_PULSES (-2)    /* np_d >= n_d in some dimension, or too many pulses */
+#define HX_ERR_RANGE (-3)     /* an input position outside [0, L) or NaN */
+#define HX_ERR_CAPACITY (-4)  /* caller buffer smaller than the layout needs */
+#define HX_ERR_CUDA (-5)      /* a CUDA runtime call failed */
+#define HX_ERR_TIMEOUT (-6)   /* a device-side wait for a pulse signal ran out of time */
+#define HX_ERR_STATE (-7)     /* exchange before a successful hx_build_maps */
+#define HX_ERR_NOMEM (-8)     /* host or device allocation failed */
+
+/* hx_init flags */
+#define HX_FLAG_UNORDERED_FORCES 0x1u /* force adds by atomics: order-free, within 1e-6 relative
+                                          of the ordered result; default is ordered and bit-exact */
+#define HX_FLAG_NO_GRAPH 0x2u          /* launch the fused kernels directly, not through a CUDA graph */
+#define HX_FLAG_COUNTER_SIGNAL 0x4u    /* every chunk adds to the pulse's arrival counter (release)
+                                          instead of the last block storing an epoch flag */
+#define HX_FLAG_FINE_WAITS 0x8u        /* a dependent chunk waits only for the pulses that delivered
+                                          the slots it reads, not for every earlier pulse */
+
+#define HX_MAX_PULSES 32
+#define HX_MAX_DOMAINS 4096
+
+/* Pulse plan of a decomposition without touching a GPU: validates the
+ * arguments like hx_init and writes *n_pulses and, per global pulse p (Z
+ * pulses first, then Y, then X), pulse_dim[p] (0=x,1=y,2=z) and pulse_k[p]
+ * (index of the pulse within its dimension). pulse_dim/pulse_k are host
+ * arrays of at least HX_MAX_PULSES entries and may be NULL.
+ * Pages: "Dependency-aware packing" (global Z -> Y -> X numbering). */
+int hx_query_plan(const double box[3], const int dims[3], double cutoff,
+                  int* n_pulses, int32_t* pulse_dim, int32_t* pulse_k);
+
+/* Creates a handle on CUDA device `device`. box (host, nm), dims (host),
+ * cutoff (nm). timeout_us bounds every device-side wait for a pulse signal
+ * (0 selects 1 s); a wait that runs out sets HX_ERR_TIMEOUT, read by
+ * hx_status, and the kernel still finishes. Errors: HX_ERR_ARG,
+ * HX_ERR_PULSES, HX_ERR_CUDA (no usable device), HX_ERR_NOMEM. */
+int hx_init(hx_handle* out, const double box[3], const int dims[3], double cutoff,
+            int device, unsigned flags, unsigned timeout_us);
+
+/* Builds the decomposition on the GPU from pos_in (device, fp32 [n_atoms][3],
+ * any order): home cells, stable home partition, then pulse by pulse in the
+ * global order the cutoff selection with stable compaction into ascending
+ * maps, the receive offsets and the forwarded coordinates (the maps are the
+ * inputs of every kernel on the pages: packSendBufKernel's `map`, the fused
+ * kernel's `indexMap`). Writes *needed (host) = slots of the layout. If
+ * coords (device, float3 slots) is non-NULL and capacity >= *needed, it also
+ * writes every domain's home coordinates and fills every halo slot (one
+ * coordinate exchange). coords == NULL only sizes the layout (maps are kept);
+ * capacity < *needed returns HX_ERR_CAPACITY with the maps kept and coords
+ * untouched. Synchronises `stream` once per pulse to read sizes. Resets all
+ * pulse signals. Errors: HX_ERR_ARG, HX_ERR_RANGE, HX_ERR_CAPACITY,
+ * HX_ERR_CUDA, HX_ERR_NOMEM. */
+int hx_build_maps(hx_handle h, const float* pos_in, int64_t n_atoms,
+                  float* coords, int64_t capacity, int64_t* needed, void* stream);
+
+/* Sizes after a build (host outputs; any may be NULL). */
+int hx_get_counts(hx_handle h, int* n_domains, int* n_pulses, int64_t* total_slots,
+                  int64_t* total_entries);
+
+/* Per-domain layout (host arrays of n_domains entries; any may be NULL):
+ * first slot, home-atom count, halo-slot count. */
+int hx_get_layout(hx_handle h, int64_t* dom_offset, int32_t* home_count, int32_t* halo_count);
+
+/* home_ids (device, int32 [n_atoms]): for the k-th home slot in layout order
+ * (domain 0's home atoms, then domain 1's, ...) the input index of its atom. */
+int hx_get_home_ids(hx_handle h, int32_t* home_ids, void* stream);
+
+/* Copies the maps to host for inspection (synchronises). maps_host (host,
+ * int32, cap entries >= total_entries) receives every map, pulse-major then
+ * sender-minor; table_host (host, int64 [n_pulses][n_domains][6]) receives
+ * per (pulse, sender): map offset, size, receiving domain, receive offset in
+ * the receiver's array, shift flag (1 when the sender adds L_d), and the
+ * length of the independent prefix (entries whose local index is below the
+ * sender's home count, the pages' dependencyAtomOffset split). Either may be
+ * NULL. HX_ERR_CAPACITY if cap < total_entries. */
+int hx_get_maps(hx_handle h, int32_t* maps_host, int64_t cap, int64_t* table_host);
+
+/* Coordinate exchange, in place on coords (device, float3 slots of the
+ * layout): for every pulse Z -> Y -> X, coords[receiver slot i] =
+ * coords[sender slot map[i]] (+L_d when shifted). One persistent kernel for
+ * all pulses: independent entries are stored at once, the forwarded tail of
+ * a pulse waits (acquire, gpu scope) for the signals of earlier pulses, and
+ * each (sender, pulse) is signalled (release, gpu scope) when all its chunks
+ * are stored. Pages: packSendBufKernel, packHaloCoords, packSubset,
+ * fusedPulsesPackAndSendKernel, signalPeerOnLastBlock. */
+int hx_exchange_coords(hx_handle h, float* coords, void* stream);
+
+/* Force exchange, in place on forces (device, float3 slots of the layout):
+ * for every pulse X -> Y -> Z (reverse), forces[sender slot map[i]] +=
+ * forces[receiver slot i], fp32, x then y then z. One persistent kernel; a
+ * (sender, pulse) starts once every later pulse that touches its targets or
+ * its source slots has signalled, so each home force is the fp32 sum in
+ * reverse pulse order (bit-exact) unless HX_FLAG_UNORDERED_FORCES. Halo slots
+ * keep their values except where they forward accumulated forces. Pages:
+ * unpackRecvBufKernel<accumulate=true>; "Force halo exchange: Reversing the
+ * dependency chain". */
+int hx_exchange_forces(hx_handle h, float* forces, void* stream);
+
+/* Unfused baseline of the same two exchanges: one stream-ordered kernel
+ * launch per pulse (all senders of that pulse in one launch), no signals.
+ * Same results bit for bit as the fused calls in ordered mode. Pages: the
+ * per-pulse packSendBufKernel / unpackRecvBufKernel loop of the MPI
+ * baseline, with the host synchronisations replaced by stream order. */
+int hx_exchange_coords_unfused(hx_handle h, float* coords, void* stream);
+int hx_exchange_forces_unfused(hx_handle h, float* forces, void* stream);
+
+/* Launches one empty kernel the way the fused exchanges are launched (graph
+ * or direct, per the handle's flags): the launch floor for latency
+ * measurements. */
+int hx_noop(hx_handle h, void* stream);
+
+/* Synchronises `stream` and returns the sticky device status: HX_OK or
+ * HX_ERR_TIMEOUT (a wait for a pulse signal ran out). *detail (host, may be
+ * NULL) receives direction*65536 + item (item = pulse*n_domains + sender)
+ * of the first wait that gave up, or -1. */
+int hx_status(hx_handle h, void* stream, int* detail);
+
+/* Synchronises `stream`, clears the status and resets every pulse signal,
+ * counter and epoch so that the next exchange starts clean. */
+int hx_clear_status(hx_handle h, void* stream);
+
+/* Fault injection for tests (host side, no device fault): the chunks of
+ * (direction 0 = coordinates / 1 = forces, domain, pulse) stop signalling,
+ * so its waiters run into the timeout. domain = -1 switches it off. */
+int hx_debug_drop_signal(hx_handle h, int direction, int domain, int pulse);
+
+/* Human-readable name of an HX_* code (static string). */
+const char* hx_error_string(int code);
+
+/* Frees everything the handle owns (synchronises its device). NULL is a no-op. */
+void hx_destroy(hx_handle h);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HX_H */

@@ -1,0 +1,273 @@
+"""GPU parity of libhx against the CPU oracle, through the C ABI.
+
+Maps, layout, home order and coordinates must match bit for bit; forces bit
+for bit in ordered mode and within 1e-6 of the sum of absolute values of the
+reduced terms (the scale of each sum) in unordered mode.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+from domain_decomposition_halo_gb300 import hx as HX
+from domain_decomposition_halo_gb300 import workloads as W
+from oracle.oracle import Oracle
+
+pytestmark = pytest.mark.gpu
+
+ALL_MODES = [0, HX.HX_FLAG_COUNTER_SIGNAL, HX.HX_FLAG_NO_GRAPH,
+             HX.HX_FLAG_COUNTER_SIGNAL | HX.HX_FLAG_NO_GRAPH]
+
+
+def _bits(a):
+    return np.ascontiguousarray(a, np.float32).view(np.uint32)
+
+
+class Case:
+    """A workload built on both sides."""
+
+    def __init__(self, w, flags=0, timeout_us=0, pos=None):
+        self.w = w
+        self.pos = W.positions(w) if pos is None else pos
+        self.o = Oracle(w.box, w.dims, w.cutoff)
+        self.o.build(self.pos)
+        self.hx = HX.HaloExchange(w.box, w.dims, w.cutoff, flags=flags, timeout_us=timeout_us)
+        self.pos_t = torch.from_numpy(self.pos).cuda()
+        self.slots = self.hx.build_maps(self.pos_t)
+        self.coords = torch.full((max(self.slots, 1), 3), float("nan"), device="cuda")[: self.slots]
+        self.hx.build_maps(self.pos_t, self.coords)
+        torch.cuda.synchronize()
+
+    def home_mask(self):
+        m = np.zeros(self.o.total_slots, bool)
+        for r in range(self.o.n_domains):
+            m[self.o.dom_offset[r]: self.o.dom_offset[r] + self.o.home[r]] = True
+        return m
+
+
+def check_build(c: Case):
+    o = c.o
+    assert c.slots == o.total_slots
+    off, home, halo = c.hx.layout()
+    assert np.array_equal(off, o.dom_offset)
+    assert np.array_equal(home, o.home)
+    assert np.array_equal(halo, o.halo)
+    ids = c.hx.home_ids().cpu().numpy()
+    assert np.array_equal(ids, o.home_ids)
+    maps, table = c.hx.maps()
+    assert np.array_equal(maps, o.maps)
+    assert np.array_equal(table, o.table)
+    assert np.array_equal(_bits(c.coords.cpu().numpy()), _bits(o.coords()))
+
+
+def check_coord_steps(c: Case, steps=3, unfused=False):
+    o = c.o
+    rng = np.random.default_rng(123)
+    hm = c.home_mask()
+    x = o.coords().copy()
+    for s in range(steps):
+        # move home atoms a little (stays inside the box: exchanged values are
+        # compared, not re-partitioned), poison every halo slot
+        if s > 0 and hm.any():
+            x[hm] = (x[hm] * np.float32(0.999) + np.float32(1e-3) * rng.random((hm.sum(), 3), np.float32)).astype(np.float32)
+        x[~hm] = np.nan
+        xt = torch.from_numpy(x).cuda()
+        if unfused:
+            c.hx.exchange_coords_unfused(xt)
+        else:
+            c.hx.exchange_coords(xt)
+        o.exchange_coords(x)
+        assert np.array_equal(_bits(xt.cpu().numpy()), _bits(x)), f"coordinate step {s}"
+    rc, det = c.hx.status()
+    assert rc == 0, (rc, det)
+
+
+def check_force_steps(c: Case, steps=2, ordered=True, unfused=False):
+    o = c.o
+    for s in range(steps):
+        f = W.forces(c.w, o.total_slots)
+        if s:
+            f = (f * np.float32(1.0 + s)).astype(np.float32)
+        ft = torch.from_numpy(f).cuda()
+        if unfused:
+            c.hx.exchange_forces_unfused(ft)
+        else:
+            c.hx.exchange_forces(ft)
+        ref = f.copy()
+        o.exchange_forces(ref)
+        got = ft.cpu().numpy()
+        if ordered:
+            assert np.array_equal(_bits(got), _bits(ref)), f"force step {s}"
+        else:
+            scale = np.abs(f).copy()
+            o.exchange_forces(scale)
+            assert np.all(np.abs(got.astype(np.float64) - ref) <= 1e-6 * scale + 1e-30), f"force step {s}"
+    rc, det = c.hx.status()
+    assert rc == 0, (rc, det)
+
+
+@pytest.mark.parametrize("name", ["C1", "C2", "C3", "C4"])
+@pytest.mark.parametrize("flags", ALL_MODES)
+def test_parity_configs(name, flags):
+    c = Case(W.WORKLOADS[name], flags=flags)
+    check_build(c)
+    check_coord_steps(c)
+    check_force_steps(c)
+
+
+def test_parity_c5_full_size():
+    """12M atoms, 256 domains: the bench's configuration and launch path."""
+    c = Case(W.WORKLOADS["C5"])
+    check_build(c)
+    check_coord_steps(c, steps=2)
+    check_force_steps(c, steps=1)
+
+
+@pytest.mark.parametrize("name", ["C2", "C3", "C4"])
+def test_unordered_forces(name):
+    c = Case(W.WORKLOADS[name], flags=HX.HX_FLAG_UNORDERED_FORCES)
+    check_force_steps(c, steps=2, ordered=False)
+
+
+@pytest.mark.parametrize("name", ["C1", "C2", "C3", "C4"])
+def test_unfused_baseline(name):
+    c = Case(W.WORKLOADS[name])
+    check_coord_steps(c, steps=2, unfused=True)
+    check_force_steps(c, steps=1, unfused=True)
+
+
+@pytest.mark.parametrize("box,dims,cutoff,n", [
+    ((3.0, 3.0, 3.0), (1, 1, 1), 1.0, 500),       # no pulses: identity
+    ((2.0, 2.0, 2.0), (2, 2, 2), 0.5, 0),         # no atoms: every pulse empty, still signalled
+    ((2.0, 2.0, 2.0), (2, 2, 2), 0.5, 7),         # ragged, mostly empty pulses
+    ((5.0, 5.0, 3.0), (5, 5, 1), 1.5, 30000),     # 2 pulses in X and Y, forwarding chains
+    ((5.0, 5.0, 5.0), (5, 5, 5), 1.5, 40000),     # 6 pulses
+    ((6.0, 4.0, 5.0), (4, 1, 5), 1.3, 30000),     # mixed pulse counts
+    ((4.0, 4.5, 4.0), (1, 3, 1), 2.9, 20000),     # np = n - 1
+    ((3.0, 3.0, 3.0), (3, 3, 3), 0.6, 2700),      # 27 domains
+    ((40.0, 3.0, 3.0), (40, 1, 1), 1.0, 36000),   # many small domains along one dim
+])
+@pytest.mark.parametrize("flags", [0, HX.HX_FLAG_COUNTER_SIGNAL])
+def test_parity_shapes(box, dims, cutoff, n, flags):
+    w = W.custom("shape", n, box, dims, cutoff, seed=7 + n)
+    c = Case(w, flags=flags)
+    check_build(c)
+    check_coord_steps(c)
+    check_force_steps(c)
+
+
+def test_boundary_atoms():
+    below = float(np.nextafter(np.float32(4.0), np.float32(0)))
+    vals = [0.0, 1.0, 2.0, 3.0, below, float(np.nextafter(np.float32(1.0), np.float32(0))),
+            float(np.nextafter(np.float32(3.0), np.float32(0))), 0.5, 2.5, -0.0]
+    pts = np.array([[a, b, c] for a in vals for b in vals[:6] for c in vals[:4]], np.float32)
+    w = W.custom("edge", len(pts), (4.0, 4.0, 4.0), (2, 2, 2), 1.0, seed=0)
+    c = Case(w, pos=pts)
+    check_build(c)
+    check_coord_steps(c)
+
+
+def test_many_steps_reuse_signals():
+    """Epoch-valued signals are never reset between launches: 200 steps."""
+    for flags in (0, HX.HX_FLAG_COUNTER_SIGNAL):
+        c = Case(W.WORKLOADS["C2"], flags=flags)
+        x = c.o.coords().copy()
+        xt = torch.from_numpy(x).cuda()
+        f0 = W.forces(c.w, c.o.total_slots)
+        for _ in range(200):
+            c.hx.exchange_coords(xt)
+            ft = torch.from_numpy(f0).cuda()
+            c.hx.exchange_forces(ft)
+        ref = f0.copy()
+        c.o.exchange_forces(ref)
+        assert np.array_equal(_bits(ft.cpu().numpy()), _bits(ref))
+        assert np.array_equal(_bits(xt.cpu().numpy()), _bits(x))
+        assert c.hx.status()[0] == 0
+
+
+def test_side_stream():
+    c = Case(W.WORKLOADS["C2"])
+    s = torch.cuda.Stream()
+    x = c.o.coords().copy()
+    hm = c.home_mask()
+    x[~hm] = np.nan
+    with torch.cuda.stream(s):
+        xt = torch.from_numpy(x).cuda(non_blocking=False)
+        c.hx.exchange_coords(xt, stream=s)
+    s.synchronize()
+    c.o.exchange_coords(x)
+    assert np.array_equal(_bits(xt.cpu().numpy()), _bits(x))
+
+
+def test_rebuild_replaces_maps():
+    c = Case(W.WORKLOADS["C1"])
+    w2 = W.WORKLOADS["C2"]
+    hx = HX.HaloExchange(w2.box, w2.dims, w2.cutoff)
+    pos = torch.from_numpy(W.positions(w2)).cuda()
+    n1 = hx.build_maps(pos)
+    coords = torch.empty((n1, 3), device="cuda")
+    hx.build_maps(pos, coords)
+    pos2 = W.positions(W.custom("again", 20000, w2.box, w2.dims, w2.cutoff, seed=99))
+    o2 = Oracle(w2.box, w2.dims, w2.cutoff)
+    o2.build(pos2)
+    n2 = hx.build_maps(torch.from_numpy(pos2).cuda())
+    coords2 = torch.empty((n2, 3), device="cuda")
+    hx.build_maps(torch.from_numpy(pos2).cuda(), coords2)
+    assert np.array_equal(_bits(coords2.cpu().numpy()), _bits(o2.coords()))
+    del c
+
+
+def test_errors():
+    w = W.WORKLOADS["C1"]
+    hx = HX.HaloExchange(w.box, w.dims, w.cutoff)
+    x = torch.zeros((10, 3), device="cuda")
+    with pytest.raises(HX.HXError) as ei:
+        hx._check_tensor = lambda *a, **k: None       # reach the C ABI's own state check
+        hx.exchange_coords(x)
+    assert ei.value.code == HX.HX_ERR_STATE
+    hx = HX.HaloExchange(w.box, w.dims, w.cutoff)
+    bad = torch.from_numpy(np.array([[1.0, 1.0, 1.0], [3.2, 1.0, 1.0]], np.float32)).cuda()
+    with pytest.raises(HX.HXError) as ei:
+        hx.build_maps(bad)
+    assert ei.value.code == HX.HX_ERR_RANGE
+    nan = torch.from_numpy(np.array([[float("nan"), 1.0, 1.0]], np.float32)).cuda()
+    with pytest.raises(HX.HXError) as ei:
+        hx.build_maps(nan)
+    assert ei.value.code == HX.HX_ERR_RANGE
+    pos = torch.from_numpy(W.positions(w)).cuda()
+    n = hx.build_maps(pos)
+    small = torch.empty((n - 1, 3), device="cuda")
+    with pytest.raises(HX.HXError) as ei:
+        hx.build_maps(pos, small)
+    assert ei.value.code == HX.HX_ERR_CAPACITY
+    with pytest.raises(HX.HXError):
+        HX.HaloExchange(w.box, w.dims, w.cutoff, device=torch.cuda.device_count())
+
+
+@pytest.mark.parametrize("direction", [0, 1])
+@pytest.mark.parametrize("flags", [0, HX.HX_FLAG_COUNTER_SIGNAL])
+def test_dropped_signal_times_out_and_recovers(direction, flags):
+    """Failure detection without a device fault: a (domain, pulse) that never
+    signals makes its waiters give up after the bounded wait; the kernel
+    finishes, hx_status reports HX_ERR_TIMEOUT and the item, and after
+    hx_clear_status the exchange is correct again."""
+    c = Case(W.WORKLOADS["C2"], flags=flags, timeout_us=20000)
+    nd = c.o.n_domains
+    pulse = 0 if direction == 0 else c.o.n_pulses - 1
+    c.hx.debug_drop_signal(direction, 3, pulse)
+    x = c.o.coords().copy()
+    xt = torch.from_numpy(x).cuda()
+    f = W.forces(c.w, c.o.total_slots)
+    ft = torch.from_numpy(f).cuda()
+    if direction == 0:
+        c.hx.exchange_coords(xt)
+    else:
+        c.hx.exchange_forces(ft)
+    rc, detail = c.hx.status()
+    assert rc == HX.HX_ERR_TIMEOUT
+    assert detail == direction * 65536 + pulse * nd + 3
+    c.hx.debug_drop_signal(direction, -1)
+    c.hx.clear_status()
+    assert c.hx.status()[0] == 0
+    check_coord_steps(c, steps=2)
+    check_force_steps(c, steps=1)
