@@ -131,7 +131,6 @@ struct hx_ctx {
 
   int32_t* d_maps = nullptr;
   int32_t* d_home_ids = nullptr;
-  Item* d_items = nullptr;
   Chunk* d_chunks[2] = {nullptr, nullptr};   // fused coordinate / force chunk lists
   Wait* d_waits[2] = {nullptr, nullptr};
   Chunk* d_uchunks = nullptr;                // unfused per-pulse chunk list
@@ -155,7 +154,6 @@ void free_tables(hx_ctx* h) {
   drop_graphs(h);
   dev_free(h->d_maps);
   dev_free(h->d_home_ids);
-  dev_free(h->d_items);
   for (int k = 0; k < 2; ++k) {
     dev_free(h->d_chunks[k]);
     dev_free(h->d_waits[k]);
@@ -181,22 +179,22 @@ int to_err(cudaError_t e) {
 
 DirParams dir_params(hx_ctx* h, int dir) {
   DirParams P;
-  const int n_items = h->pl.n_pulses * h->pl.ndom;
-  P.items = h->d_items;
+  std::memset(&P, 0, sizeof(P));
+  const size_t n_items = static_cast<size_t>(std::max(h->pl.n_pulses * h->pl.ndom, 1));
   P.chunks = h->d_chunks[dir];
   P.waits = h->d_waits[dir];
   P.maps = h->d_maps;
-  P.flags = h->d_flags + static_cast<size_t>(dir) * n_items;
-  P.blk_count = h->d_blk + static_cast<size_t>(dir) * n_items;
+  P.flags = h->d_flags + dir * n_items;
+  P.arrivals = h->d_blk + dir * n_items;
   P.ctrl = h->d_ctrl + dir;
-  P.n_chunks = h->n_chunks[dir];
+  P.n_chunks = static_cast<unsigned long long>(h->n_chunks[dir]);
   P.direction = dir;
   P.timeout_ns = h->timeout_ns;
   return P;
 }
 
 const void* kernel_for(hx_ctx* h, int kind) {
-  const int mode = (h->flags & HX_FLAG_COUNTER_SIGNAL) ? kCounter : kLastBlock;
+  const int mode = (h->flags & HX_FLAG_COUNTER_SIGNAL) ? kCounter : kLastArrival;
   if (kind == 0) return coords_kernel(mode);
   if (kind == 1) return forces_kernel(mode, !(h->flags & HX_FLAG_UNORDERED_FORCES));
   return noop_kernel();
@@ -244,9 +242,9 @@ int launch(hx_ctx* h, int kind, float* buf, cudaStream_t s) {
 }
 
 int reset_signals(hx_ctx* h, cudaStream_t s) {
-  const size_t n_items = static_cast<size_t>(h->pl.n_pulses) * h->pl.ndom;
-  HX_CUDA(cudaMemsetAsync(h->d_flags, 0, sizeof(unsigned long long) * 2 * std::max<size_t>(n_items, 1), s));
-  HX_CUDA(cudaMemsetAsync(h->d_blk, 0, sizeof(unsigned int) * 2 * std::max<size_t>(n_items, 1), s));
+  const size_t n_items = static_cast<size_t>(std::max(h->pl.n_pulses * h->pl.ndom, 1));
+  HX_CUDA(cudaMemsetAsync(h->d_flags, 0, sizeof(unsigned long long) * 2 * n_items, s));
+  HX_CUDA(cudaMemsetAsync(h->d_blk, 0, sizeof(unsigned int) * 2 * n_items, s));
   Ctrl c[2];
   std::memset(c, 0, sizeof(c));
   c[0].drop_item = c[1].drop_item = -1;
@@ -255,10 +253,78 @@ int reset_signals(hx_ctx* h, cudaStream_t s) {
   return HX_OK;
 }
 
-int64_t chunk_entries(int64_t total_entries) {
-  // Large exchanges: two block passes per chunk; small ones: one, so that the
-  // chain of dependent pulses is spread over as many blocks as possible.
-  return total_entries > (int64_t{4} << 20) ? 2 * kPass : kPass;
+// ---------------------------------------------------------------- work tables
+//
+// A "part" is a run of entries of one item that is listed as a unit: the
+// independent prefix and the forwarded tail of a coordinate item, or a whole
+// force item. Parts are emitted in a topological order of their waits
+// (Kahn's algorithm) that prefers the lowest (domain, pulse) key, so the
+// chunks of one domain's pulses sit close together in the list and run
+// close together in time: the domain's slots are fetched into L2 once per
+// launch instead of once per pulse.
+
+struct Part {
+  int item;
+  int begin, end;       // entry range within the item's map
+  int halo_src;
+  long long key;        // emission priority (smaller first)
+  std::vector<int> deps;          // items that must be complete before this part
+  std::vector<std::vector<int>> chunk_waits;  // per chunk (fine waits) or one shared list
+};
+
+struct ItemInfo {
+  int r, p, q;           // sender, pulse, receiver
+  int64_t src, dst, map; // slot of sender base, slot of receive-range start, first map entry
+  int size, split, dim, shift_flag;
+};
+
+// Sorted-array helpers for the fine waits.
+bool any_in_range(const int32_t* a, int n, int64_t lo, int64_t hi) {   // any a[i] in [lo, hi)
+  const int32_t* it = std::lower_bound(a, a + n, static_cast<int32_t>(std::min<int64_t>(lo, INT32_MAX)));
+  return it != a + n && *it < hi;
+}
+
+bool sorted_intersect(const int32_t* a, int na, const int32_t* b, int nb) {
+  int i = 0, k = 0;
+  while (i < na && k < nb) {
+    if (a[i] == b[k]) return true;
+    if (a[i] < b[k]) ++i;
+    else ++k;
+  }
+  return false;
+}
+
+// Emits parts in a locality-preferring topological order; returns the order.
+std::vector<int> order_parts(const std::vector<Part>& parts, int n_items, std::vector<int>* item_parts_left) {
+  std::vector<std::vector<int>> waiters(n_items);
+  std::vector<int> unmet(parts.size(), 0);
+  for (size_t i = 0; i < parts.size(); ++i) {
+    unmet[i] = static_cast<int>(parts[i].deps.size());
+    for (int it : parts[i].deps) waiters[it].push_back(static_cast<int>(i));
+  }
+  auto cmp = [&](int a, int b) { return parts[a].key > parts[b].key; };
+  std::vector<int> heap;
+  for (size_t i = 0; i < parts.size(); ++i)
+    if (unmet[i] == 0) heap.push_back(static_cast<int>(i));
+  std::make_heap(heap.begin(), heap.end(), cmp);
+  std::vector<int> order;
+  order.reserve(parts.size());
+  while (!heap.empty()) {
+    std::pop_heap(heap.begin(), heap.end(), cmp);
+    const int i = heap.back();
+    heap.pop_back();
+    order.push_back(i);
+    const int it = parts[i].item;
+    if (--(*item_parts_left)[it] == 0) {
+      for (int w : waiters[it]) {
+        if (--unmet[w] == 0) {
+          heap.push_back(w);
+          std::push_heap(heap.begin(), heap.end(), cmp);
+        }
+      }
+    }
+  }
+  return order;   // shorter than parts only if the waits had a cycle (they cannot)
 }
 
 // Work tables of the fused and unfused kernels from the host copy of the plan.
@@ -266,109 +332,218 @@ int build_tables(hx_ctx* h, cudaStream_t s) {
   const Plan& pl = h->pl;
   const int P = pl.n_pulses, nd = pl.ndom;
   const int n_items = P * nd;
-  const int64_t CH = chunk_entries(h->total_entries);
-  std::vector<Item> items(std::max(n_items, 1));
-  std::vector<Chunk> cch, fch, uch;
-  std::vector<Wait> cw, fw;
-  for (int p = 0; p < P; ++p) {
+  const bool fine = (h->flags & HX_FLAG_FINE_WAITS) != 0;
+  const bool ordered = !(h->flags & HX_FLAG_UNORDERED_FORCES);
+  std::vector<ItemInfo> items(std::max(n_items, 1));
+  for (int p = 0; p < P; ++p)
     for (int r = 0; r < nd; ++r) {
       const int t = p * nd + r;
-      Item& it = items[t];
-      std::memset(&it, 0, sizeof(it));
-      it.src_base = h->dom_offset[r];
-      it.dst_base = h->dom_offset[h->t_recv[t]] + h->t_off[t];
-      it.map_off = h->t_map_off[t];
+      ItemInfo& it = items[t];
+      it.r = r;
+      it.p = p;
+      it.q = h->t_recv[t];
+      it.src = h->dom_offset[r];
+      it.dst = h->dom_offset[it.q] + h->t_off[t];
+      it.map = h->t_map_off[t];
       it.size = h->t_size[t];
       it.split = h->t_split[t];
       it.dim = pl.pulse_dim[p];
-      it.do_shift = h->t_shift[t];
-      it.shift = pl.boxf[it.dim];
+      it.shift_flag = h->t_shift[t];
     }
+  std::vector<int32_t> maps;
+  if (fine && h->total_entries > 0) {
+    maps.resize(h->total_entries);
+    HX_CUDA(cudaMemcpy(maps.data(), h->d_maps, sizeof(int32_t) * h->total_entries, cudaMemcpyDeviceToHost));
   }
-  auto add_chunks = [&](std::vector<Chunk>& out, int t, int begin, int end, int halo_src, int woff, int wcnt,
-                        bool always_one) {
-    int made = 0;
-    for (int64_t b = begin; b < end; b += CH) {
-      out.push_back({t, static_cast<int32_t>(b), static_cast<int32_t>(std::min<int64_t>(end, b + CH)), woff, wcnt,
-                     halo_src});
-      ++made;
+  // upper_q(r): the domain that sends into r in pulse q
+  auto upper = [&](int r, int q) { return neighbour(pl, r, pl.pulse_dim[q], +1); };
+
+  for (int dir = 0; dir < 2; ++dir) {
+    std::vector<Part> parts;
+    auto chunks_of = [](int begin, int end) { return std::max(1, (end - begin + kChunk - 1) / kChunk); };
+    if (dir == 0) {
+      for (int p = 0; p < P; ++p)
+        for (int r = 0; r < nd; ++r) {
+          const int t = p * nd + r;
+          const ItemInfo& it = items[t];
+          if (it.split > 0 || it.size == 0) {
+            Part a;
+            a.item = t;
+            a.begin = 0;
+            a.end = it.split;
+            a.halo_src = 0;
+            a.key = (static_cast<long long>(r) * P + p) * 2;
+            parts.push_back(std::move(a));
+          }
+          if (it.split < it.size) {
+            Part b;
+            b.item = t;
+            b.begin = it.split;
+            b.end = it.size;
+            b.halo_src = 1;
+            b.key = (static_cast<long long>(r) * P + p) * 2 + 1;
+            // forwarded entries read r's receive ranges of pulses q < p
+            const int nch = chunks_of(b.begin, b.end);
+            std::vector<int> all;
+            for (int q = 0; q < p; ++q) all.push_back(q * nd + upper(r, q));
+            for (int c = 0; c < nch; ++c) {
+              const int cb = b.begin + c * kChunk, ce = std::min(b.end, cb + kChunk);
+              if (!fine) {
+                b.chunk_waits.push_back(all);
+                continue;
+              }
+              std::vector<int> w;
+              const int32_t* m = maps.data() + it.map + cb;
+              for (int q = 0; q < p; ++q) {
+                const int64_t lo = h->t_off[q * nd + upper(r, q)];
+                const int64_t hi = lo + h->t_size[q * nd + upper(r, q)];
+                if (any_in_range(m, ce - cb, lo, hi)) w.push_back(q * nd + upper(r, q));
+              }
+              b.chunk_waits.push_back(w);
+            }
+            parts.push_back(std::move(b));
+          }
+        }
+    } else {
+      for (int p = P - 1; p >= 0; --p)
+        for (int r = 0; r < nd; ++r) {
+          const int t = p * nd + r;
+          const ItemInfo& it = items[t];
+          Part a;
+          a.item = t;
+          a.begin = 0;
+          a.end = it.size;
+          a.halo_src = 1;
+          a.key = static_cast<long long>(r) * P + (P - 1 - p);
+          const int nch = chunks_of(a.begin, a.end);
+          std::vector<int> all;
+          for (int pp = p + 1; pp < P; ++pp) {
+            all.push_back(pp * nd + it.q);                       // writes of the slots read here
+            if (ordered && it.q != r) all.push_back(pp * nd + r); // earlier adds into the same targets
+          }
+          for (int c = 0; c < nch; ++c) {
+            const int cb = c * kChunk, ce = std::min(it.size, cb + kChunk);
+            if (!fine) {
+              a.chunk_waits.push_back(all);
+              continue;
+            }
+            std::vector<int> w;
+            const int64_t slot_lo = h->t_off[t] + cb, slot_hi = h->t_off[t] + ce;
+            for (int pp = p + 1; pp < P; ++pp) {
+              const int tq = pp * nd + it.q, tr = pp * nd + r;
+              // q forwards some of the slots this chunk reads in pulse pp
+              const bool need_q = any_in_range(maps.data() + items[tq].map, items[tq].size, slot_lo, slot_hi);
+              // r adds into some of this chunk's targets in pulse pp
+              const bool need_r = ordered && sorted_intersect(maps.data() + items[tr].map, items[tr].size,
+                                                              maps.data() + it.map + cb, ce - cb);
+              if (tq == tr) {
+                if (need_q || need_r) w.push_back(tq);
+              } else {
+                if (need_q) w.push_back(tq);
+                if (need_r) w.push_back(tr);
+              }
+            }
+            a.chunk_waits.push_back(w);
+          }
+          parts.push_back(std::move(a));
+        }
     }
-    if (made == 0 && always_one) {
-      out.push_back({t, begin, begin, woff, wcnt, halo_src});
-      ++made;
+    // deps per part; which items anybody waits for; drop unneeded empty parts
+    std::vector<char> waited(std::max(n_items, 1), 0);
+    for (auto& pt : parts) {
+      std::vector<int> d;
+      for (auto& w : pt.chunk_waits) d.insert(d.end(), w.begin(), w.end());
+      std::sort(d.begin(), d.end());
+      d.erase(std::unique(d.begin(), d.end()), d.end());
+      pt.deps = d;
+      for (int it : d) waited[it] = 1;
     }
-    return made;
-  };
-  // Coordinates: all independent parts (pulse order), then the dependent
-  // tails (pulse order). A dependent tail of (r, p) waits for the pulses
-  // p' < p into r, i.e. for items (upper_{p'}(r), p').
-  for (int p = 0; p < P; ++p)
-    for (int r = 0; r < nd; ++r) {
-      const int t = p * nd + r;
-      items[t].coord_chunks = add_chunks(cch, t, 0, items[t].split, 0, 0, 0, items[t].size == 0);
+    std::vector<Part> kept;
+    for (auto& pt : parts)
+      if (pt.end > pt.begin || waited[pt.item]) kept.push_back(std::move(pt));
+    parts.swap(kept);
+    std::vector<int> item_chunks(std::max(n_items, 1), 0), parts_left(std::max(n_items, 1), 0);
+    for (auto& pt : parts) {
+      item_chunks[pt.item] += chunks_of(pt.begin, pt.end);
+      parts_left[pt.item] += 1;
     }
-  for (int p = 0; p < P; ++p)
-    for (int r = 0; r < nd; ++r) {
-      const int t = p * nd + r;
-      if (items[t].split >= items[t].size) continue;
-      const int woff = static_cast<int>(cw.size());
-      for (int q = 0; q < p; ++q) cw.push_back({q * nd + neighbour(pl, r, pl.pulse_dim[q], +1), 0});
-      const int wcnt = static_cast<int>(cw.size()) - woff;
-      items[t].coord_chunks += add_chunks(cch, t, items[t].split, items[t].size, 1, woff, wcnt, false);
-    }
-  for (auto& w : cw) w.chunks = items[w.item].coord_chunks;
-  // Forces: pulses last to first. (r, p) waits for (r, p') and for its
-  // receiver's (q, p'), p' > p; unordered mode keeps only the receiver's.
-  const bool ordered = !(h->flags & HX_FLAG_UNORDERED_FORCES);
-  for (int p = P - 1; p >= 0; --p)
-    for (int r = 0; r < nd; ++r) {
-      const int t = p * nd + r;
-      const int q = h->t_recv[t];
-      const int woff = static_cast<int>(fw.size());
-      for (int pp = p + 1; pp < P; ++pp) {
-        fw.push_back({pp * nd + q, 0});
-        if (ordered && r != q) fw.push_back({pp * nd + r, 0});
+    std::vector<int> order = order_parts(parts, std::max(n_items, 1), &parts_left);
+    if (order.size() != parts.size()) return HX_ERR_STATE;
+    std::vector<Chunk> chunks;
+    std::vector<Wait> waits;
+    for (int pi : order) {
+      const Part& pt = parts[pi];
+      const ItemInfo& it = items[pt.item];
+      const int nch = chunks_of(pt.begin, pt.end);
+      for (int c = 0; c < nch; ++c) {
+        const int cb = pt.begin + c * kChunk, ce = std::min(pt.end, cb + kChunk);
+        Chunk ch;
+        std::memset(&ch, 0, sizeof(ch));
+        ch.src = it.src;
+        ch.dst = it.dst + cb;
+        ch.map = it.map + cb;
+        ch.n = ce - cb;
+        ch.item = pt.item;
+        ch.item_chunks = item_chunks[pt.item];
+        const std::vector<int>& w = pt.chunk_waits.empty() ? std::vector<int>() : pt.chunk_waits[c];
+        ch.wait_off = static_cast<int32_t>(waits.size());
+        ch.wait_cnt = static_cast<int32_t>(w.size());
+        for (int x : w) waits.push_back({x, 0});
+        ch.flags = (pt.halo_src ? kHaloSrc : 0) | (waited[pt.item] ? kSignal : 0) |
+                   (dir == 0 && it.shift_flag ? kShift : 0);
+        ch.dim = it.dim;
+        ch.shift = pl.boxf[it.dim];
+        chunks.push_back(ch);
       }
-      const int wcnt = static_cast<int>(fw.size()) - woff;
-      items[t].force_chunks = add_chunks(fch, t, 0, items[t].size, 1, woff, wcnt, true);
     }
-  for (auto& w : fw) w.chunks = items[w.item].force_chunks;
-  // Unfused: per pulse, every item's entries, no waits.
+    for (auto& w : waits) w.chunks = item_chunks[w.item];
+    h->n_chunks[dir] = static_cast<int>(chunks.size());
+    HX_CUDA(dev_alloc(&h->d_chunks[dir], chunks.size()));
+    HX_CUDA(dev_alloc(&h->d_waits[dir], waits.size()));
+    if (!chunks.empty())
+      HX_CUDA(cudaMemcpy(h->d_chunks[dir], chunks.data(), sizeof(Chunk) * chunks.size(), cudaMemcpyHostToDevice));
+    if (!waits.empty())
+      HX_CUDA(cudaMemcpy(h->d_waits[dir], waits.data(), sizeof(Wait) * waits.size(), cudaMemcpyHostToDevice));
+  }
+
+  // Unfused: per pulse, every item's entries in sender order, no waits or signals.
+  std::vector<Chunk> uch;
   h->u_begin.assign(P + 1, 0);
   for (int p = 0; p < P; ++p) {
     h->u_begin[p] = static_cast<int>(uch.size());
-    for (int r = 0; r < nd; ++r) add_chunks(uch, p * nd + r, 0, h->t_size[p * nd + r], 1, 0, 0, false);
+    for (int r = 0; r < nd; ++r) {
+      const ItemInfo& it = items[p * nd + r];
+      for (int cb = 0; cb < it.size; cb += kChunk) {
+        Chunk ch;
+        std::memset(&ch, 0, sizeof(ch));
+        ch.src = it.src;
+        ch.dst = it.dst + cb;
+        ch.map = it.map + cb;
+        ch.n = std::min(it.size - cb, kChunk);
+        ch.item = p * nd + r;
+        ch.flags = kHaloSrc | (it.shift_flag ? kShift : 0);
+        ch.dim = it.dim;
+        ch.shift = pl.boxf[it.dim];
+        uch.push_back(ch);
+      }
+    }
   }
   h->u_begin[P] = static_cast<int>(uch.size());
-
-  h->n_chunks[0] = static_cast<int>(cch.size());
-  h->n_chunks[1] = static_cast<int>(fch.size());
-  HX_CUDA(dev_alloc(&h->d_items, items.size()));
-  HX_CUDA(dev_alloc(&h->d_chunks[0], cch.size()));
-  HX_CUDA(dev_alloc(&h->d_chunks[1], fch.size()));
-  HX_CUDA(dev_alloc(&h->d_waits[0], cw.size()));
-  HX_CUDA(dev_alloc(&h->d_waits[1], fw.size()));
   HX_CUDA(dev_alloc(&h->d_uchunks, uch.size()));
-  HX_CUDA(dev_alloc(&h->d_flags, 2 * static_cast<size_t>(std::max(n_items, 1))));
-  HX_CUDA(dev_alloc(&h->d_blk, 2 * static_cast<size_t>(std::max(n_items, 1))));
-  HX_CUDA(dev_alloc(&h->d_ctrl, 2));
-  HX_CUDA(cudaMemcpyAsync(h->d_items, items.data(), sizeof(Item) * items.size(), cudaMemcpyHostToDevice, s));
-  if (!cch.empty())
-    HX_CUDA(cudaMemcpyAsync(h->d_chunks[0], cch.data(), sizeof(Chunk) * cch.size(), cudaMemcpyHostToDevice, s));
-  if (!fch.empty())
-    HX_CUDA(cudaMemcpyAsync(h->d_chunks[1], fch.data(), sizeof(Chunk) * fch.size(), cudaMemcpyHostToDevice, s));
-  if (!cw.empty())
-    HX_CUDA(cudaMemcpyAsync(h->d_waits[0], cw.data(), sizeof(Wait) * cw.size(), cudaMemcpyHostToDevice, s));
-  if (!fw.empty())
-    HX_CUDA(cudaMemcpyAsync(h->d_waits[1], fw.data(), sizeof(Wait) * fw.size(), cudaMemcpyHostToDevice, s));
   if (!uch.empty())
-    HX_CUDA(cudaMemcpyAsync(h->d_uchunks, uch.data(), sizeof(Chunk) * uch.size(), cudaMemcpyHostToDevice, s));
-  // Persistent grid: every block co-resident.
+    HX_CUDA(cudaMemcpy(h->d_uchunks, uch.data(), sizeof(Chunk) * uch.size(), cudaMemcpyHostToDevice));
+
+  const size_t n_flags = 2 * static_cast<size_t>(std::max(n_items, 1));
+  HX_CUDA(dev_alloc(&h->d_flags, n_flags));
+  HX_CUDA(dev_alloc(&h->d_blk, n_flags));
+  HX_CUDA(dev_alloc(&h->d_ctrl, 2));
+  // Persistent grid: every warp co-resident, one warp per chunk at most.
   for (int k = 0; k < 2; ++k) {
     const int per_sm = std::max(1, max_blocks_per_sm(kernel_for(h, k)));
-    h->grid[k] = std::max(1, std::min(h->n_chunks[k], per_sm * h->sm_count));
+    const int warps = std::max(1, std::min(h->n_chunks[k], per_sm * h->sm_count * kWarps));
+    h->grid[k] = (warps + kWarps - 1) / kWarps;
   }
-  return reset_signals(h, s);   // synchronises: the host vectors above may go
+  return reset_signals(h, s);
 }
 
 struct BuildScratch {
@@ -674,7 +849,7 @@ int exchange(hx_handle h, float* buf, void* stream, int kind) {
   if (!h) return HX_ERR_ARG;
   if (!h->built) return HX_ERR_STATE;
   if (!buf && h->total_slots > 0) return HX_ERR_ARG;   // an empty layout touches no memory
-  if (h->pl.n_pulses == 0) return HX_OK;
+  if (h->pl.n_pulses == 0 || h->n_chunks[kind] == 0) return HX_OK;   // nothing moves
   const int rc = ensure_device(h);
   if (rc != HX_OK) return rc;
   return launch(h, kind, buf, static_cast<cudaStream_t>(stream));
@@ -694,8 +869,8 @@ int hx_exchange_coords_unfused(hx_handle h, float* coords, void* stream) {
   if (rc != HX_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   for (int p = 0; p < h->pl.n_pulses; ++p) {
-    PulseParams pp{h->d_items, h->d_uchunks, h->d_maps, h->u_begin[p]};
-    rc = to_err(launch_pack_pulse(coords, pp, h->u_begin[p + 1] - h->u_begin[p], s));
+    PulseParams pp{h->d_uchunks, h->d_maps, h->u_begin[p], h->u_begin[p + 1] - h->u_begin[p]};
+    rc = to_err(launch_pack_pulse(coords, pp, s));
     if (rc != HX_OK) return rc;
   }
   return HX_OK;
@@ -709,8 +884,8 @@ int hx_exchange_forces_unfused(hx_handle h, float* forces, void* stream) {
   if (rc != HX_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   for (int p = h->pl.n_pulses - 1; p >= 0; --p) {
-    PulseParams pp{h->d_items, h->d_uchunks, h->d_maps, h->u_begin[p]};
-    rc = to_err(launch_unpack_pulse(forces, pp, h->u_begin[p + 1] - h->u_begin[p], s));
+    PulseParams pp{h->d_uchunks, h->d_maps, h->u_begin[p], h->u_begin[p + 1] - h->u_begin[p]};
+    rc = to_err(launch_unpack_pulse(forces, pp, s));
     if (rc != HX_OK) return rc;
   }
   return HX_OK;

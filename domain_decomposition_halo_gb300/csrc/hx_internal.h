@@ -6,85 +6,84 @@
 
 namespace hx {
 
-constexpr int kThreads = 256;          // threads per block of every exchange kernel
-constexpr int kUnroll = 4;             // entries in flight per thread
-constexpr int kPass = kThreads * kUnroll;  // entries per block pass (1024)
+constexpr int kThreads = 256;                 // threads per block of the exchange kernels
+constexpr int kWarps = kThreads / 32;         // independent warps per block
+constexpr int kRounds = 8;                    // 32-entry rounds per warp chunk
+constexpr int kChunk = 32 * kRounds;          // map entries per warp chunk (256)
 
-// One (sender, pulse) unit: pulse p of sender r sends S entries to its lower
-// neighbour q along dim(p). Index t = p * n_domains + r.
-struct Item {
-  int64_t src_base;   // first slot of the sender's array (dom_offset[r])
-  int64_t dst_base;   // first slot of the receive range in q (dom_offset[q] + off)
-  int64_t map_off;    // first entry of this map in the maps array
-  int32_t size;       // S
-  int32_t split;      // entries [0, split) read home slots (independent)
-  int32_t dim;        // 0, 1, 2
-  int32_t do_shift;   // 1 when the sender sits in cell 0 along dim
-  float shift;        // (float)L_dim
-  int32_t coord_chunks;  // chunks of the coordinate exchange for this item
-  int32_t force_chunks;  // chunks of the force exchange for this item
-  int32_t pad;
+// One warp's unit of work: up to kChunk consecutive entries of one
+// (sender, pulse) map. Everything the warp needs is in this 64-byte record,
+// so a chunk costs one descriptor load.
+enum ChunkFlags : int32_t {
+  kHaloSrc = 1,      // entries read slots written earlier in the same launch
+  kSignal = 2,       // some later chunk waits for this chunk's item
+  kShift = 4,        // add `shift` to component `dim` (coordinates only)
 };
 
-// A contiguous range of map entries of one item, claimed by one block.
-struct Chunk {
-  int32_t item;
-  int32_t begin;
-  int32_t end;
-  int32_t wait_off;   // waits in the direction's wait list before the body
+struct alignas(16) Chunk {
+  int64_t src;        // first slot of the sender's array (gather source / force targets)
+  int64_t dst;        // receiver-side slot of this chunk's first entry
+  int64_t map;        // index of this chunk's first entry in the maps array
+  int32_t n;          // entries (0..kChunk; 0 only for a pure signal)
+  int32_t item;       // pulse * n_domains + sender
+  int32_t item_chunks;  // chunks that make up the item (signal arithmetic)
+  int32_t wait_off;   // this chunk's waits in the direction's wait list
   int32_t wait_cnt;
-  int32_t halo_src;   // 1 when the entries read slots written during the launch
+  int32_t flags;      // ChunkFlags
+  int32_t dim;        // component the shift applies to
+  float shift;        // (float)L_dim
 };
+static_assert(sizeof(Chunk) == 64, "chunk descriptor must stay one 64-byte record");
 
-// Wait for item `item` of the same direction to have signalled this epoch;
-// `chunks` = how many chunk signals complete it (counter mode).
+// Wait for `item` of the same direction to have been signalled by all of its
+// `chunks` in the current launch.
 struct Wait {
   int32_t item;
   int32_t chunks;
 };
 
-// Per-direction control block (device memory, zeroed at build time).
+// Per-direction control block (device memory; zeroed at build and by
+// hx_clear_status, never reset between launches).
 struct Ctrl {
-  unsigned int ticket;        // next chunk to hand out (minus gridDim.x)
-  unsigned int exit_count;    // blocks that finished this launch (wraps)
-  unsigned long long epoch;   // launches completed
+  unsigned long long ticket;  // chunk tickets handed out since the last reset; a
+                              // launch takes exactly n_chunks, so ticket / n_chunks
+                              // numbers the launch (its epoch is that + 1)
   int status;                 // 0 or an HX_ERR_* code (sticky)
   int detail;                 // item of the first wait that gave up
   int drop_item;              // debug: item whose signals are dropped, or -1
-  int pad;
+  int pad[3];
 };
 
 struct DirParams {
-  const Item* items;
   const Chunk* chunks;
   const Wait* waits;
   const int32_t* maps;
-  unsigned long long* flags;  // per item: epoch flag or arrival counter
-  unsigned int* blk_count;    // per item: last-block election counters
+  unsigned long long* flags;  // per item: epoch flag (last-arrival mode) or arrival counter
+  unsigned int* arrivals;     // per item: last-arrival election counters
   Ctrl* ctrl;
-  int n_chunks;
+  unsigned long long n_chunks;
   int direction;              // 0 coordinates, 1 forces
+  int pad;
   unsigned long long timeout_ns;
 };
 
-// Unfused baseline: one launch per pulse over that pulse's chunk range.
+// Unfused baseline: one launch per pulse over that pulse's chunks.
 struct PulseParams {
-  const Item* items;
   const Chunk* chunks;
   const int32_t* maps;
   int chunk_begin;
+  int n_chunks;
 };
 
-// ---- launch wrappers (hx_kernels.cu) ----
-enum SignalMode { kLastBlock = 0, kCounter = 1 };
+enum SignalMode { kLastArrival = 0, kCounter = 1 };
 
+// ---- exchange kernels (hx_kernels.cu) ----
 const void* coords_kernel(int signal_mode);
 const void* forces_kernel(int signal_mode, bool ordered);
 const void* noop_kernel();
 int max_blocks_per_sm(const void* fn);
-
-cudaError_t launch_pack_pulse(float* x, const PulseParams& p, int n_chunks, cudaStream_t s);
-cudaError_t launch_unpack_pulse(float* f, const PulseParams& p, int n_chunks, cudaStream_t s);
+cudaError_t launch_pack_pulse(float* x, const PulseParams& p, cudaStream_t s);
+cudaError_t launch_unpack_pulse(float* f, const PulseParams& p, cudaStream_t s);
 
 // ---- map builder (hx_build.cu) ----
 struct BuildTile {          // candidates [local_begin, local_begin + n) of one sender

@@ -16,7 +16,8 @@ from oracle.oracle import Oracle
 pytestmark = pytest.mark.gpu
 
 ALL_MODES = [0, HX.HX_FLAG_COUNTER_SIGNAL, HX.HX_FLAG_NO_GRAPH,
-             HX.HX_FLAG_COUNTER_SIGNAL | HX.HX_FLAG_NO_GRAPH]
+             HX.HX_FLAG_COUNTER_SIGNAL | HX.HX_FLAG_NO_GRAPH, HX.HX_FLAG_FINE_WAITS,
+             HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_COUNTER_SIGNAL]
 
 
 def _bits(a):
@@ -115,17 +116,19 @@ def test_parity_configs(name, flags):
     check_force_steps(c)
 
 
-def test_parity_c5_full_size():
+@pytest.mark.parametrize("flags", [0, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_COUNTER_SIGNAL])
+def test_parity_c5_full_size(flags):
     """12M atoms, 256 domains: the bench's configuration and launch path."""
-    c = Case(W.WORKLOADS["C5"])
+    c = Case(W.WORKLOADS["C5"], flags=flags)
     check_build(c)
     check_coord_steps(c, steps=2)
     check_force_steps(c, steps=1)
 
 
 @pytest.mark.parametrize("name", ["C2", "C3", "C4"])
-def test_unordered_forces(name):
-    c = Case(W.WORKLOADS[name], flags=HX.HX_FLAG_UNORDERED_FORCES)
+@pytest.mark.parametrize("extra", [0, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_COUNTER_SIGNAL])
+def test_unordered_forces(name, extra):
+    c = Case(W.WORKLOADS[name], flags=HX.HX_FLAG_UNORDERED_FORCES | extra)
     check_force_steps(c, steps=2, ordered=False)
 
 
@@ -147,7 +150,7 @@ def test_unfused_baseline(name):
     ((3.0, 3.0, 3.0), (3, 3, 3), 0.6, 2700),      # 27 domains
     ((40.0, 3.0, 3.0), (40, 1, 1), 1.0, 36000),   # many small domains along one dim
 ])
-@pytest.mark.parametrize("flags", [0, HX.HX_FLAG_COUNTER_SIGNAL])
+@pytest.mark.parametrize("flags", [0, HX.HX_FLAG_COUNTER_SIGNAL, HX.HX_FLAG_FINE_WAITS])
 def test_parity_shapes(box, dims, cutoff, n, flags):
     w = W.custom("shape", n, box, dims, cutoff, seed=7 + n)
     c = Case(w, flags=flags)
@@ -245,7 +248,7 @@ def test_errors():
 
 
 @pytest.mark.parametrize("direction", [0, 1])
-@pytest.mark.parametrize("flags", [0, HX.HX_FLAG_COUNTER_SIGNAL])
+@pytest.mark.parametrize("flags", [0, HX.HX_FLAG_COUNTER_SIGNAL, HX.HX_FLAG_FINE_WAITS])
 def test_dropped_signal_times_out_and_recovers(direction, flags):
     """Failure detection without a device fault: a (domain, pulse) that never
     signals makes its waiters give up after the bounded wait; the kernel
