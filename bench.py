@@ -48,7 +48,19 @@ def parse_args():
     ap.add_argument("--workload", default="C5", choices=sorted(W.WORKLOADS))
     ap.add_argument("--no-extras", action="store_true", help="skip the secondary measurements")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU baseline budget")
+    ap.add_argument("--flags", default="fine",
+                    help="comma list of libhx modes: fine, counter, nograph, unordered, pages (= none)")
     return ap.parse_args()
+
+
+def hx_flags(spec: str) -> int:
+    from domain_decomposition_halo_gb300 import hx as HX
+    table = {"fine": HX.HX_FLAG_FINE_WAITS, "counter": HX.HX_FLAG_COUNTER_SIGNAL, "nograph": HX.HX_FLAG_NO_GRAPH,
+             "unordered": HX.HX_FLAG_UNORDERED_FORCES, "pages": 0, "": 0}
+    flags = 0
+    for name in spec.split(","):
+        flags |= table[name.strip()]
+    return flags
 
 
 def dist_env():
@@ -56,6 +68,18 @@ def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return world, rank, local
+
+
+def max_over_ranks(value: float, device=None) -> float:
+    """The job's time is the slowest rank's: all-reduce(MAX) of one scalar
+    (not on the data path; replicas exchange nothing else)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
 
 
 def workload_label(w):
@@ -172,7 +196,8 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=dev)
     w = W.WORKLOADS[args.workload]
     pos = W.positions(w)
-    hx = HaloExchange(w.box, w.dims, w.cutoff, device=local)
+    flags = hx_flags(args.flags)
+    hx = HaloExchange(w.box, w.dims, w.cutoff, device=local, flags=flags)
     pos_t = torch.from_numpy(pos).to(dev)
     slots = hx.build_maps(pos_t)
     coords = torch.empty((slots, 3), device=dev)
@@ -213,9 +238,7 @@ def run_ours(args):
     coord_ms = statistics.fmean(e[0].elapsed_time(e[1]) for e in ev)
     force_ms = statistics.fmean(e[1].elapsed_time(e[2]) for e in ev)
     if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+        total_ms = max_over_ranks(total_ms, dev)
         torch.distributed.barrier()
     rc, detail = hx.status()
     if rc != 0:
@@ -270,7 +293,8 @@ def run_ours(args):
             "domains": n_dom, "pulses": n_pulses, "map_entries": entries, "slots": slots,
             "l2": f"inputs larger than L2: coords+forces {2 * slots * 12 / 2**20:.0f} MiB vs L2 129 MiB; no flush",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-            "launch": "one CUDA-graph launch per direction per step",
+            "launch": ("one direct launch" if flags & 0x2 else "one CUDA-graph launch") + " per direction per step",
+            "hx_flags": args.flags,
         },
         "effective_gbs": round(step_gbs, 1),
         "roofline": {
@@ -288,7 +312,7 @@ def run_ours(args):
         "build_maps_us": round(statistics.median(t_build), 1),
     }
     if rank == 0 and not args.no_extras:
-        out["secondary"] = secondary(hx, coords, forces, w, dev, peak)
+        out["secondary"] = secondary(hx, coords, forces, w, dev, peak, flags)
     del hx
     if rank == 0:
         out["cpu_baseline"] = cpu_baseline(w, pos, args.cpu_seconds)
@@ -301,7 +325,7 @@ def _flush(buf):
     buf.add_(1.0)
 
 
-def secondary(hx_main, coords, forces, w_main, dev, peak):
+def secondary(hx_main, coords, forces, w_main, dev, peak, flags):
     """Cold-L2 numbers of the headline workload, the 1M-atom configuration,
     and the small configurations' step latency against the launch floor."""
     import torch
@@ -347,7 +371,7 @@ def secondary(hx_main, coords, forces, w_main, dev, peak):
         if name == w_main.name:
             continue
         w = W.WORKLOADS[name]
-        hx = HaloExchange(w.box, w.dims, w.cutoff, device=dev.index)
+        hx = HaloExchange(w.box, w.dims, w.cutoff, device=dev.index, flags=flags)
         pos = torch.from_numpy(W.positions(w)).to(dev)
         slots = hx.build_maps(pos)
         x = torch.empty((slots, 3), device=dev)

@@ -14,7 +14,7 @@
 #include <new>
 #include <vector>
 
-#include "../../include/hx.h"
+#include "hx.h"
 #include "hx_internal.h"
 
 using namespace hx;
@@ -139,6 +139,7 @@ struct hx_ctx {
   Ctrl* d_ctrl = nullptr;                    // [2]
   int n_chunks[2] = {0, 0};
   int grid[2] = {0, 0};
+  size_t n_flags = 1;                        // flags (and election counters) per direction
   std::vector<int> u_begin;                  // per pulse, first unfused chunk (P + 1 entries)
   std::vector<GraphEntry> graphs;
 };
@@ -180,7 +181,7 @@ int to_err(cudaError_t e) {
 DirParams dir_params(hx_ctx* h, int dir) {
   DirParams P;
   std::memset(&P, 0, sizeof(P));
-  const size_t n_items = static_cast<size_t>(std::max(h->pl.n_pulses * h->pl.ndom, 1));
+  const size_t n_items = h->n_flags;
   P.chunks = h->d_chunks[dir];
   P.waits = h->d_waits[dir];
   P.maps = h->d_maps;
@@ -194,7 +195,8 @@ DirParams dir_params(hx_ctx* h, int dir) {
 }
 
 const void* kernel_for(hx_ctx* h, int kind) {
-  const int mode = (h->flags & HX_FLAG_COUNTER_SIGNAL) ? kCounter : kLastArrival;
+  const int mode = (h->flags & HX_FLAG_FINE_WAITS) ? kChunkFlag
+                   : (h->flags & HX_FLAG_COUNTER_SIGNAL) ? kCounter : kLastArrival;
   if (kind == 0) return coords_kernel(mode);
   if (kind == 1) return forces_kernel(mode, !(h->flags & HX_FLAG_UNORDERED_FORCES));
   return noop_kernel();
@@ -242,7 +244,7 @@ int launch(hx_ctx* h, int kind, float* buf, cudaStream_t s) {
 }
 
 int reset_signals(hx_ctx* h, cudaStream_t s) {
-  const size_t n_items = static_cast<size_t>(std::max(h->pl.n_pulses * h->pl.ndom, 1));
+  const size_t n_items = h->n_flags;
   HX_CUDA(cudaMemsetAsync(h->d_flags, 0, sizeof(unsigned long long) * 2 * n_items, s));
   HX_CUDA(cudaMemsetAsync(h->d_blk, 0, sizeof(unsigned int) * 2 * n_items, s));
   Ctrl c[2];
@@ -255,22 +257,24 @@ int reset_signals(hx_ctx* h, cudaStream_t s) {
 
 // ---------------------------------------------------------------- work tables
 //
-// A "part" is a run of entries of one item that is listed as a unit: the
-// independent prefix and the forwarded tail of a coordinate item, or a whole
-// force item. Parts are emitted in a topological order of their waits
-// (Kahn's algorithm) that prefers the lowest (domain, pulse) key, so the
-// chunks of one domain's pulses sit close together in the list and run
-// close together in time: the domain's slots are fetched into L2 once per
-// launch instead of once per pulse.
-
-struct Part {
-  int item;
-  int begin, end;       // entry range within the item's map
-  int halo_src;
-  long long key;        // emission priority (smaller first)
-  std::vector<int> deps;          // items that must be complete before this part
-  std::vector<std::vector<int>> chunk_waits;  // per chunk (fine waits) or one shared list
-};
+// Every (sender, pulse) item is cut into warp chunks of up to kChunk entries
+// (a coordinate item into its independent prefix and its forwarded tail).
+// Each chunk gets the list of what it must wait for:
+//   coarse (the pages' rule): a forwarded coordinate chunk waits for every
+//     earlier pulse into its sender; a force chunk of pulse p waits for every
+//     later pulse of its receiver (the slots it reads) and of its sender (the
+//     targets it adds into) - per-item signals;
+//   fine: the exact producer chunks - the chunks that stored the slots a
+//     forwarded coordinate chunk reads, the later-pulse chunks that add into
+//     the slots a force chunk reads or into the targets it adds into - each
+//     with its own signal.
+// Chunks are then listed in a topological order of those waits (Kahn's
+// algorithm, so a warp only ever waits for chunks handed out before its own)
+// that follows a priority: domains in a folded order where the neighbours a
+// pulse depends on sit close together, a domain's pulses together, and a
+// consumer one resident-warp window behind its producers. A domain's slots
+// are then fetched into L2 about once per launch, and a waiting chunk finds
+// its producers mostly done.
 
 struct ItemInfo {
   int r, p, q;           // sender, pulse, receiver
@@ -278,53 +282,56 @@ struct ItemInfo {
   int size, split, dim, shift_flag;
 };
 
-// Sorted-array helpers for the fine waits.
-bool any_in_range(const int32_t* a, int n, int64_t lo, int64_t hi) {   // any a[i] in [lo, hi)
-  const int32_t* it = std::lower_bound(a, a + n, static_cast<int32_t>(std::min<int64_t>(lo, INT32_MAX)));
-  return it != a + n && *it < hi;
+struct Rec {             // one chunk before ordering
+  int item;
+  int begin, end;        // entry range within the item's map
+  int halo_src;
+  int stage;             // position of the chunk's pulse in the launch's dependency order
+  long long key;         // priority (smaller first)
+  std::vector<int> deps;   // chunk records that must be listed earlier
+  std::vector<int> wait;   // coarse: items to wait for; fine: chunk records to wait for
+};
+
+// Position of cell c in the folded ring order 0, n-1, 1, n-2, ...: cells that
+// are neighbours on the periodic ring are at most two positions apart.
+int fold(int c, int n) { return (2 * c < n) ? 2 * c : 2 * (n - 1 - c) + 1; }
+
+int64_t domain_rank(const Plan& pl, int r) {
+  int c[3];
+  cell_of(pl, r, c);
+  // the first-communicating dimension (Z) varies fastest, X slowest
+  return fold(c[2], pl.dims[2]) + static_cast<int64_t>(pl.dims[2]) *
+                                      (fold(c[1], pl.dims[1]) + static_cast<int64_t>(pl.dims[1]) * fold(c[0], pl.dims[0]));
 }
 
-bool sorted_intersect(const int32_t* a, int na, const int32_t* b, int nb) {
-  int i = 0, k = 0;
-  while (i < na && k < nb) {
-    if (a[i] == b[k]) return true;
-    if (a[i] < b[k]) ++i;
-    else ++k;
+// Kahn's algorithm over chunk records by ascending key.
+std::vector<int> order_chunks(const std::vector<Rec>& recs) {
+  const int n = static_cast<int>(recs.size());
+  std::vector<std::vector<int>> users(n);
+  std::vector<int> unmet(n, 0);
+  for (int i = 0; i < n; ++i) {
+    unmet[i] = static_cast<int>(recs[i].deps.size());
+    for (int d : recs[i].deps) users[d].push_back(i);
   }
-  return false;
-}
-
-// Emits parts in a locality-preferring topological order; returns the order.
-std::vector<int> order_parts(const std::vector<Part>& parts, int n_items, std::vector<int>* item_parts_left) {
-  std::vector<std::vector<int>> waiters(n_items);
-  std::vector<int> unmet(parts.size(), 0);
-  for (size_t i = 0; i < parts.size(); ++i) {
-    unmet[i] = static_cast<int>(parts[i].deps.size());
-    for (int it : parts[i].deps) waiters[it].push_back(static_cast<int>(i));
-  }
-  auto cmp = [&](int a, int b) { return parts[a].key > parts[b].key; };
+  auto cmp = [&](int a, int b) { return recs[a].key != recs[b].key ? recs[a].key > recs[b].key : a > b; };
   std::vector<int> heap;
-  for (size_t i = 0; i < parts.size(); ++i)
-    if (unmet[i] == 0) heap.push_back(static_cast<int>(i));
+  for (int i = 0; i < n; ++i)
+    if (unmet[i] == 0) heap.push_back(i);
   std::make_heap(heap.begin(), heap.end(), cmp);
   std::vector<int> order;
-  order.reserve(parts.size());
+  order.reserve(n);
   while (!heap.empty()) {
     std::pop_heap(heap.begin(), heap.end(), cmp);
     const int i = heap.back();
     heap.pop_back();
     order.push_back(i);
-    const int it = parts[i].item;
-    if (--(*item_parts_left)[it] == 0) {
-      for (int w : waiters[it]) {
-        if (--unmet[w] == 0) {
-          heap.push_back(w);
-          std::push_heap(heap.begin(), heap.end(), cmp);
-        }
+    for (int u : users[i])
+      if (--unmet[u] == 0) {
+        heap.push_back(u);
+        std::push_heap(heap.begin(), heap.end(), cmp);
       }
-    }
   }
-  return order;   // shorter than parts only if the waits had a cycle (they cannot)
+  return order;   // shorter than recs only if the waits had a cycle (they cannot)
 }
 
 // Work tables of the fused and unfused kernels from the host copy of the plan.
@@ -355,148 +362,194 @@ int build_tables(hx_ctx* h, cudaStream_t s) {
     maps.resize(h->total_entries);
     HX_CUDA(cudaMemcpy(maps.data(), h->d_maps, sizeof(int32_t) * h->total_entries, cudaMemcpyDeviceToHost));
   }
-  // upper_q(r): the domain that sends into r in pulse q
   auto upper = [&](int r, int q) { return neighbour(pl, r, pl.pulse_dim[q], +1); };
+  std::vector<int64_t> rank(nd);
+  for (int r = 0; r < nd; ++r) rank[r] = domain_rank(pl, r);
+  for (int k = 0; k < 2; ++k) {
+    const int per_sm = std::max(1, max_blocks_per_sm(kernel_for(h, k)));
+    h->grid[k] = per_sm * h->sm_count;   // upper bound; trimmed to the chunk count below
+  }
 
   for (int dir = 0; dir < 2; ++dir) {
-    std::vector<Part> parts;
-    auto chunks_of = [](int begin, int end) { return std::max(1, (end - begin + kChunk - 1) / kChunk); };
-    if (dir == 0) {
-      for (int p = 0; p < P; ++p)
-        for (int r = 0; r < nd; ++r) {
-          const int t = p * nd + r;
-          const ItemInfo& it = items[t];
-          if (it.split > 0 || it.size == 0) {
-            Part a;
-            a.item = t;
-            a.begin = 0;
-            a.end = it.split;
-            a.halo_src = 0;
-            a.key = (static_cast<long long>(r) * P + p) * 2;
-            parts.push_back(std::move(a));
-          }
-          if (it.split < it.size) {
-            Part b;
-            b.item = t;
-            b.begin = it.split;
-            b.end = it.size;
-            b.halo_src = 1;
-            b.key = (static_cast<long long>(r) * P + p) * 2 + 1;
-            // forwarded entries read r's receive ranges of pulses q < p
-            const int nch = chunks_of(b.begin, b.end);
-            std::vector<int> all;
-            for (int q = 0; q < p; ++q) all.push_back(q * nd + upper(r, q));
-            for (int c = 0; c < nch; ++c) {
-              const int cb = b.begin + c * kChunk, ce = std::min(b.end, cb + kChunk);
-              if (!fine) {
-                b.chunk_waits.push_back(all);
-                continue;
-              }
-              std::vector<int> w;
-              const int32_t* m = maps.data() + it.map + cb;
-              for (int q = 0; q < p; ++q) {
-                const int64_t lo = h->t_off[q * nd + upper(r, q)];
-                const int64_t hi = lo + h->t_size[q * nd + upper(r, q)];
-                if (any_in_range(m, ce - cb, lo, hi)) w.push_back(q * nd + upper(r, q));
-              }
-              b.chunk_waits.push_back(w);
-            }
-            parts.push_back(std::move(b));
-          }
-        }
-    } else {
-      for (int p = P - 1; p >= 0; --p)
-        for (int r = 0; r < nd; ++r) {
-          const int t = p * nd + r;
-          const ItemInfo& it = items[t];
-          Part a;
-          a.item = t;
-          a.begin = 0;
-          a.end = it.size;
-          a.halo_src = 1;
-          a.key = static_cast<long long>(r) * P + (P - 1 - p);
-          const int nch = chunks_of(a.begin, a.end);
-          std::vector<int> all;
-          for (int pp = p + 1; pp < P; ++pp) {
-            all.push_back(pp * nd + it.q);                       // writes of the slots read here
-            if (ordered && it.q != r) all.push_back(pp * nd + r); // earlier adds into the same targets
-          }
-          for (int c = 0; c < nch; ++c) {
-            const int cb = c * kChunk, ce = std::min(it.size, cb + kChunk);
-            if (!fine) {
-              a.chunk_waits.push_back(all);
-              continue;
-            }
-            std::vector<int> w;
-            const int64_t slot_lo = h->t_off[t] + cb, slot_hi = h->t_off[t] + ce;
+    std::vector<Rec> recs;
+    std::vector<std::vector<int>> item_recs(std::max(n_items, 1));   // chunk records of each item, in entry order
+    auto add_part = [&](int t, int begin, int end, int halo_src, int stage, bool keep_empty) {
+      if (end <= begin && !keep_empty) return;
+      for (int b = begin;; b += kChunk) {
+        Rec rc;
+        rc.item = t;
+        rc.begin = b;
+        rc.end = std::min(end, b + kChunk);
+        rc.halo_src = halo_src;
+        rc.stage = stage;
+        rc.key = 0;
+        item_recs[t].push_back(static_cast<int>(recs.size()));
+        recs.push_back(std::move(rc));
+        if (b + kChunk >= end) break;
+      }
+    };
+    // chunk record of item t holding entry e (item_recs are in entry order)
+    auto rec_of_entry = [&](int t, int e) {
+      const std::vector<int>& v = item_recs[t];
+      int lo = 0, hi = static_cast<int>(v.size()) - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) / 2;
+        if (recs[v[mid]].begin <= e) lo = mid;
+        else hi = mid - 1;
+      }
+      return v[lo];
+    };
+    // Coarse waits may name empty items: those keep one empty chunk to signal.
+    std::vector<char> coarse_waited(std::max(n_items, 1), 0);
+    if (!fine) {
+      if (dir == 0) {
+        for (int p = 0; p < P; ++p)
+          for (int r = 0; r < nd; ++r)
+            if (items[p * nd + r].split < items[p * nd + r].size)
+              for (int q = 0; q < p; ++q) coarse_waited[q * nd + upper(r, q)] = 1;
+      } else {
+        for (int p = 0; p < P; ++p)
+          for (int r = 0; r < nd; ++r)
             for (int pp = p + 1; pp < P; ++pp) {
-              const int tq = pp * nd + it.q, tr = pp * nd + r;
-              // q forwards some of the slots this chunk reads in pulse pp
-              const bool need_q = any_in_range(maps.data() + items[tq].map, items[tq].size, slot_lo, slot_hi);
-              // r adds into some of this chunk's targets in pulse pp
-              const bool need_r = ordered && sorted_intersect(maps.data() + items[tr].map, items[tr].size,
-                                                              maps.data() + it.map + cb, ce - cb);
-              if (tq == tr) {
-                if (need_q || need_r) w.push_back(tq);
-              } else {
-                if (need_q) w.push_back(tq);
-                if (need_r) w.push_back(tr);
-              }
+              coarse_waited[pp * nd + items[p * nd + r].q] = 1;
+              if (ordered) coarse_waited[pp * nd + r] = 1;
             }
-            a.chunk_waits.push_back(w);
-          }
-          parts.push_back(std::move(a));
-        }
-    }
-    // deps per part; which items anybody waits for; drop unneeded empty parts
-    std::vector<char> waited(std::max(n_items, 1), 0);
-    for (auto& pt : parts) {
-      std::vector<int> d;
-      for (auto& w : pt.chunk_waits) d.insert(d.end(), w.begin(), w.end());
-      std::sort(d.begin(), d.end());
-      d.erase(std::unique(d.begin(), d.end()), d.end());
-      pt.deps = d;
-      for (int it : d) waited[it] = 1;
-    }
-    std::vector<Part> kept;
-    for (auto& pt : parts)
-      if (pt.end > pt.begin || waited[pt.item]) kept.push_back(std::move(pt));
-    parts.swap(kept);
-    std::vector<int> item_chunks(std::max(n_items, 1), 0), parts_left(std::max(n_items, 1), 0);
-    for (auto& pt : parts) {
-      item_chunks[pt.item] += chunks_of(pt.begin, pt.end);
-      parts_left[pt.item] += 1;
-    }
-    std::vector<int> order = order_parts(parts, std::max(n_items, 1), &parts_left);
-    if (order.size() != parts.size()) return HX_ERR_STATE;
-    std::vector<Chunk> chunks;
-    std::vector<Wait> waits;
-    for (int pi : order) {
-      const Part& pt = parts[pi];
-      const ItemInfo& it = items[pt.item];
-      const int nch = chunks_of(pt.begin, pt.end);
-      for (int c = 0; c < nch; ++c) {
-        const int cb = pt.begin + c * kChunk, ce = std::min(pt.end, cb + kChunk);
-        Chunk ch;
-        std::memset(&ch, 0, sizeof(ch));
-        ch.src = it.src;
-        ch.dst = it.dst + cb;
-        ch.map = it.map + cb;
-        ch.n = ce - cb;
-        ch.item = pt.item;
-        ch.item_chunks = item_chunks[pt.item];
-        const std::vector<int>& w = pt.chunk_waits.empty() ? std::vector<int>() : pt.chunk_waits[c];
-        ch.wait_off = static_cast<int32_t>(waits.size());
-        ch.wait_cnt = static_cast<int32_t>(w.size());
-        for (int x : w) waits.push_back({x, 0});
-        ch.flags = (pt.halo_src ? kHaloSrc : 0) | (waited[pt.item] ? kSignal : 0) |
-                   (dir == 0 && it.shift_flag ? kShift : 0);
-        ch.dim = it.dim;
-        ch.shift = pl.boxf[it.dim];
-        chunks.push_back(ch);
       }
     }
-    for (auto& w : waits) w.chunks = item_chunks[w.item];
+    for (int p = 0; p < P; ++p)
+      for (int r = 0; r < nd; ++r) {
+        const int t = p * nd + r;
+        const ItemInfo& it = items[t];
+        if (dir == 0) {
+          add_part(t, 0, it.split, 0, 0, it.size == 0 && coarse_waited[t]);
+          add_part(t, it.split, it.size, 1, p, false);
+        } else {
+          add_part(t, 0, it.size, 1, P - 1 - p, it.size == 0 && coarse_waited[t]);
+        }
+      }
+    // waits
+    for (size_t ci = 0; ci < recs.size(); ++ci) {
+      Rec& rc = recs[ci];
+      const ItemInfo& it = items[rc.item];
+      const int r = it.r, p = it.p;
+      if (dir == 0) {
+        if (!rc.halo_src) continue;
+        if (!fine) {
+          for (int q = 0; q < p; ++q) rc.wait.push_back(q * nd + upper(r, q));
+          continue;
+        }
+        // producers: chunks of (upper(r, q), q) that stored the slots read here
+        const int32_t* m = maps.data() + it.map;
+        for (int i = rc.begin; i < rc.end; ++i) {
+          for (int q = 0; q < p; ++q) {
+            const int tq = q * nd + upper(r, q);
+            const int64_t lo = h->t_off[tq], n = items[tq].size;
+            if (m[i] >= lo && m[i] < lo + n) {
+              rc.wait.push_back(rec_of_entry(tq, static_cast<int>(m[i] - lo)));
+              break;
+            }
+          }
+        }
+      } else {
+        if (!fine) {
+          for (int pp = p + 1; pp < P; ++pp) {
+            rc.wait.push_back(pp * nd + it.q);
+            if (ordered && it.q != r) rc.wait.push_back(pp * nd + r);
+          }
+          continue;
+        }
+        if (rc.end <= rc.begin) continue;
+        const int32_t* m = maps.data() + it.map;
+        const int64_t slot_lo = h->t_off[rc.item] + rc.begin, slot_hi = h->t_off[rc.item] + rc.end;
+        for (int pp = p + 1; pp < P; ++pp) {
+          // later-pulse chunks of the receiver that add into the slots read here
+          const int tq = pp * nd + it.q;
+          const int32_t* mq = maps.data() + items[tq].map;
+          const int nq = items[tq].size;
+          const int i1 = static_cast<int>(std::lower_bound(mq, mq + nq, static_cast<int32_t>(slot_lo)) - mq);
+          const int i2 = static_cast<int>(std::lower_bound(mq, mq + nq, static_cast<int32_t>(slot_hi)) - mq);
+          if (i1 < i2) {
+            const int c1 = rec_of_entry(tq, i1), c2 = rec_of_entry(tq, i2 - 1);
+            for (int c = c1; c <= c2; ++c) rc.wait.push_back(c);   // records of one item are consecutive
+          }
+          if (!ordered) continue;
+          // later-pulse chunks of the sender that add into the same targets
+          const int tr = pp * nd + r;
+          const int32_t* mr = maps.data() + items[tr].map;
+          const int nr = items[tr].size;
+          int k = static_cast<int>(std::lower_bound(mr, mr + nr, m[rc.begin]) - mr);
+          for (int i = rc.begin; i < rc.end && k < nr; ++i) {
+            while (k < nr && mr[k] < m[i]) ++k;
+            if (k < nr && mr[k] == m[i]) rc.wait.push_back(rec_of_entry(tr, k));
+          }
+        }
+      }
+      std::sort(rc.wait.begin(), rc.wait.end());
+      rc.wait.erase(std::unique(rc.wait.begin(), rc.wait.end()), rc.wait.end());
+    }
+    // listing dependencies (chunk records) and who gets signalled
+    std::vector<char> rec_waited(recs.size(), 0), item_waited(std::max(n_items, 1), 0);
+    for (auto& rc : recs) {
+      if (fine) {
+        rc.deps = rc.wait;
+        for (int d : rc.wait) rec_waited[d] = 1;
+      } else {
+        for (int t : rc.wait) {
+          item_waited[t] = 1;
+          rc.deps.insert(rc.deps.end(), item_recs[t].begin(), item_recs[t].end());
+        }
+      }
+    }
+    // priority: base order (domain rank, stage, pulse, entry), then a lag of
+    // one resident-warp window per stage
+    {
+      std::vector<int> base(recs.size());
+      for (size_t i = 0; i < recs.size(); ++i) base[i] = static_cast<int>(i);
+      std::sort(base.begin(), base.end(), [&](int a, int b) {
+        const Rec& x = recs[a];
+        const Rec& y = recs[b];
+        const ItemInfo& ix = items[x.item];
+        const ItemInfo& iy = items[y.item];
+        if (rank[ix.r] != rank[iy.r]) return rank[ix.r] < rank[iy.r];
+        if (x.stage != y.stage) return x.stage < y.stage;
+        if (ix.p != iy.p) return ix.p < iy.p;
+        return x.begin < y.begin;
+      });
+      const long long window = static_cast<long long>(h->grid[dir]) * kWarps;
+      for (size_t k = 0; k < base.size(); ++k)
+        recs[base[k]].key = static_cast<long long>(k) + window * recs[base[k]].stage;
+    }
+    std::vector<int> order = order_chunks(recs);
+    if (order.size() != recs.size()) return HX_ERR_STATE;
+    std::vector<int> pos(recs.size());
+    for (size_t k = 0; k < order.size(); ++k) pos[order[k]] = static_cast<int>(k);
+    std::vector<int> item_chunks(std::max(n_items, 1), 0);
+    for (auto& rc : recs) item_chunks[rc.item] += 1;
+    std::vector<Chunk> chunks;
+    std::vector<Wait> waits;
+    chunks.reserve(order.size());
+    for (int ri : order) {
+      const Rec& rc = recs[ri];
+      const ItemInfo& it = items[rc.item];
+      Chunk ch;
+      std::memset(&ch, 0, sizeof(ch));
+      ch.src = it.src;
+      ch.dst = it.dst + rc.begin;
+      ch.map = it.map + rc.begin;
+      ch.n = rc.end - rc.begin;
+      ch.item = rc.item;
+      ch.item_chunks = item_chunks[rc.item];
+      ch.wait_off = static_cast<int32_t>(waits.size());
+      ch.wait_cnt = static_cast<int32_t>(rc.wait.size());
+      for (int w : rc.wait) waits.push_back(fine ? Wait{pos[w], 1} : Wait{w, 0});
+      const bool sig = fine ? rec_waited[ri] != 0 : item_waited[rc.item] != 0;
+      ch.flags = (rc.halo_src ? kHaloSrc : 0) | (sig ? kSignal : 0) | (dir == 0 && it.shift_flag ? kShift : 0);
+      ch.dim = it.dim;
+      ch.shift = pl.boxf[it.dim];
+      chunks.push_back(ch);
+    }
+    if (!fine)
+      for (auto& w : waits) w.chunks = item_chunks[w.item];
     h->n_chunks[dir] = static_cast<int>(chunks.size());
     HX_CUDA(dev_alloc(&h->d_chunks[dir], chunks.size()));
     HX_CUDA(dev_alloc(&h->d_waits[dir], waits.size()));
@@ -533,14 +586,15 @@ int build_tables(hx_ctx* h, cudaStream_t s) {
   if (!uch.empty())
     HX_CUDA(cudaMemcpy(h->d_uchunks, uch.data(), sizeof(Chunk) * uch.size(), cudaMemcpyHostToDevice));
 
-  const size_t n_flags = 2 * static_cast<size_t>(std::max(n_items, 1));
-  HX_CUDA(dev_alloc(&h->d_flags, n_flags));
-  HX_CUDA(dev_alloc(&h->d_blk, n_flags));
+  // one flag (and one election counter) per item or per chunk, per direction
+  h->n_flags = std::max<size_t>({static_cast<size_t>(std::max(n_items, 1)), static_cast<size_t>(h->n_chunks[0]),
+                                 static_cast<size_t>(h->n_chunks[1])});
+  HX_CUDA(dev_alloc(&h->d_flags, 2 * h->n_flags));
+  HX_CUDA(dev_alloc(&h->d_blk, 2 * h->n_flags));
   HX_CUDA(dev_alloc(&h->d_ctrl, 2));
   // Persistent grid: every warp co-resident, one warp per chunk at most.
   for (int k = 0; k < 2; ++k) {
-    const int per_sm = std::max(1, max_blocks_per_sm(kernel_for(h, k)));
-    const int warps = std::max(1, std::min(h->n_chunks[k], per_sm * h->sm_count * kWarps));
+    const int warps = std::max(1, std::min(h->n_chunks[k], h->grid[k] * kWarps));
     h->grid[k] = (warps + kWarps - 1) / kWarps;
   }
   return reset_signals(h, s);

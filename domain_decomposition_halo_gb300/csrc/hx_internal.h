@@ -6,17 +6,25 @@
 
 namespace hx {
 
+#ifndef HX_ROUNDS
+#define HX_ROUNDS 8
+#endif
+#ifndef HX_MIN_BLOCKS
+#define HX_MIN_BLOCKS 3
+#endif
+
 constexpr int kThreads = 256;                 // threads per block of the exchange kernels
 constexpr int kWarps = kThreads / 32;         // independent warps per block
-constexpr int kRounds = 8;                    // 32-entry rounds per warp chunk
-constexpr int kChunk = 32 * kRounds;          // map entries per warp chunk (256)
+constexpr int kRounds = HX_ROUNDS;            // 32-entry rounds per warp chunk
+constexpr int kChunk = 32 * kRounds;          // map entries per warp chunk
+constexpr int kMinBlocks = HX_MIN_BLOCKS;     // resident blocks per SM the register budget allows
 
 // One warp's unit of work: up to kChunk consecutive entries of one
 // (sender, pulse) map. Everything the warp needs is in this 64-byte record,
 // so a chunk costs one descriptor load.
 enum ChunkFlags : int32_t {
   kHaloSrc = 1,      // entries read slots written earlier in the same launch
-  kSignal = 2,       // some later chunk waits for this chunk's item
+  kSignal = 2,       // some later chunk waits for this chunk (or for its item)
   kShift = 4,        // add `shift` to component `dim` (coordinates only)
 };
 
@@ -36,7 +44,8 @@ struct alignas(16) Chunk {
 static_assert(sizeof(Chunk) == 64, "chunk descriptor must stay one 64-byte record");
 
 // Wait for `item` of the same direction to have been signalled by all of its
-// `chunks` in the current launch.
+// `chunks` in the current launch (per-chunk flags: `item` is the chunk's
+// position in the list and `chunks` is 1).
 struct Wait {
   int32_t item;
   int32_t chunks;
@@ -58,7 +67,7 @@ struct DirParams {
   const Chunk* chunks;
   const Wait* waits;
   const int32_t* maps;
-  unsigned long long* flags;  // per item: epoch flag (last-arrival mode) or arrival counter
+  unsigned long long* flags;  // per item (epoch flag or arrival counter) or per chunk (epoch flag)
   unsigned int* arrivals;     // per item: last-arrival election counters
   Ctrl* ctrl;
   unsigned long long n_chunks;
@@ -75,7 +84,10 @@ struct PulseParams {
   int n_chunks;
 };
 
-enum SignalMode { kLastArrival = 0, kCounter = 1 };
+// kLastArrival: per-item epoch flag stored by the item's last chunk (the
+// pages' last-block election); kCounter: per-item arrival counter; kChunkFlag:
+// one epoch flag per chunk, for chunk-granular waits.
+enum SignalMode { kLastArrival = 0, kCounter = 1, kChunkFlag = 2 };
 
 // ---- exchange kernels (hx_kernels.cu) ----
 const void* coords_kernel(int signal_mode);

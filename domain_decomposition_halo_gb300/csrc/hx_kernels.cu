@@ -100,16 +100,19 @@ __device__ bool wait_chunk(const DirParams& P, const Chunk& ch, unsigned long lo
         (MODE == kCounter) ? epoch * static_cast<unsigned long long>(wt.chunks) : epoch;
     unsigned long long t0 = 0;
     unsigned iter = 0;
-    // last-arrival flags hold an epoch (compared for equality, as the pages'
-    // signal wait does); arrival counters only grow
+    // epoch flags (per item or per chunk) are compared for equality, as the
+    // pages' signal wait does; arrival counters only grow
     while ((MODE == kCounter) ? (ld_acquire_u64(flag) < target) : (ld_acquire_u64(flag) != target)) {
       if ((iter++ & 31u) == 0u) {
         const unsigned long long now = global_timer_ns();
         if (t0 == 0) t0 = now;
         if (ld_relaxed_s32(&P.ctrl->status) != 0) return false;
         if (now - t0 > P.timeout_ns) {
-          if (atomicCAS(&P.ctrl->status, 0, kErrTimeout) == 0)
-            atomicExch(&P.ctrl->detail, P.direction * 65536 + wt.item);
+          if (atomicCAS(&P.ctrl->status, 0, kErrTimeout) == 0) {
+            // report the (sender, pulse) item, also when the wait was on one chunk of it
+            const int item = (MODE == kChunkFlag) ? P.chunks[wt.item].item : wt.item;
+            atomicExch(&P.ctrl->detail, P.direction * 65536 + item);
+          }
           return false;
         }
       }
@@ -120,10 +123,12 @@ __device__ bool wait_chunk(const DirParams& P, const Chunk& ch, unsigned long lo
 
 // Lane 0 only, after the warp's stores (ordered by the preceding __syncwarp).
 template <int MODE>
-__device__ __forceinline__ void signal_chunk(const DirParams& P, const Chunk& ch, unsigned long long epoch,
-                                             int drop_item) {
+__device__ __forceinline__ void signal_chunk(const DirParams& P, const Chunk& ch, unsigned long long c,
+                                             unsigned long long epoch, int drop_item) {
   const bool drop = ch.item == drop_item;
-  if (MODE == kCounter) {
+  if (MODE == kChunkFlag) {
+    if (!drop) st_release_u64(P.flags + c, epoch);
+  } else if (MODE == kCounter) {
     if (!drop) red_release_add_u64(P.flags + ch.item, 1ull);
   } else {
     const unsigned last = static_cast<unsigned>(ch.item_chunks - 1);
@@ -288,20 +293,20 @@ __device__ __forceinline__ void run_warps(float* __restrict__ buf, const DirPara
     else forces_chunk<KIND == 1>(buf, ch, j);
     if (ch.flags & kSignal) {
       __syncwarp();
-      if (lane == 0) signal_chunk<MODE>(P, ch, epoch, drop_item);
+      if (lane == 0) signal_chunk<MODE>(P, ch, c, epoch, drop_item);
     }
     c = (t - base) + W;
   }
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(kThreads) k_coords_fused(float* __restrict__ x, DirParams P) {
+__global__ void __launch_bounds__(kThreads, kMinBlocks) k_coords_fused(float* __restrict__ x, DirParams P) {
   __shared__ float s_stage[kWarps][96];
   run_warps<MODE, 0>(x, P, s_stage[threadIdx.x >> 5]);
 }
 
 template <int MODE, bool ORDERED>
-__global__ void __launch_bounds__(kThreads) k_forces_fused(float* __restrict__ f, DirParams P) {
+__global__ void __launch_bounds__(kThreads, kMinBlocks) k_forces_fused(float* __restrict__ f, DirParams P) {
   run_warps<MODE, ORDERED ? 1 : 2>(f, P, nullptr);
 }
 
@@ -331,11 +336,15 @@ __global__ void k_noop() {}
 }  // namespace
 
 const void* coords_kernel(int signal_mode) {
+  if (signal_mode == kChunkFlag) return reinterpret_cast<const void*>(&k_coords_fused<kChunkFlag>);
   return signal_mode == kCounter ? reinterpret_cast<const void*>(&k_coords_fused<kCounter>)
                                  : reinterpret_cast<const void*>(&k_coords_fused<kLastArrival>);
 }
 
 const void* forces_kernel(int signal_mode, bool ordered) {
+  if (signal_mode == kChunkFlag)
+    return ordered ? reinterpret_cast<const void*>(&k_forces_fused<kChunkFlag, true>)
+                   : reinterpret_cast<const void*>(&k_forces_fused<kChunkFlag, false>);
   if (signal_mode == kCounter)
     return ordered ? reinterpret_cast<const void*>(&k_forces_fused<kCounter, true>)
                    : reinterpret_cast<const void*>(&k_forces_fused<kCounter, false>);

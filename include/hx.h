@@ -72,10 +72,12 @@ typedef struct hx_ctx* hx_handle;
 #define HX_FLAG_UNORDERED_FORCES 0x1u /* force adds by atomics: order-free, within 1e-6 relative
                                           of the ordered result; default is ordered and bit-exact */
 #define HX_FLAG_NO_GRAPH 0x2u          /* launch the fused kernels directly, not through a CUDA graph */
-#define HX_FLAG_COUNTER_SIGNAL 0x4u    /* every chunk adds to the pulse's arrival counter (release)
-                                          instead of the last block storing an epoch flag */
-#define HX_FLAG_FINE_WAITS 0x8u        /* a dependent chunk waits only for the pulses that delivered
-                                          the slots it reads, not for every earlier pulse */
+#define HX_FLAG_COUNTER_SIGNAL 0x4u    /* every chunk adds to its pulse's arrival counter (release)
+                                          instead of the last chunk storing an epoch flag */
+#define HX_FLAG_FINE_WAITS 0x8u        /* chunk-granular dependencies: a chunk waits only for the
+                                          chunks that wrote the slots it reads or, for forces, that
+                                          add into its targets, each signalled by its own epoch flag
+                                          (HX_FLAG_COUNTER_SIGNAL is then ignored) */
 
 #define HX_MAX_PULSES 32
 #define HX_MAX_DOMAINS 4096

@@ -1,0 +1,39 @@
+"""Host-side logic of bench.py that needs no GPU."""
+import numpy as np
+
+import bench
+from domain_decomposition_halo_gb300 import workloads as W
+
+
+def test_reference_sample_keeps_per_domain_geometry():
+    w = W.WORKLOADS["C5"]
+    for k in range(1, 6):
+        s = bench.sample_workload(w, k)
+        per_dom_box = [b / n for b, n in zip(s.box, s.dims)]
+        assert np.allclose(per_dom_box, [b / n for b, n in zip(w.box, w.dims)])
+        n_dom = s.dims[0] * s.dims[1] * s.dims[2]
+        assert s.n_atoms // n_dom == w.n_atoms // (w.dims[0] * w.dims[1] * w.dims[2])
+        assert n_dom == (w.dims[0] * w.dims[1] * w.dims[2]) >> k
+        assert s.cutoff == w.cutoff and s.order == w.order and s.forces == w.forces
+        assert all(n >= 2 for n in s.dims)
+
+
+def test_flag_names():
+    from domain_decomposition_halo_gb300 import hx as HX
+    assert bench.hx_flags("fine") == HX.HX_FLAG_FINE_WAITS
+    assert bench.hx_flags("pages") == 0
+    assert bench.hx_flags("fine,nograph,unordered") == (HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_NO_GRAPH |
+                                                        HX.HX_FLAG_UNORDERED_FORCES)
+
+
+def test_traffic_needs_matching_digest(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    (tmp_path / "domain_decomposition_halo_gb300" / "csrc").mkdir(parents=True)
+    for name in ("hx_kernels.cu", "hx_internal.h"):
+        (tmp_path / "domain_decomposition_halo_gb300" / "csrc" / name).write_text("x")
+    (tmp_path / "profiles").mkdir()
+    digest = bench.kernel_source_digest()
+    (tmp_path / "profiles" / "k_C5.md").write_text(f"traffic_bytes_per_launch: 123\nkernel_source_digest: {digest}\n")
+    assert bench.profiled_traffic("k", "C5") == 123.0
+    (tmp_path / "profiles" / "k_C5.md").write_text("traffic_bytes_per_launch: 123\nkernel_source_digest: 0000\n")
+    assert bench.profiled_traffic("k", "C5") is None

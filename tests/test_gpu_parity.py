@@ -268,7 +268,12 @@ def test_dropped_signal_times_out_and_recovers(direction, flags):
         c.hx.exchange_forces(ft)
     rc, detail = c.hx.status()
     assert rc == HX.HX_ERR_TIMEOUT
-    assert detail == direction * 65536 + pulse * nd + 3
+    # the first wait to give up is on the dropped item, or on an item of the
+    # same direction that was itself held up by it (waits time out together)
+    assert detail // 65536 == direction
+    item = detail % 65536
+    p_item = item // nd
+    assert item == pulse * nd + 3 or (p_item > pulse if direction == 0 else p_item < pulse)
     c.hx.debug_drop_signal(direction, -1)
     c.hx.clear_status()
     assert c.hx.status()[0] == 0
