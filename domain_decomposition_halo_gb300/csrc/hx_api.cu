@@ -140,6 +140,11 @@ struct hx_ctx {
   int n_chunks[2] = {0, 0};
   int grid[2] = {0, 0};
   size_t n_flags = 1;                        // flags (and election counters) per direction
+  bool tiles = false;                        // fused path runs the tile kernels
+  TileUnit* d_units[2] = {nullptr, nullptr};
+  TileSeg* d_segs[2] = {nullptr, nullptr};
+  Wait* d_twaits[2] = {nullptr, nullptr};
+  int n_units[2] = {0, 0};
   std::vector<int> u_begin;                  // per pulse, first unfused chunk (P + 1 entries)
   std::vector<GraphEntry> graphs;
 };
@@ -160,6 +165,12 @@ void free_tables(hx_ctx* h) {
     dev_free(h->d_waits[k]);
   }
   dev_free(h->d_uchunks);
+  for (int k = 0; k < 2; ++k) {
+    dev_free(h->d_units[k]);
+    dev_free(h->d_segs[k]);
+    dev_free(h->d_twaits[k]);
+    h->n_units[k] = 0;
+  }
   dev_free(h->d_flags);
   dev_free(h->d_blk);
   dev_free(h->d_ctrl);
@@ -204,20 +215,45 @@ const void* kernel_for(hx_ctx* h, int kind) {
 
 // Launch a fused exchange (kind 0/1) or the no-op (kind 2): directly, or via
 // a cached single-node graph keyed by (kind, buffer pointer).
+TileParams tile_params(hx_ctx* h, int dir) {
+  TileParams P;
+  std::memset(&P, 0, sizeof(P));
+  P.units = h->d_units[dir];
+  P.segs = h->d_segs[dir];
+  P.waits = h->d_twaits[dir];
+  P.maps = h->d_maps;
+  P.flags = h->d_flags + static_cast<size_t>(dir) * h->n_flags;
+  P.ctrl = h->d_ctrl + dir;
+  P.n_units = static_cast<unsigned long long>(h->n_units[dir]);
+  P.direction = dir;
+  P.timeout_ns = h->timeout_ns;
+  return P;
+}
+
 int launch(hx_ctx* h, int kind, float* buf, cudaStream_t s) {
   DirParams P;
+  TileParams TP;
   void* args2[2];
   void** args = nullptr;
   dim3 grid(1), block(kind == 2 ? 1 : kThreads);
-  if (kind != 2) {
+  size_t smem = 0;
+  const void* fn = kernel_for(h, kind);
+  if (kind != 2 && h->tiles) {
+    TP = tile_params(h, kind);
+    args2[0] = &buf;
+    args2[1] = &TP;
+    args = args2;
+    grid = dim3(static_cast<unsigned>(h->grid[kind]));
+    smem = tiles_smem_bytes();
+    fn = tiles_kernel(kind);
+  } else if (kind != 2) {
     P = dir_params(h, kind);
     args2[0] = &buf;
     args2[1] = &P;
     args = args2;
     grid = dim3(static_cast<unsigned>(h->grid[kind]));
   }
-  const void* fn = kernel_for(h, kind);
-  if (h->flags & HX_FLAG_NO_GRAPH) return to_err(cudaLaunchKernel(fn, grid, block, args, 0, s));
+  if (h->flags & HX_FLAG_NO_GRAPH) return to_err(cudaLaunchKernel(fn, grid, block, args, smem, s));
   for (auto& g : h->graphs)
     if (g.kind == kind && g.ptr == buf) return to_err(cudaGraphLaunch(g.exec, s));
   cudaGraph_t graph;
@@ -227,7 +263,7 @@ int launch(hx_ctx* h, int kind, float* buf, cudaStream_t s) {
   kp.func = const_cast<void*>(fn);
   kp.gridDim = grid;
   kp.blockDim = block;
-  kp.sharedMemBytes = 0;
+  kp.sharedMemBytes = static_cast<unsigned>(smem);
   kp.kernelParams = args;
   cudaGraphNode_t node;
   cudaError_t e = cudaGraphAddKernelNode(&node, graph, nullptr, 0, &kp);
@@ -334,6 +370,182 @@ std::vector<int> order_chunks(const std::vector<Rec>& recs) {
   return order;   // shorter than recs only if the waits had a cycle (they cannot)
 }
 
+// ---------------------------------------------------------------- tile tables
+//
+// Each domain's array is cut into ranges (home, then the slots received in
+// each pulse) and each range into tiles of up to kTile slots. A tile gets
+// one segment per (sender, pulse) map that has entries inside it: for
+// coordinates the maps it is a source of, for forces the maps it is a target
+// of (segments last pulse first). Dependencies:
+//   coordinates: a tile of received slots waits for the tiles of the sending
+//     domain that stored those slots;
+//   forces: a tile waits for the tiles of its receivers that hold the slots
+//     it reads, when those tiles are themselves targets of later pulses.
+// Tiles are listed by Kahn's algorithm with the same priority as the chunk
+// lists (folded domain order, dependency depth, a lag of one resident window
+// per depth).
+
+struct TRec {
+  int r;              // domain
+  int range;          // -1 home, else the pulse whose received slots the tile holds
+  int a, n;           // local index of the first slot, slot count
+  std::vector<TileSeg> segs;
+  std::vector<int> seg_pulse;
+  std::vector<int> deps;   // TRec indices
+  int stage = 0;
+  long long key = 0;
+};
+
+int build_tile_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::vector<int32_t>& maps,
+                      const std::vector<int64_t>& rank) {
+  const Plan& pl = h->pl;
+  const int P = pl.n_pulses, nd = pl.ndom;
+  auto upper = [&](int r, int q) { return neighbour(pl, r, pl.pulse_dim[q], +1); };
+  for (int dir = 0; dir < 2; ++dir) {
+    std::vector<TRec> recs;
+    // tiles of (domain, range): index list in slot order
+    std::vector<std::vector<std::vector<int>>> by_range(nd, std::vector<std::vector<int>>(P + 1));
+    for (int r = 0; r < nd; ++r) {
+      for (int rg = -1; rg < P; ++rg) {
+        int lo, len;
+        if (rg < 0) {
+          lo = 0;
+          len = h->home[r];
+        } else {
+          const int tu = rg * nd + upper(r, rg);
+          lo = h->t_off[tu];
+          len = h->t_size[tu];
+        }
+        for (int a = lo; a < lo + len; a += kTile) {
+          TRec t;
+          t.r = r;
+          t.range = rg;
+          t.a = a;
+          t.n = std::min(kTile, lo + len - a);
+          for (int k = 0; k < P; ++k) {
+            const int p = dir == 0 ? k : P - 1 - k;
+            const ItemInfo& it = items[p * nd + r];
+            if (it.size == 0) continue;
+            const int32_t* m = maps.data() + it.map;
+            const int i1 = static_cast<int>(std::lower_bound(m, m + it.size, t.a) - m);
+            const int i2 = static_cast<int>(std::lower_bound(m, m + it.size, t.a + t.n) - m);
+            if (i2 <= i1) continue;
+            TileSeg sg;
+            std::memset(&sg, 0, sizeof(sg));
+            sg.map = it.map + i1;
+            sg.other = it.dst + i1;
+            sg.n = i2 - i1;
+            sg.dim = it.dim;
+            sg.shift = pl.boxf[it.dim];
+            sg.do_shift = (dir == 0) ? it.shift_flag : 0;
+            t.segs.push_back(sg);
+            t.seg_pulse.push_back(p);
+          }
+          if (t.segs.empty()) continue;
+          by_range[r][rg + 1].push_back(static_cast<int>(recs.size()));
+          recs.push_back(std::move(t));
+        }
+      }
+    }
+    // dependencies
+    for (size_t i = 0; i < recs.size(); ++i) {
+      TRec& t = recs[i];
+      if (dir == 0) {
+        if (t.range < 0) continue;
+        // slots [a, a+n) of r's range `p0` are entries [a - off, a - off + n) of the map (u, p0)
+        const int p0 = t.range, u = upper(t.r, p0);
+        const int64_t e0 = t.a - h->t_off[p0 * nd + u], e1 = e0 + t.n;
+        for (int rg = 0; rg <= P; ++rg)
+          for (int j : by_range[u][rg]) {
+            const TRec& s = recs[j];
+            for (size_t k = 0; k < s.segs.size(); ++k) {
+              if (s.seg_pulse[k] != p0) continue;
+              const int64_t b0 = s.segs[k].map - items[p0 * nd + u].map, b1 = b0 + s.segs[k].n;
+              if (b0 < e1 && e0 < b1) t.deps.push_back(j);
+            }
+          }
+      } else {
+        // the slots read by segment (r, p) are q's slots [other, other + n) in q's range p
+        for (size_t k = 0; k < t.segs.size(); ++k) {
+          const int p = t.seg_pulse[k];
+          const int q = items[p * nd + t.r].q;
+          const int64_t s0 = t.segs[k].other - h->dom_offset[q], s1 = s0 + t.segs[k].n;
+          for (int j : by_range[q][p + 1]) {
+            const TRec& s = recs[j];
+            if (s.a < s1 && s0 < s.a + s.n) t.deps.push_back(j);
+          }
+        }
+      }
+      std::sort(t.deps.begin(), t.deps.end());
+      t.deps.erase(std::unique(t.deps.begin(), t.deps.end()), t.deps.end());
+    }
+    // dependency depth, then priority: base order + one resident window per depth
+    {
+      std::vector<Rec> tmp(recs.size());
+      for (size_t i = 0; i < recs.size(); ++i) tmp[i].deps = recs[i].deps;
+      std::vector<int> topo = order_chunks(tmp);   // any topological order
+      if (topo.size() != recs.size()) return HX_ERR_STATE;
+      for (int i : topo)
+        for (int d : recs[i].deps) recs[i].stage = std::max(recs[i].stage, recs[d].stage + 1);
+      std::vector<int> base(recs.size());
+      for (size_t i = 0; i < recs.size(); ++i) base[i] = static_cast<int>(i);
+      std::sort(base.begin(), base.end(), [&](int x, int y) {
+        const TRec& a = recs[x];
+        const TRec& b = recs[y];
+        if (rank[a.r] != rank[b.r]) return rank[a.r] < rank[b.r];
+        if (a.stage != b.stage) return a.stage < b.stage;
+        if (a.range != b.range) return a.range < b.range;
+        return a.a < b.a;
+      });
+      const long long window = h->grid[dir];
+      std::vector<Rec> ord(recs.size());
+      for (size_t k = 0; k < base.size(); ++k) {
+        ord[base[k]].key = static_cast<long long>(k) + window * recs[base[k]].stage;
+        recs[base[k]].key = ord[base[k]].key;
+      }
+      for (size_t i = 0; i < recs.size(); ++i) ord[i].deps = recs[i].deps;
+      std::vector<int> order = order_chunks(ord);
+      if (order.size() != recs.size()) return HX_ERR_STATE;
+      std::vector<int> pos(recs.size());
+      for (size_t k = 0; k < order.size(); ++k) pos[order[k]] = static_cast<int>(k);
+      std::vector<char> waited(recs.size(), 0);
+      for (auto& t : recs)
+        for (int d : t.deps) waited[d] = 1;
+      std::vector<TileUnit> units;
+      std::vector<TileSeg> segs;
+      std::vector<Wait> waits;
+      for (int i : order) {
+        const TRec& t = recs[i];
+        TileUnit u;
+        std::memset(&u, 0, sizeof(u));
+        u.base = h->dom_offset[t.r] + t.a;
+        u.n = t.n;
+        u.local_a = t.a;
+        u.seg_off = static_cast<int32_t>(segs.size());
+        u.seg_cnt = static_cast<int32_t>(t.segs.size());
+        segs.insert(segs.end(), t.segs.begin(), t.segs.end());
+        u.wait_off = static_cast<int32_t>(waits.size());
+        u.wait_cnt = static_cast<int32_t>(t.deps.size());
+        for (int d : t.deps) waits.push_back({pos[d], 1});
+        u.flags = (waited[i] ? kSignal : 0) | (dir == 0 && t.range >= 0 ? kHaloSrc : 0);
+        u.item = t.seg_pulse[0] * nd + t.r;
+        units.push_back(u);
+      }
+      h->n_units[dir] = static_cast<int>(units.size());
+      HX_CUDA(dev_alloc(&h->d_units[dir], units.size()));
+      HX_CUDA(dev_alloc(&h->d_segs[dir], segs.size()));
+      HX_CUDA(dev_alloc(&h->d_twaits[dir], waits.size()));
+      if (!units.empty())
+        HX_CUDA(cudaMemcpy(h->d_units[dir], units.data(), sizeof(TileUnit) * units.size(), cudaMemcpyHostToDevice));
+      if (!segs.empty())
+        HX_CUDA(cudaMemcpy(h->d_segs[dir], segs.data(), sizeof(TileSeg) * segs.size(), cudaMemcpyHostToDevice));
+      if (!waits.empty())
+        HX_CUDA(cudaMemcpy(h->d_twaits[dir], waits.data(), sizeof(Wait) * waits.size(), cudaMemcpyHostToDevice));
+    }
+  }
+  return HX_OK;
+}
+
 // Work tables of the fused and unfused kernels from the host copy of the plan.
 int build_tables(hx_ctx* h, cudaStream_t s) {
   const Plan& pl = h->pl;
@@ -358,19 +570,24 @@ int build_tables(hx_ctx* h, cudaStream_t s) {
       it.shift_flag = h->t_shift[t];
     }
   std::vector<int32_t> maps;
-  if (fine && h->total_entries > 0) {
+  if ((fine || (h->flags & HX_FLAG_TILES)) && h->total_entries > 0) {   // fine waits and tiles read the maps
     maps.resize(h->total_entries);
     HX_CUDA(cudaMemcpy(maps.data(), h->d_maps, sizeof(int32_t) * h->total_entries, cudaMemcpyDeviceToHost));
   }
   auto upper = [&](int r, int q) { return neighbour(pl, r, pl.pulse_dim[q], +1); };
   std::vector<int64_t> rank(nd);
   for (int r = 0; r < nd; ++r) rank[r] = domain_rank(pl, r);
+  h->tiles = (h->flags & HX_FLAG_TILES) != 0;
   for (int k = 0; k < 2; ++k) {
-    const int per_sm = std::max(1, max_blocks_per_sm(kernel_for(h, k)));
-    h->grid[k] = per_sm * h->sm_count;   // upper bound; trimmed to the chunk count below
+    const int per_sm = std::max(1, h->tiles ? tiles_blocks_per_sm(k) : max_blocks_per_sm(kernel_for(h, k)));
+    h->grid[k] = per_sm * h->sm_count;   // upper bound; trimmed to the work count below
+  }
+  if (h->tiles) {
+    const int rc = build_tile_tables(h, items, maps, rank);
+    if (rc != HX_OK) return rc;
   }
 
-  for (int dir = 0; dir < 2; ++dir) {
+  for (int dir = 0; dir < 2 && !h->tiles; ++dir) {
     std::vector<Rec> recs;
     std::vector<std::vector<int>> item_recs(std::max(n_items, 1));   // chunk records of each item, in entry order
     auto add_part = [&](int t, int begin, int end, int halo_src, int stage, bool keep_empty) {
@@ -588,14 +805,20 @@ int build_tables(hx_ctx* h, cudaStream_t s) {
 
   // one flag (and one election counter) per item or per chunk, per direction
   h->n_flags = std::max<size_t>({static_cast<size_t>(std::max(n_items, 1)), static_cast<size_t>(h->n_chunks[0]),
-                                 static_cast<size_t>(h->n_chunks[1])});
+                                 static_cast<size_t>(h->n_chunks[1]), static_cast<size_t>(h->n_units[0]),
+                                 static_cast<size_t>(h->n_units[1])});
   HX_CUDA(dev_alloc(&h->d_flags, 2 * h->n_flags));
   HX_CUDA(dev_alloc(&h->d_blk, 2 * h->n_flags));
   HX_CUDA(dev_alloc(&h->d_ctrl, 2));
-  // Persistent grid: every warp co-resident, one warp per chunk at most.
+  // Persistent grid: every warp (tile mode: every block) co-resident, and no
+  // more of them than there is work.
   for (int k = 0; k < 2; ++k) {
-    const int warps = std::max(1, std::min(h->n_chunks[k], h->grid[k] * kWarps));
-    h->grid[k] = (warps + kWarps - 1) / kWarps;
+    if (h->tiles) {
+      h->grid[k] = std::max(1, std::min(h->n_units[k], h->grid[k]));
+    } else {
+      const int warps = std::max(1, std::min(h->n_chunks[k], h->grid[k] * kWarps));
+      h->grid[k] = (warps + kWarps - 1) / kWarps;
+    }
   }
   return reset_signals(h, s);
 }
@@ -809,7 +1032,7 @@ int build(hx_ctx* h, const float* pos, int64_t n, float* coords, int64_t capacit
   if (capacity < h->total_slots) return HX_ERR_CAPACITY;
   // 4. fill the caller's array: home coordinates, then one coordinate exchange
   HX_CUDA(launch_place_home(b.home_xyz, b.home_dom, b.home_start, b.dom_off, n, coords, s));
-  if (P > 0 && h->n_chunks[0] > 0) {
+  if (P > 0 && (h->tiles ? h->n_units[0] : h->n_chunks[0]) > 0) {
     rc = launch(h, 0, coords, s);
     if (rc != HX_OK) return rc;
   }
@@ -903,7 +1126,7 @@ int exchange(hx_handle h, float* buf, void* stream, int kind) {
   if (!h) return HX_ERR_ARG;
   if (!h->built) return HX_ERR_STATE;
   if (!buf && h->total_slots > 0) return HX_ERR_ARG;   // an empty layout touches no memory
-  if (h->pl.n_pulses == 0 || h->n_chunks[kind] == 0) return HX_OK;   // nothing moves
+  if (h->pl.n_pulses == 0 || (h->tiles ? h->n_units[kind] : h->n_chunks[kind]) == 0) return HX_OK;   // nothing moves
   const int rc = ensure_device(h);
   if (rc != HX_OK) return rc;
   return launch(h, kind, buf, static_cast<cudaStream_t>(stream));

@@ -97,6 +97,57 @@ int max_blocks_per_sm(const void* fn);
 cudaError_t launch_pack_pulse(float* x, const PulseParams& p, cudaStream_t s);
 cudaError_t launch_unpack_pulse(float* f, const PulseParams& p, cudaStream_t s);
 
+// ---- tile kernels (hx_tiles.cu) ----
+//
+// A tile is up to kTile consecutive slots of one domain's array, inside one
+// range (home, or the slots received in one pulse). Coordinates: a tile is a
+// source - the block loads it into shared memory once and serves the gathers
+// of every pulse that selects from it. Forces: a tile is a target - the block
+// loads it, adds every pulse's contributions in reverse pulse order in shared
+// memory, and writes it back.
+constexpr int kTile = 2048;
+
+struct alignas(16) TileUnit {
+  int64_t base;       // caller-array slot of the tile's first slot
+  int32_t n;          // slots in the tile
+  int32_t local_a;    // local index of the first slot within its domain
+  int32_t seg_off;    // this tile's segments in the direction's segment list
+  int32_t seg_cnt;
+  int32_t wait_off;   // producer tiles to wait for (positions in the list)
+  int32_t wait_cnt;
+  int32_t flags;      // kSignal; kHaloSrc = load with plain loads after the waits
+  int32_t item;       // pulse * n_domains + domain of its first segment (status, fault injection)
+  int32_t pad[6];
+};
+static_assert(sizeof(TileUnit) == 64, "tile record must stay 64 bytes");
+
+struct alignas(16) TileSeg {   // entries [map, map + n) of one (sender, pulse) map that fall in the tile
+  int64_t map;        // first entry in the maps array
+  int64_t other;      // receiver-side slot of that entry (coordinates: destination, forces: source)
+  int32_t n;
+  int32_t dim;
+  float shift;
+  int32_t do_shift;
+};
+static_assert(sizeof(TileSeg) == 32, "segment record must stay 32 bytes");
+
+struct TileParams {
+  const TileUnit* units;
+  const TileSeg* segs;
+  const Wait* waits;
+  const int32_t* maps;
+  unsigned long long* flags;  // per tile: epoch flag
+  Ctrl* ctrl;
+  unsigned long long n_units;
+  int direction;
+  int pad;
+  unsigned long long timeout_ns;
+};
+
+const void* tiles_kernel(int kind);   // 0 coordinates, 1 forces
+size_t tiles_smem_bytes();
+int tiles_blocks_per_sm(int kind);
+
 // ---- map builder (hx_build.cu) ----
 struct BuildTile {          // candidates [local_begin, local_begin + n) of one sender
   int32_t sender;

@@ -29,6 +29,7 @@ HX_FLAG_UNORDERED_FORCES = 0x1
 HX_FLAG_NO_GRAPH = 0x2
 HX_FLAG_COUNTER_SIGNAL = 0x4
 HX_FLAG_FINE_WAITS = 0x8
+HX_FLAG_TILES = 0x10
 
 HX_MAX_PULSES = 32
 

@@ -78,6 +78,10 @@ typedef struct hx_ctx* hx_handle;
                                           chunks that wrote the slots it reads or, for forces, that
                                           add into its targets, each signalled by its own epoch flag
                                           (HX_FLAG_COUNTER_SIGNAL is then ignored) */
+#define HX_FLAG_TILES 0x10u            /* tile-staged kernels: each block copies a tile of up to 2048
+                                          consecutive slots into shared memory (TMA bulk copy) and serves
+                                          every pulse's gathers (coordinates) or reverse-ordered adds
+                                          (forces) from it; per-tile signals; same results bit for bit */
 
 #define HX_MAX_PULSES 32
 #define HX_MAX_DOMAINS 4096

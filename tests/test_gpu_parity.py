@@ -17,7 +17,8 @@ pytestmark = pytest.mark.gpu
 
 ALL_MODES = [0, HX.HX_FLAG_COUNTER_SIGNAL, HX.HX_FLAG_NO_GRAPH,
              HX.HX_FLAG_COUNTER_SIGNAL | HX.HX_FLAG_NO_GRAPH, HX.HX_FLAG_FINE_WAITS,
-             HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_COUNTER_SIGNAL]
+             HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_COUNTER_SIGNAL, HX.HX_FLAG_TILES,
+             HX.HX_FLAG_TILES | HX.HX_FLAG_NO_GRAPH]
 
 
 def _bits(a):
@@ -116,7 +117,7 @@ def test_parity_configs(name, flags):
     check_force_steps(c)
 
 
-@pytest.mark.parametrize("flags", [0, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_COUNTER_SIGNAL])
+@pytest.mark.parametrize("flags", [0, HX.HX_FLAG_FINE_WAITS, HX.HX_FLAG_TILES])
 def test_parity_c5_full_size(flags):
     """12M atoms, 256 domains: the bench's configuration and launch path."""
     c = Case(W.WORKLOADS["C5"], flags=flags)
@@ -150,13 +151,40 @@ def test_unfused_baseline(name):
     ((3.0, 3.0, 3.0), (3, 3, 3), 0.6, 2700),      # 27 domains
     ((40.0, 3.0, 3.0), (40, 1, 1), 1.0, 36000),   # many small domains along one dim
 ])
-@pytest.mark.parametrize("flags", [0, HX.HX_FLAG_COUNTER_SIGNAL, HX.HX_FLAG_FINE_WAITS])
+@pytest.mark.parametrize("flags", [0, HX.HX_FLAG_COUNTER_SIGNAL, HX.HX_FLAG_FINE_WAITS, HX.HX_FLAG_TILES])
 def test_parity_shapes(box, dims, cutoff, n, flags):
     w = W.custom("shape", n, box, dims, cutoff, seed=7 + n)
     c = Case(w, flags=flags)
     check_build(c)
     check_coord_steps(c)
     check_force_steps(c)
+
+
+@pytest.mark.parametrize("flags", [0, HX.HX_FLAG_TILES])
+def test_misaligned_buffers(flags):
+    """Caller buffers that start 4 or 8 bytes past a 16-byte boundary (tile
+    mode copies aligned middles in bulk and the edges with plain loads)."""
+    w = W.WORKLOADS["C2"]
+    c = Case(w, flags=flags)
+    for shift in (1, 2, 3):
+        x = c.o.coords().copy()
+        hm = c.home_mask()
+        x[~hm] = np.nan
+        big = torch.zeros(x.size + 8, device="cuda")
+        xt = big[shift: shift + x.size].view(-1, 3)
+        xt.copy_(torch.from_numpy(x))
+        c.hx.exchange_coords(xt)
+        c.o.exchange_coords(x)
+        assert np.array_equal(_bits(xt.cpu().numpy()), _bits(x))
+        f = W.forces(w, c.o.total_slots)
+        fbig = torch.zeros(f.size + 8, device="cuda")
+        ft = fbig[shift: shift + f.size].view(-1, 3)
+        ft.copy_(torch.from_numpy(f))
+        c.hx.exchange_forces(ft)
+        ref = f.copy()
+        c.o.exchange_forces(ref)
+        assert np.array_equal(_bits(ft.cpu().numpy()), _bits(ref))
+    assert c.hx.status()[0] == 0
 
 
 def test_boundary_atoms():
@@ -172,7 +200,7 @@ def test_boundary_atoms():
 
 def test_many_steps_reuse_signals():
     """Epoch-valued signals are never reset between launches: 200 steps."""
-    for flags in (0, HX.HX_FLAG_COUNTER_SIGNAL):
+    for flags in (0, HX.HX_FLAG_COUNTER_SIGNAL, HX.HX_FLAG_FINE_WAITS, HX.HX_FLAG_TILES):
         c = Case(W.WORKLOADS["C2"], flags=flags)
         x = c.o.coords().copy()
         xt = torch.from_numpy(x).cuda()
@@ -248,7 +276,7 @@ def test_errors():
 
 
 @pytest.mark.parametrize("direction", [0, 1])
-@pytest.mark.parametrize("flags", [0, HX.HX_FLAG_COUNTER_SIGNAL, HX.HX_FLAG_FINE_WAITS])
+@pytest.mark.parametrize("flags", [0, HX.HX_FLAG_COUNTER_SIGNAL, HX.HX_FLAG_FINE_WAITS, HX.HX_FLAG_TILES])
 def test_dropped_signal_times_out_and_recovers(direction, flags):
     """Failure detection without a device fault: a (domain, pulse) that never
     signals makes its waiters give up after the bounded wait; the kernel
