@@ -49,14 +49,14 @@ def parse_args():
     ap.add_argument("--no-extras", action="store_true", help="skip the secondary measurements")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU baseline budget")
     ap.add_argument("--flags", default="fine",
-                    help="comma list of libhx modes: fine, counter, nograph, unordered, pages (= none)")
+                    help="comma list of libhx modes: fine, tiles, counter, nograph, unordered, pages (= none)")
     return ap.parse_args()
 
 
 def hx_flags(spec: str) -> int:
     from domain_decomposition_halo_gb300 import hx as HX
     table = {"fine": HX.HX_FLAG_FINE_WAITS, "counter": HX.HX_FLAG_COUNTER_SIGNAL, "nograph": HX.HX_FLAG_NO_GRAPH,
-             "unordered": HX.HX_FLAG_UNORDERED_FORCES, "pages": 0, "": 0}
+             "unordered": HX.HX_FLAG_UNORDERED_FORCES, "tiles": HX.HX_FLAG_TILES, "pages": 0, "": 0}
     flags = 0
     for name in spec.split(","):
         flags |= table[name.strip()]

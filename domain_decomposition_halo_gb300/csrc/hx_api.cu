@@ -219,7 +219,7 @@ TileParams tile_params(hx_ctx* h, int dir) {
   TileParams P;
   std::memset(&P, 0, sizeof(P));
   P.units = h->d_units[dir];
-  P.segs = h->d_segs[dir];
+  P.extra = h->d_segs[dir];
   P.waits = h->d_twaits[dir];
   P.maps = h->d_maps;
   P.flags = h->d_flags + static_cast<size_t>(dir) * h->n_flags;
@@ -244,7 +244,7 @@ int launch(hx_ctx* h, int kind, float* buf, cudaStream_t s) {
     args2[1] = &TP;
     args = args2;
     grid = dim3(static_cast<unsigned>(h->grid[kind]));
-    smem = tiles_smem_bytes();
+    smem = tiles_smem_bytes(kind);
     fn = tiles_kernel(kind);
   } else if (kind != 2) {
     P = dir_params(h, kind);
@@ -416,12 +416,34 @@ int build_tile_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::
           lo = h->t_off[tu];
           len = h->t_size[tu];
         }
-        for (int a = lo; a < lo + len; a += kTile) {
+        // entries of every map of r that fall in slots [a, b)
+        auto entries_in = [&](int a, int b) {
+          int e = 0;
+          for (int p = 0; p < P; ++p) {
+            const ItemInfo& it = items[p * nd + r];
+            if (it.size == 0) continue;
+            const int32_t* m = maps.data() + it.map;
+            e += static_cast<int>(std::lower_bound(m, m + it.size, b) - std::lower_bound(m, m + it.size, a));
+          }
+          return e;
+        };
+        for (int a = lo, b = lo; a < lo + len; a = b) {
+          // at most kTile slots and kTileEntries entries (a slot has at most one entry per pulse)
+          b = std::min(lo + len, a + kTile);
+          if (entries_in(a, b) > kTileEntries) {
+            int good = a + 1, bad = b;
+            while (bad - good > 1) {
+              const int mid = good + (bad - good) / 2;
+              if (entries_in(a, mid) <= kTileEntries) good = mid;
+              else bad = mid;
+            }
+            b = good;
+          }
           TRec t;
           t.r = r;
           t.range = rg;
           t.a = a;
-          t.n = std::min(kTile, lo + len - a);
+          t.n = b - a;
           for (int k = 0; k < P; ++k) {
             const int p = dir == 0 ? k : P - 1 - k;
             const ItemInfo& it = items[p * nd + r];
@@ -500,7 +522,7 @@ int build_tile_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::
       const long long window = h->grid[dir];
       std::vector<Rec> ord(recs.size());
       for (size_t k = 0; k < base.size(); ++k) {
-        ord[base[k]].key = static_cast<long long>(k) + window * recs[base[k]].stage;
+        ord[base[k]].key = static_cast<long long>(k) + 3 * window * recs[base[k]].stage;
         recs[base[k]].key = ord[base[k]].key;
       }
       for (size_t i = 0; i < recs.size(); ++i) ord[i].deps = recs[i].deps;
@@ -512,8 +534,9 @@ int build_tile_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::
       for (auto& t : recs)
         for (int d : t.deps) waited[d] = 1;
       std::vector<TileUnit> units;
-      std::vector<TileSeg> segs;
+      std::vector<TileSeg> segs;   // segments past kInlineSegs
       std::vector<Wait> waits;
+      const int tile_bytes = kTile * 12 + 16, map_bytes = kTileEntries * 4 + 32 * kTileSegs;
       for (int i : order) {
         const TRec& t = recs[i];
         TileUnit u;
@@ -521,14 +544,25 @@ int build_tile_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::
         u.base = h->dom_offset[t.r] + t.a;
         u.n = t.n;
         u.local_a = t.a;
-        u.seg_off = static_cast<int32_t>(segs.size());
         u.seg_cnt = static_cast<int32_t>(t.segs.size());
-        segs.insert(segs.end(), t.segs.begin(), t.segs.end());
+        u.extra_off = static_cast<int32_t>(segs.size());
+        // stage regions: each run's region starts on a 16-byte boundary and is 16 bytes longer than the run
+        int moff = tile_bytes, soff = tile_bytes + map_bytes;
+        for (size_t k = 0; k < t.segs.size(); ++k) {
+          TileSeg sg = t.segs[k];
+          sg.map_off = moff;
+          sg.src_off = dir == 1 ? soff : 0;
+          moff += ((4 * sg.n + 15) & ~15) + 16;
+          soff += ((12 * sg.n + 15) & ~15) + 16;
+          if (static_cast<int>(k) < kInlineSegs) u.seg[k] = sg;
+          else segs.push_back(sg);
+        }
         u.wait_off = static_cast<int32_t>(waits.size());
         u.wait_cnt = static_cast<int32_t>(t.deps.size());
         for (int d : t.deps) waits.push_back({pos[d], 1});
         u.flags = (waited[i] ? kSignal : 0) | (dir == 0 && t.range >= 0 ? kHaloSrc : 0);
         u.item = t.seg_pulse[0] * nd + t.r;
+        for (const TileSeg& sg : t.segs) u.entries += sg.n;
         units.push_back(u);
       }
       h->n_units[dir] = static_cast<int>(units.size());

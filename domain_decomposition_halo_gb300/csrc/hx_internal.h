@@ -105,21 +105,10 @@ cudaError_t launch_unpack_pulse(float* f, const PulseParams& p, cudaStream_t s);
 // of every pulse that selects from it. Forces: a tile is a target - the block
 // loads it, adds every pulse's contributions in reverse pulse order in shared
 // memory, and writes it back.
-constexpr int kTile = 2048;
-
-struct alignas(16) TileUnit {
-  int64_t base;       // caller-array slot of the tile's first slot
-  int32_t n;          // slots in the tile
-  int32_t local_a;    // local index of the first slot within its domain
-  int32_t seg_off;    // this tile's segments in the direction's segment list
-  int32_t seg_cnt;
-  int32_t wait_off;   // producer tiles to wait for (positions in the list)
-  int32_t wait_cnt;
-  int32_t flags;      // kSignal; kHaloSrc = load with plain loads after the waits
-  int32_t item;       // pulse * n_domains + domain of its first segment (status, fault injection)
-  int32_t pad[6];
-};
-static_assert(sizeof(TileUnit) == 64, "tile record must stay 64 bytes");
+constexpr int kTile = 1024;          // slots per tile at most
+constexpr int kTileEntries = 1024;   // map entries per tile at most (all segments together)
+constexpr int kTileSegs = 32;        // segments per tile at most (one per pulse)
+constexpr int kInlineSegs = 4;       // segments carried inside the tile record
 
 struct alignas(16) TileSeg {   // entries [map, map + n) of one (sender, pulse) map that fall in the tile
   int64_t map;        // first entry in the maps array
@@ -128,12 +117,31 @@ struct alignas(16) TileSeg {   // entries [map, map + n) of one (sender, pulse) 
   int32_t dim;
   float shift;
   int32_t do_shift;
+  int32_t map_off;    // stage byte offset of the region the map run is copied to
+  int32_t src_off;    // stage byte offset of the region the received-force run is copied to
+  int32_t pad[2];
 };
-static_assert(sizeof(TileSeg) == 32, "segment record must stay 32 bytes");
+static_assert(sizeof(TileSeg) == 48, "segment record must stay 48 bytes");
+
+struct alignas(16) TileUnit {  // one 256-byte record, read by 16 threads in one round trip
+  int64_t base;       // caller-array slot of the tile's first slot
+  int32_t n;          // slots in the tile
+  int32_t local_a;    // local index of the first slot within its domain
+  int32_t seg_cnt;
+  int32_t extra_off;  // segments past kInlineSegs in the direction's overflow list
+  int32_t wait_off;   // producer tiles to wait for (positions in the list)
+  int32_t wait_cnt;
+  int32_t flags;      // kSignal; kHaloSrc = slots written earlier in the same launch
+  int32_t item;       // pulse * n_domains + domain of its first segment (status, fault injection)
+  int32_t entries;    // entries of all segments
+  int32_t pad[5];
+  TileSeg seg[kInlineSegs];
+};
+static_assert(sizeof(TileUnit) == 256, "tile record must stay 256 bytes");
 
 struct TileParams {
   const TileUnit* units;
-  const TileSeg* segs;
+  const TileSeg* extra;       // segments past kInlineSegs
   const Wait* waits;
   const int32_t* maps;
   unsigned long long* flags;  // per tile: epoch flag
@@ -145,7 +153,7 @@ struct TileParams {
 };
 
 const void* tiles_kernel(int kind);   // 0 coordinates, 1 forces
-size_t tiles_smem_bytes();
+size_t tiles_smem_bytes(int kind);
 int tiles_blocks_per_sm(int kind);
 
 // ---- map builder (hx_build.cu) ----
