@@ -1076,6 +1076,47 @@ int build(hx_ctx* h, const float* pos, int64_t n, float* coords, int64_t capacit
 
 }  // namespace
 
+// ------------------------------------------------------------------ scratch-free launch
+
+int hx::handle_device(const hx_ctx* h) { return h->device; }
+
+int hx::launch_coords_with_scratch(hx_ctx* h, float* coords, cudaStream_t s, Ctrl* ctrl,
+                                   unsigned long long* flags, unsigned int* arrivals, size_t max_flags) {
+  if (!h->built) return HX_ERR_STATE;
+  if (!coords && h->total_slots > 0) return HX_ERR_ARG;
+  const int work = h->tiles ? h->n_units[0] : h->n_chunks[0];
+  if (h->pl.n_pulses == 0 || work == 0) return HX_OK;
+  // flags are indexed by item (pulse signals) or by list position (chunk / tile signals)
+  const size_t need = std::max<size_t>(static_cast<size_t>(h->pl.n_pulses) * h->pl.ndom, static_cast<size_t>(work));
+  if (need > max_flags) return HX_ERR_CAPACITY;
+  HX_CUDA(cudaMemsetAsync(ctrl, 0, sizeof(Ctrl), s));
+  HX_CUDA(cudaMemsetAsync(&ctrl->drop_item, 0xff, sizeof(int), s));   // -1: no fault injection
+  HX_CUDA(cudaMemsetAsync(flags, 0, sizeof(unsigned long long) * need, s));
+  HX_CUDA(cudaMemsetAsync(arrivals, 0, sizeof(unsigned int) * need, s));
+  void* args[2];
+  DirParams P;
+  TileParams TP;
+  const void* fn;
+  size_t smem = 0;
+  args[0] = &coords;
+  if (h->tiles) {
+    TP = tile_params(h, 0);
+    TP.flags = flags;
+    TP.ctrl = ctrl;
+    args[1] = &TP;
+    fn = tiles_kernel(0);
+    smem = tiles_smem_bytes(0);
+  } else {
+    P = dir_params(h, 0);
+    P.flags = flags;
+    P.arrivals = arrivals;
+    P.ctrl = ctrl;
+    args[1] = &P;
+    fn = kernel_for(h, 0);
+  }
+  return to_err(cudaLaunchKernel(fn, dim3(static_cast<unsigned>(h->grid[0])), dim3(kThreads), args, smem, s));
+}
+
 // ------------------------------------------------------------------ C ABI
 
 extern "C" {

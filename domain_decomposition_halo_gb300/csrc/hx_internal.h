@@ -4,6 +4,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+struct hx_ctx;
+
 namespace hx {
 
 #ifndef HX_ROUNDS
@@ -155,6 +157,15 @@ struct TileParams {
 const void* tiles_kernel(int kind);   // 0 coordinates, 1 forces
 size_t tiles_smem_bytes(int kind);
 int tiles_blocks_per_sm(int kind);
+
+// ---- launch with caller-independent scratch (hx_api.cu, for hx_noalloc.cu) ----
+// Runs the handle's fused coordinate exchange with its signal flags, election
+// counters and control block at the given device addresses instead of the
+// handle's own; clears them first on `s`. No allocation. HX_ERR_CAPACITY when
+// the handle's work list needs more than `max_flags` flags.
+int launch_coords_with_scratch(hx_ctx* h, float* coords, cudaStream_t s, Ctrl* ctrl, unsigned long long* flags,
+                               unsigned int* arrivals, size_t max_flags);
+int handle_device(const hx_ctx* h);
 
 // ---- map builder (hx_build.cu) ----
 struct BuildTile {          // candidates [local_begin, local_begin + n) of one sender

@@ -47,6 +47,7 @@ SIGNATURES = {
     "hx_exchange_forces": (_I, [_P, _P, _P]),
     "hx_exchange_coords_unfused": (_I, [_P, _P, _P]),
     "hx_exchange_forces_unfused": (_I, [_P, _P, _P]),
+    "hx_exchange_coords_static": (_I, [_P, _P, _P]),
     "hx_noop": (_I, [_P, _P]),
     "hx_status": (_I, [_P, _P, _P]),
     "hx_clear_status": (_I, [_P, _P]),
@@ -230,6 +231,13 @@ class HaloExchange:
         self._check_tensor(forces, 3 * self.total_slots, "forces")
         _check(self._lib.hx_exchange_forces_unfused(self._h, forces.data_ptr(), _stream_ptr(stream)),
                "hx_exchange_forces_unfused")
+
+    def exchange_coords_static(self, coords, stream=None) -> None:
+        """hx_exchange_coords without any device allocation: for callers that
+        must not allocate while they run (see include/hx.h)."""
+        self._check_tensor(coords, 3 * self.total_slots, "coords")
+        _check(self._lib.hx_exchange_coords_static(self._h, coords.data_ptr(), _stream_ptr(stream)),
+               "hx_exchange_coords_static")
 
     def noop(self, stream=None) -> None:
         _check(self._lib.hx_noop(self._h, _stream_ptr(stream)), "hx_noop")

@@ -170,6 +170,27 @@ int hx_exchange_forces(hx_handle h, float* forces, void* stream);
 int hx_exchange_coords_unfused(hx_handle h, float* coords, void* stream);
 int hx_exchange_forces_unfused(hx_handle h, float* forces, void* stream);
 
+/* Same as hx_exchange_coords, for callers that must not allocate device
+ * memory while they run (an engine that reserves all GPU memory for its own
+ * arena, or code that may only use memory it has accounted for). The pages
+ * have no counterpart: this concerns how the library holds its scratch.
+ * The call never allocates: the kernel's signal flags, election counters and
+ * control block live in one fixed file-scope device array of
+ * HX_STATIC_MAX_FLAGS flags (about 384 KB, held by every GPU that loads the
+ * library until the process exits), cleared on `stream` at each call, and
+ * the kernel is launched directly, without a CUDA graph. The first call on a
+ * device looks up that array's device address (cudaGetSymbolAddress); make
+ * that first call before any stream capture. All calls share the one array,
+ * so calls whose work overlaps on the GPU (other streams, other handles on
+ * the same device) race: serialise them. Device-side time-outs of this call
+ * are recorded in that array, not in the handle (hx_status does not see
+ * them). Errors: HX_ERR_ARG, HX_ERR_STATE, HX_ERR_CUDA, and HX_ERR_CAPACITY
+ * when the handle's work list needs more than HX_STATIC_MAX_FLAGS signal
+ * flags (its item count, chunk count or tile count, whichever it signals by);
+ * nothing is launched then. */
+#define HX_STATIC_MAX_FLAGS 32768
+int hx_exchange_coords_static(hx_handle h, float* coords, void* stream);
+
 /* Launches one empty kernel the way the fused exchanges are launched (graph
  * or direct, per the handle's flags): the launch floor for latency
  * measurements. */
