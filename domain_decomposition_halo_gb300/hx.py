@@ -107,11 +107,18 @@ def query_plan(box, dims, cutoff: float) -> Tuple[np.ndarray, np.ndarray]:
     return pd[: n.value].copy(), pk[: n.value].copy()
 
 
-def _stream_ptr(stream) -> Optional[int]:
-    import torch
+def _stream_ptr(stream, device: int = 0) -> Optional[int]:
     if stream is None:
-        stream = torch.cuda.current_stream()
+        return _current_raw_stream(device)
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _current_raw_stream(device: int) -> int:
+    import torch
+    raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+    if raw is not None:
+        return raw(device)
+    return torch.cuda.current_stream(device).cuda_stream
 
 
 class HaloExchange:
@@ -125,6 +132,9 @@ class HaloExchange:
         _check(self._lib.hx_init(ctypes.byref(h), b.ctypes.data, d.ctypes.data, float(cutoff), int(device),
                                  int(flags), int(timeout_us)), "hx_init")
         self._h = h
+        self._hv = h.value
+        self._fn = {name: getattr(self._lib, name) for name in SIGNATURES}
+        self._validated = {}   # argument name -> (id, data_ptr, numel) of the last tensor that passed the checks
         self.device = int(device)
         self.box = tuple(float(v) for v in box)
         self.dims = tuple(int(v) for v in dims)
@@ -138,6 +148,8 @@ class HaloExchange:
         if getattr(self, "_h", None) is not None and self._h.value:
             self._lib.hx_destroy(self._h)
         self._h = None
+        self._hv = None
+        self._validated = {}
 
     def __del__(self):
         try:
@@ -173,7 +185,7 @@ class HaloExchange:
             self._check_tensor(coords, 0, "coords")
         rc = self._lib.hx_build_maps(self._h, pos.data_ptr() if n else None, n,
                                      coords.data_ptr() if coords is not None else None, cap,
-                                     ctypes.byref(needed), _stream_ptr(stream))
+                                     ctypes.byref(needed), _stream_ptr(stream, self.device))
         if rc not in (HX_OK, HX_ERR_CAPACITY) or (rc == HX_ERR_CAPACITY and coords is not None):
             _check(rc, "hx_build_maps")
         self.n_atoms = n
@@ -202,7 +214,7 @@ class HaloExchange:
             out = torch.empty(max(self.n_atoms, 1), dtype=torch.int32, device=f"cuda:{self.device}")[: self.n_atoms]
         if self.n_atoms:
             self._check_tensor(out, self.n_atoms, "home_ids", torch.int32)
-        _check(self._lib.hx_get_home_ids(self._h, out.data_ptr() if self.n_atoms else None, _stream_ptr(stream)),
+        _check(self._lib.hx_get_home_ids(self._h, out.data_ptr() if self.n_atoms else None, _stream_ptr(stream, self.device)),
                "hx_get_home_ids")
         return out
 
@@ -214,42 +226,59 @@ class HaloExchange:
         return m[:te], table[: npl * nd].reshape(npl, nd, 6)
 
     # ------------------------------------------------------------ per step
+    def _step_ptr(self, t, what: str) -> int:
+        """Data pointer of a per-step buffer. The full checks run once per
+        tensor object and storage; later calls with the same tensor only
+        compare its pointer and size."""
+        ptr = t.data_ptr()
+        key = (id(t), ptr, t.numel(), self.total_slots)
+        if self._validated.get(what) != key:
+            self._check_tensor(t, 3 * self.total_slots, what)
+            self._validated[what] = key
+        return ptr
+
     def exchange_coords(self, coords, stream=None) -> None:
-        self._check_tensor(coords, 3 * self.total_slots, "coords")
-        _check(self._lib.hx_exchange_coords(self._h, coords.data_ptr(), _stream_ptr(stream)), "hx_exchange_coords")
+        rc = self._fn["hx_exchange_coords"](self._hv, self._step_ptr(coords, "coords"),
+                                            _stream_ptr(stream, self.device))
+        if rc:
+            _check(rc, "hx_exchange_coords")
 
     def exchange_forces(self, forces, stream=None) -> None:
-        self._check_tensor(forces, 3 * self.total_slots, "forces")
-        _check(self._lib.hx_exchange_forces(self._h, forces.data_ptr(), _stream_ptr(stream)), "hx_exchange_forces")
+        rc = self._fn["hx_exchange_forces"](self._hv, self._step_ptr(forces, "forces"),
+                                            _stream_ptr(stream, self.device))
+        if rc:
+            _check(rc, "hx_exchange_forces")
 
     def exchange_coords_unfused(self, coords, stream=None) -> None:
         self._check_tensor(coords, 3 * self.total_slots, "coords")
-        _check(self._lib.hx_exchange_coords_unfused(self._h, coords.data_ptr(), _stream_ptr(stream)),
+        _check(self._lib.hx_exchange_coords_unfused(self._h, coords.data_ptr(), _stream_ptr(stream, self.device)),
                "hx_exchange_coords_unfused")
 
     def exchange_forces_unfused(self, forces, stream=None) -> None:
         self._check_tensor(forces, 3 * self.total_slots, "forces")
-        _check(self._lib.hx_exchange_forces_unfused(self._h, forces.data_ptr(), _stream_ptr(stream)),
+        _check(self._lib.hx_exchange_forces_unfused(self._h, forces.data_ptr(), _stream_ptr(stream, self.device)),
                "hx_exchange_forces_unfused")
 
     def exchange_coords_static(self, coords, stream=None) -> None:
         """hx_exchange_coords without any device allocation: for callers that
         must not allocate while they run (see include/hx.h)."""
         self._check_tensor(coords, 3 * self.total_slots, "coords")
-        _check(self._lib.hx_exchange_coords_static(self._h, coords.data_ptr(), _stream_ptr(stream)),
+        _check(self._lib.hx_exchange_coords_static(self._h, coords.data_ptr(), _stream_ptr(stream, self.device)),
                "hx_exchange_coords_static")
 
     def noop(self, stream=None) -> None:
-        _check(self._lib.hx_noop(self._h, _stream_ptr(stream)), "hx_noop")
+        rc = self._fn["hx_noop"](self._hv, _stream_ptr(stream, self.device))
+        if rc:
+            _check(rc, "hx_noop")
 
     # ------------------------------------------------------------ status
     def status(self, stream=None) -> Tuple[int, int]:
         detail = ctypes.c_int(-1)
-        rc = self._lib.hx_status(self._h, _stream_ptr(stream), ctypes.byref(detail))
+        rc = self._lib.hx_status(self._h, _stream_ptr(stream, self.device), ctypes.byref(detail))
         return rc, detail.value
 
     def clear_status(self, stream=None) -> None:
-        _check(self._lib.hx_clear_status(self._h, _stream_ptr(stream)), "hx_clear_status")
+        _check(self._lib.hx_clear_status(self._h, _stream_ptr(stream, self.device)), "hx_clear_status")
 
     def debug_drop_signal(self, direction: int, domain: int, pulse: int = 0) -> None:
         _check(self._lib.hx_debug_drop_signal(self._h, int(direction), int(domain), int(pulse)),
