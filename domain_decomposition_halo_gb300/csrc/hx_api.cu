@@ -12,6 +12,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <new>
+#include <thread>
 #include <vector>
 
 #include "hx.h"
@@ -93,6 +94,49 @@ int make_plan(const double box[3], const int dims[3], double cutoff, Plan* pl) {
   }
   pl->n_pulses = p;
   return HX_OK;
+}
+
+// The home cell min(n-1, floor((double)x * n / L)) of an fp32 position.
+int home_cell(float x, int n, double L) {
+  const int c = static_cast<int>(std::floor(static_cast<double>(x) * static_cast<double>(n) / L));
+  return c > n - 1 ? n - 1 : c;
+}
+
+float float_of_bits(uint32_t b) {
+  float f;
+  std::memcpy(&f, &b, sizeof(f));
+  return f;
+}
+
+// Smallest non-negative fp32 (by bit pattern, which orders them) for which
+// pred holds; pred must be monotone and hold at `hi`.
+template <class Pred>
+float smallest_float(Pred pred, uint32_t hi) {
+  uint32_t lo = 0;
+  if (pred(float_of_bits(0))) return 0.0f;
+  while (hi - lo > 1) {
+    const uint32_t mid = lo + (hi - lo) / 2;
+    if (pred(float_of_bits(mid))) hi = mid;
+    else lo = mid;
+  }
+  return float_of_bits(hi);
+}
+
+// Per dimension: the first fp32 at or above L, then the first fp32 of cells
+// 1 .. n-1 (the face tables of k_cells).
+std::vector<float> face_tables(const Plan& pl) {
+  std::vector<float> out;
+  for (int d = 0; d < 3; ++d) {
+    const double L = pl.box[d];
+    const int n = pl.dims[d];
+    const float limit = smallest_float([&](float x) { return static_cast<double>(x) >= L; }, 0x7f800000u);
+    out.push_back(limit);
+    uint32_t limit_bits;
+    std::memcpy(&limit_bits, &limit, sizeof(limit_bits));
+    for (int c = 1; c < n; ++c)
+      out.push_back(smallest_float([&](float x) { return home_cell(x, n, L) >= c; }, limit_bits));
+  }
+  return out;
 }
 
 void cell_of(const Plan& pl, int r, int c[3]) {
@@ -311,6 +355,25 @@ int reset_signals(hx_ctx* h, cudaStream_t s) {
 // consumer one resident-warp window behind its producers. A domain's slots
 // are then fetched into L2 about once per launch, and a waiting chunk finds
 // its producers mostly done.
+
+// Runs body(i) for i in [0, n) on the host's cores (iterations must be
+// independent).
+template <class Body>
+void parallel_for(size_t n, Body body) {
+  const size_t hw = std::max<size_t>(1, std::min<size_t>(16, std::thread::hardware_concurrency()));
+  const size_t workers = std::min(hw, std::max<size_t>(1, n / 256));
+  if (workers <= 1) {
+    for (size_t i = 0; i < n; ++i) body(i);
+    return;
+  }
+  std::vector<std::thread> pool;
+  pool.reserve(workers);
+  for (size_t w = 0; w < workers; ++w)
+    pool.emplace_back([&, w] {
+      for (size_t i = w; i < n; i += workers) body(i);
+    });
+  for (auto& t : pool) t.join();
+}
 
 struct ItemInfo {
   int r, p, q;           // sender, pulse, receiver
@@ -608,7 +671,10 @@ int build_tables(hx_ctx* h, cudaStream_t s) {
     maps.resize(h->total_entries);
     HX_CUDA(cudaMemcpy(maps.data(), h->d_maps, sizeof(int32_t) * h->total_entries, cudaMemcpyDeviceToHost));
   }
-  auto upper = [&](int r, int q) { return neighbour(pl, r, pl.pulse_dim[q], +1); };
+  std::vector<int> upper_tab(static_cast<size_t>(nd) * std::max(P, 1));
+  for (int r = 0; r < nd; ++r)
+    for (int q = 0; q < P; ++q) upper_tab[static_cast<size_t>(r) * P + q] = neighbour(pl, r, pl.pulse_dim[q], +1);
+  auto upper = [&](int r, int q) { return upper_tab[static_cast<size_t>(r) * P + q]; };
   std::vector<int64_t> rank(nd);
   for (int r = 0; r < nd; ++r) rank[r] = domain_rank(pl, r);
   h->tiles = (h->flags & HX_FLAG_TILES) != 0;
@@ -678,28 +744,36 @@ int build_tables(hx_ctx* h, cudaStream_t s) {
           add_part(t, 0, it.size, 1, P - 1 - p, it.size == 0 && coarse_waited[t]);
         }
       }
-    // waits
-    for (size_t ci = 0; ci < recs.size(); ++ci) {
+    // waits (records are independent: spread over the host's cores)
+    parallel_for(recs.size(), [&](size_t ci) {
       Rec& rc = recs[ci];
       const ItemInfo& it = items[rc.item];
       const int r = it.r, p = it.p;
       if (dir == 0) {
-        if (!rc.halo_src) continue;
+        if (!rc.halo_src) return;
         if (!fine) {
           for (int q = 0; q < p; ++q) rc.wait.push_back(q * nd + upper(r, q));
-          continue;
+          return;
         }
-        // producers: chunks of (upper(r, q), q) that stored the slots read here
+        // producers: chunks of (upper(r, q), q) that stored the slots read
+        // here. The entries ascend, r's receive ranges follow pulse order, and
+        // an item's records follow entry order, so both cursors only move on.
         const int32_t* m = maps.data() + it.map;
+        int q = 0, k = 0;
         for (int i = rc.begin; i < rc.end; ++i) {
-          for (int q = 0; q < p; ++q) {
+          while (q < p) {
             const int tq = q * nd + upper(r, q);
-            const int64_t lo = h->t_off[tq], n = items[tq].size;
-            if (m[i] >= lo && m[i] < lo + n) {
-              rc.wait.push_back(rec_of_entry(tq, static_cast<int>(m[i] - lo)));
-              break;
-            }
+            if (m[i] < h->t_off[tq] + items[tq].size) break;
+            ++q;
+            k = 0;
           }
+          if (q >= p) break;
+          const int tq = q * nd + upper(r, q);
+          const int64_t e = m[i] - h->t_off[tq];
+          if (e < 0) continue;   // a home slot (cannot occur in a forwarded tail)
+          const std::vector<int>& v = item_recs[tq];
+          while (k + 1 < static_cast<int>(v.size()) && recs[v[k + 1]].begin <= e) ++k;
+          if (rc.wait.empty() || rc.wait.back() != v[k]) rc.wait.push_back(v[k]);
         }
       } else {
         if (!fine) {
@@ -707,9 +781,11 @@ int build_tables(hx_ctx* h, cudaStream_t s) {
             rc.wait.push_back(pp * nd + it.q);
             if (ordered && it.q != r) rc.wait.push_back(pp * nd + r);
           }
-          continue;
+          std::sort(rc.wait.begin(), rc.wait.end());
+          rc.wait.erase(std::unique(rc.wait.begin(), rc.wait.end()), rc.wait.end());
+          return;
         }
-        if (rc.end <= rc.begin) continue;
+        if (rc.end <= rc.begin) return;
         const int32_t* m = maps.data() + it.map;
         const int64_t slot_lo = h->t_off[rc.item] + rc.begin, slot_hi = h->t_off[rc.item] + rc.end;
         for (int pp = p + 1; pp < P; ++pp) {
@@ -729,15 +805,23 @@ int build_tables(hx_ctx* h, cudaStream_t s) {
           const int32_t* mr = maps.data() + items[tr].map;
           const int nr = items[tr].size;
           int k = static_cast<int>(std::lower_bound(mr, mr + nr, m[rc.begin]) - mr);
+          if (k >= nr) continue;
+          const std::vector<int>& v = item_recs[tr];
+          int rec = 0;
+          const int first = rec_of_entry(tr, k);
+          while (v[rec] != first) ++rec;
           for (int i = rc.begin; i < rc.end && k < nr; ++i) {
             while (k < nr && mr[k] < m[i]) ++k;
-            if (k < nr && mr[k] == m[i]) rc.wait.push_back(rec_of_entry(tr, k));
+            if (k < nr && mr[k] == m[i]) {
+              while (rec + 1 < static_cast<int>(v.size()) && recs[v[rec + 1]].begin <= k) ++rec;
+              if (rc.wait.empty() || rc.wait.back() != v[rec]) rc.wait.push_back(v[rec]);
+            }
           }
         }
       }
       std::sort(rc.wait.begin(), rc.wait.end());
       rc.wait.erase(std::unique(rc.wait.begin(), rc.wait.end()), rc.wait.end());
-    }
+    });
     // listing dependencies (chunk records) and who gets signalled
     std::vector<char> rec_waited(recs.size(), 0), item_waited(std::max(n_items, 1), 0);
     for (auto& rc : recs) {
@@ -859,6 +943,7 @@ int build_tables(hx_ctx* h, cudaStream_t s) {
 
 struct BuildScratch {
   int32_t* dom_id = nullptr;
+  float* faces = nullptr;
   int32_t* hist = nullptr;
   int32_t* hist_scan = nullptr;
   int* err = nullptr;
@@ -873,7 +958,7 @@ struct BuildScratch {
   std::vector<float*> recv;     // per pulse: received coordinates, sender-major
   std::vector<int32_t*> maps;   // per pulse: maps, sender-major
   ~BuildScratch() {
-    dev_free(dom_id); dev_free(hist); dev_free(hist_scan); dev_free(err); dev_free(home_xyz);
+    dev_free(dom_id); dev_free(faces); dev_free(hist); dev_free(hist_scan); dev_free(err); dev_free(home_xyz);
     dev_free(home_dom); dev_free(home_start); dev_free(dom_off); dev_free(tiles); dev_free(tile_cnt);
     dev_free(tile_off); dev_free(bufs);
     for (auto* p : recv) dev_free(p);
@@ -895,7 +980,10 @@ int build(hx_ctx* h, const float* pos, int64_t n, float* coords, int64_t capacit
   HX_CUDA(dev_alloc(&b.home_dom, n));
   HX_CUDA(dev_alloc(&h->d_home_ids, n));
   HX_CUDA(cudaMemsetAsync(b.err, 0, sizeof(int), s));
-  HX_CUDA(launch_cells(pos, n, pl.dims, pl.box, nd, b.dom_id, b.hist, ntiles, b.err, s));
+  const std::vector<float> faces = face_tables(pl);
+  HX_CUDA(dev_alloc(&b.faces, faces.size()));
+  HX_CUDA(cudaMemcpyAsync(b.faces, faces.data(), sizeof(float) * faces.size(), cudaMemcpyHostToDevice, s));
+  HX_CUDA(launch_cells(pos, n, pl.dims, b.faces, nd, b.dom_id, b.hist, ntiles, b.err, s));
   HX_CUDA(scan_exclusive(b.hist, b.hist_scan, static_cast<int64_t>(nd) * ntiles, s));
   std::vector<int32_t> first(nd, 0);
   if (ntiles > 0)

@@ -11,8 +11,10 @@
 //      of "Enabling parallelism across pulses through kernel fusion" needs),
 //      together with the shifted coordinates the receiver gets, which later
 //      pulses read as their forwarded candidates.
-// All selection decisions are one fp32 subtraction and a strict compare, the
-// home cell one fp64 multiply, divide and floor, so they are bit-reproducible.
+// All selection decisions are one fp32 subtraction and a strict compare; the
+// home cell is the fp64 floor of x * n / L, found by fp32 compares against
+// face tables the host derives from that expression, so both are
+// bit-reproducible.
 #include <cstdint>
 
 #include "hx_internal.h"
@@ -23,16 +25,27 @@ namespace {
 constexpr int kScanBlock = 2048;   // elements per scan block (256 threads x 8)
 constexpr unsigned kFull = 0xffffffffu;
 
-struct Geometry {
-  double box[3];
+// Home cells by comparison against per-dimension face tables: faces[off[d]]
+// is the smallest fp32 value whose fp64 widening reaches L_d (positions at or
+// above it are out of range), faces[off[d] + c] (c = 1 .. n_d-1) the smallest
+// fp32 x with min(n_d-1, floor((double)x * n_d / L_d)) >= c. That cell
+// function is monotone in x, so counting the faces at or below x gives
+// exactly the cell the fp64 expression gives, with fp32 compares only.
+struct FaceTables {
   int dims[3];
+  int off[3];
+  int total;
 };
 
-__global__ void __launch_bounds__(256) k_cells(const float* __restrict__ pos, int64_t n, Geometry g,
-                                               int ndom, int32_t* __restrict__ dom_id,
-                                               int32_t* __restrict__ hist, int ntiles, int* err) {
-  extern __shared__ int s_hist[];
+__global__ void __launch_bounds__(256) k_cells(const float* __restrict__ pos, int64_t n, FaceTables g,
+                                               const float* __restrict__ faces, int ndom,
+                                               int32_t* __restrict__ dom_id, int32_t* __restrict__ hist,
+                                               int ntiles, int* err) {
+  extern __shared__ int s_mem[];
+  int* s_hist = s_mem;
+  float* s_face = reinterpret_cast<float*>(s_mem + ndom);
   for (int d = threadIdx.x; d < ndom; d += blockDim.x) s_hist[d] = 0;
+  for (int k = threadIdx.x; k < g.total; k += blockDim.x) s_face[k] = faces[k];
   __syncthreads();
   const int64_t tile_start = static_cast<int64_t>(blockIdx.x) * kPartTile;
   for (int k = 0; k < kPartTile / 256; ++k) {
@@ -42,12 +55,16 @@ __global__ void __launch_bounds__(256) k_cells(const float* __restrict__ pos, in
     bool ok = true;
 #pragma unroll
     for (int d = 0; d < 3; ++d) {
-      const double x = static_cast<double>(pos[3 * i + d]);
-      ok = ok && (x >= 0.0 && x < g.box[d]);
-      // floor(x * n / L) in fp64: x * n is exact for an fp32 x and a small n
-      int cd = static_cast<int>(floor(__ddiv_rn(x * static_cast<double>(g.dims[d]), g.box[d])));
-      cd = cd < 0 ? 0 : (cd > g.dims[d] - 1 ? g.dims[d] - 1 : cd);
-      c[d] = cd;
+      const float x = pos[3 * i + d];
+      const float* f = s_face + g.off[d];
+      ok = ok && (x >= 0.0f && x < f[0]);   // NaN fails both
+      int lo = 0, hi = g.dims[d] - 1;       // cell = number of faces f[1..n-1] at or below x
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (f[mid] <= x) lo = mid;
+        else hi = mid - 1;
+      }
+      c[d] = lo;
     }
     if (!ok) atomicOr(err, 1);
     const int r = c[0] + g.dims[0] * (c[1] + g.dims[1] * c[2]);
@@ -235,20 +252,23 @@ __global__ void k_place_home(const float* __restrict__ home_xyz, const int32_t* 
 
 }  // namespace
 
-cudaError_t launch_cells(const float* pos, int64_t n, const int* dims, const double* box, int ndom,
+cudaError_t launch_cells(const float* pos, int64_t n, const int* dims, const float* faces, int ndom,
                          int32_t* dom_id, int32_t* hist, int ntiles, int* err, cudaStream_t s) {
   if (ntiles <= 0) return cudaSuccess;
-  Geometry g;
+  FaceTables g;
+  int total = 0;
   for (int d = 0; d < 3; ++d) {
-    g.box[d] = box[d];
     g.dims[d] = dims[d];
+    g.off[d] = total;
+    total += dims[d];
   }
-  const size_t smem = sizeof(int) * static_cast<size_t>(ndom);
+  g.total = total;
+  const size_t smem = sizeof(int) * static_cast<size_t>(ndom) + sizeof(float) * static_cast<size_t>(total);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(k_cells, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  k_cells<<<ntiles, 256, smem, s>>>(pos, n, g, ndom, dom_id, hist, ntiles, err);
+  k_cells<<<ntiles, 256, smem, s>>>(pos, n, g, faces, ndom, dom_id, hist, ntiles, err);
   return cudaGetLastError();
 }
 

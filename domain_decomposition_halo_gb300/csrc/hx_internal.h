@@ -183,7 +183,7 @@ struct BuildTile {          // candidates [local_begin, local_begin + n) of one 
 constexpr int kPartTile = 2048;   // atoms per partition tile
 constexpr int kSelTile = 2048;    // candidates per selection tile
 
-cudaError_t launch_cells(const float* pos, int64_t n, const int* dims, const double* box,
+cudaError_t launch_cells(const float* pos, int64_t n, const int* dims, const float* faces,
                          int ndom, int32_t* dom_id, int32_t* hist, int ntiles, int* err,
                          cudaStream_t s);
 cudaError_t launch_scatter_home(const float* pos, int64_t n, int ndom, const int32_t* dom_id,
