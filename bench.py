@@ -362,7 +362,7 @@ def secondary(hx_main, coords, forces, w_main, dev, peak, flags):
             ts.append(a.elapsed_time(b) * 1e3)
         return statistics.median(ts)
 
-    res = {}
+    res = {"overlap_with_local_kernel_us": overlap_probe(dev, flags)}
     entries = hx_main.counts()[3]
     cold = timed(hx_main, coords, forces, 30, True)
     res[w_main.name + "_cold_l2"] = {"us_step": round(cold, 2),
@@ -403,6 +403,61 @@ def secondary(hx_main, coords, forces, w_main, dev, peak, flags):
         res[name] = entry
         del hx
     return res
+
+
+def overlap_probe(dev, flags, names=("C2", "C4"), reps=40):
+    """Exchange latency while a local kernel fills the GPU (the pages'
+    section "SM occupancy and kernel scheduling"): a stream of short-block
+    elementwise kernels runs on a low-priority stream, one step (coordinates
+    + forces) is issued on a high-priority stream, and its event-timed
+    latency is compared for the fused path (one launch per direction) and
+    the per-pulse unfused path (one launch per pulse and direction)."""
+    import torch
+
+    from domain_decomposition_halo_gb300 import HaloExchange
+
+    lo = torch.cuda.Stream(device=dev, priority=0)
+    hi = torch.cuda.Stream(device=dev, priority=-5)
+    filler = torch.ones(64 * 2 ** 20, device=dev)   # 256 MB: every launch is thousands of short blocks
+    out = {}
+    for name in names:
+        w = W.WORKLOADS[name]
+        hx = HaloExchange(w.box, w.dims, w.cutoff, device=dev.index, flags=flags)
+        pos = torch.from_numpy(W.positions(w)).to(dev)
+        slots = hx.build_maps(pos)
+        x = torch.empty((slots, 3), device=dev)
+        hx.build_maps(pos, x)
+        f = torch.from_numpy(W.forces(w, slots)).to(dev)
+        res = {}
+        for fused in (True, False):
+            def step():
+                if fused:
+                    hx.exchange_coords(x, stream=hi)
+                    hx.exchange_forces(f, stream=hi)
+                else:
+                    hx.exchange_coords_unfused(x, stream=hi)
+                    hx.exchange_forces_unfused(f, stream=hi)
+            for loaded in (False, True):
+                ts = []
+                for _ in range(reps):
+                    torch.cuda.synchronize()
+                    if loaded:
+                        with torch.cuda.stream(lo):
+                            for _ in range(8):
+                                filler.mul_(1.0000001)
+                        time.sleep(50e-6)   # let the filler occupy the SMs
+                    a = torch.cuda.Event(enable_timing=True)
+                    b = torch.cuda.Event(enable_timing=True)
+                    a.record(hi)
+                    step()
+                    b.record(hi)
+                    torch.cuda.synchronize()
+                    ts.append(a.elapsed_time(b) * 1e3)
+                res[("fused" if fused else "unfused") + ("_loaded" if loaded else "_idle")] = round(statistics.median(ts), 2)
+        res["launches_per_step"] = {"fused": 2, "unfused": 2 * hx.counts()[1]}
+        out[name] = res
+        del hx
+    return out
 
 
 def cpu_baseline(w, pos, budget_s):
