@@ -288,6 +288,7 @@ int launch(hx_ctx* h, int kind, float* buf, cudaStream_t s) {
     args2[1] = &TP;
     args = args2;
     grid = dim3(static_cast<unsigned>(h->grid[kind]));
+    block = dim3(kTileThreads);
     smem = tiles_smem_bytes(kind);
     fn = tiles_kernel(kind);
   } else if (kind != 2) {
@@ -1202,7 +1203,8 @@ int hx::launch_coords_with_scratch(hx_ctx* h, float* coords, cudaStream_t s, Ctr
     args[1] = &P;
     fn = kernel_for(h, 0);
   }
-  return to_err(cudaLaunchKernel(fn, dim3(static_cast<unsigned>(h->grid[0])), dim3(kThreads), args, smem, s));
+  return to_err(cudaLaunchKernel(fn, dim3(static_cast<unsigned>(h->grid[0])), dim3(h->tiles ? kTileThreads : kThreads),
+                                args, smem, s));
 }
 
 // ------------------------------------------------------------------ C ABI

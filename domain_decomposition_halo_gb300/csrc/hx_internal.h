@@ -154,6 +154,9 @@ struct TileParams {
   unsigned long long timeout_ns;
 };
 
+constexpr int kTileConsumerWarps = 8;                         // warps that process staged tiles
+constexpr int kTileThreads = (kTileConsumerWarps + 1) * 32;   // plus one producer warp
+
 const void* tiles_kernel(int kind);   // 0 coordinates, 1 forces
 size_t tiles_smem_bytes(int kind);
 int tiles_blocks_per_sm(int kind);

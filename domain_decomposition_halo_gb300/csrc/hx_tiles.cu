@@ -39,15 +39,20 @@ struct StageLayout {
 };
 
 template <int KIND>
+struct Stages {
+  static constexpr int kCount = KIND == 1 ? 3 : 4;   // ring depth: as many as 2-3 blocks per SM allow
+};
+
+template <int KIND>
 struct alignas(16) TileSmem {
-  alignas(16) unsigned char stage[2][StageLayout<KIND>::kBytes];
-  TileUnit desc[2];                               // records of the current and the next unit
-  TileSeg extra[2][kTileSegs - kInlineSegs];      // their segments past the inline ones
-  float out[kWarps][96];                          // per-warp transpose for coalesced runs (coordinates)
-  unsigned long long mbar[2];                     // bulk-copy completion, one per stage
-  unsigned long long next_unit;
-  unsigned long long launch;                      // launches completed before this one
-  int prefetched[2];
+  alignas(16) unsigned char stage[Stages<KIND>::kCount][StageLayout<KIND>::kBytes];
+  TileUnit desc[Stages<KIND>::kCount];                      // record of the unit in each stage
+  TileSeg extra[Stages<KIND>::kCount][kTileSegs - kInlineSegs];
+  float out[kTileConsumerWarps][96];                        // per-warp transpose (coordinates)
+  unsigned long long full[Stages<KIND>::kCount];            // copies of a stage landed (producer -> consumers)
+  unsigned long long empty[Stages<KIND>::kCount];           // consumers done with a stage (consumers -> producer)
+  long long unit_of[Stages<KIND>::kCount];                  // unit in each stage, -1 = no more units
+  unsigned long long epoch;
 };
 
 __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
@@ -85,6 +90,13 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(unsigned long long* bar, u
                : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive(unsigned long long* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// Bounded wait for the phase of `bar` with the given parity; false on time-out.
+__device__ __forceinline__ bool mbar_wait(unsigned long long* bar, unsigned parity, unsigned long long limit_ns);
+
 __device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, unsigned parity) {
   unsigned ok;
   asm volatile(
@@ -107,52 +119,69 @@ __device__ __forceinline__ void bulk_load(void* dst, unsigned long long src, uns
       : "memory");
 }
 
+__device__ __forceinline__ bool mbar_wait(unsigned long long* bar, unsigned parity, unsigned long long limit_ns) {
+  unsigned long long t0 = 0;
+  unsigned iter = 0;
+  while (!mbar_try_wait(bar, parity)) {
+    if ((++iter & 63u) == 0u) {
+      const unsigned long long now = global_timer_ns();
+      if (t0 == 0) t0 = now;
+      if (now - t0 > limit_ns) return false;
+    }
+  }
+  return true;
+}
+
+// Named barrier of the consumer warps only (the producer warp runs ahead).
+__device__ __forceinline__ void consumers_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kTileConsumerWarps * 32) : "memory");
+}
+
 __device__ __forceinline__ void record_timeout(const TileParams& P, int item) {
   if (atomicCAS(&P.ctrl->status, 0, kErrTimeout) == 0) atomicExch(&P.ctrl->detail, P.direction * 65536 + item);
 }
 
-// Threads 0..15: copy unit c's record into `d`, then (when it has more than
-// kInlineSegs segments) its overflow segments into `extra`. Ends with a
-// block barrier.
-template <int KIND>
+// Producer warp: copy unit c's record into `d`, and its segments past the
+// inline ones into `extra`.
 __device__ void load_desc(const TileParams& P, unsigned long long c, TileUnit* d, TileSeg* extra) {
-  if (threadIdx.x < 16)
-    reinterpret_cast<int4*>(d)[threadIdx.x] = __ldg(reinterpret_cast<const int4*>(P.units + c) + threadIdx.x);
-  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  if (lane < 16)
+    reinterpret_cast<int4*>(d)[lane] = __ldg(reinterpret_cast<const int4*>(P.units + c) + lane);
+  __syncwarp();
   const int more = d->seg_cnt - kInlineSegs;
-  if (more > 0) {
-    for (int w = threadIdx.x; w < 3 * more; w += kThreads)
-      reinterpret_cast<int4*>(extra)[w] = __ldg(reinterpret_cast<const int4*>(P.extra + d->extra_off) + w);
-    __syncthreads();
-  }
+  for (int w = lane; w < 3 * more; w += 32)
+    reinterpret_cast<int4*>(extra)[w] = __ldg(reinterpret_cast<const int4*>(P.extra + d->extra_off) + w);
+  __syncwarp();
 }
 
 __device__ __forceinline__ const TileSeg& seg_of(const TileUnit& d, const TileSeg* extra, int s) {
   return s < kInlineSegs ? d.seg[s] : extra[s - kInlineSegs];
 }
 
-// Thread 0: are (block = wait until) all producer tiles of u at this epoch?
-__device__ bool producers_done(const TileParams& P, const TileUnit& u, unsigned long long epoch, bool block) {
-  for (int w = 0; w < u.wait_cnt; ++w) {
+// Producer warp: wait until every tile that u reads has been signalled at
+// this epoch. Lanes take the wait list in strides of 32 and the warp joins at
+// the end, so one unit's flags are polled in parallel rather than one after
+// another. A wait that runs out records a timeout and gives up.
+__device__ void producers_wait(const TileParams& P, const TileUnit& u, unsigned long long epoch) {
+  const int lane = threadIdx.x & 31;
+  for (int w = lane; w < u.wait_cnt; w += 32) {
     const Wait wt = P.waits[u.wait_off + w];
     const unsigned long long* flag = P.flags + wt.item;
-    if (ld_acquire_u64(flag) == epoch) continue;
-    if (!block) return false;
     unsigned long long t0 = 0;
     unsigned iter = 0;
     while (ld_acquire_u64(flag) != epoch) {
       if ((iter++ & 31u) == 0u) {
         const unsigned long long now = global_timer_ns();
         if (t0 == 0) t0 = now;
-        if (ld_relaxed_s32(&P.ctrl->status) != 0) return true;
+        if (ld_relaxed_s32(&P.ctrl->status) != 0) break;
         if (now - t0 > P.timeout_ns) {
           record_timeout(P, __ldg(&P.units[wt.item].item));
-          return true;
+          break;
         }
       }
     }
   }
-  return true;
+  __syncwarp();   // orders every lane's acquire before lane 0 issues the copies
 }
 
 // Run k of a unit: 0 = its slots, then per segment its map run and (forces)
@@ -180,39 +209,22 @@ __device__ __forceinline__ void run_of(const float* __restrict__ x, const TilePa
   }
 }
 
-// All threads: start the copies of a unit into stage buffer `st`. Every run
-// lands at (its global address mod 16) inside its 16-byte-aligned region;
-// thread 0 bulk-copies the aligned middles (one mbarrier phase), and the
-// head and tail words (under 16 bytes each) go by plain loads.
+// Producer warp: start the copies of a unit into stage buffer `st`. Every
+// run lands at (its global address mod 16) inside its 16-byte-aligned
+// region; the head and tail words (under 16 bytes each) go by plain loads of
+// the warp's lanes, then lane 0 arrives on `full` expecting the bytes of the
+// aligned middles and issues them as bulk copies.
 template <int KIND>
 __device__ void issue_stage(const float* __restrict__ x, const TileParams& P, const TileUnit& d,
-                            const TileSeg* extra, unsigned char* st, unsigned long long* bar) {
+                            const TileSeg* extra, unsigned char* st, unsigned long long* full) {
+  const int lane = threadIdx.x & 31;
   const int n_runs = 1 + (KIND == 1 ? 2 : 1) * d.seg_cnt;
-  if (threadIdx.x == 0) {
-    unsigned total = 0;
-    for (int k = 0; k < n_runs; ++k) {
-      unsigned long long g;
-      unsigned bytes, region;
-      run_of<KIND>(x, P, d, extra, k, g, bytes, region);
-      const unsigned long long a0 = (g + 15ull) & ~15ull, a1 = (g + bytes) & ~15ull;
-      if (a1 > a0) total += static_cast<unsigned>(a1 - a0);
-    }
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // earlier generic use of the stage
-    mbar_arrive_expect_tx(bar, total);
-    for (int k = 0; k < n_runs; ++k) {
-      unsigned long long g;
-      unsigned bytes, region;
-      run_of<KIND>(x, P, d, extra, k, g, bytes, region);
-      const unsigned long long a0 = (g + 15ull) & ~15ull, a1 = (g + bytes) & ~15ull;
-      if (a1 > a0) bulk_load(st + region + (g & 15ull) + (a0 - g), a0, static_cast<unsigned>(a1 - a0), bar);
-    }
-  }
-  for (int k = threadIdx.x >> 3; k < n_runs; k += kThreads / 8) {
+  for (int k = lane >> 3; k < n_runs; k += 4) {
     unsigned long long g;
     unsigned bytes, region;
     run_of<KIND>(x, P, d, extra, k, g, bytes, region);
     const unsigned long long a0 = (g + 15ull) & ~15ull, a1 = (g + bytes) & ~15ull;
-    const int w = threadIdx.x & 7;
+    const int w = lane & 7;
     if (a1 > a0) {
       const unsigned head = static_cast<unsigned>(a0 - g) / 4, tail = static_cast<unsigned>(g + bytes - a1) / 4;
       unsigned long long word;
@@ -229,6 +241,27 @@ __device__ void issue_stage(const float* __restrict__ x, const TileParams& P, co
         *reinterpret_cast<float*>(st + region + (g & 15ull) + o) = *reinterpret_cast<const float*>(g + o);
     }
   }
+  __syncwarp();
+  if (lane == 0) {
+    unsigned total = 0;
+    for (int k = 0; k < n_runs; ++k) {
+      unsigned long long g;
+      unsigned bytes, region;
+      run_of<KIND>(x, P, d, extra, k, g, bytes, region);
+      const unsigned long long a0 = (g + 15ull) & ~15ull, a1 = (g + bytes) & ~15ull;
+      if (a1 > a0) total += static_cast<unsigned>(a1 - a0);
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // earlier generic use of the stage
+    mbar_arrive_expect_tx(full, total);
+    for (int k = 0; k < n_runs; ++k) {
+      unsigned long long g;
+      unsigned bytes, region;
+      run_of<KIND>(x, P, d, extra, k, g, bytes, region);
+      const unsigned long long a0 = (g + 15ull) & ~15ull, a1 = (g + bytes) & ~15ull;
+      if (a1 > a0) bulk_load(st + region + (g & 15ull) + (a0 - g), a0, static_cast<unsigned>(a1 - a0), full);
+    }
+  }
+  __syncwarp();
 }
 
 // Coordinates: out[i] = tile[map[i] - local_a] (+shift), per segment, as
@@ -244,7 +277,7 @@ __device__ void coords_unit(float* __restrict__ x, const TileParams& P, const Ti
         st + sg.map_off + (reinterpret_cast<unsigned long long>(P.maps + sg.map) & 15ull));
     float* dst = x + 3 * sg.other;
     const int rounds = (sg.n + 31) / 32;
-    for (int r = warp; r < rounds; r += kWarps) {
+    for (int r = warp; r < rounds; r += kTileConsumerWarps) {
       const int e = r * 32 + lane;
       const int n_round = min(32, sg.n - r * 32);
       if (e < sg.n) {
@@ -283,95 +316,103 @@ __device__ void forces_unit(float* __restrict__ f, const TileUnit& d, const Tile
         st + sg.map_off + (reinterpret_cast<unsigned long long>(P.maps + sg.map) & 15ull));
     const float* src = reinterpret_cast<const float*>(
         st + sg.src_off + (reinterpret_cast<unsigned long long>(f + 3 * sg.other) & 15ull));
-    for (int e = threadIdx.x; e < sg.n; e += kThreads) {
+    for (int e = threadIdx.x; e < sg.n; e += kTileConsumerWarps * 32) {
       float* t = tile + 3 * (map[e] - d.local_a);
       t[0] = __fadd_rn(t[0], src[3 * e]);
       t[1] = __fadd_rn(t[1], src[3 * e + 1]);
       t[2] = __fadd_rn(t[2], src[3 * e + 2]);
     }
-    __syncthreads();
+    consumers_sync();
   }
   float* out = f + 3 * d.base;
-  for (int k = threadIdx.x; k < 3 * d.n; k += kThreads) out[k] = tile[k];
+  for (int k = threadIdx.x; k < 3 * d.n; k += kTileConsumerWarps * 32) out[k] = tile[k];
 }
 
 template <int KIND>
-__global__ void __launch_bounds__(kThreads) k_tiles(float* __restrict__ x, TileParams P) {
+__global__ void __launch_bounds__(kTileThreads) k_tiles(float* __restrict__ x, TileParams P) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   TileSmem<KIND>& S = *reinterpret_cast<TileSmem<KIND>*>(smem_raw);
+  constexpr int kS = Stages<KIND>::kCount;
   const unsigned long long N = P.n_units;
-  unsigned long long c = blockIdx.x;
-  if (c >= N) return;
-  const unsigned long long G = gridDim.x;
+  if (blockIdx.x >= N) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    mbar_init(&S.mbar[0], 1);
-    mbar_init(&S.mbar[1], 1);
+    for (int k = 0; k < kS; ++k) {
+      mbar_init(&S.full[k], 1);
+      mbar_init(&S.empty[k], kTileConsumerWarps);
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    // the ticket of this block's first unit numbers the launch and names the next unit
-    const unsigned long long t = atomicAdd(&P.ctrl->ticket, 1ull);
-    S.launch = t / N;
-    S.next_unit = (t % N) + G;
-    S.prefetched[0] = S.prefetched[1] = 0;
   }
-  load_desc<KIND>(P, c, &S.desc[0], S.extra[0]);   // its barrier publishes the fields above
-  const unsigned long long epoch = S.launch + 1ull;
-  const unsigned long long base = S.launch * N;
+  __syncthreads();
+
+  if (warp == kTileConsumerWarps) {
+    // ---------------- producer: records, waits, copies, tickets ----------------
+    unsigned long long c = blockIdx.x, base = 0, epoch = 0, t = 0;
+    if (lane == 0) {
+      t = atomicAdd(&P.ctrl->ticket, 1ull);   // the ticket of the first unit numbers the launch
+      base = t - t % N;
+      epoch = base / N + 1ull;
+      S.epoch = epoch;
+    }
+    t = __shfl_sync(0xffffffffu, t, 0);
+    base = __shfl_sync(0xffffffffu, base, 0);
+    epoch = __shfl_sync(0xffffffffu, epoch, 0);
+    unsigned long long nxt = (t - base) + gridDim.x;
+    unsigned empty_parity[kS];
+    for (int k = 0; k < kS; ++k) empty_parity[k] = 1u;   // a fresh stage counts as emptied
+    int slot = 0;
+    while (c < N) {
+      if (!mbar_wait(&S.empty[slot], empty_parity[slot], P.timeout_ns)) {
+        if (lane == 0) record_timeout(P, -1);
+      }
+      empty_parity[slot] ^= 1u;
+      unsigned long long tn = 0;
+      if (lane == 0 && nxt < N) tn = atomicAdd(&P.ctrl->ticket, 1ull);   // the ticket of `nxt`
+      load_desc(P, c, &S.desc[slot], S.extra[slot]);
+      producers_wait(P, S.desc[slot], epoch);
+      if (lane == 0) {
+        if (S.desc[slot].wait_cnt > 0) asm volatile("fence.proxy.async.global;" ::: "memory");
+        S.unit_of[slot] = static_cast<long long>(c);
+      }
+      __syncwarp();
+      issue_stage<KIND>(x, P, S.desc[slot], S.extra[slot], S.stage[slot], &S.full[slot]);
+      tn = __shfl_sync(0xffffffffu, tn, 0);
+      c = nxt;
+      nxt = (c < N) ? (tn - base) + gridDim.x : N;
+      slot = slot + 1 == kS ? 0 : slot + 1;
+    }
+    // no more units: hand the consumers an end marker
+    if (!mbar_wait(&S.empty[slot], empty_parity[slot], P.timeout_ns)) {
+      if (lane == 0) record_timeout(P, -1);
+    }
+    if (lane == 0) {
+      S.unit_of[slot] = -1;
+      mbar_arrive(&S.full[slot]);
+    }
+    return;
+  }
+
+  // ---------------- consumers: shared-memory work, stores, signals ----------------
   const int drop_item = *reinterpret_cast<const volatile int*>(&P.ctrl->drop_item);
-  unsigned parity[2] = {0u, 0u};
-  unsigned long long nxt = S.next_unit;
-  int cur = 0;
-  while (c < N) {
-    const TileUnit& d = S.desc[cur];
-    unsigned long long t_next = 0;
-    if (threadIdx.x == 0 && nxt < N) t_next = atomicAdd(&P.ctrl->ticket, 1ull);   // the ticket of `nxt`
-    // the current unit: when it was not prefetched, wait for its producers and copy it now
-    if (!S.prefetched[cur]) {
-      if (threadIdx.x == 0) {
-        producers_done(P, d, epoch, true);
-        if (d.wait_cnt > 0) asm volatile("fence.proxy.async.global;" ::: "memory");
-      }
-      __syncthreads();
-      issue_stage<KIND>(x, P, d, S.extra[cur], S.stage[cur], &S.mbar[cur]);
+  unsigned full_parity[kS];
+  for (int k = 0; k < kS; ++k) full_parity[k] = 0u;
+  int slot = 0;
+  while (true) {
+    if (!mbar_wait(&S.full[slot], full_parity[slot], P.timeout_ns)) {
+      if (threadIdx.x == 0) record_timeout(P, -1);
     }
-    // the next unit's record, then its copies when nothing it reads is still being written
-    if (nxt < N) {
-      load_desc<KIND>(P, nxt, &S.desc[cur ^ 1], S.extra[cur ^ 1]);
-      if (threadIdx.x == 0) {
-        const bool ready = producers_done(P, S.desc[cur ^ 1], epoch, false);
-        if (ready && S.desc[cur ^ 1].wait_cnt > 0) asm volatile("fence.proxy.async.global;" ::: "memory");
-        S.prefetched[cur ^ 1] = ready ? 1 : 0;
-      }
-      __syncthreads();
-      if (S.prefetched[cur ^ 1]) issue_stage<KIND>(x, P, S.desc[cur ^ 1], S.extra[cur ^ 1], S.stage[cur ^ 1], &S.mbar[cur ^ 1]);
-    }
-    {
-      unsigned long long t0 = 0;
-      unsigned iter = 0;
-      while (!mbar_try_wait(&S.mbar[cur], parity[cur])) {
-        if ((++iter & 63u) == 0u) {   // a bulk copy always completes; bound the wait all the same
-          const unsigned long long now = global_timer_ns();
-          if (t0 == 0) t0 = now;
-          if (now - t0 > P.timeout_ns) {
-            if (threadIdx.x == 0) record_timeout(P, d.item);
-            break;
-          }
-        }
-      }
-      parity[cur] ^= 1u;
-    }
-    __syncthreads();   // plain-loaded edges of the runs are visible too
-    if (KIND == 0) coords_unit(x, P, d, S.extra[cur], S.stage[cur], S.out);
-    else forces_unit(x, d, S.extra[cur], S.stage[cur], P);
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      if ((d.flags & kSignal) && d.item != drop_item) st_release_u64(P.flags + c, epoch);
-      S.prefetched[cur] = 0;
-      S.next_unit = (nxt < N) ? (t_next - base) + G : N;
-    }
-    __syncthreads();
-    c = nxt;
-    nxt = S.next_unit;
-    cur ^= 1;
+    full_parity[slot] ^= 1u;
+    const long long c = S.unit_of[slot];
+    if (c < 0) break;
+    const TileUnit& d = S.desc[slot];
+    if (KIND == 0) coords_unit(x, P, d, S.extra[slot], S.stage[slot], S.out);
+    else forces_unit(x, d, S.extra[slot], S.stage[slot], P);
+    consumers_sync();   // every store of this unit is issued
+    if (threadIdx.x == 0 && (d.flags & kSignal) && d.item != drop_item)
+      st_release_u64(P.flags + c, S.epoch);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.empty[slot]);
+    slot = slot + 1 == kS ? 0 : slot + 1;
   }
 }
 
@@ -390,7 +431,7 @@ int tiles_blocks_per_sm(int kind) {
       cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
     return 0;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kThreads, smem) != cudaSuccess) return 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kTileThreads, smem) != cudaSuccess) return 0;
   return n;
 }
 
