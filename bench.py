@@ -48,15 +48,17 @@ def parse_args():
     ap.add_argument("--workload", default="C5", choices=sorted(W.WORKLOADS))
     ap.add_argument("--no-extras", action="store_true", help="skip the secondary measurements")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU baseline budget")
-    ap.add_argument("--flags", default="fine",
-                    help="comma list of libhx modes: fine, tiles, counter, nograph, unordered, pages (= none)")
+    ap.add_argument("--flags", default="fine,sweepf",
+                    help="comma list of libhx modes: fine, sweepf (forces by the slot sweep), sweep, tiles, "
+                         "counter, nograph, unordered, pages (= none)")
     return ap.parse_args()
 
 
 def hx_flags(spec: str) -> int:
     from domain_decomposition_halo_gb300 import hx as HX
     table = {"fine": HX.HX_FLAG_FINE_WAITS, "counter": HX.HX_FLAG_COUNTER_SIGNAL, "nograph": HX.HX_FLAG_NO_GRAPH,
-             "unordered": HX.HX_FLAG_UNORDERED_FORCES, "tiles": HX.HX_FLAG_TILES, "pages": 0, "": 0}
+             "unordered": HX.HX_FLAG_UNORDERED_FORCES, "tiles": HX.HX_FLAG_TILES, "sweep": HX.HX_FLAG_SWEEP,
+             "sweepf": HX.HX_FLAG_SWEEP_FORCES, "pages": 0, "": 0}
     flags = 0
     for name in spec.split(","):
         flags |= table[name.strip()]
@@ -98,10 +100,25 @@ def measured_hbm_peak():
 
 def kernel_source_digest():
     h = hashlib.sha256()
-    for name in ("hx_kernels.cu", "hx_internal.h"):
+    for name in ("hx_kernels.cu", "hx_sweep.cu", "hx_internal.h"):
         with open(os.path.join(ROOT, "domain_decomposition_halo_gb300", "csrc", name), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
+
+
+def kernel_impl(flags: int, direction: int) -> str:
+    """The device function that runs a direction's fused exchange under `flags`."""
+    from domain_decomposition_halo_gb300 import hx as HX
+    if flags & HX.HX_FLAG_TILES:
+        return f"k_tiles<{direction}> (tile pipeline)"
+    if flags & HX.HX_FLAG_SWEEP or (direction == 1 and flags & HX.HX_FLAG_SWEEP_FORCES):
+        return f"k_sweep<{direction}> (slot sweep)"
+    mode = ("chunk flags" if flags & HX.HX_FLAG_FINE_WAITS else
+            "counter" if flags & HX.HX_FLAG_COUNTER_SIGNAL else "last arrival")
+    if direction == 0:
+        return f"k_coords_fused<{mode}> (chunks)"
+    order = "unordered" if flags & HX.HX_FLAG_UNORDERED_FORCES else "ordered"
+    return f"k_forces_fused<{mode}, {order}> (chunks)"
 
 
 def profiled_traffic(kernel: str, workload: str):
@@ -298,7 +315,8 @@ def run_ours(args):
         },
         "effective_gbs": round(step_gbs, 1),
         "roofline": {
-            "bound": "hbm", "kernel": dominant, "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "bound": "hbm", "kernel": dominant, "kernel_impl": kernel_impl(flags, 1 if dominant == "hx_forces_fused" else 0),
+            "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
             "algorithmic_bytes_per_launch": dom_bytes,
             "traffic": profiled_traffic(dominant, w.name),

@@ -184,7 +184,7 @@ struct hx_ctx {
   int n_chunks[2] = {0, 0};
   int grid[2] = {0, 0};
   size_t n_flags = 1;                        // flags (and election counters) per direction
-  bool tiles = false;                        // fused path runs the tile kernels
+  int family[2] = {0, 0};                    // kernel family of each direction's fused path (Family)
   TileUnit* d_units[2] = {nullptr, nullptr};
   TileSeg* d_segs[2] = {nullptr, nullptr};
   Wait* d_twaits[2] = {nullptr, nullptr};
@@ -274,6 +274,24 @@ TileParams tile_params(hx_ctx* h, int dir) {
   return P;
 }
 
+// Work items of the fused list of direction `dir`: units or chunks.
+int work_items(const hx_ctx* h, int dir) { return h->family[dir] == kFamChunks ? h->n_chunks[dir] : h->n_units[dir]; }
+
+// Launch shape of a direction's fused kernel.
+const void* fused_kernel(hx_ctx* h, int dir) {
+  if (h->family[dir] == kFamTiles) return tiles_kernel(dir);
+  if (h->family[dir] == kFamSweep) return sweep_kernel(dir);
+  return kernel_for(h, dir);
+}
+unsigned fused_threads(const hx_ctx* h, int dir) {
+  return h->family[dir] == kFamTiles ? kTileThreads : kThreads;
+}
+size_t fused_smem(const hx_ctx* h, int dir) {
+  if (h->family[dir] == kFamTiles) return tiles_smem_bytes(dir);
+  if (h->family[dir] == kFamSweep) return sweep_smem_bytes(dir);
+  return 0;
+}
+
 int launch(hx_ctx* h, int kind, float* buf, cudaStream_t s) {
   DirParams P;
   TileParams TP;
@@ -282,15 +300,15 @@ int launch(hx_ctx* h, int kind, float* buf, cudaStream_t s) {
   dim3 grid(1), block(kind == 2 ? 1 : kThreads);
   size_t smem = 0;
   const void* fn = kernel_for(h, kind);
-  if (kind != 2 && h->tiles) {
+  if (kind != 2 && h->family[kind] != kFamChunks) {
     TP = tile_params(h, kind);
     args2[0] = &buf;
     args2[1] = &TP;
     args = args2;
     grid = dim3(static_cast<unsigned>(h->grid[kind]));
-    block = dim3(kTileThreads);
-    smem = tiles_smem_bytes(kind);
-    fn = tiles_kernel(kind);
+    block = dim3(fused_threads(h, kind));
+    smem = fused_smem(h, kind);
+    fn = fused_kernel(h, kind);
   } else if (kind != 2) {
     P = dir_params(h, kind);
     args2[0] = &buf;
@@ -461,11 +479,12 @@ struct TRec {
 };
 
 int build_tile_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::vector<int32_t>& maps,
-                      const std::vector<int64_t>& rank) {
+                      const std::vector<int64_t>& rank, int max_slots, int max_entries, long long lag,
+                      int tile_bytes, int map_bytes, int src_bytes, int dir) {
   const Plan& pl = h->pl;
   const int P = pl.n_pulses, nd = pl.ndom;
   auto upper = [&](int r, int q) { return neighbour(pl, r, pl.pulse_dim[q], +1); };
-  for (int dir = 0; dir < 2; ++dir) {
+  {
     std::vector<TRec> recs;
     // tiles of (domain, range): index list in slot order
     std::vector<std::vector<std::vector<int>>> by_range(nd, std::vector<std::vector<int>>(P + 1));
@@ -493,12 +512,12 @@ int build_tile_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::
         };
         for (int a = lo, b = lo; a < lo + len; a = b) {
           // at most kTile slots and kTileEntries entries (a slot has at most one entry per pulse)
-          b = std::min(lo + len, a + kTile);
-          if (entries_in(a, b) > kTileEntries) {
+          b = std::min(lo + len, a + max_slots);
+          if (entries_in(a, b) > max_entries) {
             int good = a + 1, bad = b;
             while (bad - good > 1) {
               const int mid = good + (bad - good) / 2;
-              if (entries_in(a, mid) <= kTileEntries) good = mid;
+              if (entries_in(a, mid) <= max_entries) good = mid;
               else bad = mid;
             }
             b = good;
@@ -583,10 +602,9 @@ int build_tile_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::
         if (a.range != b.range) return a.range < b.range;
         return a.a < b.a;
       });
-      const long long window = h->grid[dir];
       std::vector<Rec> ord(recs.size());
       for (size_t k = 0; k < base.size(); ++k) {
-        ord[base[k]].key = static_cast<long long>(k) + 3 * window * recs[base[k]].stage;
+        ord[base[k]].key = static_cast<long long>(k) + lag * recs[base[k]].stage;
         recs[base[k]].key = ord[base[k]].key;
       }
       for (size_t i = 0; i < recs.size(); ++i) ord[i].deps = recs[i].deps;
@@ -600,7 +618,6 @@ int build_tile_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::
       std::vector<TileUnit> units;
       std::vector<TileSeg> segs;   // segments past kInlineSegs
       std::vector<Wait> waits;
-      const int tile_bytes = kTile * 12 + 16, map_bytes = kTileEntries * 4 + 32 * kTileSegs;
       for (int i : order) {
         const TRec& t = recs[i];
         TileUnit u;
@@ -621,6 +638,9 @@ int build_tile_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::
           if (static_cast<int>(k) < kInlineSegs) u.seg[k] = sg;
           else segs.push_back(sg);
         }
+        // the stage regions must fit the kernel's buffer
+        if (moff > tile_bytes + map_bytes || (dir == 1 && soff > tile_bytes + map_bytes + src_bytes))
+          return HX_ERR_STATE;
         u.wait_off = static_cast<int32_t>(waits.size());
         u.wait_cnt = static_cast<int32_t>(t.deps.size());
         for (int d : t.deps) waits.push_back({pos[d], 1});
@@ -668,7 +688,7 @@ int build_tables(hx_ctx* h, cudaStream_t s) {
       it.shift_flag = h->t_shift[t];
     }
   std::vector<int32_t> maps;
-  if ((fine || (h->flags & HX_FLAG_TILES)) && h->total_entries > 0) {   // fine waits and tiles read the maps
+  if ((fine || (h->flags & (HX_FLAG_TILES | HX_FLAG_SWEEP | HX_FLAG_SWEEP_FORCES))) && h->total_entries > 0) {   // fine waits and units read the maps
     maps.resize(h->total_entries);
     HX_CUDA(cudaMemcpy(maps.data(), h->d_maps, sizeof(int32_t) * h->total_entries, cudaMemcpyDeviceToHost));
   }
@@ -678,17 +698,32 @@ int build_tables(hx_ctx* h, cudaStream_t s) {
   auto upper = [&](int r, int q) { return upper_tab[static_cast<size_t>(r) * P + q]; };
   std::vector<int64_t> rank(nd);
   for (int r = 0; r < nd; ++r) rank[r] = domain_rank(pl, r);
-  h->tiles = (h->flags & HX_FLAG_TILES) != 0;
+  h->family[0] = (h->flags & HX_FLAG_TILES) ? kFamTiles : (h->flags & HX_FLAG_SWEEP) ? kFamSweep : kFamChunks;
+  h->family[1] = (h->flags & (HX_FLAG_SWEEP | HX_FLAG_SWEEP_FORCES)) ? kFamSweep : h->family[0];
   for (int k = 0; k < 2; ++k) {
-    const int per_sm = std::max(1, h->tiles ? tiles_blocks_per_sm(k) : max_blocks_per_sm(kernel_for(h, k)));
+    const int per_sm = std::max(1, h->family[k] == kFamTiles   ? tiles_blocks_per_sm(k)
+                                   : h->family[k] == kFamSweep ? sweep_blocks_per_sm(k)
+                                                               : max_blocks_per_sm(kernel_for(h, k)));
     h->grid[k] = per_sm * h->sm_count;   // upper bound; trimmed to the work count below
   }
-  if (h->tiles) {
-    const int rc = build_tile_tables(h, items, maps, rank);
+  // Unit lists. A dependent unit is placed a few resident windows after the
+  // units it waits for: tile mode three stages per block, sweep four units
+  // per resident warp (the measured best on the 12M-atom workload).
+  for (int dir = 0; dir < 2; ++dir) {
+    int rc = HX_OK;
+    if (h->family[dir] == kFamTiles) {
+      rc = build_tile_tables(h, items, maps, rank, kTile, kTileEntries, 3ll * h->grid[dir], kTile * 12 + 16,
+                             kTileEntries * 4 + 32 * kTileSegs, kTileEntries * 12 + 32 * kTileSegs, dir);
+    } else if (h->family[dir] == kFamSweep) {
+      if (P > kSweepSegs) return HX_ERR_PULSES;   // a unit's runs must fit one warp's stage
+      rc = build_tile_tables(h, items, maps, rank, kSweepSlots, kSweepEntries, 4ll * h->grid[dir] * kWarps,
+                             kSweepTileBytes, kSweepMapBytes, kSweepSrcBytes, dir);
+    }
     if (rc != HX_OK) return rc;
   }
 
-  for (int dir = 0; dir < 2 && !h->tiles; ++dir) {
+  for (int dir = 0; dir < 2; ++dir) {
+    if (h->family[dir] != kFamChunks) continue;
     std::vector<Rec> recs;
     std::vector<std::vector<int>> item_recs(std::max(n_items, 1));   // chunk records of each item, in entry order
     auto add_part = [&](int t, int begin, int end, int halo_src, int stage, bool keep_empty) {
@@ -932,8 +967,11 @@ int build_tables(hx_ctx* h, cudaStream_t s) {
   // Persistent grid: every warp (tile mode: every block) co-resident, and no
   // more of them than there is work.
   for (int k = 0; k < 2; ++k) {
-    if (h->tiles) {
+    if (h->family[k] == kFamTiles) {
       h->grid[k] = std::max(1, std::min(h->n_units[k], h->grid[k]));
+    } else if (h->family[k] == kFamSweep) {
+      const int warps = std::max(1, std::min(h->n_units[k], h->grid[k] * kWarps));
+      h->grid[k] = (warps + kWarps - 1) / kWarps;
     } else {
       const int warps = std::max(1, std::min(h->n_chunks[k], h->grid[k] * kWarps));
       h->grid[k] = (warps + kWarps - 1) / kWarps;
@@ -1155,7 +1193,7 @@ int build(hx_ctx* h, const float* pos, int64_t n, float* coords, int64_t capacit
   if (capacity < h->total_slots) return HX_ERR_CAPACITY;
   // 4. fill the caller's array: home coordinates, then one coordinate exchange
   HX_CUDA(launch_place_home(b.home_xyz, b.home_dom, b.home_start, b.dom_off, n, coords, s));
-  if (P > 0 && (h->tiles ? h->n_units[0] : h->n_chunks[0]) > 0) {
+  if (P > 0 && work_items(h, 0) > 0) {
     rc = launch(h, 0, coords, s);
     if (rc != HX_OK) return rc;
   }
@@ -1173,7 +1211,7 @@ int hx::launch_coords_with_scratch(hx_ctx* h, float* coords, cudaStream_t s, Ctr
                                    unsigned long long* flags, unsigned int* arrivals, size_t max_flags) {
   if (!h->built) return HX_ERR_STATE;
   if (!coords && h->total_slots > 0) return HX_ERR_ARG;
-  const int work = h->tiles ? h->n_units[0] : h->n_chunks[0];
+  const int work = work_items(h, 0);
   if (h->pl.n_pulses == 0 || work == 0) return HX_OK;
   // flags are indexed by item (pulse signals) or by list position (chunk / tile signals)
   const size_t need = std::max<size_t>(static_cast<size_t>(h->pl.n_pulses) * h->pl.ndom, static_cast<size_t>(work));
@@ -1188,13 +1226,13 @@ int hx::launch_coords_with_scratch(hx_ctx* h, float* coords, cudaStream_t s, Ctr
   const void* fn;
   size_t smem = 0;
   args[0] = &coords;
-  if (h->tiles) {
+  if (h->family[0] != kFamChunks) {
     TP = tile_params(h, 0);
     TP.flags = flags;
     TP.ctrl = ctrl;
     args[1] = &TP;
-    fn = tiles_kernel(0);
-    smem = tiles_smem_bytes(0);
+    fn = fused_kernel(h, 0);
+    smem = fused_smem(h, 0);
   } else {
     P = dir_params(h, 0);
     P.flags = flags;
@@ -1203,7 +1241,7 @@ int hx::launch_coords_with_scratch(hx_ctx* h, float* coords, cudaStream_t s, Ctr
     args[1] = &P;
     fn = kernel_for(h, 0);
   }
-  return to_err(cudaLaunchKernel(fn, dim3(static_cast<unsigned>(h->grid[0])), dim3(h->tiles ? kTileThreads : kThreads),
+  return to_err(cudaLaunchKernel(fn, dim3(static_cast<unsigned>(h->grid[0])), dim3(fused_threads(h, 0)),
                                 args, smem, s));
 }
 
@@ -1253,6 +1291,11 @@ int hx_init(hx_handle* out, const double box[3], const int dims[3], double cutof
   if (!h) return HX_ERR_NOMEM;
   h->pl = pl;
   h->device = device;
+  const unsigned families = flags & (HX_FLAG_TILES | HX_FLAG_SWEEP | HX_FLAG_SWEEP_FORCES);
+  if (families & (families - 1)) {   // at most one of the alternative kernel families
+    delete h;
+    return HX_ERR_ARG;
+  }
   h->flags = flags;
   h->timeout_ns = 1000ull * (timeout_us ? timeout_us : 1000000u);
   if (cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
@@ -1291,7 +1334,7 @@ int exchange(hx_handle h, float* buf, void* stream, int kind) {
   if (!h) return HX_ERR_ARG;
   if (!h->built) return HX_ERR_STATE;
   if (!buf && h->total_slots > 0) return HX_ERR_ARG;   // an empty layout touches no memory
-  if (h->pl.n_pulses == 0 || (h->tiles ? h->n_units[kind] : h->n_chunks[kind]) == 0) return HX_OK;   // nothing moves
+  if (h->pl.n_pulses == 0 || work_items(h, kind) == 0) return HX_OK;   // nothing moves
   const int rc = ensure_device(h);
   if (rc != HX_OK) return rc;
   return launch(h, kind, buf, static_cast<cudaStream_t>(stream));

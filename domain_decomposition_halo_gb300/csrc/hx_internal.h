@@ -161,6 +161,32 @@ const void* tiles_kernel(int kind);   // 0 coordinates, 1 forces
 size_t tiles_smem_bytes(int kind);
 int tiles_blocks_per_sm(int kind);
 
+// Kernel family of one direction's fused exchange.
+enum Family : int { kFamChunks = 0, kFamTiles = 1, kFamSweep = 2 };
+
+// ---- slot-sweep kernels (hx_sweep.cu): one warp per unit, same unit records ----
+#ifndef HX_SWEEP_SLOTS
+#define HX_SWEEP_SLOTS 256
+#endif
+#ifndef HX_SWEEP_ENTRIES
+#define HX_SWEEP_ENTRIES 256
+#endif
+constexpr int kSweepSlots = HX_SWEEP_SLOTS;       // slots of one unit: a warp's staged tile
+constexpr int kSweepEntries = HX_SWEEP_ENTRIES;   // map entries of one unit at most
+constexpr int kSweepSegs = 8;                     // segments (pulses) of one unit at most
+static_assert(1 + 2 * kSweepSegs <= 32, "a sweep unit stages one run per lane");
+// Stage layout of one warp: slots, then map runs, then (forces) received
+// runs; every run has a 16-byte-aligned region 16 bytes longer than itself.
+constexpr int kSweepTileBytes = kSweepSlots * 12 + 16;
+constexpr int kSweepMapBytes = kSweepEntries * 4 + 32 * kSweepSegs;
+constexpr int kSweepSrcBytes = kSweepEntries * 12 + 32 * kSweepSegs;
+constexpr int sweep_stage_bytes(int kind) {
+  return kSweepTileBytes + kSweepMapBytes + (kind == 1 ? kSweepSrcBytes : 0);
+}
+const void* sweep_kernel(int kind);              // 0 coordinates, 1 forces
+size_t sweep_smem_bytes(int kind);               // dynamic shared memory of a block
+int sweep_blocks_per_sm(int kind);
+
 // ---- launch with caller-independent scratch (hx_api.cu, for hx_noalloc.cu) ----
 // Runs the handle's fused coordinate exchange with its signal flags, election
 // counters and control block at the given device addresses instead of the

@@ -1,0 +1,420 @@
+// Slot-sweep exchange kernels of libhx (sm_103a).
+//
+// Same operation as the chunk kernels of hx_kernels.cu. Coordinates use the
+// gather packed[i] = x[map[i]] of packSendBufKernel, with the periodic
+// shift. Forces use the accumulation forces[map[i]] += packed[i] of
+// unpackRecvBufKernel<accumulate>, last pulse first ("Force halo exchange:
+// Reversing the dependency chain").
+//
+// The two differ only in the unit of work. A chunk is a run of one pulse's
+// map. A sweep unit is a run of up to kSweepSlots consecutive slots of one
+// sender's array, with every pulse's map entries that fall in it:
+//   - coordinates: the unit is a source. Its slots and its map runs are
+//     staged in shared memory; every pulse's gathers are served from there
+//     and each pulse's run is stored into the receiver, coalesced;
+//   - forces: the unit is a target. Its slots, its map runs and the received
+//     force runs are staged; the runs are added last pulse first and the
+//     slots are written back.
+//
+// Why this pays on one GPU: with random in-domain order nearly every
+// 64-byte granule of a sender's slots holds some pulse's selected atom. The
+// chunk kernels therefore touch the whole home region once per pulse, in
+// scattered 12-byte accesses. A sweep touches it once in total, as
+// sequential streams, and every per-entry access stays in shared memory.
+// Each contiguous run is one TMA bulk copy (cp.async.bulk) issued by one lane
+// and completing on the warp's mbarrier, so moving a unit's bytes costs a
+// handful of instructions instead of one per 128 bytes per lane.
+//
+// Dependencies and signals are per unit, as in the chunk kernels' fine mode
+// ("Enabling parallelism across pulses through kernel fusion"): a unit of
+// received slots waits for the units that stored them (coordinates), and a
+// unit waits for the receivers' units that still add into the slots it reads
+// (forces). Each warp is independent. It draws units by ticket, in a
+// topological order, and so never waits on a unit that no running warp has
+// claimed.
+#include <cstdint>
+
+#include "hx_internal.h"
+
+namespace hx {
+namespace {
+
+constexpr int kErrTimeout = -6;
+constexpr unsigned kFull = 0xffffffffu;
+
+// A warp's stage buffer: the unit's slots, its map runs and (forces) its
+// received runs, each in its own 16-byte-aligned region at the run's global
+// address mod 16. The region offsets are in the unit's segment records.
+template <int KIND>
+struct alignas(16) WarpSmem {
+  alignas(16) unsigned char stage[sweep_stage_bytes(KIND)];
+  TileUnit desc[2];              // the current unit's record and the next one's
+  float out[96];                 // one 32-entry round, transposed for coalesced stores
+  unsigned long long bar;        // completion of the unit's bulk copies
+};
+
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ int ld_relaxed_s32(const int* p) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ unsigned long long global_timer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ unsigned smem_addr(const void* p) {
+  return static_cast<unsigned>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(unsigned long long* bar, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(unsigned long long* bar, unsigned bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, unsigned parity) {
+  unsigned ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for the phase of `bar` with the given parity; false on time-out.
+__device__ __forceinline__ bool mbar_wait(unsigned long long* bar, unsigned parity, unsigned long long limit_ns) {
+  unsigned long long t0 = 0;
+  unsigned iter = 0;
+  while (!mbar_try_wait(bar, parity)) {
+    if ((++iter & 63u) == 0u) {
+      const unsigned long long now = global_timer_ns();
+      if (t0 == 0) t0 = now;
+      if (now - t0 > limit_ns) return false;
+    }
+  }
+  return true;
+}
+
+// Global -> shared bulk copy (TMA); both addresses and the size are
+// multiples of 16 bytes.
+__device__ __forceinline__ void bulk_load(void* dst, unsigned long long src, unsigned bytes, unsigned long long* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void record_timeout(const TileParams& P, int item) {
+  if (atomicCAS(&P.ctrl->status, 0, kErrTimeout) == 0) atomicExch(&P.ctrl->detail, P.direction * 65536 + item);
+}
+
+__device__ __forceinline__ TileSeg seg_at(const TileParams& P, const TileUnit& d, int s) {
+  return s < kInlineSegs ? d.seg[s] : P.extra[d.extra_off + s - kInlineSegs];
+}
+
+// Whole warp: wait until every unit that d depends on has been signalled at
+// this epoch. Lanes take the wait list in strides of 32; a wait that runs
+// out records a timeout and gives up. The closing __syncwarp orders every
+// lane's acquire before the warp's loads.
+__device__ void wait_units(const TileParams& P, const TileUnit& d, unsigned long long epoch) {
+  const int lane = threadIdx.x & 31;
+  for (int w = lane; w < d.wait_cnt; w += 32) {
+    const Wait wt = P.waits[d.wait_off + w];
+    const unsigned long long* flag = P.flags + wt.item;
+    unsigned long long t0 = 0;
+    unsigned iter = 0;
+    while (ld_acquire_u64(flag) != epoch) {
+      if ((iter++ & 31u) == 0u) {
+        const unsigned long long now = global_timer_ns();
+        if (t0 == 0) t0 = now;
+        if (ld_relaxed_s32(&P.ctrl->status) != 0) break;
+        if (now - t0 > P.timeout_ns) {
+          record_timeout(P, __ldg(&P.units[wt.item].item));
+          break;
+        }
+      }
+    }
+  }
+  __syncwarp();
+}
+
+// Run k of a unit: 0 = its slots, then per segment its map run and (forces)
+// its received-force run: global address, bytes, stage region offset.
+template <int KIND>
+__device__ __forceinline__ void run_of(const float* x, const TileParams& P, const TileUnit& d, int k,
+                                       unsigned long long& g, unsigned& bytes, unsigned& region) {
+  if (k == 0) {
+    g = reinterpret_cast<unsigned long long>(x + 3 * d.base);
+    bytes = 12u * static_cast<unsigned>(d.n);
+    region = 0;
+    return;
+  }
+  const int per = KIND == 1 ? 2 : 1;
+  const TileSeg sg = seg_at(P, d, (k - 1) / per);
+  if ((k - 1) % per == 0) {
+    g = reinterpret_cast<unsigned long long>(P.maps + sg.map);
+    bytes = 4u * static_cast<unsigned>(sg.n);
+    region = static_cast<unsigned>(sg.map_off);
+  } else {
+    g = reinterpret_cast<unsigned long long>(x + 3 * sg.other);
+    bytes = 12u * static_cast<unsigned>(sg.n);
+    region = static_cast<unsigned>(sg.src_off);
+  }
+}
+
+// Whole warp: stage every run of the unit, one run per lane (a unit has at
+// most 1 + 2 * kSweepSegs <= 32 runs). Each run lands at (its global address
+// mod 16) inside its region. Lane 0 announces the bytes of all the runs'
+// 16-byte-aligned middles on the warp's mbarrier; then every lane issues its
+// run's middle as one bulk copy and copies the head and tail words (under 16
+// bytes each) with plain loads. Runs of under 32 bytes go entirely by plain
+// loads. The caller waits on the mbarrier and then on the warp (__syncwarp).
+template <int KIND>
+__device__ void stage_unit(const float* x, const TileParams& P, const TileUnit& d, unsigned char* st,
+                           unsigned long long* bar) {
+  const int lane = threadIdx.x & 31;
+  const int n_runs = 1 + (KIND == 1 ? 2 : 1) * d.seg_cnt;
+  unsigned long long g = 0, a0 = 0, a1 = 0;
+  unsigned bytes = 0, region = 0, middle = 0;
+  if (lane < n_runs) {
+    run_of<KIND>(x, P, d, lane, g, bytes, region);
+    a0 = (g + 15ull) & ~15ull;
+    a1 = (g + bytes) & ~15ull;
+    if (a1 > a0) middle = static_cast<unsigned>(a1 - a0);
+  }
+  const unsigned total = __reduce_add_sync(kFull, middle);
+  if (lane == 0) {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the stage's earlier generic use
+    mbar_arrive_expect_tx(bar, total);
+  }
+  __syncwarp();
+  if (lane < n_runs) {
+    unsigned char* dst = st + region + (g & 15ull);
+    // Plain words: up to 3 before and 3 after an aligned middle, or a whole
+    // run of under 32 bytes (at most 7 words). All loads are issued before
+    // any store so that they are in flight together.
+    if (middle > 0) bulk_load(dst + (a0 - g), a0, middle, bar);
+    const unsigned nh = middle > 0 ? static_cast<unsigned>(a0 - g) / 4 : bytes / 4;
+    const unsigned nt = middle > 0 ? static_cast<unsigned>(g + bytes - a1) / 4 : 0u;
+    const unsigned tail0 = static_cast<unsigned>(a1 - g);
+    float v[8];
+#pragma unroll
+    for (unsigned k = 0; k < 8; ++k) {
+      const unsigned off = k < nh ? 4u * k : tail0 + 4u * (k - nh);
+      if (k < nh + nt) v[k] = __ldcg(reinterpret_cast<const float*>(g + off));
+    }
+#pragma unroll
+    for (unsigned k = 0; k < 8; ++k) {
+      const unsigned off = k < nh ? 4u * k : tail0 + 4u * (k - nh);
+      if (k < nh + nt) *reinterpret_cast<float*>(dst + off) = v[k];
+    }
+  }
+}
+
+// 16-byte global -> shared copy that completes asynchronously;
+// cp_async_wait_all waits for all of this thread's copies.
+__device__ __forceinline__ void cp_async_16(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem_dst)), "l"(gmem_src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Store one round of up to 32 consecutive entries as contiguous floats with
+// coalesced stores (transposed through the warp's `out`).
+__device__ __forceinline__ void store_round(float* __restrict__ dst, int n_round, float v0, float v1, float v2,
+                                            float* out) {
+  const int lane = threadIdx.x & 31;
+  if (lane < n_round) {
+    out[3 * lane + 0] = v0;
+    out[3 * lane + 1] = v1;
+    out[3 * lane + 2] = v2;
+  }
+  __syncwarp();
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    const int idx = k * 32 + lane;
+    if (idx < 3 * n_round) dst[idx] = out[idx];
+  }
+  __syncwarp();
+}
+
+// Coordinates of one staged unit: every pulse's gathers.
+__device__ __forceinline__ void coords_unit(float* __restrict__ x, const TileParams& P, const TileUnit& d,
+                                            WarpSmem<0>& S) {
+  const int lane = threadIdx.x & 31;
+  const float* tile = reinterpret_cast<const float*>(
+      S.stage + (reinterpret_cast<unsigned long long>(x + 3 * d.base) & 15ull));
+  for (int s = 0; s < d.seg_cnt; ++s) {
+    const TileSeg sg = seg_at(P, d, s);
+    const int32_t* smap = reinterpret_cast<const int32_t*>(
+        S.stage + sg.map_off + (reinterpret_cast<unsigned long long>(P.maps + sg.map) & 15ull));
+    float* dst = x + 3 * sg.other;
+    for (int i0 = 0; i0 < sg.n; i0 += 32) {
+      const int i = i0 + lane;
+      const int n_round = sg.n - i0;
+      float v0 = 0.f, v1 = 0.f, v2 = 0.f;
+      if (i < sg.n) {
+        const int j = smap[i] - d.local_a;
+        v0 = tile[3 * j + 0];
+        v1 = tile[3 * j + 1];
+        v2 = tile[3 * j + 2];
+        if (sg.do_shift) {   // no add otherwise: unshifted values keep every bit (-0.0 included)
+          if (sg.dim == 0) v0 = __fadd_rn(v0, sg.shift);
+          else if (sg.dim == 1) v1 = __fadd_rn(v1, sg.shift);
+          else v2 = __fadd_rn(v2, sg.shift);
+        }
+      }
+      store_round(dst + 3 * i0, n_round < 32 ? n_round : 32, v0, v1, v2, S.out);
+    }
+  }
+}
+
+// Forces of one staged unit: each segment's received run added into the
+// slots, segments in list order (last pulse first), a warp barrier between
+// segments since one slot can be a target in several pulses; entries of one
+// segment have distinct targets. Then the slots are written back: float4
+// stores for the 16-byte-aligned middle (the stage keeps the global address
+// mod 16), plain stores for the words around it.
+__device__ __forceinline__ void forces_unit(float* __restrict__ f, const TileParams& P, const TileUnit& d,
+                                            WarpSmem<1>& S) {
+  const int lane = threadIdx.x & 31;
+  const unsigned long long gt = reinterpret_cast<unsigned long long>(f + 3 * d.base);
+  float* tile = reinterpret_cast<float*>(S.stage + (gt & 15ull));
+  for (int s = 0; s < d.seg_cnt; ++s) {
+    const TileSeg sg = seg_at(P, d, s);
+    const int32_t* smap = reinterpret_cast<const int32_t*>(
+        S.stage + sg.map_off + (reinterpret_cast<unsigned long long>(P.maps + sg.map) & 15ull));
+    const float* src = reinterpret_cast<const float*>(
+        S.stage + sg.src_off + (reinterpret_cast<unsigned long long>(f + 3 * sg.other) & 15ull));
+    for (int i = lane; i < sg.n; i += 32) {
+      float* t = tile + 3 * (smap[i] - d.local_a);
+      t[0] = __fadd_rn(t[0], src[3 * i + 0]);
+      t[1] = __fadd_rn(t[1], src[3 * i + 1]);
+      t[2] = __fadd_rn(t[2], src[3 * i + 2]);
+    }
+    __syncwarp();   // the next (earlier) pulse adds after this one
+  }
+  const unsigned bytes = 12u * static_cast<unsigned>(d.n);
+  const unsigned long long a0 = (gt + 15ull) & ~15ull, a1 = (gt + bytes) & ~15ull;
+  if (a1 > a0) {
+    const unsigned head = static_cast<unsigned>(a0 - gt) / 4, tail = static_cast<unsigned>(gt + bytes - a1) / 4;
+    const int n4 = static_cast<int>((a1 - a0) / 16);
+    const float4* s4 = reinterpret_cast<const float4*>(tile + head);
+    float4* d4 = reinterpret_cast<float4*>(a0);
+    for (int q = lane; q < n4; q += 32) d4[q] = s4[q];
+    if (lane < static_cast<int>(head)) f[3 * d.base + lane] = tile[lane];
+    else if (lane >= 4 && lane < 4 + static_cast<int>(tail)) {
+      const int k = static_cast<int>((a1 - gt) / 4) + (lane - 4);
+      f[3 * d.base + k] = tile[k];
+    }
+  } else {
+    for (int k = lane; k < 3 * d.n; k += 32) f[3 * d.base + k] = tile[k];
+  }
+}
+
+// KIND 0 = coordinates, 1 = forces (ordered).
+template <int KIND>
+__global__ void __launch_bounds__(kThreads) k_sweep(float* __restrict__ buf, TileParams P) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const int lane = threadIdx.x & 31;
+  WarpSmem<KIND>& S = reinterpret_cast<WarpSmem<KIND>*>(smem_raw)[threadIdx.x >> 5];
+  const unsigned long long W = static_cast<unsigned long long>(gridDim.x) * kWarps;
+  const unsigned long long N = P.n_units;
+  unsigned long long c = static_cast<unsigned long long>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+  if (c >= N) return;
+  const int drop_item = *reinterpret_cast<const volatile int*>(&P.ctrl->drop_item);
+  if (lane == 0) {
+    mbar_init(&S.bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncwarp();
+  unsigned parity = 0;
+  // The warp's first unit is its global index; each ticket names one more
+  // (ticket t of the launch -> unit t - base + W). The next unit's record is
+  // copied in while the current unit is staged and processed. A warp holds up
+  // to three claims (current, next, the ticket after it) and works through
+  // them in list order, which keeps the topological order deadlock-free.
+  unsigned long long t = 0;
+  if (lane == 0) t = atomicAdd(&P.ctrl->ticket, 1ull);
+  if (lane < 16) cp_async_16(reinterpret_cast<int4*>(&S.desc[0]) + lane, reinterpret_cast<const int4*>(P.units + c) + lane);
+  cp_async_wait_all();
+  __syncwarp();
+  t = __shfl_sync(kFull, t, 0);
+  const unsigned long long base = t - t % N;   // every ticket of one launch lies in [base, base + N)
+  const unsigned long long epoch = base / N + 1ull;
+  int b = 0;
+  while (true) {
+    const unsigned long long cn = (t - base) + W;   // this warp's next unit
+    if (cn < N) {
+      if (lane == 0) t = atomicAdd(&P.ctrl->ticket, 1ull);
+      if (lane < 16)
+        cp_async_16(reinterpret_cast<int4*>(&S.desc[b ^ 1]) + lane, reinterpret_cast<const int4*>(P.units + cn) + lane);
+    }
+    const TileUnit& d = S.desc[b];
+    if (d.wait_cnt > 0) {
+      wait_units(P, d, epoch);
+      // bulk copies (async proxy) then read what other warps stored (generic proxy) before their signals
+      if (lane == 0) asm volatile("fence.proxy.async.global;" ::: "memory");
+      __syncwarp();
+    }
+    stage_unit<KIND>(buf, P, d, S.stage, &S.bar);
+    if (!mbar_wait(&S.bar, parity, P.timeout_ns)) {
+      if (lane == 0) record_timeout(P, d.item);
+    }
+    parity ^= 1u;
+    __syncwarp();   // the lanes' edge words are in place
+    if constexpr (KIND == 0) coords_unit(buf, P, d, S);
+    else forces_unit(buf, P, d, S);
+    if (d.flags & kSignal) {
+      __syncwarp();   // every lane's stores precede lane 0's release
+      if (lane == 0 && d.item != drop_item) st_release_u64(P.flags + c, epoch);
+    }
+    if (cn >= N) break;
+    cp_async_wait_all();   // the next record
+    __syncwarp();          // ... for every lane; the stage is rewritten for the next unit
+    t = __shfl_sync(kFull, t, 0);
+    c = cn;
+    b ^= 1;
+  }
+}
+
+}  // namespace
+
+const void* sweep_kernel(int kind) {
+  return kind == 0 ? reinterpret_cast<const void*>(&k_sweep<0>) : reinterpret_cast<const void*>(&k_sweep<1>);
+}
+
+size_t sweep_smem_bytes(int kind) { return kWarps * (kind == 0 ? sizeof(WarpSmem<0>) : sizeof(WarpSmem<1>)); }
+
+int sweep_blocks_per_sm(int kind) {
+  const void* fn = sweep_kernel(kind);
+  const size_t smem = sweep_smem_bytes(kind);
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
+    return 0;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kThreads, smem) != cudaSuccess) return 0;
+  return n;
+}
+
+}  // namespace hx

@@ -30,6 +30,8 @@ HX_FLAG_NO_GRAPH = 0x2
 HX_FLAG_COUNTER_SIGNAL = 0x4
 HX_FLAG_FINE_WAITS = 0x8
 HX_FLAG_TILES = 0x10
+HX_FLAG_SWEEP = 0x20
+HX_FLAG_SWEEP_FORCES = 0x40
 
 HX_MAX_PULSES = 32
 

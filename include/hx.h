@@ -78,10 +78,21 @@ typedef struct hx_ctx* hx_handle;
                                           chunks that wrote the slots it reads or, for forces, that
                                           add into its targets, each signalled by its own epoch flag
                                           (HX_FLAG_COUNTER_SIGNAL is then ignored) */
-#define HX_FLAG_TILES 0x10u            /* tile-staged kernels: each block copies a tile of up to 2048
-                                          consecutive slots into shared memory (TMA bulk copy) and serves
-                                          every pulse's gathers (coordinates) or reverse-ordered adds
-                                          (forces) from it; per-tile signals; same results bit for bit */
+#define HX_FLAG_TILES 0x10u            /* tile-staged kernels: a producer warp per block copies tiles of
+                                          up to 1024 consecutive slots of one sender into shared memory
+                                          (TMA bulk copies) and consumer warps serve every pulse's
+                                          gathers (coordinates) or reverse-ordered adds (forces) from
+                                          them; per-tile signals; same results bit for bit */
+#define HX_FLAG_SWEEP 0x20u            /* slot-sweep kernels: every warp takes units of up to 512
+                                          consecutive slots of one sender, copies them into its shared
+                                          memory with coalesced loads and serves every pulse's gathers
+                                          or reverse-ordered adds from them; per-unit signals; same
+                                          results bit for bit. Plans of more than 8 pulses get
+                                          HX_ERR_PULSES from hx_build_maps */
+#define HX_FLAG_SWEEP_FORCES 0x40u     /* the force exchange by the slot-sweep kernel, the coordinate
+                                          exchange by the chunk kernels (with HX_FLAG_FINE_WAITS or
+                                          the other chunk flags). At most one of HX_FLAG_TILES,
+                                          HX_FLAG_SWEEP and HX_FLAG_SWEEP_FORCES (else HX_ERR_ARG) */
 
 #define HX_MAX_PULSES 32
 #define HX_MAX_DOMAINS 4096
@@ -176,7 +187,7 @@ int hx_exchange_forces_unfused(hx_handle h, float* forces, void* stream);
  * have no counterpart: this concerns how the library holds its scratch.
  * The call never allocates: the kernel's signal flags, election counters and
  * control block live in one fixed file-scope device array of
- * HX_STATIC_MAX_FLAGS flags (about 384 KB, held by every GPU that loads the
+ * HX_STATIC_MAX_FLAGS flags (about 1.5 MB, held by every GPU that loads the
  * library until the process exits), cleared on `stream` at each call, and
  * the kernel is launched directly, without a CUDA graph. The first call on a
  * device looks up that array's device address (cudaGetSymbolAddress); make
@@ -186,9 +197,9 @@ int hx_exchange_forces_unfused(hx_handle h, float* forces, void* stream);
  * are recorded in that array, not in the handle (hx_status does not see
  * them). Errors: HX_ERR_ARG, HX_ERR_STATE, HX_ERR_CUDA, and HX_ERR_CAPACITY
  * when the handle's work list needs more than HX_STATIC_MAX_FLAGS signal
- * flags (its item count, chunk count or tile count, whichever it signals by);
+ * flags (its item count, chunk count or unit count, whichever it signals by);
  * nothing is launched then. */
-#define HX_STATIC_MAX_FLAGS 32768
+#define HX_STATIC_MAX_FLAGS 131072
 int hx_exchange_coords_static(hx_handle h, float* coords, void* stream);
 
 /* Launches one empty kernel the way the fused exchanges are launched (graph

@@ -18,7 +18,9 @@ pytestmark = pytest.mark.gpu
 ALL_MODES = [0, HX.HX_FLAG_COUNTER_SIGNAL, HX.HX_FLAG_NO_GRAPH,
              HX.HX_FLAG_COUNTER_SIGNAL | HX.HX_FLAG_NO_GRAPH, HX.HX_FLAG_FINE_WAITS,
              HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_COUNTER_SIGNAL, HX.HX_FLAG_TILES,
-             HX.HX_FLAG_TILES | HX.HX_FLAG_NO_GRAPH]
+             HX.HX_FLAG_TILES | HX.HX_FLAG_NO_GRAPH, HX.HX_FLAG_SWEEP,
+             HX.HX_FLAG_SWEEP | HX.HX_FLAG_NO_GRAPH, HX.HX_FLAG_SWEEP_FORCES,
+             HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES]
 
 
 def _bits(a):
@@ -117,7 +119,8 @@ def test_parity_configs(name, flags):
     check_force_steps(c)
 
 
-@pytest.mark.parametrize("flags", [0, HX.HX_FLAG_FINE_WAITS, HX.HX_FLAG_TILES])
+@pytest.mark.parametrize("flags", [0, HX.HX_FLAG_FINE_WAITS, HX.HX_FLAG_TILES, HX.HX_FLAG_SWEEP,
+                                   HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES])
 def test_parity_c5_full_size(flags):
     """12M atoms, 256 domains: the bench's configuration and launch path."""
     c = Case(W.WORKLOADS["C5"], flags=flags)
@@ -151,7 +154,8 @@ def test_unfused_baseline(name):
     ((3.0, 3.0, 3.0), (3, 3, 3), 0.6, 2700),      # 27 domains
     ((40.0, 3.0, 3.0), (40, 1, 1), 1.0, 36000),   # many small domains along one dim
 ])
-@pytest.mark.parametrize("flags", [0, HX.HX_FLAG_COUNTER_SIGNAL, HX.HX_FLAG_FINE_WAITS, HX.HX_FLAG_TILES])
+@pytest.mark.parametrize("flags", [0, HX.HX_FLAG_COUNTER_SIGNAL, HX.HX_FLAG_FINE_WAITS, HX.HX_FLAG_TILES,
+                                   HX.HX_FLAG_SWEEP, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES])
 def test_parity_shapes(box, dims, cutoff, n, flags):
     w = W.custom("shape", n, box, dims, cutoff, seed=7 + n)
     c = Case(w, flags=flags)
@@ -160,7 +164,7 @@ def test_parity_shapes(box, dims, cutoff, n, flags):
     check_force_steps(c)
 
 
-@pytest.mark.parametrize("flags", [0, HX.HX_FLAG_TILES])
+@pytest.mark.parametrize("flags", [0, HX.HX_FLAG_TILES, HX.HX_FLAG_SWEEP])
 def test_misaligned_buffers(flags):
     """Caller buffers that start 4 or 8 bytes past a 16-byte boundary (tile
     mode copies aligned middles in bulk and the edges with plain loads)."""
@@ -200,7 +204,8 @@ def test_boundary_atoms():
 
 def test_many_steps_reuse_signals():
     """Epoch-valued signals are never reset between launches: 200 steps."""
-    for flags in (0, HX.HX_FLAG_COUNTER_SIGNAL, HX.HX_FLAG_FINE_WAITS, HX.HX_FLAG_TILES):
+    for flags in (0, HX.HX_FLAG_COUNTER_SIGNAL, HX.HX_FLAG_FINE_WAITS, HX.HX_FLAG_TILES, HX.HX_FLAG_SWEEP,
+                  HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES):
         c = Case(W.WORKLOADS["C2"], flags=flags)
         x = c.o.coords().copy()
         xt = torch.from_numpy(x).cuda()
@@ -271,12 +276,18 @@ def test_errors():
     with pytest.raises(HX.HXError) as ei:
         hx.build_maps(pos, small)
     assert ei.value.code == HX.HX_ERR_CAPACITY
+    for bad in (HX.HX_FLAG_TILES | HX.HX_FLAG_SWEEP, HX.HX_FLAG_SWEEP | HX.HX_FLAG_SWEEP_FORCES,
+                HX.HX_FLAG_TILES | HX.HX_FLAG_SWEEP_FORCES):
+        with pytest.raises(HX.HXError) as ei:   # the unit kernel families are alternatives
+            HX.HaloExchange(w.box, w.dims, w.cutoff, flags=bad)
+        assert ei.value.code == HX.HX_ERR_ARG
     with pytest.raises(HX.HXError):
         HX.HaloExchange(w.box, w.dims, w.cutoff, device=torch.cuda.device_count())
 
 
 @pytest.mark.parametrize("direction", [0, 1])
-@pytest.mark.parametrize("flags", [0, HX.HX_FLAG_COUNTER_SIGNAL, HX.HX_FLAG_FINE_WAITS, HX.HX_FLAG_TILES])
+@pytest.mark.parametrize("flags", [0, HX.HX_FLAG_COUNTER_SIGNAL, HX.HX_FLAG_FINE_WAITS, HX.HX_FLAG_TILES,
+                                   HX.HX_FLAG_SWEEP, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES])
 def test_dropped_signal_times_out_and_recovers(direction, flags):
     """Failure detection without a device fault: a (domain, pulse) that never
     signals makes its waiters give up after the bounded wait; the kernel
@@ -301,9 +312,9 @@ def test_dropped_signal_times_out_and_recovers(direction, flags):
     assert detail // 65536 == direction
     item = detail % 65536
     p_item = item // nd
-    if flags & HX.HX_FLAG_TILES:
-        # a tile is labelled by its first map's (pulse, domain); a cascade can
-        # report any tile downstream of the dropped one
+    if flags & (HX.HX_FLAG_TILES | HX.HX_FLAG_SWEEP) or (direction == 1 and flags & HX.HX_FLAG_SWEEP_FORCES):
+        # a unit is labelled by its first map's (pulse, domain); a cascade can
+        # report any unit downstream of the dropped one
         assert 0 <= item < c.o.n_pulses * nd
     else:
         assert item == pulse * nd + 3 or (p_item > pulse if direction == 0 else p_item < pulse)
