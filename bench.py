@@ -98,9 +98,13 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# Sources of the fused exchange kernels that the profiles under profiles/ describe.
+KERNEL_SOURCES = ("hx_kernels.cu", "hx_sweep.cu", "hx_internal.h")
+
+
 def kernel_source_digest():
     h = hashlib.sha256()
-    for name in ("hx_kernels.cu", "hx_sweep.cu", "hx_internal.h"):
+    for name in KERNEL_SOURCES:
         with open(os.path.join(ROOT, "domain_decomposition_halo_gb300", "csrc", name), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

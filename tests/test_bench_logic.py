@@ -29,7 +29,7 @@ def test_flag_names():
 def test_traffic_needs_matching_digest(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     (tmp_path / "domain_decomposition_halo_gb300" / "csrc").mkdir(parents=True)
-    for name in ("hx_kernels.cu", "hx_internal.h"):
+    for name in bench.KERNEL_SOURCES:
         (tmp_path / "domain_decomposition_halo_gb300" / "csrc" / name).write_text("x")
     (tmp_path / "profiles").mkdir()
     digest = bench.kernel_source_digest()
