@@ -969,8 +969,8 @@ int build_tables(hx_ctx* h, cudaStream_t s) {
   for (int k = 0; k < 2; ++k) {
     if (h->family[k] == kFamTiles) {
       h->grid[k] = std::max(1, std::min(h->n_units[k], h->grid[k]));
-    } else if (h->family[k] == kFamSweep) {
-      const int warps = std::max(1, std::min(h->n_units[k], h->grid[k] * kWarps));
+    } else if (h->family[k] == kFamSweep) {   // one warp per batch of units
+      const int warps = std::max(1, std::min((h->n_units[k] + kSweepBatch - 1) / kSweepBatch, h->grid[k] * kWarps));
       h->grid[k] = (warps + kWarps - 1) / kWarps;
     } else {
       const int warps = std::max(1, std::min(h->n_chunks[k], h->grid[k] * kWarps));

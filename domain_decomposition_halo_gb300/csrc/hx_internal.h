@@ -173,6 +173,10 @@ enum Family : int { kFamChunks = 0, kFamTiles = 1, kFamSweep = 2 };
 #endif
 constexpr int kSweepSlots = HX_SWEEP_SLOTS;       // slots of one unit: a warp's staged tile
 constexpr int kSweepEntries = HX_SWEEP_ENTRIES;   // map entries of one unit at most
+#ifndef HX_SWEEP_BATCH
+#define HX_SWEEP_BATCH 2
+#endif
+constexpr int kSweepBatch = HX_SWEEP_BATCH;       // consecutive units claimed by one ticket
 constexpr int kSweepSegs = 8;                     // segments (pulses) of one unit at most
 static_assert(1 + 2 * kSweepSegs <= 32, "a sweep unit stages one run per lane");
 // Stage layout of one warp: slots, then map runs, then (forces) received

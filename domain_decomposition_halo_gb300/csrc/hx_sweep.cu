@@ -340,8 +340,10 @@ __global__ void __launch_bounds__(kThreads) k_sweep(float* __restrict__ buf, Til
   WarpSmem<KIND>& S = reinterpret_cast<WarpSmem<KIND>*>(smem_raw)[threadIdx.x >> 5];
   const unsigned long long W = static_cast<unsigned long long>(gridDim.x) * kWarps;
   const unsigned long long N = P.n_units;
-  unsigned long long c = static_cast<unsigned long long>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
-  if (c >= N) return;
+  const unsigned long long NB = (N + kSweepBatch - 1) / kSweepBatch;   // batches of units per launch
+  const unsigned long long b0 = static_cast<unsigned long long>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+  if (b0 >= NB) return;
+  unsigned long long c = b0 * kSweepBatch;
   const int drop_item = *reinterpret_cast<const volatile int*>(&P.ctrl->drop_item);
   if (lane == 0) {
     mbar_init(&S.bar, 1);
@@ -349,24 +351,28 @@ __global__ void __launch_bounds__(kThreads) k_sweep(float* __restrict__ buf, Til
   }
   __syncwarp();
   unsigned parity = 0;
-  // The warp's first unit is its global index; each ticket names one more
-  // (ticket t of the launch -> unit t - base + W). The next unit's record is
-  // copied in while the current unit is staged and processed. A warp holds up
-  // to three claims (current, next, the ticket after it) and works through
-  // them in list order, which keeps the topological order deadlock-free.
+  // Units are claimed in batches of kSweepBatch consecutive units. The
+  // warp's first batch is its global index; each ticket, drawn when the warp
+  // starts a batch, names its following batch (ticket t of the launch ->
+  // batch t - base + W), so a launch draws exactly NB tickets. The next
+  // unit's record is copied in while the current unit is staged and
+  // processed. A warp works through its claims in list order, which keeps
+  // the topological order deadlock-free.
   unsigned long long t = 0;
   if (lane == 0) t = atomicAdd(&P.ctrl->ticket, 1ull);
   if (lane < 16) cp_async_16(reinterpret_cast<int4*>(&S.desc[0]) + lane, reinterpret_cast<const int4*>(P.units + c) + lane);
   cp_async_wait_all();
   __syncwarp();
   t = __shfl_sync(kFull, t, 0);
-  const unsigned long long base = t - t % N;   // every ticket of one launch lies in [base, base + N)
-  const unsigned long long epoch = base / N + 1ull;
+  const unsigned long long base = t - t % NB;   // every ticket of one launch lies in [base, base + NB)
+  const unsigned long long epoch = base / NB + 1ull;
   int b = 0;
   while (true) {
-    const unsigned long long cn = (t - base) + W;   // this warp's next unit
+    const bool same_batch = (c + 1) % kSweepBatch != 0;
+    const unsigned long long cn = same_batch ? c + 1 : ((t - base) + W) * kSweepBatch;   // this warp's next unit
+    const bool new_ticket = !same_batch && cn < N;
     if (cn < N) {
-      if (lane == 0) t = atomicAdd(&P.ctrl->ticket, 1ull);
+      if (new_ticket && lane == 0) t = atomicAdd(&P.ctrl->ticket, 1ull);
       if (lane < 16)
         cp_async_16(reinterpret_cast<int4*>(&S.desc[b ^ 1]) + lane, reinterpret_cast<const int4*>(P.units + cn) + lane);
     }
@@ -392,7 +398,7 @@ __global__ void __launch_bounds__(kThreads) k_sweep(float* __restrict__ buf, Til
     if (cn >= N) break;
     cp_async_wait_all();   // the next record
     __syncwarp();          // ... for every lane; the stage is rewritten for the next unit
-    t = __shfl_sync(kFull, t, 0);
+    if (new_ticket) t = __shfl_sync(kFull, t, 0);
     c = cn;
     b ^= 1;
   }
