@@ -384,7 +384,12 @@ def secondary(hx_main, coords, forces, w_main, dev, peak, flags):
             ts.append(a.elapsed_time(b) * 1e3)
         return statistics.median(ts)
 
-    res = {"overlap_with_local_kernel_us": overlap_probe(dev, flags)}
+    # the probe in the run's modes, and with both directions on the chunk kernels
+    from domain_decomposition_halo_gb300 import hx as HX
+    chunk_flags = flags & ~(HX.HX_FLAG_SWEEP | HX.HX_FLAG_SWEEP_FORCES | HX.HX_FLAG_TILES)
+    res = {"overlap_with_local_kernel_us": {"run_modes": overlap_probe(dev, flags)}}
+    if chunk_flags != flags:
+        res["overlap_with_local_kernel_us"]["chunk_kernels"] = overlap_probe(dev, chunk_flags)
     entries = hx_main.counts()[3]
     cold = timed(hx_main, coords, forces, 30, True)
     res[w_main.name + "_cold_l2"] = {"us_step": round(cold, 2),

@@ -56,9 +56,10 @@ struct Wait {
 // Per-direction control block (device memory; zeroed at build and by
 // hx_clear_status, never reset between launches).
 struct Ctrl {
-  unsigned long long ticket;  // chunk tickets handed out since the last reset; a
-                              // launch takes exactly n_chunks, so ticket / n_chunks
-                              // numbers the launch (its epoch is that + 1)
+  unsigned long long ticket;  // work tickets handed out since the last reset; every
+                              // launch draws the same number (fixed by its work list
+                              // and grid), so ticket / that number numbers the launch
+                              // (its epoch is that + 1)
   int status;                 // 0 or an HX_ERR_* code (sticky)
   int detail;                 // item of the first wait that gave up
   int drop_item;              // debug: item whose signals are dropped, or -1
