@@ -58,7 +58,8 @@ def hx_flags(spec: str) -> int:
     from domain_decomposition_halo_gb300 import hx as HX
     table = {"fine": HX.HX_FLAG_FINE_WAITS, "counter": HX.HX_FLAG_COUNTER_SIGNAL, "nograph": HX.HX_FLAG_NO_GRAPH,
              "unordered": HX.HX_FLAG_UNORDERED_FORCES, "tiles": HX.HX_FLAG_TILES, "sweep": HX.HX_FLAG_SWEEP,
-             "sweepf": HX.HX_FLAG_SWEEP_FORCES, "pages": 0, "": 0}
+             "sweepf": HX.HX_FLAG_SWEEP_FORCES, "cluster": HX.HX_FLAG_CLUSTER,
+             "resolved": HX.HX_FLAG_RESOLVED, "pages": 0, "": 0}
     flags = 0
     for name in spec.split(","):
         flags |= table[name.strip()]

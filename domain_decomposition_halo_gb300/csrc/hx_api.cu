@@ -191,6 +191,10 @@ struct hx_ctx {
   int n_units[2] = {0, 0};
   std::vector<int> u_begin;                  // per pulse, first unfused chunk (P + 1 entries)
   std::vector<GraphEntry> graphs;
+  int2* d_res_halo = nullptr;                // resolved mode: (slot, origin) per halo slot
+  uint8_t* d_res_mask = nullptr;             // ... and its shift mask
+  TreeRec* d_res_trees = nullptr;            // ... and the force trees
+  int64_t n_res_halo = 0, n_res_trees = 0;
 };
 
 namespace {
@@ -209,6 +213,10 @@ void free_tables(hx_ctx* h) {
     dev_free(h->d_waits[k]);
   }
   dev_free(h->d_uchunks);
+  dev_free(h->d_res_halo);
+  dev_free(h->d_res_mask);
+  dev_free(h->d_res_trees);
+  h->n_res_halo = h->n_res_trees = 0;
   for (int k = 0; k < 2; ++k) {
     dev_free(h->d_units[k]);
     dev_free(h->d_segs[k]);
@@ -275,16 +283,46 @@ TileParams tile_params(hx_ctx* h, int dir) {
 }
 
 // Work items of the fused list of direction `dir`: units or chunks.
-int work_items(const hx_ctx* h, int dir) { return h->family[dir] == kFamChunks ? h->n_chunks[dir] : h->n_units[dir]; }
+int work_items(const hx_ctx* h, int dir) {
+  if (h->family[dir] == kFamCluster) return h->u_begin.empty() ? 0 : h->u_begin.back();
+  if (h->family[dir] == kFamResolved) return static_cast<int>(dir == 0 ? h->n_res_halo : h->n_res_trees);
+  return h->family[dir] == kFamChunks ? h->n_chunks[dir] : h->n_units[dir];
+}
 
 // Launch shape of a direction's fused kernel.
 const void* fused_kernel(hx_ctx* h, int dir) {
   if (h->family[dir] == kFamTiles) return tiles_kernel(dir);
   if (h->family[dir] == kFamSweep) return sweep_kernel(dir);
+  if (h->family[dir] == kFamCluster) return cluster_kernel(dir);
+  if (h->family[dir] == kFamResolved) return resolved_kernel(dir);
   return kernel_for(h, dir);
 }
 unsigned fused_threads(const hx_ctx* h, int dir) {
+  if (h->family[dir] == kFamCluster) return kClusterThreads;
+  if (h->family[dir] == kFamResolved) return 256;
   return h->family[dir] == kFamTiles ? kTileThreads : kThreads;
+}
+
+ResolvedParams resolved_params(hx_ctx* h) {
+  ResolvedParams P;
+  std::memset(&P, 0, sizeof(P));
+  P.halo = h->d_res_halo;
+  P.shift_mask = h->d_res_mask;
+  P.trees = h->d_res_trees;
+  P.n_halo = h->n_res_halo;
+  P.n_trees = h->n_res_trees;
+  for (int d = 0; d < 3; ++d) P.box[d] = h->pl.boxf[d];
+  return P;
+}
+
+ClusterParams cluster_params(hx_ctx* h) {
+  ClusterParams P;
+  std::memset(&P, 0, sizeof(P));
+  P.chunks = h->d_uchunks;
+  P.maps = h->d_maps;
+  P.n_pulses = h->pl.n_pulses;
+  for (int p = 0; p <= h->pl.n_pulses; ++p) P.begin[p] = h->u_begin[p];
+  return P;
 }
 size_t fused_smem(const hx_ctx* h, int dir) {
   if (h->family[dir] == kFamTiles) return tiles_smem_bytes(dir);
@@ -295,12 +333,30 @@ size_t fused_smem(const hx_ctx* h, int dir) {
 int launch(hx_ctx* h, int kind, float* buf, cudaStream_t s) {
   DirParams P;
   TileParams TP;
+  ClusterParams CP;
+  ResolvedParams RP;
   void* args2[2];
   void** args = nullptr;
   dim3 grid(1), block(kind == 2 ? 1 : kThreads);
   size_t smem = 0;
   const void* fn = kernel_for(h, kind);
-  if (kind != 2 && h->family[kind] != kFamChunks) {
+  if (kind != 2 && h->family[kind] == kFamResolved) {
+    RP = resolved_params(h);
+    args2[0] = &buf;
+    args2[1] = &RP;
+    args = args2;
+    grid = dim3(static_cast<unsigned>(h->grid[kind]));
+    block = dim3(256);
+    fn = resolved_kernel(kind);
+  } else if (kind != 2 && h->family[kind] == kFamCluster) {
+    CP = cluster_params(h);
+    args2[0] = &buf;
+    args2[1] = &CP;
+    args = args2;
+    grid = dim3(kClusterCtas);
+    block = dim3(kClusterThreads);
+    fn = cluster_kernel(kind);
+  } else if (kind != 2 && h->family[kind] != kFamChunks) {
     TP = tile_params(h, kind);
     args2[0] = &buf;
     args2[1] = &TP;
@@ -664,6 +720,78 @@ int build_tile_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::
   return HX_OK;
 }
 
+// Resolved tables: every halo slot's origin and shift mask (pulses in order,
+// each received slot inheriting from the slot it was sent from), and one
+// tree per home atom that has copies, its adds sorted by descending pulse.
+int build_resolved_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::vector<int32_t>& maps,
+                          cudaStream_t s) {
+  const Plan& pl = h->pl;
+  const int P = pl.n_pulses, nd = pl.ndom;
+  const int64_t S = h->total_slots;
+  if (S >= (int64_t{1} << 31)) return HX_ERR_CAPACITY;   // slots are int32 in the records
+  std::vector<int32_t> origin(S), parent(S, -1);
+  std::vector<uint8_t> mask(S, 0), pulse(S, 0);
+  for (int64_t k = 0; k < S; ++k) origin[k] = static_cast<int32_t>(k);
+  for (int p = 0; p < P; ++p)
+    for (int r = 0; r < nd; ++r) {
+      const ItemInfo& it = items[p * nd + r];
+      for (int i = 0; i < it.size; ++i) {
+        const int64_t dst = it.dst + i, src = it.src + maps[it.map + i];
+        origin[dst] = origin[src];
+        mask[dst] = static_cast<uint8_t>(mask[src] | (it.shift_flag ? 1 << it.dim : 0));
+        parent[dst] = static_cast<int32_t>(src);
+        pulse[dst] = static_cast<uint8_t>(p);
+      }
+    }
+  std::vector<int2> halo;
+  std::vector<uint8_t> hmask;
+  std::vector<int32_t> tree_of(S, -1), node_idx(S, 0);
+  std::vector<TreeRec> trees;
+  for (int r = 0; r < nd; ++r)
+    for (int64_t k = h->dom_offset[r] + h->home[r]; k < h->dom_offset[r] + h->home[r] + h->halo[r]; ++k) {
+      halo.push_back(make_int2(static_cast<int>(k), origin[k]));
+      hmask.push_back(mask[k]);
+      int32_t& t = tree_of[origin[k]];
+      if (t < 0) {
+        t = static_cast<int32_t>(trees.size());
+        TreeRec rec;
+        std::memset(&rec, 0, sizeof(rec));
+        rec.node[0] = origin[k];
+        rec.n_nodes = 1;
+        trees.push_back(rec);
+      }
+      TreeRec& rec = trees[t];
+      if (rec.n_nodes >= kTreeNodes) return HX_ERR_PULSES;   // more copies than a tree record holds
+      node_idx[k] = rec.n_nodes;
+      rec.node[rec.n_nodes++] = static_cast<int32_t>(k);
+    }
+  for (TreeRec& rec : trees) {
+    int order[kTreeNodes];
+    const int m = rec.n_nodes - 1;   // copies = adds
+    for (int j = 0; j < m; ++j) order[j] = j + 1;
+    std::stable_sort(order, order + m, [&](int a, int b) { return pulse[rec.node[a]] > pulse[rec.node[b]]; });
+    for (int e = 0; e < m; ++e) {
+      const int32_t src = rec.node[order[e]];
+      const int32_t par = parent[src];
+      const int tg = par == rec.node[0] ? 0 : node_idx[par];
+      rec.ev[e] = static_cast<uint8_t>(tg | (order[e] << 4));
+    }
+  }
+  h->n_res_halo = static_cast<int64_t>(halo.size());
+  h->n_res_trees = static_cast<int64_t>(trees.size());
+  HX_CUDA(dev_alloc(&h->d_res_halo, halo.size()));
+  HX_CUDA(dev_alloc(&h->d_res_mask, hmask.size()));
+  HX_CUDA(dev_alloc(&h->d_res_trees, trees.size()));
+  if (!halo.empty()) {
+    HX_CUDA(cudaMemcpyAsync(h->d_res_halo, halo.data(), sizeof(int2) * halo.size(), cudaMemcpyHostToDevice, s));
+    HX_CUDA(cudaMemcpyAsync(h->d_res_mask, hmask.data(), hmask.size(), cudaMemcpyHostToDevice, s));
+  }
+  if (!trees.empty())
+    HX_CUDA(cudaMemcpyAsync(h->d_res_trees, trees.data(), sizeof(TreeRec) * trees.size(), cudaMemcpyHostToDevice, s));
+  HX_CUDA(cudaStreamSynchronize(s));   // the host vectors go out of scope
+  return HX_OK;
+}
+
 // Work tables of the fused and unfused kernels from the host copy of the plan.
 int build_tables(hx_ctx* h, cudaStream_t s) {
   const Plan& pl = h->pl;
@@ -688,7 +816,8 @@ int build_tables(hx_ctx* h, cudaStream_t s) {
       it.shift_flag = h->t_shift[t];
     }
   std::vector<int32_t> maps;
-  if ((fine || (h->flags & (HX_FLAG_TILES | HX_FLAG_SWEEP | HX_FLAG_SWEEP_FORCES))) && h->total_entries > 0) {   // fine waits and units read the maps
+  if ((fine || (h->flags & (HX_FLAG_TILES | HX_FLAG_SWEEP | HX_FLAG_SWEEP_FORCES | HX_FLAG_RESOLVED))) &&
+      h->total_entries > 0) {   // fine waits, units and resolved tables read the maps
     maps.resize(h->total_entries);
     HX_CUDA(cudaMemcpy(maps.data(), h->d_maps, sizeof(int32_t) * h->total_entries, cudaMemcpyDeviceToHost));
   }
@@ -698,12 +827,18 @@ int build_tables(hx_ctx* h, cudaStream_t s) {
   auto upper = [&](int r, int q) { return upper_tab[static_cast<size_t>(r) * P + q]; };
   std::vector<int64_t> rank(nd);
   for (int r = 0; r < nd; ++r) rank[r] = domain_rank(pl, r);
-  h->family[0] = (h->flags & HX_FLAG_TILES) ? kFamTiles : (h->flags & HX_FLAG_SWEEP) ? kFamSweep : kFamChunks;
+  h->family[0] = (h->flags & HX_FLAG_TILES)     ? kFamTiles
+                 : (h->flags & HX_FLAG_SWEEP)   ? kFamSweep
+                 : (h->flags & HX_FLAG_CLUSTER) ? kFamCluster
+                 : (h->flags & HX_FLAG_RESOLVED) ? kFamResolved
+                                                : kFamChunks;
   h->family[1] = (h->flags & (HX_FLAG_SWEEP | HX_FLAG_SWEEP_FORCES)) ? kFamSweep : h->family[0];
   for (int k = 0; k < 2; ++k) {
-    const int per_sm = std::max(1, h->family[k] == kFamTiles   ? tiles_blocks_per_sm(k)
-                                   : h->family[k] == kFamSweep ? sweep_blocks_per_sm(k)
-                                                               : max_blocks_per_sm(kernel_for(h, k)));
+    const int per_sm = std::max(1, h->family[k] == kFamTiles     ? tiles_blocks_per_sm(k)
+                                   : h->family[k] == kFamSweep   ? sweep_blocks_per_sm(k)
+                                   : h->family[k] == kFamCluster ? 1
+                                   : h->family[k] == kFamResolved ? 1
+                                                                 : max_blocks_per_sm(kernel_for(h, k)));
     h->grid[k] = per_sm * h->sm_count;   // upper bound; trimmed to the work count below
   }
   // Unit lists. A dependent unit is placed a few resident windows after the
@@ -930,6 +1065,11 @@ int build_tables(hx_ctx* h, cudaStream_t s) {
       HX_CUDA(cudaMemcpy(h->d_waits[dir], waits.data(), sizeof(Wait) * waits.size(), cudaMemcpyHostToDevice));
   }
 
+  if (h->family[0] == kFamResolved) {
+    const int rc = build_resolved_tables(h, items, maps, s);
+    if (rc != HX_OK) return rc;
+  }
+
   // Unfused: per pulse, every item's entries in sender order, no waits or signals.
   std::vector<Chunk> uch;
   h->u_begin.assign(P + 1, 0);
@@ -967,7 +1107,12 @@ int build_tables(hx_ctx* h, cudaStream_t s) {
   // Persistent grid: every warp (tile mode: every block) co-resident, and no
   // more of them than there is work.
   for (int k = 0; k < 2; ++k) {
-    if (h->family[k] == kFamTiles) {
+    if (h->family[k] == kFamResolved) {
+      const int64_t n = k == 0 ? h->n_res_halo : h->n_res_trees;
+      h->grid[k] = static_cast<int>(std::max<int64_t>(1, (n + 255) / 256));
+    } else if (h->family[k] == kFamCluster) {
+      h->grid[k] = kClusterCtas;   // exactly one cluster
+    } else if (h->family[k] == kFamTiles) {
       h->grid[k] = std::max(1, std::min(h->n_units[k], h->grid[k]));
     } else if (h->family[k] == kFamSweep) {   // one warp per batch of units
       const int warps = std::max(1, std::min((h->n_units[k] + kSweepBatch - 1) / kSweepBatch, h->grid[k] * kWarps));
@@ -1213,6 +1358,16 @@ int hx::launch_coords_with_scratch(hx_ctx* h, float* coords, cudaStream_t s, Ctr
   if (!coords && h->total_slots > 0) return HX_ERR_ARG;
   const int work = work_items(h, 0);
   if (h->pl.n_pulses == 0 || work == 0) return HX_OK;
+  if (h->family[0] == kFamResolved) {   // no dependencies, no scratch at all
+    ResolvedParams RP = resolved_params(h);
+    void* rargs[2] = {&coords, &RP};
+    return to_err(cudaLaunchKernel(resolved_kernel(0), dim3(static_cast<unsigned>(h->grid[0])), dim3(256), rargs, 0, s));
+  }
+  if (h->family[0] == kFamCluster) {   // cluster barriers, no scratch at all
+    ClusterParams CP = cluster_params(h);
+    void* cargs[2] = {&coords, &CP};
+    return to_err(cudaLaunchKernel(cluster_kernel(0), dim3(kClusterCtas), dim3(kClusterThreads), cargs, 0, s));
+  }
   // flags are indexed by item (pulse signals) or by list position (chunk / tile signals)
   const size_t need = std::max<size_t>(static_cast<size_t>(h->pl.n_pulses) * h->pl.ndom, static_cast<size_t>(work));
   if (need > max_flags) return HX_ERR_CAPACITY;
@@ -1291,7 +1446,8 @@ int hx_init(hx_handle* out, const double box[3], const int dims[3], double cutof
   if (!h) return HX_ERR_NOMEM;
   h->pl = pl;
   h->device = device;
-  const unsigned families = flags & (HX_FLAG_TILES | HX_FLAG_SWEEP | HX_FLAG_SWEEP_FORCES);
+  const unsigned families =
+      flags & (HX_FLAG_TILES | HX_FLAG_SWEEP | HX_FLAG_SWEEP_FORCES | HX_FLAG_CLUSTER | HX_FLAG_RESOLVED);
   if (families & (families - 1)) {   // at most one of the alternative kernel families
     delete h;
     return HX_ERR_ARG;

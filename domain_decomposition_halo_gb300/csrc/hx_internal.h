@@ -4,6 +4,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "hx.h"
+
 struct hx_ctx;
 
 namespace hx {
@@ -98,6 +100,38 @@ const void* forces_kernel(int signal_mode, bool ordered);
 const void* noop_kernel();
 int max_blocks_per_sm(const void* fn);
 cudaError_t launch_pack_pulse(float* x, const PulseParams& p, cudaStream_t s);
+
+// ---- cluster kernels (hx_kernels.cu): one thread-block cluster walks the pulses ----
+constexpr int kClusterCtas = 8;           // CTAs of the one cluster (portable cluster size)
+constexpr int kClusterThreads = 512;      // threads per CTA
+struct ClusterParams {
+  const Chunk* chunks;                    // the per-pulse chunk list, pulse after pulse
+  const int32_t* maps;
+  int begin[HX_MAX_PULSES + 1];           // first chunk of each pulse; begin[n_pulses] = end
+  int n_pulses;
+  int pad;
+};
+const void* cluster_kernel(int kind);     // 0 coordinates, 1 forces (ordered)
+
+// ---- resolved kernels (hx_resolved.cu): the forwarding unrolled at build time ----
+constexpr int kTreeNodes = 8;             // a home atom and at most 7 copies
+struct alignas(16) TreeRec {
+  int32_t node[kTreeNodes];               // global slots; node[0] is the home atom
+  uint8_t ev[kTreeNodes];                 // adds in order: target (low 4 bits) += source (high 4 bits)
+  int32_t n_nodes;                        // nodes used; n_nodes - 1 adds
+  int32_t pad;
+};
+static_assert(sizeof(TreeRec) == 48, "tree record must stay 48 bytes");
+struct ResolvedParams {
+  const int2* halo;                       // per halo slot: (slot, origin home slot)
+  const uint8_t* shift_mask;              // per halo slot: bit d = add box[d] to component d
+  const TreeRec* trees;                   // home atoms that have copies
+  int64_t n_halo;
+  int64_t n_trees;
+  float box[3];
+  int pad;
+};
+const void* resolved_kernel(int kind);    // 0 coordinates, 1 forces (ordered)
 cudaError_t launch_unpack_pulse(float* f, const PulseParams& p, cudaStream_t s);
 
 // ---- tile kernels (hx_tiles.cu) ----
@@ -163,7 +197,7 @@ size_t tiles_smem_bytes(int kind);
 int tiles_blocks_per_sm(int kind);
 
 // Kernel family of one direction's fused exchange.
-enum Family : int { kFamChunks = 0, kFamTiles = 1, kFamSweep = 2 };
+enum Family : int { kFamChunks = 0, kFamTiles = 1, kFamSweep = 2, kFamCluster = 3, kFamResolved = 4 };
 
 // ---- slot-sweep kernels (hx_sweep.cu): one warp per unit, same unit records ----
 #ifndef HX_SWEEP_SLOTS

@@ -32,6 +32,8 @@ HX_FLAG_FINE_WAITS = 0x8
 HX_FLAG_TILES = 0x10
 HX_FLAG_SWEEP = 0x20
 HX_FLAG_SWEEP_FORCES = 0x40
+HX_FLAG_CLUSTER = 0x80
+HX_FLAG_RESOLVED = 0x100
 
 HX_MAX_PULSES = 32
 

@@ -92,7 +92,24 @@ typedef struct hx_ctx* hx_handle;
 #define HX_FLAG_SWEEP_FORCES 0x40u     /* the force exchange by the slot-sweep kernel, the coordinate
                                           exchange by the chunk kernels (with HX_FLAG_FINE_WAITS or
                                           the other chunk flags). At most one of HX_FLAG_TILES,
-                                          HX_FLAG_SWEEP and HX_FLAG_SWEEP_FORCES (else HX_ERR_ARG) */
+                                          HX_FLAG_SWEEP, HX_FLAG_SWEEP_FORCES, HX_FLAG_CLUSTER and
+                                          HX_FLAG_RESOLVED (else HX_ERR_ARG) */
+#define HX_FLAG_CLUSTER 0x80u          /* both directions by one thread-block cluster of 8 CTAs that
+                                          walks the pulses in order (forces in reverse), with a
+                                          cluster barrier (release/acquire) between pulses instead of
+                                          flags: for small decompositions, where the launch and the
+                                          dependency chain set the step time. Forces are ordered
+                                          (HX_FLAG_UNORDERED_FORCES is ignored); there are no
+                                          device waits, so no time-outs and no signal to drop */
+#define HX_FLAG_RESOLVED 0x100u        /* the forwarding unrolled at build time: every halo slot is
+                                          gathered straight from its origin home atom (plus the
+                                          shifts its path added), and every home atom's force tree
+                                          (the atom and its copies) is summed in the staged order
+                                          by one thread; one independent pass per direction, same
+                                          results bit for bit. Forces are ordered
+                                          (HX_FLAG_UNORDERED_FORCES is ignored); no device waits.
+                                          A home atom may have at most 7 copies (else HX_ERR_PULSES
+                                          from hx_build_maps) */
 
 #define HX_MAX_PULSES 32
 #define HX_MAX_DOMAINS 4096

@@ -20,7 +20,9 @@ ALL_MODES = [0, HX.HX_FLAG_COUNTER_SIGNAL, HX.HX_FLAG_NO_GRAPH,
              HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_COUNTER_SIGNAL, HX.HX_FLAG_TILES,
              HX.HX_FLAG_TILES | HX.HX_FLAG_NO_GRAPH, HX.HX_FLAG_SWEEP,
              HX.HX_FLAG_SWEEP | HX.HX_FLAG_NO_GRAPH, HX.HX_FLAG_SWEEP_FORCES,
-             HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES]
+             HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES, HX.HX_FLAG_CLUSTER,
+             HX.HX_FLAG_CLUSTER | HX.HX_FLAG_NO_GRAPH, HX.HX_FLAG_RESOLVED,
+             HX.HX_FLAG_RESOLVED | HX.HX_FLAG_NO_GRAPH]
 
 
 def _bits(a):
@@ -120,7 +122,7 @@ def test_parity_configs(name, flags):
 
 
 @pytest.mark.parametrize("flags", [0, HX.HX_FLAG_FINE_WAITS, HX.HX_FLAG_TILES, HX.HX_FLAG_SWEEP,
-                                   HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES])
+                                   HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES, HX.HX_FLAG_RESOLVED])
 def test_parity_c5_full_size(flags):
     """12M atoms, 256 domains: the bench's configuration and launch path."""
     c = Case(W.WORKLOADS["C5"], flags=flags)
@@ -155,10 +157,22 @@ def test_unfused_baseline(name):
     ((40.0, 3.0, 3.0), (40, 1, 1), 1.0, 36000),   # many small domains along one dim
 ])
 @pytest.mark.parametrize("flags", [0, HX.HX_FLAG_COUNTER_SIGNAL, HX.HX_FLAG_FINE_WAITS, HX.HX_FLAG_TILES,
-                                   HX.HX_FLAG_SWEEP, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES])
+                                   HX.HX_FLAG_SWEEP, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES,
+                                   HX.HX_FLAG_CLUSTER, HX.HX_FLAG_RESOLVED])
 def test_parity_shapes(box, dims, cutoff, n, flags):
     w = W.custom("shape", n, box, dims, cutoff, seed=7 + n)
-    c = Case(w, flags=flags)
+    pulse_dims, _ = HX.query_plan(box, dims, cutoff)
+    copies_bound = int(np.prod([1 + int(np.sum(pulse_dims == d)) for d in range(3)]))
+    if flags & HX.HX_FLAG_RESOLVED and copies_bound > 8:
+        # a home atom may have more than 7 copies: the resolved tables refuse
+        # the plan at build time if one does (and are exact if none does)
+        try:
+            c = Case(w, flags=flags)
+        except HX.HXError as e:
+            assert e.code == HX.HX_ERR_PULSES
+            return
+    else:
+        c = Case(w, flags=flags)
     check_build(c)
     check_coord_steps(c)
     check_force_steps(c)
@@ -205,7 +219,7 @@ def test_boundary_atoms():
 def test_many_steps_reuse_signals():
     """Epoch-valued signals are never reset between launches: 200 steps."""
     for flags in (0, HX.HX_FLAG_COUNTER_SIGNAL, HX.HX_FLAG_FINE_WAITS, HX.HX_FLAG_TILES, HX.HX_FLAG_SWEEP,
-                  HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES):
+                  HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES, HX.HX_FLAG_CLUSTER, HX.HX_FLAG_RESOLVED):
         c = Case(W.WORKLOADS["C2"], flags=flags)
         x = c.o.coords().copy()
         xt = torch.from_numpy(x).cuda()
@@ -277,7 +291,8 @@ def test_errors():
         hx.build_maps(pos, small)
     assert ei.value.code == HX.HX_ERR_CAPACITY
     for bad in (HX.HX_FLAG_TILES | HX.HX_FLAG_SWEEP, HX.HX_FLAG_SWEEP | HX.HX_FLAG_SWEEP_FORCES,
-                HX.HX_FLAG_TILES | HX.HX_FLAG_SWEEP_FORCES):
+                HX.HX_FLAG_TILES | HX.HX_FLAG_SWEEP_FORCES, HX.HX_FLAG_CLUSTER | HX.HX_FLAG_SWEEP_FORCES,
+                HX.HX_FLAG_RESOLVED | HX.HX_FLAG_CLUSTER):
         with pytest.raises(HX.HXError) as ei:   # the unit kernel families are alternatives
             HX.HaloExchange(w.box, w.dims, w.cutoff, flags=bad)
         assert ei.value.code == HX.HX_ERR_ARG
