@@ -395,11 +395,9 @@ def secondary(hx_main, coords, forces, w_main, dev, peak, flags):
     cold = timed(hx_main, coords, forces, 30, True)
     res[w_main.name + "_cold_l2"] = {"us_step": round(cold, 2),
                                      "frac_of_peak": round(68 * entries / (cold * 1e-6) / 1e9 / peak, 4)}
-    for name in ("C1", "C2", "C3", "C4"):
-        if name == w_main.name:
-            continue
+    def small(name, mode_flags):
         w = W.WORKLOADS[name]
-        hx = HaloExchange(w.box, w.dims, w.cutoff, device=dev.index, flags=flags)
+        hx = HaloExchange(w.box, w.dims, w.cutoff, device=dev.index, flags=mode_flags)
         pos = torch.from_numpy(W.positions(w)).to(dev)
         slots = hx.build_maps(pos)
         x = torch.empty((slots, 3), device=dev)
@@ -428,8 +426,17 @@ def secondary(hx_main, coords, forces, w_main, dev, peak, flags):
                  "frac_of_peak_back_to_back": round(68 * ent / (back_to_back * 1e-6) / 1e9 / peak, 4)}
         if name == "C4":
             entry["cold_l2"] = True
-        res[name] = entry
         del hx
+        return entry
+
+    # the small configurations in the run's modes, and with the forwarding
+    # resolved at build time (HX_FLAG_RESOLVED), the mode made for them
+    for name in ("C1", "C2", "C3", "C4"):
+        if name == w_main.name:
+            continue
+        res[name] = small(name, flags)
+        if not flags & HX.HX_FLAG_RESOLVED:
+            res[name]["resolved"] = small(name, HX.HX_FLAG_RESOLVED)
     return res
 
 

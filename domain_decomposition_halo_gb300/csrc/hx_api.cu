@@ -1446,9 +1446,12 @@ int hx_init(hx_handle* out, const double box[3], const int dims[3], double cutof
   if (!h) return HX_ERR_NOMEM;
   h->pl = pl;
   h->device = device;
-  const unsigned families =
-      flags & (HX_FLAG_TILES | HX_FLAG_SWEEP | HX_FLAG_SWEEP_FORCES | HX_FLAG_CLUSTER | HX_FLAG_RESOLVED);
-  if (families & (families - 1)) {   // at most one of the alternative kernel families
+  // at most one kernel family for the coordinates (forces follow it), and
+  // HX_FLAG_SWEEP_FORCES only over the chunk or resolved coordinate kernels
+  const unsigned families = flags & (HX_FLAG_TILES | HX_FLAG_SWEEP | HX_FLAG_CLUSTER | HX_FLAG_RESOLVED);
+  const bool sweep_forces_clash =
+      (flags & HX_FLAG_SWEEP_FORCES) && (flags & (HX_FLAG_TILES | HX_FLAG_SWEEP | HX_FLAG_CLUSTER));
+  if ((families & (families - 1)) || sweep_forces_clash) {
     delete h;
     return HX_ERR_ARG;
   }

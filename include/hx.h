@@ -91,9 +91,11 @@ typedef struct hx_ctx* hx_handle;
                                           HX_ERR_PULSES from hx_build_maps */
 #define HX_FLAG_SWEEP_FORCES 0x40u     /* the force exchange by the slot-sweep kernel, the coordinate
                                           exchange by the chunk kernels (with HX_FLAG_FINE_WAITS or
-                                          the other chunk flags). At most one of HX_FLAG_TILES,
-                                          HX_FLAG_SWEEP, HX_FLAG_SWEEP_FORCES, HX_FLAG_CLUSTER and
-                                          HX_FLAG_RESOLVED (else HX_ERR_ARG) */
+                                          the other chunk flags) or, with HX_FLAG_RESOLVED, by the
+                                          resolved gather. At most one of HX_FLAG_TILES,
+                                          HX_FLAG_SWEEP, HX_FLAG_CLUSTER and HX_FLAG_RESOLVED, and
+                                          HX_FLAG_SWEEP_FORCES with none of the first three (else
+                                          HX_ERR_ARG) */
 #define HX_FLAG_CLUSTER 0x80u          /* both directions by one thread-block cluster of 8 CTAs that
                                           walks the pulses in order (forces in reverse), with a
                                           cluster barrier (release/acquire) between pulses instead of

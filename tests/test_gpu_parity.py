@@ -22,7 +22,7 @@ ALL_MODES = [0, HX.HX_FLAG_COUNTER_SIGNAL, HX.HX_FLAG_NO_GRAPH,
              HX.HX_FLAG_SWEEP | HX.HX_FLAG_NO_GRAPH, HX.HX_FLAG_SWEEP_FORCES,
              HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES, HX.HX_FLAG_CLUSTER,
              HX.HX_FLAG_CLUSTER | HX.HX_FLAG_NO_GRAPH, HX.HX_FLAG_RESOLVED,
-             HX.HX_FLAG_RESOLVED | HX.HX_FLAG_NO_GRAPH]
+             HX.HX_FLAG_RESOLVED | HX.HX_FLAG_NO_GRAPH, HX.HX_FLAG_RESOLVED | HX.HX_FLAG_SWEEP_FORCES]
 
 
 def _bits(a):
@@ -292,7 +292,7 @@ def test_errors():
     assert ei.value.code == HX.HX_ERR_CAPACITY
     for bad in (HX.HX_FLAG_TILES | HX.HX_FLAG_SWEEP, HX.HX_FLAG_SWEEP | HX.HX_FLAG_SWEEP_FORCES,
                 HX.HX_FLAG_TILES | HX.HX_FLAG_SWEEP_FORCES, HX.HX_FLAG_CLUSTER | HX.HX_FLAG_SWEEP_FORCES,
-                HX.HX_FLAG_RESOLVED | HX.HX_FLAG_CLUSTER):
+                HX.HX_FLAG_RESOLVED | HX.HX_FLAG_CLUSTER, HX.HX_FLAG_CLUSTER | HX.HX_FLAG_SWEEP):
         with pytest.raises(HX.HXError) as ei:   # the unit kernel families are alternatives
             HX.HaloExchange(w.box, w.dims, w.cutoff, flags=bad)
         assert ei.value.code == HX.HX_ERR_ARG
