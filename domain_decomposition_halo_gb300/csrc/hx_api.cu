@@ -842,8 +842,9 @@ int build_tables(hx_ctx* h, cudaStream_t s) {
     h->grid[k] = per_sm * h->sm_count;   // upper bound; trimmed to the work count below
   }
   // Unit lists. A dependent unit is placed a few resident windows after the
-  // units it waits for: tile mode three stages per block, sweep four units
-  // per resident warp (the measured best on the 12M-atom workload).
+  // units it waits for: tile mode three stages per block, sweep eight units
+  // per resident warp (measured on the 12M-atom workload: lags of 2, 3, 4, 6
+  // and 10 windows gave forces in 112.6, 100.5, 94.2, 92.2 and 92.2 us).
   for (int dir = 0; dir < 2; ++dir) {
     int rc = HX_OK;
     if (h->family[dir] == kFamTiles) {
@@ -851,7 +852,7 @@ int build_tables(hx_ctx* h, cudaStream_t s) {
                              kTileEntries * 4 + 32 * kTileSegs, kTileEntries * 12 + 32 * kTileSegs, dir);
     } else if (h->family[dir] == kFamSweep) {
       if (P > kSweepSegs) return HX_ERR_PULSES;   // a unit's runs must fit one warp's stage
-      rc = build_tile_tables(h, items, maps, rank, kSweepSlots, kSweepEntries, 4ll * h->grid[dir] * kWarps,
+      rc = build_tile_tables(h, items, maps, rank, kSweepSlots, kSweepEntries, 8ll * h->grid[dir] * kWarps,
                              kSweepTileBytes, kSweepMapBytes, kSweepSrcBytes, dir);
     }
     if (rc != HX_OK) return rc;
