@@ -434,9 +434,9 @@ int reset_signals(hx_ctx* h, cudaStream_t s) {
 // Runs body(i) for i in [0, n) on the host's cores (iterations must be
 // independent).
 template <class Body>
-void parallel_for(size_t n, Body body) {
+void parallel_for(size_t n, Body body, size_t grain = 256) {
   const size_t hw = std::max<size_t>(1, std::min<size_t>(16, std::thread::hardware_concurrency()));
-  const size_t workers = std::min(hw, std::max<size_t>(1, n / 256));
+  const size_t workers = std::min(hw, std::max<size_t>(1, n / grain));
   if (workers <= 1) {
     for (size_t i = 0; i < n; ++i) body(i);
     return;
@@ -479,15 +479,25 @@ int64_t domain_rank(const Plan& pl, int r) {
 }
 
 // Kahn's algorithm over chunk records by ascending key.
-std::vector<int> order_chunks(const std::vector<Rec>& recs) {
-  const int n = static_cast<int>(recs.size());
-  std::vector<std::vector<int>> users(n);
-  std::vector<int> unmet(n, 0);
+// Kahn's algorithm: a topological order of n records whose dependency lists
+// deps(i) name earlier-done records, taking among the ready ones the smallest
+// key(i) (ties by index). Users are kept in one flat list.
+template <class Deps, class Key>
+std::vector<int> kahn_order(int n, Deps deps, Key key) {
+  std::vector<int> first(n + 1, 0), unmet(n, 0);
   for (int i = 0; i < n; ++i) {
-    unmet[i] = static_cast<int>(recs[i].deps.size());
-    for (int d : recs[i].deps) users[d].push_back(i);
+    const auto& d = deps(i);
+    unmet[i] = static_cast<int>(d.size());
+    for (int x : d) ++first[x + 1];
   }
-  auto cmp = [&](int a, int b) { return recs[a].key != recs[b].key ? recs[a].key > recs[b].key : a > b; };
+  for (int i = 0; i < n; ++i) first[i + 1] += first[i];
+  std::vector<int> users(first[n]), fill(first.begin(), first.end() - 1);
+  for (int i = 0; i < n; ++i)
+    for (int x : deps(i)) users[fill[x]++] = i;
+  auto cmp = [&](int a, int b) {
+    const long long ka = key(a), kb = key(b);
+    return ka != kb ? ka > kb : a > b;
+  };
   std::vector<int> heap;
   for (int i = 0; i < n; ++i)
     if (unmet[i] == 0) heap.push_back(i);
@@ -499,13 +509,19 @@ std::vector<int> order_chunks(const std::vector<Rec>& recs) {
     const int i = heap.back();
     heap.pop_back();
     order.push_back(i);
-    for (int u : users[i])
-      if (--unmet[u] == 0) {
-        heap.push_back(u);
+    for (int k = first[i]; k < first[i + 1]; ++k)
+      if (--unmet[users[k]] == 0) {
+        heap.push_back(users[k]);
         std::push_heap(heap.begin(), heap.end(), cmp);
       }
   }
-  return order;   // shorter than recs only if the waits had a cycle (they cannot)
+  return order;   // shorter than n only if the waits had a cycle (they cannot)
+}
+
+std::vector<int> order_chunks(const std::vector<Rec>& recs) {
+  return kahn_order(
+      static_cast<int>(recs.size()), [&](int i) -> const std::vector<int>& { return recs[i].deps; },
+      [&](int i) { return recs[i].key; });
 }
 
 // ---------------------------------------------------------------- tile tables
@@ -541,10 +557,12 @@ int build_tile_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::
   const int P = pl.n_pulses, nd = pl.ndom;
   auto upper = [&](int r, int q) { return neighbour(pl, r, pl.pulse_dim[q], +1); };
   {
-    std::vector<TRec> recs;
-    // tiles of (domain, range): index list in slot order
+    // tiles of each domain, cut on all host cores, then listed domain after domain;
+    // by_range: per (domain, range) the tiles' indices in slot order
+    std::vector<std::vector<TRec>> per(nd);
     std::vector<std::vector<std::vector<int>>> by_range(nd, std::vector<std::vector<int>>(P + 1));
-    for (int r = 0; r < nd; ++r) {
+    parallel_for(nd, [&](size_t ri) {
+      const int r = static_cast<int>(ri);
       for (int rg = -1; rg < P; ++rg) {
         int lo, len;
         if (rg < 0) {
@@ -603,16 +621,24 @@ int build_tile_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::
             t.seg_pulse.push_back(p);
           }
           if (t.segs.empty()) continue;
-          by_range[r][rg + 1].push_back(static_cast<int>(recs.size()));
-          recs.push_back(std::move(t));
+          by_range[r][rg + 1].push_back(static_cast<int>(per[r].size()));
+          per[r].push_back(std::move(t));
         }
       }
+    }, 1);
+    std::vector<TRec> recs;
+    for (int r = 0; r < nd; ++r) {
+      const int base = static_cast<int>(recs.size());
+      for (auto& lst : by_range[r])
+        for (int& i : lst) i += base;
+      for (TRec& t : per[r]) recs.push_back(std::move(t));
     }
-    // dependencies
-    for (size_t i = 0; i < recs.size(); ++i) {
+    per.clear();
+    // dependencies, one unit per task
+    parallel_for(recs.size(), [&](size_t i) {
       TRec& t = recs[i];
       if (dir == 0) {
-        if (t.range < 0) continue;
+        if (t.range < 0) return;
         // slots [a, a+n) of r's range `p0` are entries [a - off, a - off + n) of the map (u, p0)
         const int p0 = t.range, u = upper(t.r, p0);
         const int64_t e0 = t.a - h->t_off[p0 * nd + u], e1 = e0 + t.n;
@@ -639,12 +665,12 @@ int build_tile_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::
       }
       std::sort(t.deps.begin(), t.deps.end());
       t.deps.erase(std::unique(t.deps.begin(), t.deps.end()), t.deps.end());
-    }
+    }, 64);
     // dependency depth, then priority: base order + one resident window per depth
     {
-      std::vector<Rec> tmp(recs.size());
-      for (size_t i = 0; i < recs.size(); ++i) tmp[i].deps = recs[i].deps;
-      std::vector<int> topo = order_chunks(tmp);   // any topological order
+      const int n = static_cast<int>(recs.size());
+      auto deps_of = [&](int i) -> const std::vector<int>& { return recs[i].deps; };
+      std::vector<int> topo = kahn_order(n, deps_of, [](int) { return 0ll; });   // any topological order
       if (topo.size() != recs.size()) return HX_ERR_STATE;
       for (int i : topo)
         for (int d : recs[i].deps) recs[i].stage = std::max(recs[i].stage, recs[d].stage + 1);
@@ -658,13 +684,9 @@ int build_tile_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::
         if (a.range != b.range) return a.range < b.range;
         return a.a < b.a;
       });
-      std::vector<Rec> ord(recs.size());
-      for (size_t k = 0; k < base.size(); ++k) {
-        ord[base[k]].key = static_cast<long long>(k) + lag * recs[base[k]].stage;
-        recs[base[k]].key = ord[base[k]].key;
-      }
-      for (size_t i = 0; i < recs.size(); ++i) ord[i].deps = recs[i].deps;
-      std::vector<int> order = order_chunks(ord);
+      for (size_t k = 0; k < base.size(); ++k)
+        recs[base[k]].key = static_cast<long long>(k) + lag * recs[base[k]].stage;
+      std::vector<int> order = kahn_order(n, deps_of, [&](int i) { return recs[i].key; });
       if (order.size() != recs.size()) return HX_ERR_STATE;
       std::vector<int> pos(recs.size());
       for (size_t k = 0; k < order.size(); ++k) pos[order[k]] = static_cast<int>(k);
@@ -723,68 +745,94 @@ int build_tile_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::
 // Resolved tables: every halo slot's origin and shift mask (pulses in order,
 // each received slot inheriting from the slot it was sent from), and one
 // tree per home atom that has copies, its adds sorted by descending pulse.
+// Indexed by halo slot (domain after domain) and by home atom, not by slot.
 int build_resolved_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::vector<int32_t>& maps,
                           cudaStream_t s) {
   const Plan& pl = h->pl;
   const int P = pl.n_pulses, nd = pl.ndom;
-  const int64_t S = h->total_slots;
-  if (S >= (int64_t{1} << 31)) return HX_ERR_CAPACITY;   // slots are int32 in the records
-  std::vector<int32_t> origin(S), parent(S, -1);
-  std::vector<uint8_t> mask(S, 0), pulse(S, 0);
-  for (int64_t k = 0; k < S; ++k) origin[k] = static_cast<int32_t>(k);
-  for (int p = 0; p < P; ++p)
-    for (int r = 0; r < nd; ++r) {
-      const ItemInfo& it = items[p * nd + r];
-      for (int i = 0; i < it.size; ++i) {
-        const int64_t dst = it.dst + i, src = it.src + maps[it.map + i];
-        origin[dst] = origin[src];
-        mask[dst] = static_cast<uint8_t>(mask[src] | (it.shift_flag ? 1 << it.dim : 0));
-        parent[dst] = static_cast<int32_t>(src);
-        pulse[dst] = static_cast<uint8_t>(p);
-      }
-    }
-  std::vector<int2> halo;
-  std::vector<uint8_t> hmask;
-  std::vector<int32_t> tree_of(S, -1), node_idx(S, 0);
-  std::vector<TreeRec> trees;
-  for (int r = 0; r < nd; ++r)
-    for (int64_t k = h->dom_offset[r] + h->home[r]; k < h->dom_offset[r] + h->home[r] + h->halo[r]; ++k) {
-      halo.push_back(make_int2(static_cast<int>(k), origin[k]));
-      hmask.push_back(mask[k]);
-      int32_t& t = tree_of[origin[k]];
-      if (t < 0) {
-        t = static_cast<int32_t>(trees.size());
-        TreeRec rec;
-        std::memset(&rec, 0, sizeof(rec));
-        rec.node[0] = origin[k];
-        rec.n_nodes = 1;
-        trees.push_back(rec);
-      }
-      TreeRec& rec = trees[t];
-      if (rec.n_nodes >= kTreeNodes) return HX_ERR_PULSES;   // more copies than a tree record holds
-      node_idx[k] = rec.n_nodes;
-      rec.node[rec.n_nodes++] = static_cast<int32_t>(k);
-    }
-  for (TreeRec& rec : trees) {
-    int order[kTreeNodes];
-    const int m = rec.n_nodes - 1;   // copies = adds
-    for (int j = 0; j < m; ++j) order[j] = j + 1;
-    std::stable_sort(order, order + m, [&](int a, int b) { return pulse[rec.node[a]] > pulse[rec.node[b]]; });
-    for (int e = 0; e < m; ++e) {
-      const int32_t src = rec.node[order[e]];
-      const int32_t par = parent[src];
-      const int tg = par == rec.node[0] ? 0 : node_idx[par];
-      rec.ev[e] = static_cast<uint8_t>(tg | (order[e] << 4));
-    }
+  if (h->total_slots >= (int64_t{1} << 31)) return HX_ERR_CAPACITY;   // slots are int32 in the records
+  std::vector<int64_t> hbase(nd + 1, 0), home_base(nd + 1, 0);
+  for (int r = 0; r < nd; ++r) {
+    hbase[r + 1] = hbase[r] + h->halo[r];
+    home_base[r + 1] = home_base[r] + h->home[r];
   }
-  h->n_res_halo = static_cast<int64_t>(halo.size());
+  const int64_t H = hbase[nd];
+  std::vector<int32_t> origin_home(H), origin_slot(H), parent_h(H);
+  std::vector<uint8_t> mask(H), pulse(H);
+  for (int p = 0; p < P; ++p)   // senders of one pulse write disjoint slots and read earlier pulses
+    parallel_for(nd, [&](size_t ri) {
+      const int r = static_cast<int>(ri);
+      const ItemInfo& it = items[p * nd + r];
+      const int64_t d0 = hbase[it.q] + (it.dst - h->dom_offset[it.q] - h->home[it.q]);
+      for (int i = 0; i < it.size; ++i) {
+        const int32_t mv = maps[it.map + i];
+        const int64_t k = d0 + i;
+        if (mv < h->home[r]) {
+          origin_home[k] = static_cast<int32_t>(home_base[r] + mv);
+          origin_slot[k] = static_cast<int32_t>(it.src + mv);
+          mask[k] = 0;
+          parent_h[k] = -1;
+        } else {
+          const int64_t sh = hbase[r] + (mv - h->home[r]);
+          origin_home[k] = origin_home[sh];
+          origin_slot[k] = origin_slot[sh];
+          mask[k] = mask[sh];
+          parent_h[k] = static_cast<int32_t>(sh);
+        }
+        if (it.shift_flag) mask[k] = static_cast<uint8_t>(mask[k] | (1 << it.dim));
+        pulse[k] = static_cast<uint8_t>(p);
+      }
+    }, 1);
+  std::vector<int2> halo(H);
+  for (int r = 0; r < nd; ++r)
+    for (int64_t k = hbase[r]; k < hbase[r + 1]; ++k)
+      halo[k] = make_int2(static_cast<int>(h->dom_offset[r] + h->home[r] + (k - hbase[r])), origin_slot[k]);
+  // trees: one per home atom that has copies, numbered in halo order
+  std::vector<int32_t> tree_of(home_base[nd], -1);
+  int32_t n_trees = 0;
+  for (int64_t k = 0; k < H; ++k) {
+    int32_t& t = tree_of[origin_home[k]];
+    if (t < 0) t = n_trees++;
+  }
+  std::vector<TreeRec> trees(static_cast<size_t>(n_trees));   // zero-filled
+  std::vector<uint8_t> node_idx(H);
+  for (int64_t k = 0; k < H; ++k) {
+    TreeRec& rec = trees[tree_of[origin_home[k]]];
+    if (rec.n_nodes == 0) {
+      rec.node[0] = origin_slot[k];
+      rec.n_nodes = 1;
+    }
+    if (rec.n_nodes >= kTreeNodes) return HX_ERR_PULSES;   // more copies than a tree record holds
+    node_idx[k] = static_cast<uint8_t>(rec.n_nodes);
+    rec.node[rec.n_nodes++] = halo[k].x;
+  }
+  // adds: copy j (node j > 0) into its parent, then sorted by descending pulse
+  std::vector<uint8_t> add_pulse(trees.size() * kTreeNodes, 0);
+  for (int64_t k = 0; k < H; ++k) {
+    const size_t t = static_cast<size_t>(tree_of[origin_home[k]]);
+    const int j = node_idx[k];
+    const int tg = parent_h[k] < 0 ? 0 : node_idx[parent_h[k]];
+    trees[t].ev[j - 1] = static_cast<uint8_t>(tg | (j << 4));
+    add_pulse[t * kTreeNodes + j - 1] = pulse[k];
+  }
+  parallel_for(trees.size(), [&](size_t t) {
+    TreeRec& rec = trees[t];
+    uint8_t* pu = add_pulse.data() + t * kTreeNodes;
+    const int m = rec.n_nodes - 1;
+    for (int a = 1; a < m; ++a)   // stable insertion sort by descending pulse
+      for (int b = a; b > 0 && pu[b] > pu[b - 1]; --b) {
+        std::swap(pu[b], pu[b - 1]);
+        std::swap(rec.ev[b], rec.ev[b - 1]);
+      }
+  }, 1024);
+  h->n_res_halo = H;
   h->n_res_trees = static_cast<int64_t>(trees.size());
   HX_CUDA(dev_alloc(&h->d_res_halo, halo.size()));
-  HX_CUDA(dev_alloc(&h->d_res_mask, hmask.size()));
+  HX_CUDA(dev_alloc(&h->d_res_mask, mask.size()));
   HX_CUDA(dev_alloc(&h->d_res_trees, trees.size()));
-  if (!halo.empty()) {
+  if (H > 0) {
     HX_CUDA(cudaMemcpyAsync(h->d_res_halo, halo.data(), sizeof(int2) * halo.size(), cudaMemcpyHostToDevice, s));
-    HX_CUDA(cudaMemcpyAsync(h->d_res_mask, hmask.data(), hmask.size(), cudaMemcpyHostToDevice, s));
+    HX_CUDA(cudaMemcpyAsync(h->d_res_mask, mask.data(), mask.size(), cudaMemcpyHostToDevice, s));
   }
   if (!trees.empty())
     HX_CUDA(cudaMemcpyAsync(h->d_res_trees, trees.data(), sizeof(TreeRec) * trees.size(), cudaMemcpyHostToDevice, s));
