@@ -267,27 +267,60 @@ def run_ours(args):
         raise RuntimeError(f"device status {rc} (detail {detail}) after the timed region")
     us_step = total_ms * 1e3 / K
 
-    # end to end through the public API: host buffers in, results out, every step
+    # end to end through the public API: host buffers in, results out, every
+    # step. Copies in, the two exchanges and copies out run on three streams
+    # over two device buffer sets, so one step's copies out overlap the next
+    # step's copies in (the host link carries both directions at once); the
+    # events chain each set: in -> exchanges -> out -> next copy in.
     coords_h = coords.cpu().pin_memory()
     forces_h = forces.cpu().pin_memory()
-    coords_o = torch.empty_like(coords_h).pin_memory()
-    forces_o = torch.empty_like(forces_h).pin_memory()
+    sets = [(coords, forces), (torch.empty_like(coords), torch.empty_like(forces))]
+    outs = [(torch.empty_like(coords_h).pin_memory(), torch.empty_like(forces_h).pin_memory()) for _ in range(2)]
+    s_in, s_ex, s_out = (torch.cuda.Stream(device=dev) for _ in range(3))
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_ex = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
     n_e2e = max(3, min(K, 30))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
     for i in range(2 + n_e2e):
-        if i == 2:
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
+        if i == 2:   # two untimed steps, then the timed ones
             torch.cuda.synchronize()
-            e0.record(stream)
-        coords.copy_(coords_h, non_blocking=True)
-        forces.copy_(forces_h, non_blocking=True)
-        hx.exchange_coords(coords)
-        hx.exchange_forces(forces)
-        coords_o.copy_(coords, non_blocking=True)
-        forces_o.copy_(forces, non_blocking=True)
-    e1.record(stream)
+            e0.record(s_in)
+        k = i % 2
+        cd, fd = sets[k]
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(ev_out[k])   # this set's previous results are out
+            cd.copy_(coords_h, non_blocking=True)
+            fd.copy_(forces_h, non_blocking=True)
+            ev_in[k].record(s_in)
+        with torch.cuda.stream(s_ex):
+            s_ex.wait_event(ev_in[k])
+            hx.exchange_coords(cd)
+            hx.exchange_forces(fd)
+            ev_ex[k].record(s_ex)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_ex[k])
+            outs[k][0].copy_(cd, non_blocking=True)
+            outs[k][1].copy_(fd, non_blocking=True)
+            ev_out[k].record(s_out)
+    s_in.wait_stream(s_out)
+    e1.record(s_in)
     torch.cuda.synchronize()
     e2e_us = e0.elapsed_time(e1) * 1e3 / n_e2e
+    # every step exchanged the same inputs: each set's last results must equal
+    # one plain exchange of them (a check on the stream and event chaining)
+    cd, fd = sets[0]
+    cd.copy_(coords_h)
+    fd.copy_(forces_h)
+    hx.exchange_coords(cd)
+    hx.exchange_forces(fd)
+    torch.cuda.synchronize()
+    for co, fo in outs:
+        if not (torch.equal(co.view(torch.int32), cd.cpu().view(torch.int32)) and
+                torch.equal(fo.view(torch.int32), fd.cpu().view(torch.int32))):
+            raise RuntimeError("end-to-end pipeline results differ from a plain exchange")
     bytes_h2d = 2 * slots * 12
     bytes_d2h = 2 * slots * 12
 
@@ -330,7 +363,9 @@ def run_ours(args):
         "clocks": clk,
         "e2e": {"value": round(e2e_us, 2), "unit": "us/step", "h2d_bytes_per_step": bytes_h2d,
                 "d2h_bytes_per_step": bytes_d2h,
-                "what": "pinned host coords+forces -> device, both exchanges, coords+forces -> host, every step"},
+                "what": "pinned host coords+forces -> device, both exchanges, coords+forces -> host, every step; "
+                        "copies in, exchanges and copies out on three streams over two device buffer sets, "
+                        "so a step's copies out overlap the next step's copies in"},
         "gpu_launches": 2 * K,
         "build_maps_us": round(statistics.median(t_build), 1),
     }
