@@ -15,12 +15,16 @@
 //     force runs are copied in; the runs are added last pulse first, so each
 //     slot is the fp32 sum in reverse pulse order ("Force halo exchange:
 //     Reversing the dependency chain"), and the tile is written back.
-// Two stages per block: while one unit is processed, the copies of the
-// block's next unit are in flight, and its 256-byte record is already in
-// shared memory. With random in-domain order nearly every 64-byte granule of
-// a domain's slots holds a selected atom, so copying whole tiles moves about
-// the DRAM bytes that scattered 12-byte accesses would, as sequential
-// streams, and every per-entry access stays in shared memory.
+// Each block is a producer/consumer pipeline. One producer warp draws
+// tickets, loads unit records, waits for their producers and issues the bulk
+// copies into a ring of 3 (forces) or 4 (coordinates) stages guarded by
+// full/empty mbarriers. Eight consumer warps process the staged units and
+// send the signals. With random in-domain order nearly every 64-byte granule
+// of a domain's slots holds a selected atom, so copying whole tiles moves
+// about the DRAM bytes that scattered 12-byte accesses would, as sequential
+// streams, and every per-entry access stays in shared memory. The one
+// producer per block serialises the control path of every unit; the slot
+// sweep (hx_sweep.cu) gives each warp its own units instead.
 #include <cstdint>
 
 #include "hx_internal.h"

@@ -60,7 +60,9 @@ typedef struct hx_ctx* hx_handle;
 
 #define HX_OK 0
 #define HX_ERR_ARG (-1)       /* null pointer, cutoff <= 0, dims < 1, box <= 0, bad index */
-#define HX_ERR_PULSES (-2)    /* np_d >= n_d in some dimension, or too many pulses */
+#define HX_ERR_PULSES (-2)    /* np_d >= n_d in some dimension, or too many pulses; from
+                                 hx_build_maps also a plan beyond what the HX_FLAG_SWEEP
+                                 (8 pulses) or HX_FLAG_RESOLVED (7 copies per atom) tables hold */
 #define HX_ERR_RANGE (-3)     /* an input position outside [0, L) or NaN */
 #define HX_ERR_CAPACITY (-4)  /* caller buffer smaller than the layout needs */
 #define HX_ERR_CUDA (-5)      /* a CUDA runtime call failed */
