@@ -231,6 +231,24 @@ __device__ void stage_unit(const float* x, const TileParams& P, const TileUnit& 
   }
 }
 
+// Warm L2 with the unit's runs (aligned middles; one run per lane). Lines
+// whose producers have not signalled yet may be fetched early: L2 is where
+// later stores land, so the unit's own bulk copies still read the final data.
+template <int KIND>
+__device__ void prefetch_unit(const float* x, const TileParams& P, const TileUnit& d) {
+  const int lane = threadIdx.x & 31;
+  const int n_runs = 1 + (KIND == 1 ? 2 : 1) * d.seg_cnt;
+  if (lane < n_runs) {
+    unsigned long long g;
+    unsigned bytes, region;
+    run_of<KIND>(x, P, d, lane, g, bytes, region);
+    const unsigned long long a0 = (g + 15ull) & ~15ull, a1 = (g + bytes) & ~15ull;
+    if (a1 > a0)
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a0), "r"(static_cast<unsigned>(a1 - a0))
+                   : "memory");
+  }
+}
+
 // 16-byte global -> shared copy that completes asynchronously;
 // cp_async_wait_all waits for all of this thread's copies.
 __device__ __forceinline__ void cp_async_16(void* smem_dst, const void* gmem_src) {
@@ -384,6 +402,11 @@ __global__ void __launch_bounds__(kThreads) k_sweep(float* __restrict__ buf, Til
       __syncwarp();
     }
     stage_unit<KIND>(buf, P, d, S.stage, &S.bar);
+    if (cn < N) {   // the next record, then its runs into L2 while this unit's copies land
+      cp_async_wait_all();
+      __syncwarp();
+      prefetch_unit<KIND>(buf, P, S.desc[b ^ 1]);
+    }
     if (!mbar_wait(&S.bar, parity, P.timeout_ns)) {
       if (lane == 0) record_timeout(P, d.item);
     }
