@@ -48,9 +48,10 @@ def parse_args():
     ap.add_argument("--workload", default="C5", choices=sorted(W.WORKLOADS))
     ap.add_argument("--no-extras", action="store_true", help="skip the secondary measurements")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU baseline budget")
-    ap.add_argument("--flags", default="fine,sweepf",
-                    help="comma list of libhx modes: fine, sweepf (forces by the slot sweep), sweep, tiles, "
-                         "counter, nograph, unordered, pages (= none)")
+    ap.add_argument("--flags", default="fine,bulkstore,sweepf",
+                    help="comma list of libhx modes: fine, bulkstore (coordinates packed by bulk stores), sweepf "
+                         "(forces by the slot sweep), sweep, tiles, cluster, resolved, counter, nograph, unordered, "
+                         "pages (= none)")
     return ap.parse_args()
 
 
@@ -59,7 +60,7 @@ def hx_flags(spec: str) -> int:
     table = {"fine": HX.HX_FLAG_FINE_WAITS, "counter": HX.HX_FLAG_COUNTER_SIGNAL, "nograph": HX.HX_FLAG_NO_GRAPH,
              "unordered": HX.HX_FLAG_UNORDERED_FORCES, "tiles": HX.HX_FLAG_TILES, "sweep": HX.HX_FLAG_SWEEP,
              "sweepf": HX.HX_FLAG_SWEEP_FORCES, "cluster": HX.HX_FLAG_CLUSTER,
-             "resolved": HX.HX_FLAG_RESOLVED, "pages": 0, "": 0}
+             "resolved": HX.HX_FLAG_RESOLVED, "bulkstore": HX.HX_FLAG_BULK_STORE, "pages": 0, "": 0}
     flags = 0
     for name in spec.split(","):
         flags |= table[name.strip()]
@@ -118,9 +119,15 @@ def kernel_impl(flags: int, direction: int) -> str:
         return f"k_tiles<{direction}> (tile pipeline)"
     if flags & HX.HX_FLAG_SWEEP or (direction == 1 and flags & HX.HX_FLAG_SWEEP_FORCES):
         return f"k_sweep<{direction}> (slot sweep)"
+    if flags & HX.HX_FLAG_CLUSTER:
+        return f"k_cluster<{direction}> (one cluster)"
+    if flags & HX.HX_FLAG_RESOLVED:
+        return "k_resolved_coords (resolved)" if direction == 0 else "k_resolved_forces (resolved)"
     mode = ("chunk flags" if flags & HX.HX_FLAG_FINE_WAITS else
             "counter" if flags & HX.HX_FLAG_COUNTER_SIGNAL else "last arrival")
     if direction == 0:
+        if flags & HX.HX_FLAG_BULK_STORE:
+            return f"k_coords_bulk<{mode}> (chunks, bulk-store pack)"
         return f"k_coords_fused<{mode}> (chunks)"
     order = "unordered" if flags & HX.HX_FLAG_UNORDERED_FORCES else "ordered"
     return f"k_forces_fused<{mode}, {order}> (chunks)"

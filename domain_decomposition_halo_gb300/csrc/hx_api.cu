@@ -260,7 +260,7 @@ DirParams dir_params(hx_ctx* h, int dir) {
 const void* kernel_for(hx_ctx* h, int kind) {
   const int mode = (h->flags & HX_FLAG_FINE_WAITS) ? kChunkFlag
                    : (h->flags & HX_FLAG_COUNTER_SIGNAL) ? kCounter : kLastArrival;
-  if (kind == 0) return coords_kernel(mode);
+  if (kind == 0) return coords_kernel(mode, (h->flags & HX_FLAG_BULK_STORE) != 0);
   if (kind == 1) return forces_kernel(mode, !(h->flags & HX_FLAG_UNORDERED_FORCES));
   return noop_kernel();
 }

@@ -95,7 +95,7 @@ struct PulseParams {
 enum SignalMode { kLastArrival = 0, kCounter = 1, kChunkFlag = 2 };
 
 // ---- exchange kernels (hx_kernels.cu) ----
-const void* coords_kernel(int signal_mode);
+const void* coords_kernel(int signal_mode, bool bulk_store);   // bulk_store: gather to shared memory, bulk copy out
 const void* forces_kernel(int signal_mode, bool ordered);
 const void* noop_kernel();
 int max_blocks_per_sm(const void* fn);

@@ -262,8 +262,95 @@ __device__ __forceinline__ void forces_chunk(float* __restrict__ f, const Chunk&
   }
 }
 
+// Bulk-store pack (the pages' TMA variant, "Optimizing for efficient
+// transfers across NVIDIA NVLink-connected GPUs": gather into shared memory,
+// then one bulk copy to the peer). The warp gathers its chunk into its
+// shared-memory stage, laid out at the destination's address mod 16; lane 0
+// stores the 16-byte-aligned middle with one cp.async.bulk shared -> global,
+// and the lanes store the words around it. The store completes
+// asynchronously: the stage is reused only after the copy has read it, and a
+// signal follows only once the copy is complete and ordered before the
+// release (bulk_store_done).
+constexpr int kBulkStageBytes = kChunk * 12 + 16;
+
+__device__ __forceinline__ unsigned smem_u32(const void* p) {
+  return static_cast<unsigned>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void coords_chunk_bulk(float* __restrict__ x, const Chunk& ch, const int (&j)[kRounds],
+                                                  unsigned char* stage) {
+  const int lane = threadIdx.x & 31;
+  const float* src = x + 3 * ch.src;
+  float v[kRounds][3];
+  const bool halo = (ch.flags & kHaloSrc) != 0;
+#pragma unroll
+  for (int u = 0; u < kRounds; ++u) {
+    if (j[u] >= 0) {
+      const float* s = src + 3 * static_cast<int64_t>(j[u]);
+      if (halo) {
+        v[u][0] = s[0];
+        v[u][1] = s[1];
+        v[u][2] = s[2];
+      } else {
+        v[u][0] = __ldg(s);
+        v[u][1] = __ldg(s + 1);
+        v[u][2] = __ldg(s + 2);
+      }
+    }
+  }
+  if (ch.flags & kShift) {   // no add otherwise: unshifted values keep every bit (-0.0 included)
+#pragma unroll
+    for (int u = 0; u < kRounds; ++u) {
+      if (ch.dim == 0) v[u][0] = __fadd_rn(v[u][0], ch.shift);
+      else if (ch.dim == 1) v[u][1] = __fadd_rn(v[u][1], ch.shift);
+      else v[u][2] = __fadd_rn(v[u][2], ch.shift);
+    }
+  }
+  float* dst = x + 3 * ch.dst;
+  const unsigned long long gd = reinterpret_cast<unsigned long long>(dst);
+  float* sv = reinterpret_cast<float*>(stage + (gd & 15ull));
+  // the previous chunk's bulk store has read the stage
+  if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+  __syncwarp();
+#pragma unroll
+  for (int u = 0; u < kRounds; ++u) {
+    if (j[u] >= 0) {
+      const int e = u * 32 + lane;
+      sv[3 * e + 0] = v[u][0];
+      sv[3 * e + 1] = v[u][1];
+      sv[3 * e + 2] = v[u][2];
+    }
+  }
+  __syncwarp();
+  const unsigned bytes = 12u * static_cast<unsigned>(ch.n);
+  const unsigned long long a0 = (gd + 15ull) & ~15ull, a1 = (gd + bytes) & ~15ull;
+  if (a1 > a0) {
+    if (lane == 0) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the lanes' stage writes, to the copy
+      asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n\tcp.async.bulk.commit_group;" ::"l"(
+                       a0),
+                   "r"(smem_u32(stage + (gd & 15ull) + (a0 - gd))), "r"(static_cast<unsigned>(a1 - a0))
+                   : "memory");
+    }
+    const int head = static_cast<int>((a0 - gd) / 4), tail = static_cast<int>((gd + bytes - a1) / 4);
+    if (lane < head) dst[lane] = sv[lane];
+    else if (lane >= 4 && lane < 4 + tail) {
+      const int k = static_cast<int>((a1 - gd) / 4) + (lane - 4);
+      dst[k] = sv[k];
+    }
+  } else {
+    for (int k = lane; k < 3 * ch.n; k += 32) dst[k] = sv[k];
+  }
+}
+
+// Lane 0, before a release that covers a bulk-stored chunk: the copy has
+// completed and is ordered before later generic accesses.
+__device__ __forceinline__ void bulk_store_done() {
+  asm volatile("cp.async.bulk.wait_group 0;\n\tfence.proxy.async.global;" ::: "memory");
+}
+
 // Persistent warp loop shared by both directions. KIND 0 = coordinates,
-// 1 = forces ordered, 2 = forces unordered.
+// 1 = forces ordered, 2 = forces unordered, 3 = coordinates by bulk stores.
 template <int MODE, int KIND>
 __device__ __forceinline__ void run_warps(float* __restrict__ buf, const DirParams& P, float* stage) {
   const int lane = threadIdx.x & 31;
@@ -290,19 +377,30 @@ __device__ __forceinline__ void run_warps(float* __restrict__ buf, const DirPara
       __syncwarp();
     }
     if (KIND == 0) coords_chunk(buf, ch, j, stage);
+    else if (KIND == 3) coords_chunk_bulk(buf, ch, j, reinterpret_cast<unsigned char*>(stage));
     else forces_chunk<KIND == 1>(buf, ch, j);
     if (ch.flags & kSignal) {
       __syncwarp();
-      if (lane == 0) signal_chunk<MODE>(P, ch, c, epoch, drop_item);
+      if (lane == 0) {
+        if (KIND == 3) bulk_store_done();
+        signal_chunk<MODE>(P, ch, c, epoch, drop_item);
+      }
     }
     c = (t - base) + W;
   }
+  if (KIND == 3 && lane == 0) bulk_store_done();   // nothing in flight when the warp exits
 }
 
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) k_coords_fused(float* __restrict__ x, DirParams P) {
   __shared__ float s_stage[kWarps][96];
   run_warps<MODE, 0>(x, P, s_stage[threadIdx.x >> 5]);
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, kMinBlocks) k_coords_bulk(float* __restrict__ x, DirParams P) {
+  __shared__ __align__(16) float s_stage[kWarps][kBulkStageBytes / 4];
+  run_warps<MODE, 3>(x, P, s_stage[threadIdx.x >> 5]);
 }
 
 template <int MODE, bool ORDERED>
@@ -368,7 +466,12 @@ __global__ void k_noop() {}
 
 }  // namespace
 
-const void* coords_kernel(int signal_mode) {
+const void* coords_kernel(int signal_mode, bool bulk_store) {
+  if (bulk_store) {
+    if (signal_mode == kChunkFlag) return reinterpret_cast<const void*>(&k_coords_bulk<kChunkFlag>);
+    return signal_mode == kCounter ? reinterpret_cast<const void*>(&k_coords_bulk<kCounter>)
+                                   : reinterpret_cast<const void*>(&k_coords_bulk<kLastArrival>);
+  }
   if (signal_mode == kChunkFlag) return reinterpret_cast<const void*>(&k_coords_fused<kChunkFlag>);
   return signal_mode == kCounter ? reinterpret_cast<const void*>(&k_coords_fused<kCounter>)
                                  : reinterpret_cast<const void*>(&k_coords_fused<kLastArrival>);

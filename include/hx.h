@@ -105,6 +105,12 @@ typedef struct hx_ctx* hx_handle;
                                           dependency chain set the step time. Forces are ordered
                                           (HX_FLAG_UNORDERED_FORCES is ignored); there are no
                                           device waits, so no time-outs and no signal to drop */
+#define HX_FLAG_BULK_STORE 0x200u      /* chunk coordinate kernels pack by bulk store: each warp gathers
+                                          its chunk into shared memory and stores it to the receiver's
+                                          slots with one cp.async.bulk (the pages' TMA variant, section
+                                          "Optimizing for efficient transfers across NVIDIA
+                                          NVLink-connected GPUs"); same results bit for bit. Applies
+                                          where the chunk kernels run the coordinates */
 #define HX_FLAG_RESOLVED 0x100u        /* the forwarding unrolled at build time: every halo slot is
                                           gathered straight from its origin home atom (plus the
                                           shifts its path added), and every home atom's force tree

@@ -37,3 +37,11 @@ def test_traffic_needs_matching_digest(tmp_path, monkeypatch):
     assert bench.profiled_traffic("k", "C5") == 123.0
     (tmp_path / "profiles" / "k_C5.md").write_text("traffic_bytes_per_launch: 123\nkernel_source_digest: 0000\n")
     assert bench.profiled_traffic("k", "C5") is None
+
+
+def test_kernel_impl_names_the_launched_kernels():
+    default = bench.hx_flags("fine,bulkstore,sweepf")
+    assert bench.kernel_impl(default, 0).startswith("k_coords_bulk<chunk flags>")
+    assert bench.kernel_impl(default, 1).startswith("k_sweep<1>")
+    assert bench.kernel_impl(0, 1).startswith("k_forces_fused<last arrival, ordered>")
+    assert bench.kernel_impl(bench.hx_flags("resolved"), 1).startswith("k_resolved_forces")

@@ -22,7 +22,9 @@ ALL_MODES = [0, HX.HX_FLAG_COUNTER_SIGNAL, HX.HX_FLAG_NO_GRAPH,
              HX.HX_FLAG_SWEEP | HX.HX_FLAG_NO_GRAPH, HX.HX_FLAG_SWEEP_FORCES,
              HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES, HX.HX_FLAG_CLUSTER,
              HX.HX_FLAG_CLUSTER | HX.HX_FLAG_NO_GRAPH, HX.HX_FLAG_RESOLVED,
-             HX.HX_FLAG_RESOLVED | HX.HX_FLAG_NO_GRAPH, HX.HX_FLAG_RESOLVED | HX.HX_FLAG_SWEEP_FORCES]
+             HX.HX_FLAG_RESOLVED | HX.HX_FLAG_NO_GRAPH, HX.HX_FLAG_RESOLVED | HX.HX_FLAG_SWEEP_FORCES,
+             HX.HX_FLAG_BULK_STORE, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE,
+             HX.HX_FLAG_COUNTER_SIGNAL | HX.HX_FLAG_BULK_STORE]
 
 
 def _bits(a):
@@ -122,7 +124,8 @@ def test_parity_configs(name, flags):
 
 
 @pytest.mark.parametrize("flags", [0, HX.HX_FLAG_FINE_WAITS, HX.HX_FLAG_TILES, HX.HX_FLAG_SWEEP,
-                                   HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES, HX.HX_FLAG_RESOLVED])
+                                   HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES, HX.HX_FLAG_RESOLVED,
+                                   HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE | HX.HX_FLAG_SWEEP_FORCES])
 def test_parity_c5_full_size(flags):
     """12M atoms, 256 domains: the bench's configuration and launch path."""
     c = Case(W.WORKLOADS["C5"], flags=flags)
@@ -158,7 +161,7 @@ def test_unfused_baseline(name):
 ])
 @pytest.mark.parametrize("flags", [0, HX.HX_FLAG_COUNTER_SIGNAL, HX.HX_FLAG_FINE_WAITS, HX.HX_FLAG_TILES,
                                    HX.HX_FLAG_SWEEP, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES,
-                                   HX.HX_FLAG_CLUSTER, HX.HX_FLAG_RESOLVED])
+                                   HX.HX_FLAG_CLUSTER, HX.HX_FLAG_RESOLVED, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE])
 def test_parity_shapes(box, dims, cutoff, n, flags):
     w = W.custom("shape", n, box, dims, cutoff, seed=7 + n)
     pulse_dims, _ = HX.query_plan(box, dims, cutoff)
@@ -219,7 +222,8 @@ def test_boundary_atoms():
 def test_many_steps_reuse_signals():
     """Epoch-valued signals are never reset between launches: 200 steps."""
     for flags in (0, HX.HX_FLAG_COUNTER_SIGNAL, HX.HX_FLAG_FINE_WAITS, HX.HX_FLAG_TILES, HX.HX_FLAG_SWEEP,
-                  HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES, HX.HX_FLAG_CLUSTER, HX.HX_FLAG_RESOLVED):
+                  HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES, HX.HX_FLAG_CLUSTER, HX.HX_FLAG_RESOLVED,
+                  HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE):
         c = Case(W.WORKLOADS["C2"], flags=flags)
         x = c.o.coords().copy()
         xt = torch.from_numpy(x).cuda()
@@ -302,7 +306,8 @@ def test_errors():
 
 @pytest.mark.parametrize("direction", [0, 1])
 @pytest.mark.parametrize("flags", [0, HX.HX_FLAG_COUNTER_SIGNAL, HX.HX_FLAG_FINE_WAITS, HX.HX_FLAG_TILES,
-                                   HX.HX_FLAG_SWEEP, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES])
+                                   HX.HX_FLAG_SWEEP, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES,
+                                   HX.HX_FLAG_BULK_STORE, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE])
 def test_dropped_signal_times_out_and_recovers(direction, flags):
     """Failure detection without a device fault: a (domain, pulse) that never
     signals makes its waiters give up after the bounded wait; the kernel

@@ -22,7 +22,7 @@ pytestmark = pytest.mark.gpu
 @pytest.mark.parametrize("name", ["C2", "C5"])
 @pytest.mark.parametrize("flags", [0, HX.HX_FLAG_FINE_WAITS, HX.HX_FLAG_TILES, HX.HX_FLAG_SWEEP,
                                    HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES, HX.HX_FLAG_CLUSTER,
-                                   HX.HX_FLAG_RESOLVED])
+                                   HX.HX_FLAG_RESOLVED, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE])
 def test_static_scratch_matches_regular_exchange(name, flags):
     w = W.WORKLOADS[name]
     hx = HX.HaloExchange(w.box, w.dims, w.cutoff, flags=flags)
