@@ -307,11 +307,18 @@ __device__ __forceinline__ void coords_unit(float* __restrict__ x, const TilePar
   }
 }
 
+// Lane 0: this warp's bulk stores have read the stage / have completed and
+// are ordered before later generic accesses (before a release).
+__device__ __forceinline__ void bulk_stores_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_stores_done() {
+  asm volatile("cp.async.bulk.wait_group 0;\n\tfence.proxy.async.global;" ::: "memory");
+}
+
 // Forces of one staged unit: each segment's received run added into the
 // slots, segments in list order (last pulse first), a warp barrier between
 // segments since one slot can be a target in several pulses; entries of one
-// segment have distinct targets. Then the slots are written back: float4
-// stores for the 16-byte-aligned middle (the stage keeps the global address
+// segment have distinct targets. Then the slots are written back: one bulk
+// store for the 16-byte-aligned middle (the stage keeps the global address
 // mod 16), plain stores for the words around it.
 __device__ __forceinline__ void forces_unit(float* __restrict__ f, const TileParams& P, const TileUnit& d,
                                             WarpSmem<1>& S) {
@@ -336,10 +343,13 @@ __device__ __forceinline__ void forces_unit(float* __restrict__ f, const TilePar
   const unsigned long long a0 = (gt + 15ull) & ~15ull, a1 = (gt + bytes) & ~15ull;
   if (a1 > a0) {
     const unsigned head = static_cast<unsigned>(a0 - gt) / 4, tail = static_cast<unsigned>(gt + bytes - a1) / 4;
-    const int n4 = static_cast<int>((a1 - a0) / 16);
-    const float4* s4 = reinterpret_cast<const float4*>(tile + head);
-    float4* d4 = reinterpret_cast<float4*>(a0);
-    for (int q = lane; q < n4; q += 32) d4[q] = s4[q];
+    if (lane == 0) {   // the aligned middle in one bulk store (its completion: bulk_stores_done)
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the adds, to the copy
+      asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n\tcp.async.bulk.commit_group;" ::"l"(
+                       a0),
+                   "r"(smem_addr(tile + head)), "r"(static_cast<unsigned>(a1 - a0))
+                   : "memory");
+    }
     if (lane < static_cast<int>(head)) f[3 * d.base + lane] = tile[lane];
     else if (lane >= 4 && lane < 4 + static_cast<int>(tail)) {
       const int k = static_cast<int>((a1 - gt) / 4) + (lane - 4);
@@ -401,6 +411,10 @@ __global__ void __launch_bounds__(kThreads) k_sweep(float* __restrict__ buf, Til
       if (lane == 0) asm volatile("fence.proxy.async.global;" ::: "memory");
       __syncwarp();
     }
+    if (KIND == 1) {   // the previous unit's write-back has read the stage
+      if (lane == 0) bulk_stores_read();
+      __syncwarp();
+    }
     stage_unit<KIND>(buf, P, d, S.stage, &S.bar);
     if (cn < N) {   // the next record, then its runs into L2 while this unit's copies land
       cp_async_wait_all();
@@ -416,7 +430,10 @@ __global__ void __launch_bounds__(kThreads) k_sweep(float* __restrict__ buf, Til
     else forces_unit(buf, P, d, S);
     if (d.flags & kSignal) {
       __syncwarp();   // every lane's stores precede lane 0's release
-      if (lane == 0 && d.item != drop_item) st_release_u64(P.flags + c, epoch);
+      if (lane == 0) {
+        if (KIND == 1) bulk_stores_done();
+        if (d.item != drop_item) st_release_u64(P.flags + c, epoch);
+      }
     }
     if (cn >= N) break;
     cp_async_wait_all();   // the next record
@@ -425,6 +442,7 @@ __global__ void __launch_bounds__(kThreads) k_sweep(float* __restrict__ buf, Til
     c = cn;
     b ^= 1;
   }
+  if (KIND == 1 && lane == 0) bulk_stores_done();   // nothing in flight when the warp exits
 }
 
 }  // namespace
