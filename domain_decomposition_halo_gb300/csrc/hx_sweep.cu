@@ -49,7 +49,7 @@ template <int KIND>
 struct alignas(16) WarpSmem {
   alignas(16) unsigned char stage[sweep_stage_bytes(KIND)];
   TileUnit desc[2];              // the current unit's record and the next one's
-  float out[96];                 // one 32-entry round, transposed for coalesced stores
+  float out[KIND == 0 ? 96 : 4];  // coordinates: one 32-entry round, transposed for coalesced stores
   unsigned long long bar;        // completion of the unit's bulk copies
 };
 
