@@ -60,7 +60,8 @@ def hx_flags(spec: str) -> int:
     table = {"fine": HX.HX_FLAG_FINE_WAITS, "counter": HX.HX_FLAG_COUNTER_SIGNAL, "nograph": HX.HX_FLAG_NO_GRAPH,
              "unordered": HX.HX_FLAG_UNORDERED_FORCES, "tiles": HX.HX_FLAG_TILES, "sweep": HX.HX_FLAG_SWEEP,
              "sweepf": HX.HX_FLAG_SWEEP_FORCES, "cluster": HX.HX_FLAG_CLUSTER,
-             "resolved": HX.HX_FLAG_RESOLVED, "bulkstore": HX.HX_FLAG_BULK_STORE, "pages": 0, "": 0}
+             "resolved": HX.HX_FLAG_RESOLVED, "bulkstore": HX.HX_FLAG_BULK_STORE,
+             "pdl": HX.HX_FLAG_PDL, "pages": 0, "": 0}
     flags = 0
     for name in spec.split(","):
         flags |= table[name.strip()]
@@ -463,7 +464,8 @@ def secondary(hx_main, coords, forces, w_main, dev, peak, flags):
         single = timed(hx, x, f, 300, name == "C4")
         fl = floor(hx)
         entry = {"us_step_back_to_back": round(back_to_back, 2), "us_step_single": round(single, 2),
-                 "launch_floor_us": round(fl, 2), "single_over_floor": round(single / fl, 2),
+                 "launch_floor_us": round(fl, 2), "back_to_back_over_floor": round(back_to_back / fl, 2),
+                 "single_over_floor": round(single / fl, 2),
                  "map_entries": ent,
                  "frac_of_peak_back_to_back": round(68 * ent / (back_to_back * 1e-6) / 1e9 / peak, 4)}
         if name == "C4":
@@ -472,13 +474,14 @@ def secondary(hx_main, coords, forces, w_main, dev, peak, flags):
         return entry
 
     # the small configurations in the run's modes, and with the forwarding
-    # resolved at build time (HX_FLAG_RESOLVED), the mode made for them
+    # resolved at build time and launched with programmatic dependent launch
+    # (HX_FLAG_RESOLVED | HX_FLAG_PDL), the mode made for them
     for name in ("C1", "C2", "C3", "C4"):
         if name == w_main.name:
             continue
         res[name] = small(name, flags)
         if not flags & HX.HX_FLAG_RESOLVED:
-            res[name]["resolved"] = small(name, HX.HX_FLAG_RESOLVED)
+            res[name]["resolved_pdl"] = small(name, HX.HX_FLAG_RESOLVED | HX.HX_FLAG_PDL)
     return res
 
 

@@ -372,6 +372,23 @@ int launch(hx_ctx* h, int kind, float* buf, cudaStream_t s) {
     args = args2;
     grid = dim3(static_cast<unsigned>(h->grid[kind]));
   }
+  if (kind != 2 && h->family[kind] == kFamResolved && (h->flags & HX_FLAG_PDL)) {
+    // direct launch that may start while the stream's previous kernel finishes;
+    // the resolved kernels wait for it (griddepcontrol.wait) before touching data
+    cudaLaunchAttribute attr[1];
+    std::memset(attr, 0, sizeof(attr));
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return to_err(cudaLaunchKernelExC(&cfg, fn, args));
+  }
   if (h->flags & HX_FLAG_NO_GRAPH) return to_err(cudaLaunchKernel(fn, grid, block, args, smem, s));
   for (auto& g : h->graphs)
     if (g.kind == kind && g.ptr == buf) return to_err(cudaGraphLaunch(g.exec, s));

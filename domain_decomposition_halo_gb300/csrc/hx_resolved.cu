@@ -28,12 +28,21 @@
 namespace hx {
 namespace {
 
+// Programmatic dependent launch: let the next kernel of the stream be
+// scheduled now (it waits in griddepcontrol.wait for this one), and wait for
+// the previous kernel before reading what it wrote. Both are no-ops in a
+// launch without the programmatic-serialization attribute.
+__device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void wait_prerequisites() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // One thread per halo slot: slot = origin (+ shifts).
 __global__ void __launch_bounds__(256) k_resolved_coords(float* __restrict__ x, ResolvedParams P) {
+  allow_dependents();
   const int64_t k = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (k >= P.n_halo) return;
-  const int2 so = __ldg(P.halo + k);   // (slot, origin)
+  const int2 so = __ldg(P.halo + k);   // (slot, origin): build-time tables, read before the wait
   const unsigned mask = __ldg(P.shift_mask + k);
+  wait_prerequisites();
   float v0 = x[3 * static_cast<int64_t>(so.y) + 0];
   float v1 = x[3 * static_cast<int64_t>(so.y) + 1];
   float v2 = x[3 * static_cast<int64_t>(so.y) + 2];
@@ -48,9 +57,11 @@ __global__ void __launch_bounds__(256) k_resolved_coords(float* __restrict__ x, 
 
 // One thread per tree: replay its adds in descending pulse order.
 __global__ void __launch_bounds__(256) k_resolved_forces(float* __restrict__ f, ResolvedParams P) {
+  allow_dependents();
   const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (t >= P.n_trees) return;
-  const TreeRec r = P.trees[t];
+  const TreeRec r = P.trees[t];   // build-time table, read before the wait
+  wait_prerequisites();
   float v[kTreeNodes][3];
 #pragma unroll
   for (int j = 0; j < kTreeNodes; ++j) {

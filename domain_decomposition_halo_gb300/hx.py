@@ -35,6 +35,7 @@ HX_FLAG_SWEEP_FORCES = 0x40
 HX_FLAG_CLUSTER = 0x80
 HX_FLAG_RESOLVED = 0x100
 HX_FLAG_BULK_STORE = 0x200
+HX_FLAG_PDL = 0x400
 
 HX_MAX_PULSES = 32
 

@@ -111,6 +111,11 @@ typedef struct hx_ctx* hx_handle;
                                           "Optimizing for efficient transfers across NVIDIA
                                           NVLink-connected GPUs"); same results bit for bit. Applies
                                           where the chunk kernels run the coordinates */
+#define HX_FLAG_PDL 0x400u             /* with HX_FLAG_RESOLVED: launch the exchanges directly with
+                                          programmatic dependent launch, so a resolved exchange may be
+                                          scheduled while the stream's previous kernel finishes (it
+                                          reads its build-time tables, then waits for that kernel before
+                                          touching coordinates or forces); ignored by other modes */
 #define HX_FLAG_RESOLVED 0x100u        /* the forwarding unrolled at build time: every halo slot is
                                           gathered straight from its origin home atom (plus the
                                           shifts its path added), and every home atom's force tree

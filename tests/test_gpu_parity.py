@@ -24,7 +24,7 @@ ALL_MODES = [0, HX.HX_FLAG_COUNTER_SIGNAL, HX.HX_FLAG_NO_GRAPH,
              HX.HX_FLAG_CLUSTER | HX.HX_FLAG_NO_GRAPH, HX.HX_FLAG_RESOLVED,
              HX.HX_FLAG_RESOLVED | HX.HX_FLAG_NO_GRAPH, HX.HX_FLAG_RESOLVED | HX.HX_FLAG_SWEEP_FORCES,
              HX.HX_FLAG_BULK_STORE, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE,
-             HX.HX_FLAG_COUNTER_SIGNAL | HX.HX_FLAG_BULK_STORE]
+             HX.HX_FLAG_COUNTER_SIGNAL | HX.HX_FLAG_BULK_STORE, HX.HX_FLAG_RESOLVED | HX.HX_FLAG_PDL]
 
 
 def _bits(a):
@@ -223,7 +223,7 @@ def test_many_steps_reuse_signals():
     """Epoch-valued signals are never reset between launches: 200 steps."""
     for flags in (0, HX.HX_FLAG_COUNTER_SIGNAL, HX.HX_FLAG_FINE_WAITS, HX.HX_FLAG_TILES, HX.HX_FLAG_SWEEP,
                   HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES, HX.HX_FLAG_CLUSTER, HX.HX_FLAG_RESOLVED,
-                  HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE):
+                  HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE, HX.HX_FLAG_RESOLVED | HX.HX_FLAG_PDL):
         c = Case(W.WORKLOADS["C2"], flags=flags)
         x = c.o.coords().copy()
         xt = torch.from_numpy(x).cuda()
