@@ -343,3 +343,28 @@ def test_dropped_signal_times_out_and_recovers(direction, flags):
     assert c.hx.status()[0] == 0
     check_coord_steps(c, steps=2)
     check_force_steps(c, steps=1)
+
+
+@pytest.mark.parametrize("name", ["C4", "C5"])
+@pytest.mark.parametrize("flags", [HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE | HX.HX_FLAG_SWEEP_FORCES,
+                                   HX.HX_FLAG_RESOLVED | HX.HX_FLAG_PDL])
+def test_back_to_back_steps(name, flags):
+    """Twenty coordinate + force exchanges queued back to back on one stream
+    (no synchronisation between them, so consecutive launches may overlap
+    their start-up) give the oracle's result of the same twenty steps, bit
+    for bit: coordinates are idempotent, forces accumulate every step."""
+    c = Case(W.WORKLOADS[name], flags=flags)
+    x = c.o.coords().copy()
+    f = W.forces(c.w, c.o.total_slots)
+    xt = torch.from_numpy(x).cuda()
+    ft = torch.from_numpy(f).cuda()
+    for _ in range(20):
+        c.hx.exchange_coords(xt)
+        c.hx.exchange_forces(ft)
+    torch.cuda.synchronize()
+    assert c.hx.status()[0] == 0
+    for _ in range(20):
+        c.o.exchange_coords(x)
+        c.o.exchange_forces(f)
+    assert np.array_equal(_bits(xt.cpu().numpy()), _bits(x))
+    assert np.array_equal(_bits(ft.cpu().numpy()), _bits(f))
