@@ -884,7 +884,9 @@ int build_tables(hx_ctx* h, cudaStream_t s) {
   if ((fine || (h->flags & (HX_FLAG_TILES | HX_FLAG_SWEEP | HX_FLAG_SWEEP_FORCES | HX_FLAG_RESOLVED))) &&
       h->total_entries > 0) {   // fine waits, units and resolved tables read the maps
     maps.resize(h->total_entries);
-    HX_CUDA(cudaMemcpy(maps.data(), h->d_maps, sizeof(int32_t) * h->total_entries, cudaMemcpyDeviceToHost));
+    // the maps were assembled on `s`, which need not synchronise with the legacy stream
+    HX_CUDA(cudaMemcpyAsync(maps.data(), h->d_maps, sizeof(int32_t) * h->total_entries, cudaMemcpyDeviceToHost, s));
+    HX_CUDA(cudaStreamSynchronize(s));
   }
   std::vector<int> upper_tab(static_cast<size_t>(nd) * std::max(P, 1));
   for (int r = 0; r < nd; ++r)
