@@ -47,9 +47,9 @@
  * The library owns the maps, tables, flags and graphs of a handle until
  * hx_destroy; the caller owns every buffer it passes in. A handle is not
  * thread-safe: calls on one handle must not run concurrently from several
- * host threads, and its exchanges must not overlap on the GPU (they share
- * the handle's signal flags and tickets; successive exchanges on one stream
- * never overlap). Different handles are independent.
+ * host threads, and two exchanges of the same direction must not overlap on
+ * the GPU (they share that direction's signal flags and tickets; successive
+ * exchanges on one stream never overlap). Different handles are independent.
  */
 #ifndef HX_H
 #define HX_H
