@@ -267,6 +267,7 @@ def run_ours(args):
     total_ms = start.elapsed_time(end)
     coord_ms = statistics.fmean(e[0].elapsed_time(e[1]) for e in ev)
     force_ms = statistics.fmean(e[1].elapsed_time(e[2]) for e in ev)
+    per_step_us = [e[0].elapsed_time(e[2]) * 1e3 for e in ev]
     if world > 1:
         total_ms = max_over_ranks(total_ms, dev)
         torch.distributed.barrier()
@@ -368,6 +369,7 @@ def run_ours(args):
             "traffic": profiled_traffic(dominant, w.name),
         },
         "kernels_ms": {"hx_coords_fused": round(coord_ms, 5), "hx_forces_fused": round(force_ms, 5)},
+        "step_us_distribution": step_distribution(per_step_us),
         "clocks": clk,
         "e2e": {"value": round(e2e_us, 2), "unit": "us/step", "h2d_bytes_per_step": bytes_h2d,
                 "d2h_bytes_per_step": bytes_d2h,
@@ -387,6 +389,14 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
+def step_distribution(ts):
+    """Median, 90th percentile (nearest rank), min and max of per-step times."""
+    xs = sorted(ts)
+    p90 = xs[min(len(xs) - 1, max(0, -(-9 * len(xs) // 10) - 1))]
+    return {"median": round(statistics.median(xs), 2), "p90": round(p90, 2), "min": round(xs[0], 2),
+            "max": round(xs[-1], 2), "n": len(xs)}
+
+
 def _flush(buf):
     buf.add_(1.0)
 
@@ -401,7 +411,7 @@ def secondary(hx_main, coords, forces, w_main, dev, peak, flags):
     flush_buf = torch.zeros(2 * L2_BYTES // 4, device=dev)
     stream = torch.cuda.current_stream()
 
-    def timed(hx, x, f, reps, flush):
+    def timed(hx, x, f, reps, flush, dist=False):
         ts = []
         for _ in range(reps):
             if flush:
@@ -414,7 +424,7 @@ def secondary(hx_main, coords, forces, w_main, dev, peak, flags):
             b.record(stream)
             torch.cuda.synchronize()
             ts.append(a.elapsed_time(b) * 1e3)
-        return statistics.median(ts)
+        return step_distribution(ts) if dist else statistics.median(ts)
 
     def floor(hx, reps=300):
         ts = []
@@ -435,9 +445,9 @@ def secondary(hx_main, coords, forces, w_main, dev, peak, flags):
     if chunk_flags != flags:
         res["overlap_with_local_kernel_us"]["chunk_kernels"] = overlap_probe(dev, chunk_flags)
     entries = hx_main.counts()[3]
-    cold = timed(hx_main, coords, forces, 30, True)
-    res[w_main.name + "_cold_l2"] = {"us_step": round(cold, 2),
-                                     "frac_of_peak": round(68 * entries / (cold * 1e-6) / 1e9 / peak, 4)}
+    cold = timed(hx_main, coords, forces, 30, True, dist=True)
+    res[w_main.name + "_cold_l2"] = {"us_step": cold["median"], "p90": cold["p90"],
+                                     "frac_of_peak": round(68 * entries / (cold["median"] * 1e-6) / 1e9 / peak, 4)}
     def small(name, mode_flags):
         w = W.WORKLOADS[name]
         hx = HaloExchange(w.box, w.dims, w.cutoff, device=dev.index, flags=mode_flags)
@@ -558,9 +568,24 @@ def cpu_baseline(w, pos, budget_s):
         el = time.perf_counter() - t0
         if (el >= budget_s and n >= 3) or n >= 1000:
             break
-    return {"value": round(el / n * 1e6, 1), "unit": "us/step", "cores": 1, "kind": "oracle",
-            "sample": f"{n} full steps of {w.name} (coords + forces), one host thread, C oracle gcc -O2",
-            "host_cpus": os.cpu_count()}
+    out = {"value": round(el / n * 1e6, 1), "unit": "us/step", "cores": 1, "kind": "oracle",
+           "sample": f"{n} full steps of {w.name} (coords + forces), one host thread, C oracle gcc -O2",
+           "host_cpus": os.cpu_count()}
+    # the same loops with each pulse's senders on every host core (pulse
+    # order kept; bit-identical results), reported beside the one-core value
+    threads = min(os.cpu_count() or 1, o.max_threads()) if o.max_threads() > 1 else 1
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        o.exchange_coords_par(x, threads)
+        o.exchange_forces_par(f, threads)
+        n += 1
+        el = time.perf_counter() - t0
+        if (el >= budget_s / 3 and n >= 3) or n >= 1000:
+            break
+    out["all_cores"] = {"value": round(el / n * 1e6, 1), "unit": "us/step", "cores": threads,
+                        "sample": f"{n} full steps of {w.name}, each pulse's senders on {threads} OpenMP threads"}
+    return out
 
 
 # ---------------------------------------------------------------- reference arm

@@ -49,12 +49,18 @@
  *
  * Compile with -ffp-contract=off (there is no multiply in the exchanged
  * arithmetic, but the flag keeps the reading "one IEEE fp32 add or subtract
- * per operation" independent of the compiler).
+ * per operation" independent of the compiler). With -fopenmp the *_par
+ * exchanges run each pulse's senders on several threads, pulse order kept:
+ * the same arithmetic on independent senders, used to time the oracle on all
+ * host cores.
  */
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 #define OR_OK 0
 #define OR_ERR_ARG (-1)
@@ -391,10 +397,20 @@ void oracle_get_coords(const oracle_dd* o, float* coords) {
 
 /* Coordinate exchange on a flat array whose home slots hold current
  * coordinates: replay every pulse in order; packed[i] = data[map[i]], with
- * the periodic shift, stored at the receiver's offset. */
-void oracle_exchange_coords(const oracle_dd* o, float* x) {
+ * the periodic shift, stored at the receiver's offset.
+ *
+ * `threads` > 1 runs the senders of one pulse on that many OpenMP threads
+ * (pulse order kept). Within a pulse every sender writes only its own
+ * receiver's receive range of that pulse, and reads only its home and
+ * earlier receive ranges, so no two senders touch the same slot and the
+ * result is the same bit for bit. */
+static void exchange_coords_impl(const oracle_dd* o, float* x, int threads) {
+    (void)threads;
     for (int p = 0; p < o->n_pulses; ++p) {
         const int d = o->pulse_dim[p];
+#ifdef _OPENMP
+#pragma omp parallel for num_threads(threads) schedule(dynamic, 1) if (threads > 1)
+#endif
         for (int r = 0; r < o->ndom; ++r) {
             const size_t t = (size_t)p * o->ndom + r;
             const int32_t* m = o->maps + o->t_map_off[t];
@@ -418,9 +434,16 @@ void oracle_exchange_coords(const oracle_dd* o, float* x) {
     }
 }
 
-/* Force exchange: pulses last to first; forces[map[i]] += received[i]. */
-void oracle_exchange_forces(const oracle_dd* o, float* f) {
+/* Force exchange: pulses last to first; forces[map[i]] += received[i].
+ * With `threads` > 1 the senders of one pulse run in parallel: a sender adds
+ * only into its own home and earlier receive ranges and reads its receiver's
+ * receive range of this pulse, which no sender writes in this pulse. */
+static void exchange_forces_impl(const oracle_dd* o, float* f, int threads) {
+    (void)threads;
     for (int p = o->n_pulses - 1; p >= 0; --p) {
+#ifdef _OPENMP
+#pragma omp parallel for num_threads(threads) schedule(dynamic, 1) if (threads > 1)
+#endif
         for (int r = 0; r < o->ndom; ++r) {
             const size_t t = (size_t)p * o->ndom + r;
             const int32_t* m = o->maps + o->t_map_off[t];
@@ -434,4 +457,25 @@ void oracle_exchange_forces(const oracle_dd* o, float* f) {
             }
         }
     }
+}
+
+void oracle_exchange_coords(const oracle_dd* o, float* x) { exchange_coords_impl(o, x, 1); }
+void oracle_exchange_forces(const oracle_dd* o, float* f) { exchange_forces_impl(o, f, 1); }
+
+/* The same exchanges with the senders of each pulse spread over `threads`
+ * OpenMP threads (clamped to at least 1). Without OpenMP support at compile
+ * time they run on one thread; oracle_max_threads() then returns 1. */
+void oracle_exchange_coords_par(const oracle_dd* o, float* x, int threads) {
+    exchange_coords_impl(o, x, threads < 1 ? 1 : threads);
+}
+void oracle_exchange_forces_par(const oracle_dd* o, float* f, int threads) {
+    exchange_forces_impl(o, f, threads < 1 ? 1 : threads);
+}
+
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
 }

@@ -26,10 +26,14 @@ _libs = {}
 
 
 def compile_oracle(src: str, out: str) -> str:
-    """gcc -O2 -ffp-contract=off of one oracle source into a shared object."""
+    """gcc -O2 -ffp-contract=off of one oracle source into a shared object,
+    with OpenMP when the compiler has it (the threaded exchanges), else
+    without (they then run on one thread)."""
     tmp = out + f".tmp{os.getpid()}"
-    cmd = ["gcc", "-O2", "-std=c99", "-ffp-contract=off", "-fPIC", "-shared", "-o", tmp, src, "-lm"]
-    subprocess.run(cmd, check=True)
+    base = ["gcc", "-O2", "-std=c99", "-ffp-contract=off", "-fPIC", "-shared", "-o", tmp, src, "-lm"]
+    done = subprocess.run(base[:1] + ["-fopenmp"] + base[1:], capture_output=True)
+    if done.returncode != 0:
+        subprocess.run(base, check=True)
     os.replace(tmp, out)
     return out
 
@@ -66,6 +70,10 @@ def _load(path: Optional[str] = None) -> ctypes.CDLL:
         lib.oracle_get_coords.argtypes = [P, P]
         lib.oracle_exchange_coords.argtypes = [P, P]
         lib.oracle_exchange_forces.argtypes = [P, P]
+        lib.oracle_exchange_coords_par.argtypes = [P, P, ctypes.c_int]
+        lib.oracle_exchange_forces_par.argtypes = [P, P, ctypes.c_int]
+        lib.oracle_max_threads.restype = ctypes.c_int
+        lib.oracle_max_threads.argtypes = []
         _ = I32
         _libs[path] = lib
     return _libs[path]
@@ -160,3 +168,17 @@ class Oracle:
         """In place on a C-contiguous fp32 [total_slots, 3] array."""
         assert f.dtype == np.float32 and f.flags.c_contiguous and f.shape == (self.total_slots, 3)
         self._lib.oracle_exchange_forces(self._h, _ptr(f))
+
+    def exchange_coords_par(self, x: np.ndarray, threads: int) -> None:
+        """``exchange_coords`` with each pulse's senders on ``threads`` threads."""
+        assert x.dtype == np.float32 and x.flags.c_contiguous and x.shape == (self.total_slots, 3)
+        self._lib.oracle_exchange_coords_par(self._h, _ptr(x), int(threads))
+
+    def exchange_forces_par(self, f: np.ndarray, threads: int) -> None:
+        """``exchange_forces`` with each pulse's senders on ``threads`` threads."""
+        assert f.dtype == np.float32 and f.flags.c_contiguous and f.shape == (self.total_slots, 3)
+        self._lib.oracle_exchange_forces_par(self._h, _ptr(f), int(threads))
+
+    def max_threads(self) -> int:
+        """OpenMP's default thread count, or 1 if the oracle was built without OpenMP."""
+        return int(self._lib.oracle_max_threads())

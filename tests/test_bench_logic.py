@@ -45,3 +45,11 @@ def test_kernel_impl_names_the_launched_kernels():
     assert bench.kernel_impl(default, 1).startswith("k_sweep<1>")
     assert bench.kernel_impl(0, 1).startswith("k_forces_fused<last arrival, ordered>")
     assert bench.kernel_impl(bench.hx_flags("resolved"), 1).startswith("k_resolved_forces")
+
+
+def test_step_distribution_nearest_rank_p90():
+    d = bench.step_distribution([10.0 - k for k in range(10)])   # 1..10, unsorted
+    assert d == {"median": 5.5, "p90": 9.0, "min": 1.0, "max": 10.0, "n": 10}
+    d = bench.step_distribution(list(range(1, 21)))
+    assert d["p90"] == 18 and d["median"] == 10.5
+    assert bench.step_distribution([3.0])["p90"] == 3.0
