@@ -191,10 +191,12 @@ struct hx_ctx {
   int n_units[2] = {0, 0};
   std::vector<int> u_begin;                  // per pulse, first unfused chunk (P + 1 entries)
   std::vector<GraphEntry> graphs;
-  int2* d_res_halo = nullptr;                // resolved mode: (slot, origin) per halo slot
-  uint8_t* d_res_mask = nullptr;             // ... and its shift mask
-  TreeRec* d_res_trees = nullptr;            // ... and the force trees
-  int64_t n_res_halo = 0, n_res_trees = 0;
+  ResSeg* d_res_segs = nullptr;              // resolved mode: halo segments
+  uint32_t* d_res_om = nullptr;              // ... origin and shift mask per halo slot
+  int2* d_res_pairs = nullptr;               // ... force trees: pairs, quads, general
+  int4* d_res_quads = nullptr;
+  TreeRec* d_res_trees = nullptr;
+  int64_t n_res_halo = 0, n_res_segs = 0, n_res_pairs = 0, n_res_quads = 0, n_res_trees = 0;
 };
 
 namespace {
@@ -213,10 +215,12 @@ void free_tables(hx_ctx* h) {
     dev_free(h->d_waits[k]);
   }
   dev_free(h->d_uchunks);
-  dev_free(h->d_res_halo);
-  dev_free(h->d_res_mask);
+  dev_free(h->d_res_segs);
+  dev_free(h->d_res_om);
+  dev_free(h->d_res_pairs);
+  dev_free(h->d_res_quads);
   dev_free(h->d_res_trees);
-  h->n_res_halo = h->n_res_trees = 0;
+  h->n_res_halo = h->n_res_segs = h->n_res_pairs = h->n_res_quads = h->n_res_trees = 0;
   for (int k = 0; k < 2; ++k) {
     dev_free(h->d_units[k]);
     dev_free(h->d_segs[k]);
@@ -285,7 +289,8 @@ TileParams tile_params(hx_ctx* h, int dir) {
 // Work items of the fused list of direction `dir`: units or chunks.
 int work_items(const hx_ctx* h, int dir) {
   if (h->family[dir] == kFamCluster) return h->u_begin.empty() ? 0 : h->u_begin.back();
-  if (h->family[dir] == kFamResolved) return static_cast<int>(dir == 0 ? h->n_res_halo : h->n_res_trees);
+  if (h->family[dir] == kFamResolved)
+    return static_cast<int>(dir == 0 ? h->n_res_halo : h->n_res_pairs + h->n_res_quads + h->n_res_trees);
   return h->family[dir] == kFamChunks ? h->n_chunks[dir] : h->n_units[dir];
 }
 
@@ -306,10 +311,14 @@ unsigned fused_threads(const hx_ctx* h, int dir) {
 ResolvedParams resolved_params(hx_ctx* h) {
   ResolvedParams P;
   std::memset(&P, 0, sizeof(P));
-  P.halo = h->d_res_halo;
-  P.shift_mask = h->d_res_mask;
+  P.segs = h->d_res_segs;
+  P.origin_mask = h->d_res_om;
+  P.pairs = h->d_res_pairs;
+  P.quads = h->d_res_quads;
   P.trees = h->d_res_trees;
-  P.n_halo = h->n_res_halo;
+  P.n_segs = h->n_res_segs;
+  P.n_pairs = h->n_res_pairs;
+  P.n_quads = h->n_res_quads;
   P.n_trees = h->n_res_trees;
   for (int d = 0; d < 3; ++d) P.box[d] = h->pl.boxf[d];
   return P;
@@ -760,14 +769,16 @@ int build_tile_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::
 }
 
 // Resolved tables: every halo slot's origin and shift mask (pulses in order,
-// each received slot inheriting from the slot it was sent from), and one
-// tree per home atom that has copies, its adds sorted by descending pulse.
-// Indexed by halo slot (domain after domain) and by home atom, not by slot.
+// each received slot inheriting from the slot it was sent from), in halo
+// order (domain after domain) with one segment record per block; and one
+// tree per home atom that has copies, its adds sorted by descending pulse,
+// numbered in home-slot order and split into pairs, quads and general trees.
 int build_resolved_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::vector<int32_t>& maps,
                           cudaStream_t s) {
   const Plan& pl = h->pl;
   const int P = pl.n_pulses, nd = pl.ndom;
-  if (h->total_slots >= (int64_t{1} << 31)) return HX_ERR_CAPACITY;   // slots are int32 in the records
+  // origins share a word with the shift mask; other slots are int32 in the records
+  if (h->total_slots >= (int64_t{1} << kResOriginBits)) return HX_ERR_CAPACITY;
   std::vector<int64_t> hbase(nd + 1, 0), home_base(nd + 1, 0);
   for (int r = 0; r < nd; ++r) {
     hbase[r + 1] = hbase[r] + h->halo[r];
@@ -800,29 +811,39 @@ int build_resolved_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const s
         pulse[k] = static_cast<uint8_t>(p);
       }
     }, 1);
-  std::vector<int2> halo(H);
+  // coordinates: origin and shift mask packed per halo slot, segments per domain
+  std::vector<uint32_t> om(H);
+  for (int64_t k = 0; k < H; ++k)
+    om[k] = static_cast<uint32_t>(origin_slot[k]) | (static_cast<uint32_t>(mask[k]) << kResOriginBits);
+  std::vector<ResSeg> segs;
   for (int r = 0; r < nd; ++r)
-    for (int64_t k = hbase[r]; k < hbase[r + 1]; ++k)
-      halo[k] = make_int2(static_cast<int>(h->dom_offset[r] + h->home[r] + (k - hbase[r])), origin_slot[k]);
-  // trees: one per home atom that has copies, numbered in halo order
+    for (int64_t k = hbase[r]; k < hbase[r + 1]; k += kResSeg) {
+      ResSeg sg;
+      sg.k = static_cast<int32_t>(k);
+      sg.slot = static_cast<int32_t>(h->dom_offset[r] + h->home[r] + (k - hbase[r]));
+      sg.n = static_cast<int32_t>(std::min<int64_t>(kResSeg, hbase[r + 1] - k));
+      sg.pad = 0;
+      segs.push_back(sg);
+    }
+  // trees: one per home atom that has copies, numbered in home-slot order
   std::vector<int32_t> tree_of(home_base[nd], -1);
+  for (int64_t k = 0; k < H; ++k) tree_of[origin_home[k]] = 0;   // marks the roots
   int32_t n_trees = 0;
-  for (int64_t k = 0; k < H; ++k) {
-    int32_t& t = tree_of[origin_home[k]];
-    if (t < 0) t = n_trees++;
-  }
+  for (int64_t a = 0; a < home_base[nd]; ++a)
+    if (tree_of[a] == 0) tree_of[a] = n_trees++;
   std::vector<TreeRec> trees(static_cast<size_t>(n_trees));   // zero-filled
   std::vector<uint8_t> node_idx(H);
-  for (int64_t k = 0; k < H; ++k) {
-    TreeRec& rec = trees[tree_of[origin_home[k]]];
-    if (rec.n_nodes == 0) {
-      rec.node[0] = origin_slot[k];
-      rec.n_nodes = 1;
+  for (int r = 0; r < nd; ++r)   // nodes: the root, then its copies in halo order
+    for (int64_t k = hbase[r]; k < hbase[r + 1]; ++k) {
+      TreeRec& rec = trees[tree_of[origin_home[k]]];
+      if (rec.n_nodes == 0) {
+        rec.node[0] = origin_slot[k];
+        rec.n_nodes = 1;
+      }
+      if (rec.n_nodes >= kTreeNodes) return HX_ERR_PULSES;   // more copies than a tree record holds
+      node_idx[k] = static_cast<uint8_t>(rec.n_nodes);
+      rec.node[rec.n_nodes++] = static_cast<int32_t>(h->dom_offset[r] + h->home[r] + (k - hbase[r]));
     }
-    if (rec.n_nodes >= kTreeNodes) return HX_ERR_PULSES;   // more copies than a tree record holds
-    node_idx[k] = static_cast<uint8_t>(rec.n_nodes);
-    rec.node[rec.n_nodes++] = halo[k].x;
-  }
   // adds: copy j (node j > 0) into its parent, then sorted by descending pulse
   std::vector<uint8_t> add_pulse(trees.size() * kTreeNodes, 0);
   for (int64_t k = 0; k < H; ++k) {
@@ -842,17 +863,50 @@ int build_resolved_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const s
         std::swap(rec.ev[b], rec.ev[b - 1]);
       }
   }, 1024);
-  h->n_res_halo = H;
-  h->n_res_trees = static_cast<int64_t>(trees.size());
-  HX_CUDA(dev_alloc(&h->d_res_halo, halo.size()));
-  HX_CUDA(dev_alloc(&h->d_res_mask, mask.size()));
-  HX_CUDA(dev_alloc(&h->d_res_trees, trees.size()));
-  if (H > 0) {
-    HX_CUDA(cudaMemcpyAsync(h->d_res_halo, halo.data(), sizeof(int2) * halo.size(), cudaMemcpyHostToDevice, s));
-    HX_CUDA(cudaMemcpyAsync(h->d_res_mask, mask.data(), mask.size(), cudaMemcpyHostToDevice, s));
+  // classes, each keeping root order. A four-node tree is a quad when its
+  // last add (lowest pulse) is some copy u into the root and the two adds
+  // before it are one copy into the root and one copy into u: then the
+  // fixed order root += c, u += d, root += u is the staged order.
+  std::vector<int2> pairs;
+  std::vector<int4> quads;
+  std::vector<TreeRec> general;
+  for (const TreeRec& rec : trees) {
+    if (rec.n_nodes == 2) {
+      pairs.push_back(make_int2(rec.node[0], rec.node[1]));
+      continue;
+    }
+    if (rec.n_nodes == 4) {
+      const int tg2 = rec.ev[2] & 15, u = rec.ev[2] >> 4;
+      const int tg0 = rec.ev[0] & 15, s0 = rec.ev[0] >> 4, tg1 = rec.ev[1] & 15, s1 = rec.ev[1] >> 4;
+      if (tg2 == 0 && u != 0 && ((tg0 == 0 && tg1 == u) || (tg0 == u && tg1 == 0))) {
+        const int c = tg0 == 0 ? s0 : s1, d = tg0 == 0 ? s1 : s0;
+        quads.push_back(make_int4(rec.node[0], rec.node[u], rec.node[c], rec.node[d]));
+        continue;
+      }
+    }
+    general.push_back(rec);
   }
-  if (!trees.empty())
-    HX_CUDA(cudaMemcpyAsync(h->d_res_trees, trees.data(), sizeof(TreeRec) * trees.size(), cudaMemcpyHostToDevice, s));
+  h->n_res_halo = H;
+  h->n_res_segs = static_cast<int64_t>(segs.size());
+  h->n_res_pairs = static_cast<int64_t>(pairs.size());
+  h->n_res_quads = static_cast<int64_t>(quads.size());
+  h->n_res_trees = static_cast<int64_t>(general.size());
+  HX_CUDA(dev_alloc(&h->d_res_om, om.size()));
+  HX_CUDA(dev_alloc(&h->d_res_segs, segs.size()));
+  HX_CUDA(dev_alloc(&h->d_res_pairs, pairs.size()));
+  HX_CUDA(dev_alloc(&h->d_res_quads, quads.size()));
+  HX_CUDA(dev_alloc(&h->d_res_trees, general.size()));
+  if (H > 0) {
+    HX_CUDA(cudaMemcpyAsync(h->d_res_om, om.data(), sizeof(uint32_t) * om.size(), cudaMemcpyHostToDevice, s));
+    HX_CUDA(cudaMemcpyAsync(h->d_res_segs, segs.data(), sizeof(ResSeg) * segs.size(), cudaMemcpyHostToDevice, s));
+  }
+  if (!pairs.empty())
+    HX_CUDA(cudaMemcpyAsync(h->d_res_pairs, pairs.data(), sizeof(int2) * pairs.size(), cudaMemcpyHostToDevice, s));
+  if (!quads.empty())
+    HX_CUDA(cudaMemcpyAsync(h->d_res_quads, quads.data(), sizeof(int4) * quads.size(), cudaMemcpyHostToDevice, s));
+  if (!general.empty())
+    HX_CUDA(cudaMemcpyAsync(h->d_res_trees, general.data(), sizeof(TreeRec) * general.size(),
+                            cudaMemcpyHostToDevice, s));
   HX_CUDA(cudaStreamSynchronize(s));   // the host vectors go out of scope
   return HX_OK;
 }
@@ -1176,8 +1230,9 @@ int build_tables(hx_ctx* h, cudaStream_t s) {
   // more of them than there is work.
   for (int k = 0; k < 2; ++k) {
     if (h->family[k] == kFamResolved) {
-      const int64_t n = k == 0 ? h->n_res_halo : h->n_res_trees;
-      h->grid[k] = static_cast<int>(std::max<int64_t>(1, (n + 255) / 256));
+      // coordinates: one block per halo segment; forces: one thread per tree
+      const int64_t trees = h->n_res_pairs + h->n_res_quads + h->n_res_trees;
+      h->grid[k] = static_cast<int>(std::max<int64_t>(1, k == 0 ? h->n_res_segs : (trees + 255) / 256));
     } else if (h->family[k] == kFamCluster) {
       h->grid[k] = kClusterCtas;   // exactly one cluster
     } else if (h->family[k] == kFamTiles) {
@@ -1617,6 +1672,15 @@ int hx_get_counts(hx_handle h, int* n_domains, int* n_pulses, int64_t* total_slo
   if (!h->built) return HX_ERR_STATE;
   if (total_slots) *total_slots = h->total_slots;
   if (total_entries) *total_entries = h->total_entries;
+  return HX_OK;
+}
+
+int hx_get_resolved_counts(hx_handle h, int64_t* n_pairs, int64_t* n_quads, int64_t* n_general) {
+  if (!h) return HX_ERR_ARG;
+  if (!h->built) return HX_ERR_STATE;
+  if (n_pairs) *n_pairs = h->n_res_pairs;
+  if (n_quads) *n_quads = h->n_res_quads;
+  if (n_general) *n_general = h->n_res_trees;
   return HX_OK;
 }
 

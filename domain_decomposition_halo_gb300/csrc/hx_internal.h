@@ -122,12 +122,32 @@ struct alignas(16) TreeRec {
   int32_t pad;
 };
 static_assert(sizeof(TreeRec) == 48, "tree record must stay 48 bytes");
+// Coordinates: one block per segment of up to kResSeg consecutive halo slots
+// of one domain; per halo slot one word, the origin home slot in the low 29
+// bits and the shift mask (bit d: add box[d] to component d) in the top 3.
+constexpr int kResSeg = 256;
+constexpr int kResOriginBits = 29;
+struct ResSeg {
+  int32_t k;                              // first halo index of the segment
+  int32_t slot;                           // its global slot
+  int32_t n;                              // halo slots in the segment, 1..kResSeg
+  int32_t pad;
+};
+static_assert(sizeof(ResSeg) == 16, "segment record must stay 16 bytes");
+// Forces: trees in three classes, each in home-slot order of its root.
+//   pair (root, copy):  root += copy
+//   quad (a, b, c, d):  a += c; b += d; a += b   (c, d received in one later
+//                        pulse than b: a corner atom's two copies and the
+//                        copy of its first copy)
+//   general: TreeRec, adds replayed from the record
 struct ResolvedParams {
-  const int2* halo;                       // per halo slot: (slot, origin home slot)
-  const uint8_t* shift_mask;              // per halo slot: bit d = add box[d] to component d
-  const TreeRec* trees;                   // home atoms that have copies
-  int64_t n_halo;
-  int64_t n_trees;
+  const ResSeg* segs;
+  const uint32_t* origin_mask;            // per halo slot
+  const int2* pairs;
+  const int4* quads;
+  const TreeRec* trees;                   // the general class
+  int64_t n_segs;
+  int64_t n_pairs, n_quads, n_trees;
   float box[3];
   int pad;
 };

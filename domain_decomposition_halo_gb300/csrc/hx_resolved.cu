@@ -20,7 +20,13 @@
 // received in pulse p is sent only in later pulses). Replaying a tree's adds
 // in that order in registers gives every slot of the tree the staged fp32
 // sums exactly. One thread per tree: load the record, load the node values,
-// add, store the nodes that received adds.
+// add, store the nodes that received adds. Most trees are an atom with one
+// copy (one add) or a corner atom with two copies and the copy of its first
+// copy (three adds in a fixed order); those two shapes get compact records
+// and straight-line code, the rest the general record.
+//
+// Tables are numbered in slot order (halo slots, tree roots), so neighbouring
+// threads touch neighbouring slots.
 #include <cstdint>
 
 #include "hx_internal.h"
@@ -36,42 +42,50 @@ __device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontro
 __device__ __forceinline__ void wait_prerequisites() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // One thread per halo slot: slot = origin (+ shifts).
-__global__ void __launch_bounds__(256) k_resolved_coords(float* __restrict__ x, ResolvedParams P) {
+__global__ void __launch_bounds__(kResSeg) k_resolved_coords(float* __restrict__ x, ResolvedParams P) {
   allow_dependents();
-  const int64_t k = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (k >= P.n_halo) return;
-  const int2 so = __ldg(P.halo + k);   // (slot, origin): build-time tables, read before the wait
-  const unsigned mask = __ldg(P.shift_mask + k);
+  const ResSeg sg = P.segs[blockIdx.x];   // build-time tables, read before the wait
+  if (static_cast<int>(threadIdx.x) >= sg.n) return;
+  const uint32_t om = __ldg(P.origin_mask + sg.k + threadIdx.x);
   wait_prerequisites();
-  float v0 = x[3 * static_cast<int64_t>(so.y) + 0];
-  float v1 = x[3 * static_cast<int64_t>(so.y) + 1];
-  float v2 = x[3 * static_cast<int64_t>(so.y) + 2];
+  const int64_t o = 3 * static_cast<int64_t>(om & ((1u << kResOriginBits) - 1u));
+  const unsigned mask = om >> kResOriginBits;
+  float v0 = x[o + 0];
+  float v1 = x[o + 1];
+  float v2 = x[o + 2];
   if (mask & 1u) v0 = __fadd_rn(v0, P.box[0]);   // no add otherwise: unshifted values keep every bit
   if (mask & 2u) v1 = __fadd_rn(v1, P.box[1]);
   if (mask & 4u) v2 = __fadd_rn(v2, P.box[2]);
-  float* d = x + 3 * static_cast<int64_t>(so.x);
+  float* d = x + 3 * (static_cast<int64_t>(sg.slot) + threadIdx.x);
   d[0] = v0;
   d[1] = v1;
   d[2] = v2;
 }
 
-// One thread per tree: replay its adds in descending pulse order.
-__global__ void __launch_bounds__(256) k_resolved_forces(float* __restrict__ f, ResolvedParams P) {
-  allow_dependents();
-  const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (t >= P.n_trees) return;
-  const TreeRec r = P.trees[t];   // build-time table, read before the wait
-  wait_prerequisites();
+__device__ __forceinline__ void load3(const float* f, int slot, float (&v)[3]) {
+  const float* p = f + 3 * static_cast<int64_t>(slot);
+  v[0] = p[0];
+  v[1] = p[1];
+  v[2] = p[2];
+}
+__device__ __forceinline__ void store3(float* f, int slot, const float (&v)[3]) {
+  float* p = f + 3 * static_cast<int64_t>(slot);
+  p[0] = v[0];
+  p[1] = v[1];
+  p[2] = v[2];
+}
+__device__ __forceinline__ void add3(float (&a)[3], const float (&b)[3]) {
+  a[0] = __fadd_rn(a[0], b[0]);
+  a[1] = __fadd_rn(a[1], b[1]);
+  a[2] = __fadd_rn(a[2], b[2]);
+}
+
+// A general tree: replay its adds in descending pulse order.
+__device__ __forceinline__ void general_tree(float* __restrict__ f, const TreeRec& r) {
   float v[kTreeNodes][3];
 #pragma unroll
-  for (int j = 0; j < kTreeNodes; ++j) {
-    if (j < r.n_nodes) {
-      const float* p = f + 3 * static_cast<int64_t>(r.node[j]);
-      v[j][0] = p[0];
-      v[j][1] = p[1];
-      v[j][2] = p[2];
-    }
-  }
+  for (int j = 0; j < kTreeNodes; ++j)
+    if (j < r.n_nodes) load3(f, r.node[j], v[j]);
   unsigned target = 0;   // nodes that receive an add
 #pragma unroll
   for (int e = 0; e < kTreeNodes - 1; ++e) {
@@ -84,23 +98,52 @@ __global__ void __launch_bounds__(256) k_resolved_forces(float* __restrict__ f, 
 #pragma unroll
         for (int b = 0; b < kTreeNodes; ++b) {
           if (b != sc) continue;
-          v[a][0] = __fadd_rn(v[a][0], v[b][0]);
-          v[a][1] = __fadd_rn(v[a][1], v[b][1]);
-          v[a][2] = __fadd_rn(v[a][2], v[b][2]);
+          add3(v[a], v[b]);
         }
       }
       target |= 1u << tg;
     }
   }
 #pragma unroll
-  for (int j = 0; j < kTreeNodes; ++j) {
-    if (j < r.n_nodes && (target >> j & 1u)) {
-      float* p = f + 3 * static_cast<int64_t>(r.node[j]);
-      p[0] = v[j][0];
-      p[1] = v[j][1];
-      p[2] = v[j][2];
-    }
+  for (int j = 0; j < kTreeNodes; ++j)
+    if (j < r.n_nodes && (target >> j & 1u)) store3(f, r.node[j], v[j]);
+}
+
+// One thread per tree; the three classes lie one after another in the grid.
+__global__ void __launch_bounds__(256) k_resolved_forces(float* __restrict__ f, ResolvedParams P) {
+  allow_dependents();
+  int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t < P.n_pairs) {
+    const int2 pr = __ldg(P.pairs + t);   // build-time table, read before the wait
+    wait_prerequisites();
+    float a[3], b[3];
+    load3(f, pr.x, a);
+    load3(f, pr.y, b);
+    add3(a, b);
+    store3(f, pr.x, a);
+    return;
   }
+  t -= P.n_pairs;
+  if (t < P.n_quads) {
+    const int4 q = __ldg(P.quads + t);
+    wait_prerequisites();
+    float a[3], b[3], c[3], d[3];
+    load3(f, q.x, a);
+    load3(f, q.y, b);
+    load3(f, q.z, c);
+    load3(f, q.w, d);
+    add3(a, c);   // the later pulse: the corner copy into the atom, the copy's copy into the copy
+    add3(b, d);
+    add3(a, b);   // then the first copy into the atom
+    store3(f, q.x, a);
+    store3(f, q.y, b);
+    return;
+  }
+  t -= P.n_quads;
+  if (t >= P.n_trees) return;
+  const TreeRec r = P.trees[t];
+  wait_prerequisites();
+  general_tree(f, r);
 }
 
 }  // namespace

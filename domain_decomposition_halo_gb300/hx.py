@@ -46,6 +46,7 @@ SIGNATURES = {
     "hx_init": (_I, [_P, _P, _P, _D, _I, _U, _U]),
     "hx_build_maps": (_I, [_P, _P, _I64, _P, _I64, _P, _P]),
     "hx_get_counts": (_I, [_P, _P, _P, _P, _P]),
+    "hx_get_resolved_counts": (_I, [_P, _P, _P, _P]),
     "hx_get_layout": (_I, [_P, _P, _P, _P]),
     "hx_get_home_ids": (_I, [_P, _P, _P]),
     "hx_get_maps": (_I, [_P, _P, _I64, _P]),
@@ -204,6 +205,13 @@ class HaloExchange:
         _check(self._lib.hx_get_counts(self._h, ctypes.byref(nd), ctypes.byref(npl), ctypes.byref(ts),
                                        ctypes.byref(te)), "hx_get_counts")
         return nd.value, npl.value, ts.value, te.value
+
+    def resolved_counts(self) -> Tuple[int, int, int]:
+        """Resolved mode's force trees: (pairs, quads, general)."""
+        a, b, c = ctypes.c_int64(0), ctypes.c_int64(0), ctypes.c_int64(0)
+        _check(self._lib.hx_get_resolved_counts(self._h, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)),
+               "hx_get_resolved_counts")
+        return a.value, b.value, c.value
 
     def layout(self):
         nd = self.counts()[0]

@@ -128,7 +128,9 @@ typedef struct hx_ctx* hx_handle;
                                           results bit for bit. Forces are ordered
                                           (HX_FLAG_UNORDERED_FORCES is ignored); no device waits.
                                           A home atom may have at most 7 copies (else HX_ERR_PULSES
-                                          from hx_build_maps) */
+                                          from hx_build_maps), and a layout at most 2^29 slots (else
+                                          HX_ERR_CAPACITY: a halo slot's origin and shifts share one
+                                          32-bit word) */
 
 #define HX_MAX_PULSES 32
 #define HX_MAX_DOMAINS 4096
@@ -169,6 +171,13 @@ int hx_build_maps(hx_handle h, const float* pos_in, int64_t n_atoms,
 /* Sizes after a build (host outputs; any may be NULL). */
 int hx_get_counts(hx_handle h, int* n_domains, int* n_pulses, int64_t* total_slots,
                   int64_t* total_entries);
+
+/* Resolved mode's force trees after a build (host outputs; any may be
+ * NULL): trees that are an atom and one copy (one add), corner trees of four
+ * nodes summed in a fixed order (three adds), and general trees. All three
+ * are 0 for a handle without HX_FLAG_RESOLVED. Errors: HX_ERR_ARG,
+ * HX_ERR_STATE. */
+int hx_get_resolved_counts(hx_handle h, int64_t* n_pairs, int64_t* n_quads, int64_t* n_general);
 
 /* Per-domain layout (host arrays of n_domains entries; any may be NULL):
  * first slot, home-atom count, halo-slot count. */

@@ -181,6 +181,46 @@ def test_parity_shapes(box, dims, cutoff, n, flags):
     check_force_steps(c)
 
 
+def _copies_per_atom(o):
+    """Copies of each home atom, replaying the oracle's maps: a received
+    slot's origin is the origin of the slot it was sent from."""
+    origin = np.full(o.total_slots, -1, np.int64)
+    for r in range(o.n_domains):
+        origin[o.dom_offset[r]: o.dom_offset[r] + o.home[r]] = np.arange(o.dom_offset[r], o.dom_offset[r] + o.home[r])
+    for p in range(o.n_pulses):
+        for r in range(o.n_domains):
+            m = o.map_of(p, r)
+            q, off = int(o.table[p, r, 2]), int(o.table[p, r, 3])
+            dst = o.dom_offset[q] + off
+            origin[dst: dst + len(m)] = origin[o.dom_offset[r] + m]
+    halo = np.concatenate([origin[o.dom_offset[r] + o.home[r]: o.dom_offset[r] + o.home[r] + o.halo[r]]
+                           for r in range(o.n_domains)])
+    assert np.all(halo >= 0)
+    return np.bincount(halo, minlength=o.total_slots)
+
+
+@pytest.mark.parametrize("name", ["C1", "C2", "C3", "C4"])
+def test_resolved_tree_classes(name):
+    """Resolved mode's force trees: one per home atom with copies; an atom
+    with one copy is a pair; corner trees of four nodes may be quads; the
+    general class holds the rest. Parity of every class is in
+    test_parity_configs."""
+    c = Case(W.WORKLOADS[name], flags=HX.HX_FLAG_RESOLVED)
+    pairs, quads, general = c.hx.resolved_counts()
+    copies = _copies_per_atom(c.o)
+    assert pairs == int(np.sum(copies == 1))
+    assert pairs + quads + general == int(np.sum(copies > 0))
+    assert quads <= int(np.sum(copies == 3))
+    if name in ("C2", "C4"):   # 1 pulse per dimension: corners are quads, 3-dimension corners general
+        assert quads == int(np.sum(copies == 3)) and quads > 0 and general == int(np.sum(copies == 7)) > 0
+    if name == "C3":           # 2 pulses along x: relayed copies make three-node chains
+        assert quads == 0 and general == int(np.sum(copies == 2)) > 0
+    if name == "C1":
+        assert quads == 0 and general == 0
+    if name == "C1":   # a handle in another mode has no trees
+        assert Case(W.WORKLOADS[name], flags=HX.HX_FLAG_FINE_WAITS).hx.resolved_counts() == (0, 0, 0)
+
+
 @pytest.mark.parametrize("flags", [0, HX.HX_FLAG_TILES, HX.HX_FLAG_SWEEP])
 def test_misaligned_buffers(flags):
     """Caller buffers that start 4 or 8 bytes past a 16-byte boundary (tile
