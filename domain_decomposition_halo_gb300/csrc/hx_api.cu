@@ -304,8 +304,19 @@ const void* fused_kernel(hx_ctx* h, int dir) {
 }
 unsigned fused_threads(const hx_ctx* h, int dir) {
   if (h->family[dir] == kFamCluster) return kClusterThreads;
-  if (h->family[dir] == kFamResolved) return 256;
+  if (h->family[dir] == kFamResolved) return kResThreads;
   return h->family[dir] == kFamTiles ? kTileThreads : kThreads;
+}
+
+// Blocks of kResThreads threads that hold n items at `per` items a thread.
+int64_t resolved_blocks(int64_t n, int per) { return (n + int64_t{kResThreads} * per - 1) / (int64_t{kResThreads} * per); }
+
+// Trees a thread of one class takes: several (more loads in flight per
+// thread) only when even then the class fills the GPU several times over
+// (four waves of four blocks per SM); small decompositions keep one a thread.
+int resolved_per_thread(const hx_ctx* h, int64_t n, int most) {
+  const int64_t wave = int64_t{4} * std::max(h->sm_count, 1) * kResThreads;
+  return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(most, n / (4 * wave))));
 }
 
 ResolvedParams resolved_params(hx_ctx* h) {
@@ -320,6 +331,10 @@ ResolvedParams resolved_params(hx_ctx* h) {
   P.n_pairs = h->n_res_pairs;
   P.n_quads = h->n_res_quads;
   P.n_trees = h->n_res_trees;
+  P.pairs_per_thread = resolved_per_thread(h, h->n_res_pairs, kResPairsPerThread);
+  P.quads_per_thread = resolved_per_thread(h, h->n_res_quads, kResQuadsPerThread);
+  P.pair_blocks = static_cast<int32_t>(resolved_blocks(h->n_res_pairs, P.pairs_per_thread));
+  P.quad_blocks = static_cast<int32_t>(resolved_blocks(h->n_res_quads, P.quads_per_thread));
   for (int d = 0; d < 3; ++d) P.box[d] = h->pl.boxf[d];
   return P;
 }
@@ -355,7 +370,7 @@ int launch(hx_ctx* h, int kind, float* buf, cudaStream_t s) {
     args2[1] = &RP;
     args = args2;
     grid = dim3(static_cast<unsigned>(h->grid[kind]));
-    block = dim3(256);
+    block = dim3(kResThreads);
     fn = resolved_kernel(kind);
   } else if (kind != 2 && h->family[kind] == kFamCluster) {
     CP = cluster_params(h);
@@ -816,12 +831,13 @@ int build_resolved_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const s
   for (int64_t k = 0; k < H; ++k)
     om[k] = static_cast<uint32_t>(origin_slot[k]) | (static_cast<uint32_t>(mask[k]) << kResOriginBits);
   std::vector<ResSeg> segs;
+  const int64_t seg_len = int64_t{kResThreads} * resolved_per_thread(h, H, kResSlotsPerThread);
   for (int r = 0; r < nd; ++r)
-    for (int64_t k = hbase[r]; k < hbase[r + 1]; k += kResSeg) {
+    for (int64_t k = hbase[r]; k < hbase[r + 1]; k += seg_len) {
       ResSeg sg;
       sg.k = static_cast<int32_t>(k);
       sg.slot = static_cast<int32_t>(h->dom_offset[r] + h->home[r] + (k - hbase[r]));
-      sg.n = static_cast<int32_t>(std::min<int64_t>(kResSeg, hbase[r + 1] - k));
+      sg.n = static_cast<int32_t>(std::min<int64_t>(seg_len, hbase[r + 1] - k));
       sg.pad = 0;
       segs.push_back(sg);
     }
@@ -1230,9 +1246,11 @@ int build_tables(hx_ctx* h, cudaStream_t s) {
   // more of them than there is work.
   for (int k = 0; k < 2; ++k) {
     if (h->family[k] == kFamResolved) {
-      // coordinates: one block per halo segment; forces: one thread per tree
-      const int64_t trees = h->n_res_pairs + h->n_res_quads + h->n_res_trees;
-      h->grid[k] = static_cast<int>(std::max<int64_t>(1, k == 0 ? h->n_res_segs : (trees + 255) / 256));
+      // coordinates: one block per halo segment; forces: pair, quad, then general blocks
+      const int64_t fb = resolved_blocks(h->n_res_pairs, resolved_per_thread(h, h->n_res_pairs, kResPairsPerThread)) +
+                         resolved_blocks(h->n_res_quads, resolved_per_thread(h, h->n_res_quads, kResQuadsPerThread)) +
+                         resolved_blocks(h->n_res_trees, 1);
+      h->grid[k] = static_cast<int>(std::max<int64_t>(1, k == 0 ? h->n_res_segs : fb));
     } else if (h->family[k] == kFamCluster) {
       h->grid[k] = kClusterCtas;   // exactly one cluster
     } else if (h->family[k] == kFamTiles) {
@@ -1484,7 +1502,8 @@ int hx::launch_coords_with_scratch(hx_ctx* h, float* coords, cudaStream_t s, Ctr
   if (h->family[0] == kFamResolved) {   // no dependencies, no scratch at all
     ResolvedParams RP = resolved_params(h);
     void* rargs[2] = {&coords, &RP};
-    return to_err(cudaLaunchKernel(resolved_kernel(0), dim3(static_cast<unsigned>(h->grid[0])), dim3(256), rargs, 0, s));
+    return to_err(
+        cudaLaunchKernel(resolved_kernel(0), dim3(static_cast<unsigned>(h->grid[0])), dim3(kResThreads), rargs, 0, s));
   }
   if (h->family[0] == kFamCluster) {   // cluster barriers, no scratch at all
     ClusterParams CP = cluster_params(h);

@@ -122,10 +122,14 @@ struct alignas(16) TreeRec {
   int32_t pad;
 };
 static_assert(sizeof(TreeRec) == 48, "tree record must stay 48 bytes");
-// Coordinates: one block per segment of up to kResSeg consecutive halo slots
-// of one domain; per halo slot one word, the origin home slot in the low 29
+// Coordinates: one block per segment of consecutive halo slots of one domain
+// (up to kResSeg; the build sizes segments for the decomposition); per halo slot one word, the origin home slot in the low 29
 // bits and the shift mask (bit d: add box[d] to component d) in the top 3.
-constexpr int kResSeg = 256;
+constexpr int kResThreads = 256;
+constexpr int kResSlotsPerThread = 4;     // at most; the build picks 1..4 gathers in flight per thread
+constexpr int kResSeg = kResThreads * kResSlotsPerThread;   // largest segment
+constexpr int kResPairsPerThread = 4;      // at most; the build picks 1..4 (pairs) and 1..2 (quads)
+constexpr int kResQuadsPerThread = 2;
 constexpr int kResOriginBits = 29;
 struct ResSeg {
   int32_t k;                              // first halo index of the segment
@@ -140,6 +144,8 @@ static_assert(sizeof(ResSeg) == 16, "segment record must stay 16 bytes");
 //                        pulse than b: a corner atom's two copies and the
 //                        copy of its first copy)
 //   general: TreeRec, adds replayed from the record
+// Force grid: pair blocks (pairs_per_thread pairs a thread), then quad
+// blocks (quads_per_thread), then general blocks (one tree a thread).
 struct ResolvedParams {
   const ResSeg* segs;
   const uint32_t* origin_mask;            // per halo slot
@@ -148,6 +154,8 @@ struct ResolvedParams {
   const TreeRec* trees;                   // the general class
   int64_t n_segs;
   int64_t n_pairs, n_quads, n_trees;
+  int32_t pair_blocks, quad_blocks;
+  int32_t pairs_per_thread, quads_per_thread;
   float box[3];
   int pad;
 };

@@ -19,11 +19,11 @@
 // adds sorted by descending pulse, and adds of one pulse never chain (a slot
 // received in pulse p is sent only in later pulses). Replaying a tree's adds
 // in that order in registers gives every slot of the tree the staged fp32
-// sums exactly. One thread per tree: load the record, load the node values,
-// add, store the nodes that received adds. Most trees are an atom with one
-// copy (one add) or a corner atom with two copies and the copy of its first
-// copy (three adds in a fixed order); those two shapes get compact records
-// and straight-line code, the rest the general record.
+// sums exactly. A thread loads a tree's record, its node values, adds, and
+// stores the nodes that received adds. Most trees are an atom with one copy
+// (one add) or a corner atom with two copies and the copy of its first copy
+// (three adds in a fixed order); those two shapes get compact records and
+// straight-line code, several trees per thread, the rest the general record.
 //
 // Tables are numbered in slot order (halo slots, tree roots), so neighbouring
 // threads touch neighbouring slots.
@@ -41,25 +41,44 @@ namespace {
 __device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void wait_prerequisites() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-// One thread per halo slot: slot = origin (+ shifts).
-__global__ void __launch_bounds__(kResSeg) k_resolved_coords(float* __restrict__ x, ResolvedParams P) {
+// Up to kResSlotsPerThread halo slots per thread (as many as the segment
+// holds), strided by the block so that every load and store instruction of
+// a warp covers consecutive slots: slot = origin (+ shifts).
+__global__ void __launch_bounds__(kResThreads) k_resolved_coords(float* __restrict__ x, ResolvedParams P) {
   allow_dependents();
   const ResSeg sg = P.segs[blockIdx.x];   // build-time tables, read before the wait
-  if (static_cast<int>(threadIdx.x) >= sg.n) return;
-  const uint32_t om = __ldg(P.origin_mask + sg.k + threadIdx.x);
+  uint32_t om[kResSlotsPerThread];
+#pragma unroll
+  for (int u = 0; u < kResSlotsPerThread; ++u) {
+    const int j = u * kResThreads + static_cast<int>(threadIdx.x);
+    om[u] = j < sg.n ? __ldg(P.origin_mask + sg.k + j) : 0u;
+  }
   wait_prerequisites();
-  const int64_t o = 3 * static_cast<int64_t>(om & ((1u << kResOriginBits) - 1u));
-  const unsigned mask = om >> kResOriginBits;
-  float v0 = x[o + 0];
-  float v1 = x[o + 1];
-  float v2 = x[o + 2];
-  if (mask & 1u) v0 = __fadd_rn(v0, P.box[0]);   // no add otherwise: unshifted values keep every bit
-  if (mask & 2u) v1 = __fadd_rn(v1, P.box[1]);
-  if (mask & 4u) v2 = __fadd_rn(v2, P.box[2]);
-  float* d = x + 3 * (static_cast<int64_t>(sg.slot) + threadIdx.x);
-  d[0] = v0;
-  d[1] = v1;
-  d[2] = v2;
+  float v[kResSlotsPerThread][3];
+#pragma unroll
+  for (int u = 0; u < kResSlotsPerThread; ++u) {   // every gather issued before any is used
+    const int j = u * kResThreads + static_cast<int>(threadIdx.x);
+    if (j < sg.n) {
+      const float* s = x + 3 * static_cast<int64_t>(om[u] & ((1u << kResOriginBits) - 1u));
+      v[u][0] = s[0];
+      v[u][1] = s[1];
+      v[u][2] = s[2];
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < kResSlotsPerThread; ++u) {
+    const int j = u * kResThreads + static_cast<int>(threadIdx.x);
+    if (j < sg.n) {
+      const unsigned mask = om[u] >> kResOriginBits;
+      if (mask & 1u) v[u][0] = __fadd_rn(v[u][0], P.box[0]);   // no add otherwise: unshifted values keep every bit
+      if (mask & 2u) v[u][1] = __fadd_rn(v[u][1], P.box[1]);
+      if (mask & 4u) v[u][2] = __fadd_rn(v[u][2], P.box[2]);
+      float* d = x + 3 * (static_cast<int64_t>(sg.slot) + j);
+      d[0] = v[u][0];
+      d[1] = v[u][1];
+      d[2] = v[u][2];
+    }
+  }
 }
 
 __device__ __forceinline__ void load3(const float* f, int slot, float (&v)[3]) {
@@ -109,37 +128,72 @@ __device__ __forceinline__ void general_tree(float* __restrict__ f, const TreeRe
     if (j < r.n_nodes && (target >> j & 1u)) store3(f, r.node[j], v[j]);
 }
 
-// One thread per tree; the three classes lie one after another in the grid.
-__global__ void __launch_bounds__(256) k_resolved_forces(float* __restrict__ f, ResolvedParams P) {
+// Pair and quad blocks give each thread several trees (strided by the
+// block, all their loads issued before any add); general blocks one tree.
+__global__ void __launch_bounds__(kResThreads) k_resolved_forces(float* __restrict__ f, ResolvedParams P) {
   allow_dependents();
-  int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (t < P.n_pairs) {
-    const int2 pr = __ldg(P.pairs + t);   // build-time table, read before the wait
+  int b = static_cast<int>(blockIdx.x);
+  const int tid = static_cast<int>(threadIdx.x);
+  if (b < P.pair_blocks) {
+    constexpr int U = kResPairsPerThread;
+    const int per = P.pairs_per_thread;
+    const int64_t base = static_cast<int64_t>(b) * (kResThreads * per) + tid;
+    int2 pr[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {   // build-time table, read before the wait
+      const int64_t t = base + u * kResThreads;
+      pr[u] = u < per && t < P.n_pairs ? __ldg(P.pairs + t) : make_int2(-1, -1);
+    }
     wait_prerequisites();
-    float a[3], b[3];
-    load3(f, pr.x, a);
-    load3(f, pr.y, b);
-    add3(a, b);
-    store3(f, pr.x, a);
+    float a[U][3], c[U][3];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (pr[u].x >= 0) {
+        load3(f, pr[u].x, a[u]);
+        load3(f, pr[u].y, c[u]);
+      }
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (pr[u].x >= 0) {
+        add3(a[u], c[u]);   // root += copy
+        store3(f, pr[u].x, a[u]);
+      }
     return;
   }
-  t -= P.n_pairs;
-  if (t < P.n_quads) {
-    const int4 q = __ldg(P.quads + t);
+  b -= P.pair_blocks;
+  if (b < P.quad_blocks) {
+    constexpr int U = kResQuadsPerThread;
+    const int per = P.quads_per_thread;
+    const int64_t base = static_cast<int64_t>(b) * (kResThreads * per) + tid;
+    int4 q[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t t = base + u * kResThreads;
+      q[u] = u < per && t < P.n_quads ? __ldg(P.quads + t) : make_int4(-1, -1, -1, -1);
+    }
     wait_prerequisites();
-    float a[3], b[3], c[3], d[3];
-    load3(f, q.x, a);
-    load3(f, q.y, b);
-    load3(f, q.z, c);
-    load3(f, q.w, d);
-    add3(a, c);   // the later pulse: the corner copy into the atom, the copy's copy into the copy
-    add3(b, d);
-    add3(a, b);   // then the first copy into the atom
-    store3(f, q.x, a);
-    store3(f, q.y, b);
+    float a[U][3], bb[U][3], c[U][3], d[U][3];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (q[u].x >= 0) {
+        load3(f, q[u].x, a[u]);
+        load3(f, q[u].y, bb[u]);
+        load3(f, q[u].z, c[u]);
+        load3(f, q[u].w, d[u]);
+      }
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (q[u].x >= 0) {
+        add3(a[u], c[u]);    // the later pulse: the corner copy into the atom, the copy's copy into the copy
+        add3(bb[u], d[u]);
+        add3(a[u], bb[u]);   // then the first copy into the atom
+        store3(f, q[u].x, a[u]);
+        store3(f, q[u].y, bb[u]);
+      }
     return;
   }
-  t -= P.n_quads;
+  b -= P.quad_blocks;
+  const int64_t t = static_cast<int64_t>(b) * kResThreads + tid;
   if (t >= P.n_trees) return;
   const TreeRec r = P.trees[t];
   wait_prerequisites();
