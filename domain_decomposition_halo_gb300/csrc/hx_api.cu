@@ -193,8 +193,7 @@ struct hx_ctx {
   std::vector<GraphEntry> graphs;
   ResSeg* d_res_segs = nullptr;              // resolved mode: halo segments
   uint32_t* d_res_om = nullptr;              // ... origin and shift mask per halo slot
-  int2* d_res_pairs = nullptr;               // ... force trees: pairs, quads, general
-  int4* d_res_quads = nullptr;
+  int4* d_res_recs = nullptr;                // ... force trees: pairs and quads, general ones apart
   TreeRec* d_res_trees = nullptr;
   int64_t n_res_halo = 0, n_res_segs = 0, n_res_pairs = 0, n_res_quads = 0, n_res_trees = 0;
 };
@@ -217,8 +216,7 @@ void free_tables(hx_ctx* h) {
   dev_free(h->d_uchunks);
   dev_free(h->d_res_segs);
   dev_free(h->d_res_om);
-  dev_free(h->d_res_pairs);
-  dev_free(h->d_res_quads);
+  dev_free(h->d_res_recs);
   dev_free(h->d_res_trees);
   h->n_res_halo = h->n_res_segs = h->n_res_pairs = h->n_res_quads = h->n_res_trees = 0;
   for (int k = 0; k < 2; ++k) {
@@ -324,17 +322,13 @@ ResolvedParams resolved_params(hx_ctx* h) {
   std::memset(&P, 0, sizeof(P));
   P.segs = h->d_res_segs;
   P.origin_mask = h->d_res_om;
-  P.pairs = h->d_res_pairs;
-  P.quads = h->d_res_quads;
+  P.recs = h->d_res_recs;
   P.trees = h->d_res_trees;
   P.n_segs = h->n_res_segs;
-  P.n_pairs = h->n_res_pairs;
-  P.n_quads = h->n_res_quads;
+  P.n_recs = h->n_res_pairs + h->n_res_quads;
   P.n_trees = h->n_res_trees;
-  P.pairs_per_thread = resolved_per_thread(h, h->n_res_pairs, kResPairsPerThread);
-  P.quads_per_thread = resolved_per_thread(h, h->n_res_quads, kResQuadsPerThread);
-  P.pair_blocks = static_cast<int32_t>(resolved_blocks(h->n_res_pairs, P.pairs_per_thread));
-  P.quad_blocks = static_cast<int32_t>(resolved_blocks(h->n_res_quads, P.quads_per_thread));
+  P.trees_per_thread = resolved_per_thread(h, P.n_recs, kResTreesPerThread);
+  P.rec_blocks = static_cast<int32_t>(resolved_blocks(P.n_recs, P.trees_per_thread));
   for (int d = 0; d < 3; ++d) P.box[d] = h->pl.boxf[d];
   return P;
 }
@@ -787,7 +781,8 @@ int build_tile_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::
 // each received slot inheriting from the slot it was sent from), in halo
 // order (domain after domain) with one segment record per block; and one
 // tree per home atom that has copies, its adds sorted by descending pulse,
-// numbered in home-slot order and split into pairs, quads and general trees.
+// numbered in home-slot order: pairs and quads as 16-byte records, the
+// other trees as general records, each list in root order.
 int build_resolved_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::vector<int32_t>& maps,
                           cudaStream_t s) {
   const Plan& pl = h->pl;
@@ -879,16 +874,18 @@ int build_resolved_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const s
         std::swap(rec.ev[b], rec.ev[b - 1]);
       }
   }, 1024);
-  // classes, each keeping root order. A four-node tree is a quad when its
+  // records in root order. A four-node tree is a quad when its
   // last add (lowest pulse) is some copy u into the root and the two adds
   // before it are one copy into the root and one copy into u: then the
   // fixed order root += c, u += d, root += u is the staged order.
-  std::vector<int2> pairs;
-  std::vector<int4> quads;
+  std::vector<int4> recs;
   std::vector<TreeRec> general;
+  recs.reserve(trees.size());
+  int64_t n_pairs = 0, n_quads = 0;
   for (const TreeRec& rec : trees) {
     if (rec.n_nodes == 2) {
-      pairs.push_back(make_int2(rec.node[0], rec.node[1]));
+      recs.push_back(make_int4(rec.node[0], rec.node[1], -1, -1));
+      ++n_pairs;
       continue;
     }
     if (rec.n_nodes == 4) {
@@ -896,7 +893,8 @@ int build_resolved_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const s
       const int tg0 = rec.ev[0] & 15, s0 = rec.ev[0] >> 4, tg1 = rec.ev[1] & 15, s1 = rec.ev[1] >> 4;
       if (tg2 == 0 && u != 0 && ((tg0 == 0 && tg1 == u) || (tg0 == u && tg1 == 0))) {
         const int c = tg0 == 0 ? s0 : s1, d = tg0 == 0 ? s1 : s0;
-        quads.push_back(make_int4(rec.node[0], rec.node[u], rec.node[c], rec.node[d]));
+        recs.push_back(make_int4(rec.node[0], rec.node[u], rec.node[c], rec.node[d]));
+        ++n_quads;
         continue;
       }
     }
@@ -904,22 +902,19 @@ int build_resolved_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const s
   }
   h->n_res_halo = H;
   h->n_res_segs = static_cast<int64_t>(segs.size());
-  h->n_res_pairs = static_cast<int64_t>(pairs.size());
-  h->n_res_quads = static_cast<int64_t>(quads.size());
+  h->n_res_pairs = n_pairs;
+  h->n_res_quads = n_quads;
   h->n_res_trees = static_cast<int64_t>(general.size());
   HX_CUDA(dev_alloc(&h->d_res_om, om.size()));
   HX_CUDA(dev_alloc(&h->d_res_segs, segs.size()));
-  HX_CUDA(dev_alloc(&h->d_res_pairs, pairs.size()));
-  HX_CUDA(dev_alloc(&h->d_res_quads, quads.size()));
+  HX_CUDA(dev_alloc(&h->d_res_recs, recs.size()));
   HX_CUDA(dev_alloc(&h->d_res_trees, general.size()));
   if (H > 0) {
     HX_CUDA(cudaMemcpyAsync(h->d_res_om, om.data(), sizeof(uint32_t) * om.size(), cudaMemcpyHostToDevice, s));
     HX_CUDA(cudaMemcpyAsync(h->d_res_segs, segs.data(), sizeof(ResSeg) * segs.size(), cudaMemcpyHostToDevice, s));
   }
-  if (!pairs.empty())
-    HX_CUDA(cudaMemcpyAsync(h->d_res_pairs, pairs.data(), sizeof(int2) * pairs.size(), cudaMemcpyHostToDevice, s));
-  if (!quads.empty())
-    HX_CUDA(cudaMemcpyAsync(h->d_res_quads, quads.data(), sizeof(int4) * quads.size(), cudaMemcpyHostToDevice, s));
+  if (!recs.empty())
+    HX_CUDA(cudaMemcpyAsync(h->d_res_recs, recs.data(), sizeof(int4) * recs.size(), cudaMemcpyHostToDevice, s));
   if (!general.empty())
     HX_CUDA(cudaMemcpyAsync(h->d_res_trees, general.data(), sizeof(TreeRec) * general.size(),
                             cudaMemcpyHostToDevice, s));
@@ -1247,8 +1242,8 @@ int build_tables(hx_ctx* h, cudaStream_t s) {
   for (int k = 0; k < 2; ++k) {
     if (h->family[k] == kFamResolved) {
       // coordinates: one block per halo segment; forces: pair, quad, then general blocks
-      const int64_t fb = resolved_blocks(h->n_res_pairs, resolved_per_thread(h, h->n_res_pairs, kResPairsPerThread)) +
-                         resolved_blocks(h->n_res_quads, resolved_per_thread(h, h->n_res_quads, kResQuadsPerThread)) +
+      const int64_t n = h->n_res_pairs + h->n_res_quads;
+      const int64_t fb = resolved_blocks(n, resolved_per_thread(h, n, kResTreesPerThread)) +
                          resolved_blocks(h->n_res_trees, 1);
       h->grid[k] = static_cast<int>(std::max<int64_t>(1, k == 0 ? h->n_res_segs : fb));
     } else if (h->family[k] == kFamCluster) {

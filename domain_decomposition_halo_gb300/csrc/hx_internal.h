@@ -128,8 +128,6 @@ static_assert(sizeof(TreeRec) == 48, "tree record must stay 48 bytes");
 constexpr int kResThreads = 256;
 constexpr int kResSlotsPerThread = 4;     // at most; the build picks 1..4 gathers in flight per thread
 constexpr int kResSeg = kResThreads * kResSlotsPerThread;   // largest segment
-constexpr int kResPairsPerThread = 4;      // at most; the build picks 1..4 (pairs) and 1..2 (quads)
-constexpr int kResQuadsPerThread = 2;
 constexpr int kResOriginBits = 29;
 struct ResSeg {
   int32_t k;                              // first halo index of the segment
@@ -138,24 +136,23 @@ struct ResSeg {
   int32_t pad;
 };
 static_assert(sizeof(ResSeg) == 16, "segment record must stay 16 bytes");
-// Forces: trees in three classes, each in home-slot order of its root.
-//   pair (root, copy):  root += copy
-//   quad (a, b, c, d):  a += c; b += d; a += b   (c, d received in one later
-//                        pulse than b: a corner atom's two copies and the
-//                        copy of its first copy)
-//   general: TreeRec, adds replayed from the record
-// Force grid: pair blocks (pairs_per_thread pairs a thread), then quad
-// blocks (quads_per_thread), then general blocks (one tree a thread).
+// Forces: one 16-byte record per tree, in home-slot order of its root:
+//   pair (root, copy, -1, -1):  root += copy
+//   quad (a, b, c, d):          a += c; b += d; a += b   (c, d received in
+//                                one later pulse than b: a corner atom's two
+//                                copies and the copy of its first copy)
+// Other trees (general) keep a TreeRec and run in blocks of their own after
+// the record blocks, one tree a thread, their adds replayed from the record.
+constexpr int kResTreesPerThread = 2;      // at most; the build picks 1..2
 struct ResolvedParams {
   const ResSeg* segs;
   const uint32_t* origin_mask;            // per halo slot
-  const int2* pairs;
-  const int4* quads;
-  const TreeRec* trees;                   // the general class
+  const int4* recs;                       // pairs and quads
+  const TreeRec* trees;                   // general trees
   int64_t n_segs;
-  int64_t n_pairs, n_quads, n_trees;
-  int32_t pair_blocks, quad_blocks;
-  int32_t pairs_per_thread, quads_per_thread;
+  int64_t n_recs, n_trees;
+  int32_t trees_per_thread;
+  int32_t rec_blocks;                     // blocks of the records; general blocks follow
   float box[3];
   int pad;
 };

@@ -22,8 +22,8 @@
 // sums exactly. A thread loads a tree's record, its node values, adds, and
 // stores the nodes that received adds. Most trees are an atom with one copy
 // (one add) or a corner atom with two copies and the copy of its first copy
-// (three adds in a fixed order); those two shapes get compact records and
-// straight-line code, several trees per thread, the rest the general record.
+// (three adds in a fixed order); those two shapes get a 16-byte record and
+// straight-line code, the rest a general record in blocks of their own.
 //
 // Tables are numbered in slot order (halo slots, tree roots), so neighbouring
 // threads touch neighbouring slots.
@@ -128,76 +128,55 @@ __device__ __forceinline__ void general_tree(float* __restrict__ f, const TreeRe
     if (j < r.n_nodes && (target >> j & 1u)) store3(f, r.node[j], v[j]);
 }
 
-// Pair and quad blocks give each thread several trees (strided by the
-// block, all their loads issued before any add); general blocks one tree.
+// Record blocks: one or two pairs or quads per thread (strided by the block;
+// all index loads, then all value loads issued before any add); pairs and
+// quads share a warp. General blocks: one general tree per thread.
 __global__ void __launch_bounds__(kResThreads) k_resolved_forces(float* __restrict__ f, ResolvedParams P) {
+  constexpr int U = kResTreesPerThread;
   allow_dependents();
-  int b = static_cast<int>(blockIdx.x);
-  const int tid = static_cast<int>(threadIdx.x);
-  if (b < P.pair_blocks) {
-    constexpr int U = kResPairsPerThread;
-    const int per = P.pairs_per_thread;
-    const int64_t base = static_cast<int64_t>(b) * (kResThreads * per) + tid;
-    int2 pr[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {   // build-time table, read before the wait
-      const int64_t t = base + u * kResThreads;
-      pr[u] = u < per && t < P.n_pairs ? __ldg(P.pairs + t) : make_int2(-1, -1);
-    }
+  if (static_cast<int>(blockIdx.x) >= P.rec_blocks) {
+    const int64_t t = static_cast<int64_t>(static_cast<int>(blockIdx.x) - P.rec_blocks) * kResThreads + threadIdx.x;
+    if (t >= P.n_trees) return;
+    const TreeRec r = P.trees[t];   // build-time table, read before the wait
     wait_prerequisites();
-    float a[U][3], c[U][3];
-#pragma unroll
-    for (int u = 0; u < U; ++u)
-      if (pr[u].x >= 0) {
-        load3(f, pr[u].x, a[u]);
-        load3(f, pr[u].y, c[u]);
-      }
-#pragma unroll
-    for (int u = 0; u < U; ++u)
-      if (pr[u].x >= 0) {
-        add3(a[u], c[u]);   // root += copy
-        store3(f, pr[u].x, a[u]);
-      }
+    general_tree(f, r);
     return;
   }
-  b -= P.pair_blocks;
-  if (b < P.quad_blocks) {
-    constexpr int U = kResQuadsPerThread;
-    const int per = P.quads_per_thread;
-    const int64_t base = static_cast<int64_t>(b) * (kResThreads * per) + tid;
-    int4 q[U];
+  const int per = P.trees_per_thread;
+  const int64_t base = static_cast<int64_t>(blockIdx.x) * (kResThreads * per) + threadIdx.x;
+  int4 rc[U];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int64_t t = base + u * kResThreads;
-      q[u] = u < per && t < P.n_quads ? __ldg(P.quads + t) : make_int4(-1, -1, -1, -1);
-    }
-    wait_prerequisites();
-    float a[U][3], bb[U][3], c[U][3], d[U][3];
-#pragma unroll
-    for (int u = 0; u < U; ++u)
-      if (q[u].x >= 0) {
-        load3(f, q[u].x, a[u]);
-        load3(f, q[u].y, bb[u]);
-        load3(f, q[u].z, c[u]);
-        load3(f, q[u].w, d[u]);
-      }
-#pragma unroll
-    for (int u = 0; u < U; ++u)
-      if (q[u].x >= 0) {
-        add3(a[u], c[u]);    // the later pulse: the corner copy into the atom, the copy's copy into the copy
-        add3(bb[u], d[u]);
-        add3(a[u], bb[u]);   // then the first copy into the atom
-        store3(f, q[u].x, a[u]);
-        store3(f, q[u].y, bb[u]);
-      }
-    return;
+  for (int u = 0; u < U; ++u) {   // build-time table, read before the wait
+    const int64_t t = base + u * kResThreads;
+    rc[u] = u < per && t < P.n_recs ? __ldg(P.recs + t) : make_int4(-1, -1, -1, -1);
   }
-  b -= P.quad_blocks;
-  const int64_t t = static_cast<int64_t>(b) * kResThreads + tid;
-  if (t >= P.n_trees) return;
-  const TreeRec r = P.trees[t];
   wait_prerequisites();
-  general_tree(f, r);
+  float a[U][3], b[U][3], c[U][3], d[U][3];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    if (rc[u].x >= 0) {
+      load3(f, rc[u].x, a[u]);
+      load3(f, rc[u].y, b[u]);
+      if (rc[u].z >= 0) {
+        load3(f, rc[u].z, c[u]);
+        load3(f, rc[u].w, d[u]);
+      }
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    if (rc[u].x >= 0) {
+      if (rc[u].z >= 0) {   // quad: the later pulse first, then the first copy into the atom
+        add3(a[u], c[u]);
+        add3(b[u], d[u]);
+        add3(a[u], b[u]);
+        store3(f, rc[u].y, b[u]);
+      } else {              // pair: root += copy
+        add3(a[u], b[u]);
+      }
+      store3(f, rc[u].x, a[u]);
+    }
+  }
 }
 
 }  // namespace
