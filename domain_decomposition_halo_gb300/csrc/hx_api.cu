@@ -1241,7 +1241,7 @@ int build_tables(hx_ctx* h, cudaStream_t s) {
   // more of them than there is work.
   for (int k = 0; k < 2; ++k) {
     if (h->family[k] == kFamResolved) {
-      // coordinates: one block per halo segment; forces: pair, quad, then general blocks
+      // coordinates: one block per halo segment; forces: general blocks, then record blocks
       const int64_t n = h->n_res_pairs + h->n_res_quads;
       const int64_t fb = resolved_blocks(n, resolved_per_thread(h, n, kResTreesPerThread)) +
                          resolved_blocks(h->n_res_trees, 1);

@@ -141,7 +141,7 @@ static_assert(sizeof(ResSeg) == 16, "segment record must stay 16 bytes");
 //   quad (a, b, c, d):          a += c; b += d; a += b   (c, d received in
 //                                one later pulse than b: a corner atom's two
 //                                copies and the copy of its first copy)
-// Other trees (general) keep a TreeRec and run in blocks of their own after
+// Other trees (general) keep a TreeRec and run in blocks of their own before
 // the record blocks, one tree a thread, their adds replayed from the record.
 constexpr int kResTreesPerThread = 2;      // at most; the build picks 1..2
 struct ResolvedParams {
@@ -152,7 +152,7 @@ struct ResolvedParams {
   int64_t n_segs;
   int64_t n_recs, n_trees;
   int32_t trees_per_thread;
-  int32_t rec_blocks;                     // blocks of the records; general blocks follow
+  int32_t rec_blocks;                     // blocks of the records, after the general blocks
   float box[3];
   int pad;
 };

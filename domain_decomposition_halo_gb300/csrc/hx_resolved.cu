@@ -23,7 +23,8 @@
 // stores the nodes that received adds. Most trees are an atom with one copy
 // (one add) or a corner atom with two copies and the copy of its first copy
 // (three adds in a fixed order); those two shapes get a 16-byte record and
-// straight-line code, the rest a general record in blocks of their own.
+// straight-line code, the rest a general record in blocks of their own,
+// scheduled first because their threads take longest.
 //
 // Tables are numbered in slot order (halo slots, tree roots), so neighbouring
 // threads touch neighbouring slots.
@@ -128,14 +129,16 @@ __device__ __forceinline__ void general_tree(float* __restrict__ f, const TreeRe
     if (j < r.n_nodes && (target >> j & 1u)) store3(f, r.node[j], v[j]);
 }
 
-// Record blocks: one or two pairs or quads per thread (strided by the block;
-// all index loads, then all value loads issued before any add); pairs and
-// quads share a warp. General blocks: one general tree per thread.
+// General blocks (first in the grid): one general tree per thread. Record
+// blocks: one or two pairs or quads per thread (strided by the block; all
+// index loads, then all value loads issued before any add); pairs and quads
+// share a warp.
 __global__ void __launch_bounds__(kResThreads) k_resolved_forces(float* __restrict__ f, ResolvedParams P) {
   constexpr int U = kResTreesPerThread;
   allow_dependents();
-  if (static_cast<int>(blockIdx.x) >= P.rec_blocks) {
-    const int64_t t = static_cast<int64_t>(static_cast<int>(blockIdx.x) - P.rec_blocks) * kResThreads + threadIdx.x;
+  const int gen_blocks = static_cast<int>(gridDim.x) - P.rec_blocks;   // first: their threads take longest
+  if (static_cast<int>(blockIdx.x) < gen_blocks) {
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * kResThreads + threadIdx.x;
     if (t >= P.n_trees) return;
     const TreeRec r = P.trees[t];   // build-time table, read before the wait
     wait_prerequisites();
@@ -143,7 +146,7 @@ __global__ void __launch_bounds__(kResThreads) k_resolved_forces(float* __restri
     return;
   }
   const int per = P.trees_per_thread;
-  const int64_t base = static_cast<int64_t>(blockIdx.x) * (kResThreads * per) + threadIdx.x;
+  const int64_t base = static_cast<int64_t>(static_cast<int>(blockIdx.x) - gen_blocks) * (kResThreads * per) + threadIdx.x;
   int4 rc[U];
 #pragma unroll
   for (int u = 0; u < U; ++u) {   // build-time table, read before the wait
