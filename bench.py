@@ -105,11 +105,21 @@ def measured_hbm_peak():
 KERNEL_SOURCES = ("hx_kernels.cu", "hx_sweep.cu", "hx_internal.h")
 
 
+_TOKENS = re.compile(r'"(?:\\.|[^"\\\n])*"|//[^\n]*|/\*.*?\*/', re.S)
+
+
+def code_only(text: str) -> str:
+    """C/C++ source without its comments and with whitespace runs collapsed:
+    what the digest hashes, so that editing a comment keeps it."""
+    text = _TOKENS.sub(lambda m: m.group(0) if m.group(0).startswith('"') else " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_digest():
     h = hashlib.sha256()
     for name in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "domain_decomposition_halo_gb300", "csrc", name), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "domain_decomposition_halo_gb300", "csrc", name), encoding="utf-8") as fh:
+            h.update(code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -53,3 +53,19 @@ def test_step_distribution_nearest_rank_p90():
     d = bench.step_distribution(list(range(1, 21)))
     assert d["p90"] == 18 and d["median"] == 10.5
     assert bench.step_distribution([3.0])["p90"] == 3.0
+
+
+def test_digest_ignores_comments_not_code(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    d = tmp_path / "domain_decomposition_halo_gb300" / "csrc"
+    d.mkdir(parents=True)
+    for name in bench.KERNEL_SOURCES:
+        (d / name).write_text('int f(int a) { return a + 1; }  // add\nconst char* s = "a // b";\n')
+    first = bench.kernel_source_digest()
+    (d / bench.KERNEL_SOURCES[0]).write_text(
+        '/* a block\n comment */ int f(int a) {\n  return a + 1;   // another\n}\nconst char* s = "a // b";\n')
+    assert bench.kernel_source_digest() == first
+    (d / bench.KERNEL_SOURCES[0]).write_text('int f(int a) { return a + 2; }\nconst char* s = "a // b";\n')
+    assert bench.kernel_source_digest() != first
+    (d / bench.KERNEL_SOURCES[0]).write_text('int f(int a) { return a + 1; }\nconst char* s = "a // c";\n')
+    assert bench.kernel_source_digest() != first   # text inside a string is code
