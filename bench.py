@@ -286,62 +286,61 @@ def run_ours(args):
         raise RuntimeError(f"device status {rc} (detail {detail}) after the timed region")
     us_step = total_ms * 1e3 / K
 
-    # end to end through the public API: host buffers in, results out, every
-    # step. Copies in, the two exchanges and copies out run on three streams
-    # over two device buffer sets, so one step's copies out overlap the next
-    # step's copies in (the host link carries both directions at once); the
-    # events chain each set: in -> exchanges -> out -> next copy in.
-    coords_h = coords.cpu().pin_memory()
-    forces_h = forces.cpu().pin_memory()
-    sets = [(coords, forces), (torch.empty_like(coords), torch.empty_like(forces))]
-    outs = [(torch.empty_like(coords_h).pin_memory(), torch.empty_like(forces_h).pin_memory()) for _ in range(2)]
-    s_in, s_ex, s_out = (torch.cuda.Stream(device=dev) for _ in range(3))
-    ev_in = [torch.cuda.Event() for _ in range(2)]
-    ev_ex = [torch.cuda.Event() for _ in range(2)]
-    ev_out = [torch.cuda.Event() for _ in range(2)]
+    # end to end through the C-ABI with host buffers: each step calls
+    # hx_exchange_coords_host (home coordinates in, halo coordinates out) and
+    # hx_exchange_forces_host (every force in, home forces out) on page-locked
+    # host buffers. Two handles with the same maps, each with its own buffers
+    # and stream, take alternate steps, so one step's copies out overlap the
+    # next step's copies in (a handle runs one exchange per direction at a
+    # time).
+    hx_b = HaloExchange(w.box, w.dims, w.cutoff, device=local, flags=flags)
+    hx_b.build_maps(pos_t, torch.empty_like(coords))
+    handles = (hx, hx_b)
+    off, home_n, _ = hx.layout()
+    home_mask = torch.zeros(slots, dtype=torch.bool)
+    for r in range(len(off)):
+        home_mask[int(off[r]): int(off[r]) + int(home_n[r])] = True
+    coords_h0 = coords.cpu()
+    coords_h0[~home_mask] = float("nan")   # halo slots come back from the device
+    forces_h0 = forces.cpu()
+    host = [(coords_h0.clone().pin_memory(), forces_h0.clone().pin_memory()) for _ in range(2)]
+    devs = [(torch.empty_like(coords), torch.empty_like(forces)) for _ in range(2)]
+    streams = [torch.cuda.Stream(device=dev) for _ in range(2)]
     n_e2e = max(3, min(K, 30))
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     for i in range(2 + n_e2e):
         if i == 2:   # two untimed steps, then the timed ones
             torch.cuda.synchronize()
-            e0.record(s_in)
+            e0.record(streams[0])
+            streams[1].wait_event(e0)
         k = i % 2
-        cd, fd = sets[k]
-        with torch.cuda.stream(s_in):
-            if i >= 2:
-                s_in.wait_event(ev_out[k])   # this set's previous results are out
-            cd.copy_(coords_h, non_blocking=True)
-            fd.copy_(forces_h, non_blocking=True)
-            ev_in[k].record(s_in)
-        with torch.cuda.stream(s_ex):
-            s_ex.wait_event(ev_in[k])
-            hx.exchange_coords(cd)
-            hx.exchange_forces(fd)
-            ev_ex[k].record(s_ex)
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(ev_ex[k])
-            outs[k][0].copy_(cd, non_blocking=True)
-            outs[k][1].copy_(fd, non_blocking=True)
-            ev_out[k].record(s_out)
-    s_in.wait_stream(s_out)
-    e1.record(s_in)
+        handles[k].exchange_coords_host(host[k][0], devs[k][0], stream=streams[k])
+        handles[k].exchange_forces_host(host[k][1], devs[k][1], stream=streams[k])
+    streams[0].wait_stream(streams[1])
+    e1.record(streams[0])
     torch.cuda.synchronize()
     e2e_us = e0.elapsed_time(e1) * 1e3 / n_e2e
-    # every step exchanged the same inputs: each set's last results must equal
-    # one plain exchange of them (a check on the stream and event chaining)
-    cd, fd = sets[0]
-    cd.copy_(coords_h)
-    fd.copy_(forces_h)
-    hx.exchange_coords(cd)
-    hx.exchange_forces(fd)
+    # checks: the coordinates on each host buffer equal a device exchange of
+    # the same home coordinates; one fresh force step equals a device one
+    ref_c = coords.clone()
+    hx.exchange_coords(ref_c)
+    ref_f = forces_h0.to(dev)
+    hx.exchange_forces(ref_f)
     torch.cuda.synchronize()
-    for co, fo in outs:
-        if not (torch.equal(co.view(torch.int32), cd.cpu().view(torch.int32)) and
-                torch.equal(fo.view(torch.int32), fd.cpu().view(torch.int32))):
-            raise RuntimeError("end-to-end pipeline results differ from a plain exchange")
-    bytes_h2d = 2 * slots * 12
-    bytes_d2h = 2 * slots * 12
+    ref_c, ref_f = ref_c.cpu(), ref_f.cpu()
+    host[0][1].copy_(forces_h0)
+    hx.exchange_forces_host(host[0][1], devs[0][1], stream=streams[0])
+    torch.cuda.synchronize()
+    for ch, _ in host:
+        if not torch.equal(ch.view(torch.int32), ref_c.view(torch.int32)):
+            raise RuntimeError("end-to-end coordinates differ from a device exchange")
+    if not torch.equal(host[0][1][home_mask].view(torch.int32), ref_f[home_mask].view(torch.int32)):
+        raise RuntimeError("end-to-end forces differ from a device exchange")
+    n_home = int(home_mask.sum())
+    bytes_h2d = 12 * n_home + 12 * slots              # home coordinates, every force
+    bytes_d2h = 12 * (slots - n_home) + 12 * n_home   # halo coordinates, home forces
+    del hx_b
 
     peak, peak_kind = measured_hbm_peak()
     dominant = "hx_forces_fused" if force_ms >= coord_ms else "hx_coords_fused"
@@ -383,9 +382,9 @@ def run_ours(args):
         "clocks": clk,
         "e2e": {"value": round(e2e_us, 2), "unit": "us/step", "h2d_bytes_per_step": bytes_h2d,
                 "d2h_bytes_per_step": bytes_d2h,
-                "what": "pinned host coords+forces -> device, both exchanges, coords+forces -> host, every step; "
-                        "copies in, exchanges and copies out on three streams over two device buffer sets, "
-                        "so a step's copies out overlap the next step's copies in"},
+                "what": "hx_exchange_coords_host + hx_exchange_forces_host every step on page-locked host "
+                        "buffers: home coordinates and every force in, halo coordinates and home forces out; "
+                        "two handles on two streams take alternate steps"},
         "gpu_launches": 2 * K,
         "build_maps_us": round(statistics.median(t_build), 1),
     }

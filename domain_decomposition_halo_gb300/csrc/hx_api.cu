@@ -16,6 +16,7 @@
 #include <vector>
 
 #include "hx.h"
+#include "hx_host.h"
 #include "hx_internal.h"
 
 using namespace hx;
@@ -196,6 +197,9 @@ struct hx_ctx {
   int4* d_res_recs = nullptr;                // ... force trees: pairs and quads, general ones apart
   TreeRec* d_res_trees = nullptr;
   int64_t n_res_halo = 0, n_res_segs = 0, n_res_pairs = 0, n_res_quads = 0, n_res_trees = 0;
+  CopyChunk* d_home_chunks = nullptr;        // host-buffer calls: every domain's home range
+  CopyChunk* d_halo_chunks = nullptr;        // ... and halo range, in pieces of one block each
+  int n_home_chunks = 0, n_halo_chunks = 0;
 };
 
 namespace {
@@ -219,6 +223,9 @@ void free_tables(hx_ctx* h) {
   dev_free(h->d_res_recs);
   dev_free(h->d_res_trees);
   h->n_res_halo = h->n_res_segs = h->n_res_pairs = h->n_res_quads = h->n_res_trees = 0;
+  dev_free(h->d_home_chunks);
+  dev_free(h->d_halo_chunks);
+  h->n_home_chunks = h->n_halo_chunks = 0;
   for (int k = 0; k < 2; ++k) {
     dev_free(h->d_units[k]);
     dev_free(h->d_segs[k]);
@@ -922,11 +929,40 @@ int build_resolved_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const s
   return HX_OK;
 }
 
+// Range pieces of the host-buffer calls: every domain's home slots and halo
+// slots, cut into pieces of at most kCopyChunkWords words.
+int build_copy_chunks(hx_ctx* h) {
+  std::vector<CopyChunk> home, halo;
+  auto cut = [](std::vector<CopyChunk>& out, int64_t first_slot, int64_t slots) {
+    for (int64_t w = 0; w < 3 * slots; w += kCopyChunkWords) {
+      CopyChunk c;
+      c.word = 3 * first_slot + w;
+      c.n = static_cast<int32_t>(std::min<int64_t>(kCopyChunkWords, 3 * slots - w));
+      c.pad = 0;
+      out.push_back(c);
+    }
+  };
+  for (int r = 0; r < h->pl.ndom; ++r) {
+    cut(home, h->dom_offset[r], h->home[r]);
+    cut(halo, h->dom_offset[r] + h->home[r], h->halo[r]);
+  }
+  h->n_home_chunks = static_cast<int>(home.size());
+  h->n_halo_chunks = static_cast<int>(halo.size());
+  HX_CUDA(dev_alloc(&h->d_home_chunks, home.size()));
+  HX_CUDA(dev_alloc(&h->d_halo_chunks, halo.size()));
+  if (!home.empty())
+    HX_CUDA(cudaMemcpy(h->d_home_chunks, home.data(), sizeof(CopyChunk) * home.size(), cudaMemcpyHostToDevice));
+  if (!halo.empty())
+    HX_CUDA(cudaMemcpy(h->d_halo_chunks, halo.data(), sizeof(CopyChunk) * halo.size(), cudaMemcpyHostToDevice));
+  return HX_OK;
+}
+
 // Work tables of the fused and unfused kernels from the host copy of the plan.
 int build_tables(hx_ctx* h, cudaStream_t s) {
   const Plan& pl = h->pl;
   const int P = pl.n_pulses, nd = pl.ndom;
   const int n_items = P * nd;
+  if (const int rc = build_copy_chunks(h); rc != HX_OK) return rc;
   const bool fine = (h->flags & HX_FLAG_FINE_WAITS) != 0;
   const bool ordered = !(h->flags & HX_FLAG_UNORDERED_FORCES);
   std::vector<ItemInfo> items(std::max(n_items, 1));
@@ -1641,6 +1677,51 @@ int exchange(hx_handle h, float* buf, void* stream, int kind) {
 int hx_exchange_coords(hx_handle h, float* coords, void* stream) { return exchange(h, coords, stream, 0); }
 
 int hx_exchange_forces(hx_handle h, float* forces, void* stream) { return exchange(h, forces, stream, 1); }
+
+namespace {
+
+// Device address of a page-locked, mapped host buffer (HX_ERR_ARG otherwise).
+int device_view(float* host, float** out) {
+  void* d = nullptr;
+  if (cudaHostGetDevicePointer(&d, host, 0) != cudaSuccess || d == nullptr) {
+    cudaGetLastError();   // not sticky; clear it for the caller's next check
+    return HX_ERR_ARG;
+  }
+  *out = static_cast<float*>(d);
+  return HX_OK;
+}
+
+int exchange_host(hx_handle h, float* host, float* dev, void* stream, int kind) {
+  if (!h) return HX_ERR_ARG;
+  if (!h->built) return HX_ERR_STATE;
+  if (h->total_slots == 0) return HX_OK;
+  if (!host || !dev) return HX_ERR_ARG;
+  int rc = ensure_device(h);
+  if (rc != HX_OK) return rc;
+  float* hv = nullptr;
+  if ((rc = device_view(host, &hv)) != HX_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (kind == 0) {   // home coordinates in, halo coordinates out
+    HX_CUDA(launch_copy_chunks(hv, dev, h->d_home_chunks, h->n_home_chunks, s));
+    if ((rc = exchange(h, dev, stream, 0)) != HX_OK) return rc;
+    HX_CUDA(launch_copy_chunks(dev, hv, h->d_halo_chunks, h->n_halo_chunks, s));
+  } else {           // every slot's force in, home forces out
+    HX_CUDA(cudaMemcpyAsync(dev, host, sizeof(float) * 3 * h->total_slots, cudaMemcpyHostToDevice, s));
+    if ((rc = exchange(h, dev, stream, 1)) != HX_OK) return rc;
+    HX_CUDA(launch_copy_chunks(dev, hv, h->d_home_chunks, h->n_home_chunks, s));
+  }
+  return HX_OK;
+}
+
+}  // namespace
+
+int hx_exchange_coords_host(hx_handle h, float* coords_host, float* coords_dev, void* stream) {
+  return exchange_host(h, coords_host, coords_dev, stream, 0);
+}
+
+int hx_exchange_forces_host(hx_handle h, float* forces_host, float* forces_dev, void* stream) {
+  return exchange_host(h, forces_host, forces_dev, stream, 1);
+}
 
 int hx_exchange_coords_unfused(hx_handle h, float* coords, void* stream) {
   if (!h) return HX_ERR_ARG;

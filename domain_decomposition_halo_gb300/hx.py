@@ -52,6 +52,8 @@ SIGNATURES = {
     "hx_get_maps": (_I, [_P, _P, _I64, _P]),
     "hx_exchange_coords": (_I, [_P, _P, _P]),
     "hx_exchange_forces": (_I, [_P, _P, _P]),
+    "hx_exchange_coords_host": (_I, [_P, _P, _P, _P]),
+    "hx_exchange_forces_host": (_I, [_P, _P, _P, _P]),
     "hx_exchange_coords_unfused": (_I, [_P, _P, _P]),
     "hx_exchange_forces_unfused": (_I, [_P, _P, _P]),
     "hx_exchange_coords_static": (_I, [_P, _P, _P]),
@@ -262,6 +264,29 @@ class HaloExchange:
                                             _stream_ptr(stream, self.device))
         if rc:
             _check(rc, "hx_exchange_forces")
+
+    def _check_host(self, t, what: str) -> None:
+        if t.is_cuda or t.dtype.itemsize != 4 or not t.is_floating_point() or not t.is_contiguous():
+            raise ValueError(f"{what} must be a contiguous float32 host tensor (page-locked)")
+        if t.numel() < 3 * self.total_slots:
+            raise ValueError(f"{what} holds {t.numel()} elements, {3 * self.total_slots} needed")
+
+    def exchange_coords_host(self, coords_host, coords_dev, stream=None) -> None:
+        """Home coordinates from ``coords_host`` (page-locked CPU fp32 [slots, 3])
+        into ``coords_dev``, the coordinate exchange there, and every halo
+        slot back into ``coords_host``; queued on ``stream``."""
+        self._check_host(coords_host, "coords_host")
+        self._check_tensor(coords_dev, 3 * self.total_slots, "coords_dev")
+        _check(self._lib.hx_exchange_coords_host(self._h, coords_host.data_ptr(), coords_dev.data_ptr(),
+                                                 _stream_ptr(stream, self.device)), "hx_exchange_coords_host")
+
+    def exchange_forces_host(self, forces_host, forces_dev, stream=None) -> None:
+        """Every slot's force from ``forces_host`` into ``forces_dev``, the force
+        exchange there, and every home force back into ``forces_host``."""
+        self._check_host(forces_host, "forces_host")
+        self._check_tensor(forces_dev, 3 * self.total_slots, "forces_dev")
+        _check(self._lib.hx_exchange_forces_host(self._h, forces_host.data_ptr(), forces_dev.data_ptr(),
+                                                 _stream_ptr(stream, self.device)), "hx_exchange_forces_host")
 
     def exchange_coords_unfused(self, coords, stream=None) -> None:
         self._check_tensor(coords, 3 * self.total_slots, "coords")

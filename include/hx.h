@@ -218,6 +218,30 @@ int hx_exchange_coords(hx_handle h, float* coords, void* stream);
  * dependency chain". */
 int hx_exchange_forces(hx_handle h, float* forces, void* stream);
 
+/* The two exchanges for data that lives in host memory: each copies the
+ * direction's inputs in, runs the exchange above on the device buffer, and
+ * copies its results out, all queued on `stream` (the host buffer holds the
+ * results once the stream has passed this point). The pages keep all data on
+ * the GPU ("From MPI baseline to optimized GPU-native halo exchange" names
+ * the CPU hand-offs as the cost); these calls only add the host copies.
+ *   host: float3 slots of the layout in page-locked host memory that is
+ *         mapped for the device (cudaHostAlloc, or cudaHostRegister with
+ *         cudaHostRegisterMapped); total_slots slots, owned by the caller.
+ *   dev:  device float3 slots of the layout, owned by the caller; its halo
+ *         (coordinates) or all (forces) slots are overwritten.
+ * hx_exchange_coords_host: every domain's home coordinates host -> dev,
+ *   hx_exchange_coords(dev), every domain's halo slots dev -> host.
+ *   Host traffic: 12 B per home slot in, 12 B per halo slot out.
+ * hx_exchange_forces_host: every slot's force host -> dev,
+ *   hx_exchange_forces(dev), every domain's home forces dev -> host.
+ *   Host traffic: 12 B per slot in, 12 B per home slot out.
+ * The copies run on the SMs through the mapped host buffer (one launch per
+ * direction for all domains' ranges), except the forces' single
+ * contiguous copy in. Errors: those of the exchange, and HX_ERR_ARG for a
+ * NULL buffer or a host buffer that is not mapped page-locked memory. */
+int hx_exchange_coords_host(hx_handle h, float* coords_host, float* coords_dev, void* stream);
+int hx_exchange_forces_host(hx_handle h, float* forces_host, float* forces_dev, void* stream);
+
 /* Unfused baseline of the same two exchanges: one stream-ordered kernel
  * launch per pulse (all senders of that pulse in one launch), no signals.
  * Same results bit for bit as the fused calls in ordered mode. Pages: the

@@ -408,3 +408,57 @@ def test_back_to_back_steps(name, flags):
         c.o.exchange_forces(f)
     assert np.array_equal(_bits(xt.cpu().numpy()), _bits(x))
     assert np.array_equal(_bits(ft.cpu().numpy()), _bits(f))
+
+
+@pytest.mark.parametrize("name", ["C1", "C2", "C3", "C4"])
+@pytest.mark.parametrize("flags", [HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE | HX.HX_FLAG_SWEEP_FORCES,
+                                   HX.HX_FLAG_RESOLVED, 0])
+def test_host_buffer_exchanges(name, flags):
+    """hx_exchange_coords_host / hx_exchange_forces_host: home coordinates in,
+    halo coordinates out; every force in, home forces out; bit-exact."""
+    w = W.WORKLOADS[name]
+    c = Case(w, flags=flags)
+    o = c.o
+    hm = c.home_mask()
+    x0 = o.coords()
+    ref = x0.copy()
+    o.exchange_coords(ref)
+    host = torch.from_numpy(x0.copy()).pin_memory()
+    host.numpy()[~hm] = np.nan   # halo slots come only from the exchange
+    dev = torch.full((c.slots, 3), float("nan"), device="cuda")
+    for _ in range(2):           # a second call on the same buffers gives the same result
+        c.hx.exchange_coords_host(host, dev)
+        torch.cuda.synchronize()
+        assert np.array_equal(_bits(host.numpy()), _bits(ref))
+    f0 = W.forces(w, c.slots)
+    fref = f0.copy()
+    o.exchange_forces(fref)
+    fh = torch.from_numpy(f0.copy()).pin_memory()
+    fd = torch.full((c.slots, 3), float("nan"), device="cuda")
+    c.hx.exchange_forces_host(fh, fd)
+    torch.cuda.synchronize()
+    got = fh.numpy()
+    assert np.array_equal(_bits(got[hm]), _bits(fref[hm]))     # home forces: the reduced sums
+    assert np.array_equal(_bits(got[~hm]), _bits(f0[~hm]))     # halo forces: left as given
+    rc, det = c.hx.status()
+    assert rc == 0, (rc, det)
+
+
+def test_host_buffer_rules():
+    w = W.WORKLOADS["C2"]
+    c = Case(w, flags=HX.HX_FLAG_FINE_WAITS)
+    dev = torch.empty((c.slots, 3), device="cuda")
+    with pytest.raises(ValueError):
+        c.hx.exchange_coords_host(torch.empty((c.slots - 1, 3)).pin_memory(), dev)   # too small
+    with pytest.raises(ValueError):
+        c.hx.exchange_coords_host(dev, dev)                                            # not a host tensor
+    # pageable memory: refused unless this system maps it for the device
+    pageable = torch.from_numpy(c.o.coords().copy())
+    try:
+        c.hx.exchange_coords_host(pageable, dev)
+        torch.cuda.synchronize()
+        ref = c.o.coords().copy()
+        c.o.exchange_coords(ref)
+        assert np.array_equal(_bits(pageable.numpy()), _bits(ref))
+    except HX.HXError as e:
+        assert e.code == HX.HX_ERR_ARG
