@@ -123,8 +123,9 @@ struct alignas(16) TreeRec {
 };
 static_assert(sizeof(TreeRec) == 48, "tree record must stay 48 bytes");
 // Coordinates: one block per segment of consecutive halo slots of one domain
-// (up to kResSeg; the build sizes segments for the decomposition); per halo slot one word, the origin home slot in the low 29
-// bits and the shift mask (bit d: add box[d] to component d) in the top 3.
+// (up to kResSeg; the build sizes segments for the decomposition). Per halo
+// slot one word: the origin home slot in the low 29 bits, the shift mask
+// (bit d: add box[d] to component d) in the top 3.
 constexpr int kResThreads = 256;
 constexpr int kResSlotsPerThread = 4;     // at most; the build picks 1..4 gathers in flight per thread
 constexpr int kResSeg = kResThreads * kResSlotsPerThread;   // largest segment
