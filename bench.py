@@ -412,7 +412,8 @@ def _flush(buf):
 
 def secondary(hx_main, coords, forces, w_main, dev, peak, flags):
     """Cold-L2 numbers of the headline workload, the 1M-atom configuration,
-    and the small configurations' step latency against the launch floor."""
+    the small configurations' step latency against the launch floor, and the
+    headline workload in resolved mode."""
     import torch
 
     from domain_decomposition_halo_gb300 import HaloExchange
@@ -501,6 +502,10 @@ def secondary(hx_main, coords, forces, w_main, dev, peak, flags):
         res[name] = small(name, flags)
         if not flags & HX.HX_FLAG_RESOLVED:
             res[name]["resolved_pdl"] = small(name, HX.HX_FLAG_RESOLVED | HX.HX_FLAG_PDL)
+    # the headline workload with the forwarding resolved at build time (not the
+    # staged path of the main number: no pulse waits or signals)
+    if not flags & HX.HX_FLAG_RESOLVED:
+        res[w_main.name + "_resolved_pdl"] = small(w_main.name, HX.HX_FLAG_RESOLVED | HX.HX_FLAG_PDL)
     return res
 
 
