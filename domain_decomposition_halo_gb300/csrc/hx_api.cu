@@ -802,7 +802,7 @@ int build_resolved_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const s
     home_base[r + 1] = home_base[r] + h->home[r];
   }
   const int64_t H = hbase[nd];
-  std::vector<int32_t> origin_home(H), origin_slot(H), parent_h(H);
+  std::vector<int32_t> origin_home(H), origin_slot(H), parent_h(H), root_dom(H);
   std::vector<uint8_t> mask(H), pulse(H);
   for (int p = 0; p < P; ++p)   // senders of one pulse write disjoint slots and read earlier pulses
     parallel_for(nd, [&](size_t ri) {
@@ -815,12 +815,14 @@ int build_resolved_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const s
         if (mv < h->home[r]) {
           origin_home[k] = static_cast<int32_t>(home_base[r] + mv);
           origin_slot[k] = static_cast<int32_t>(it.src + mv);
+          root_dom[k] = r;
           mask[k] = 0;
           parent_h[k] = -1;
         } else {
           const int64_t sh = hbase[r] + (mv - h->home[r]);
           origin_home[k] = origin_home[sh];
           origin_slot[k] = origin_slot[sh];
+          root_dom[k] = root_dom[sh];
           mask[k] = mask[sh];
           parent_h[k] = static_cast<int32_t>(sh);
         }
@@ -843,69 +845,104 @@ int build_resolved_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const s
       sg.pad = 0;
       segs.push_back(sg);
     }
-  // trees: one per home atom that has copies, numbered in home-slot order
-  std::vector<int32_t> tree_of(home_base[nd], -1);
-  for (int64_t k = 0; k < H; ++k) tree_of[origin_home[k]] = 0;   // marks the roots
-  int32_t n_trees = 0;
-  for (int64_t a = 0; a < home_base[nd]; ++a)
-    if (tree_of[a] == 0) tree_of[a] = n_trees++;
-  std::vector<TreeRec> trees(static_cast<size_t>(n_trees));   // zero-filled
+  // trees: one per home atom that has copies, numbered in home-slot order.
+  // A tree lies in its root's domain (every copy descends from the root), so
+  // the halo slots are grouped by root domain (stably: halo order kept) and
+  // each root domain's trees are built by one task, in a local array.
+  std::vector<int64_t> by_root_begin(nd + 1, 0);
+  for (int64_t k = 0; k < H; ++k) ++by_root_begin[root_dom[k] + 1];
+  for (int r = 0; r < nd; ++r) by_root_begin[r + 1] += by_root_begin[r];
+  std::vector<int32_t> by_root(H);
+  {
+    std::vector<int64_t> fill(by_root_begin.begin(), by_root_begin.end() - 1);
+    for (int64_t k = 0; k < H; ++k) by_root[fill[root_dom[k]]++] = static_cast<int32_t>(k);
+  }
   std::vector<uint8_t> node_idx(H);
-  for (int r = 0; r < nd; ++r)   // nodes: the root, then its copies in halo order
-    for (int64_t k = hbase[r]; k < hbase[r + 1]; ++k) {
-      TreeRec& rec = trees[tree_of[origin_home[k]]];
+  std::vector<std::vector<int4>> recs_of(nd);
+  std::vector<std::vector<TreeRec>> general_of(nd);
+  std::vector<int64_t> pairs_of(nd, 0), quads_of(nd, 0);
+  std::vector<char> overflow(nd, 0);
+  auto slot_of_halo = [&](int64_t k) {   // the global slot of halo index k
+    const int r = static_cast<int>(std::upper_bound(hbase.begin(), hbase.end(), k) - hbase.begin()) - 1;
+    return static_cast<int32_t>(h->dom_offset[r] + h->home[r] + (k - hbase[r]));
+  };
+  parallel_for(nd, [&](size_t ri) {
+    const int r0 = static_cast<int>(ri);
+    const int32_t* ks = by_root.data() + by_root_begin[r0];
+    const int64_t nk = by_root_begin[r0 + 1] - by_root_begin[r0];
+    std::vector<int32_t> tree_of(h->home[r0], -1);   // per home atom of r0
+    for (int64_t i = 0; i < nk; ++i) tree_of[origin_home[ks[i]] - home_base[r0]] = 0;   // marks the roots
+    int32_t n_trees = 0;
+    for (auto& t : tree_of)
+      if (t == 0) t = n_trees++;
+    std::vector<TreeRec> trees(static_cast<size_t>(n_trees));   // zero-filled
+    std::vector<uint8_t> add_pulse(trees.size() * kTreeNodes, 0);
+    for (int64_t i = 0; i < nk; ++i) {   // nodes: the root, then its copies in halo order
+      const int64_t k = ks[i];
+      TreeRec& rec = trees[tree_of[origin_home[k] - home_base[r0]]];
       if (rec.n_nodes == 0) {
         rec.node[0] = origin_slot[k];
         rec.n_nodes = 1;
       }
-      if (rec.n_nodes >= kTreeNodes) return HX_ERR_PULSES;   // more copies than a tree record holds
-      node_idx[k] = static_cast<uint8_t>(rec.n_nodes);
-      rec.node[rec.n_nodes++] = static_cast<int32_t>(h->dom_offset[r] + h->home[r] + (k - hbase[r]));
-    }
-  // adds: copy j (node j > 0) into its parent, then sorted by descending pulse
-  std::vector<uint8_t> add_pulse(trees.size() * kTreeNodes, 0);
-  for (int64_t k = 0; k < H; ++k) {
-    const size_t t = static_cast<size_t>(tree_of[origin_home[k]]);
-    const int j = node_idx[k];
-    const int tg = parent_h[k] < 0 ? 0 : node_idx[parent_h[k]];
-    trees[t].ev[j - 1] = static_cast<uint8_t>(tg | (j << 4));
-    add_pulse[t * kTreeNodes + j - 1] = pulse[k];
-  }
-  parallel_for(trees.size(), [&](size_t t) {
-    TreeRec& rec = trees[t];
-    uint8_t* pu = add_pulse.data() + t * kTreeNodes;
-    const int m = rec.n_nodes - 1;
-    for (int a = 1; a < m; ++a)   // stable insertion sort by descending pulse
-      for (int b = a; b > 0 && pu[b] > pu[b - 1]; --b) {
-        std::swap(pu[b], pu[b - 1]);
-        std::swap(rec.ev[b], rec.ev[b - 1]);
+      if (rec.n_nodes >= kTreeNodes) {   // more copies than a tree record holds
+        overflow[r0] = 1;
+        return;
       }
-  }, 1024);
-  // records in root order. A four-node tree is a quad when its
-  // last add (lowest pulse) is some copy u into the root and the two adds
-  // before it are one copy into the root and one copy into u: then the
-  // fixed order root += c, u += d, root += u is the staged order.
-  std::vector<int4> recs;
-  std::vector<TreeRec> general;
-  recs.reserve(trees.size());
-  int64_t n_pairs = 0, n_quads = 0;
-  for (const TreeRec& rec : trees) {
-    if (rec.n_nodes == 2) {
-      recs.push_back(make_int4(rec.node[0], rec.node[1], -1, -1));
-      ++n_pairs;
-      continue;
+      node_idx[k] = static_cast<uint8_t>(rec.n_nodes);
+      rec.node[rec.n_nodes++] = slot_of_halo(k);
     }
-    if (rec.n_nodes == 4) {
-      const int tg2 = rec.ev[2] & 15, u = rec.ev[2] >> 4;
-      const int tg0 = rec.ev[0] & 15, s0 = rec.ev[0] >> 4, tg1 = rec.ev[1] & 15, s1 = rec.ev[1] >> 4;
-      if (tg2 == 0 && u != 0 && ((tg0 == 0 && tg1 == u) || (tg0 == u && tg1 == 0))) {
-        const int c = tg0 == 0 ? s0 : s1, d = tg0 == 0 ? s1 : s0;
-        recs.push_back(make_int4(rec.node[0], rec.node[u], rec.node[c], rec.node[d]));
-        ++n_quads;
+    for (int64_t i = 0; i < nk; ++i) {   // adds: copy j (node j > 0) into its parent (same tree)
+      const int64_t k = ks[i];
+      const size_t t = static_cast<size_t>(tree_of[origin_home[k] - home_base[r0]]);
+      const int j = node_idx[k];
+      const int tg = parent_h[k] < 0 ? 0 : node_idx[parent_h[k]];
+      trees[t].ev[j - 1] = static_cast<uint8_t>(tg | (j << 4));
+      add_pulse[t * kTreeNodes + j - 1] = pulse[k];
+    }
+    std::vector<int4>& recs = recs_of[r0];
+    std::vector<TreeRec>& general = general_of[r0];
+    recs.reserve(trees.size());
+    for (size_t t = 0; t < trees.size(); ++t) {
+      TreeRec& rec = trees[t];
+      uint8_t* pu = add_pulse.data() + t * kTreeNodes;
+      const int m = rec.n_nodes - 1;
+      for (int a = 1; a < m; ++a)   // stable insertion sort by descending pulse
+        for (int b = a; b > 0 && pu[b] > pu[b - 1]; --b) {
+          std::swap(pu[b], pu[b - 1]);
+          std::swap(rec.ev[b], rec.ev[b - 1]);
+        }
+      // records in root order. A four-node tree is a quad when its last add
+      // (lowest pulse) is some copy u into the root and the two adds before
+      // it are one copy into the root and one copy into u: then the fixed
+      // order root += c, u += d, root += u is the staged order.
+      if (rec.n_nodes == 2) {
+        recs.push_back(make_int4(rec.node[0], rec.node[1], -1, -1));
+        ++pairs_of[r0];
         continue;
       }
+      if (rec.n_nodes == 4) {
+        const int tg2 = rec.ev[2] & 15, u = rec.ev[2] >> 4;
+        const int tg0 = rec.ev[0] & 15, s0 = rec.ev[0] >> 4, tg1 = rec.ev[1] & 15, s1 = rec.ev[1] >> 4;
+        if (tg2 == 0 && u != 0 && ((tg0 == 0 && tg1 == u) || (tg0 == u && tg1 == 0))) {
+          const int c = tg0 == 0 ? s0 : s1, d = tg0 == 0 ? s1 : s0;
+          recs.push_back(make_int4(rec.node[0], rec.node[u], rec.node[c], rec.node[d]));
+          ++quads_of[r0];
+          continue;
+        }
+      }
+      general.push_back(rec);
     }
-    general.push_back(rec);
+  }, 1);
+  for (int r = 0; r < nd; ++r)
+    if (overflow[r]) return HX_ERR_PULSES;
+  std::vector<int4> recs;
+  std::vector<TreeRec> general;
+  int64_t n_pairs = 0, n_quads = 0;
+  for (int r = 0; r < nd; ++r) {   // domain after domain: root order overall
+    recs.insert(recs.end(), recs_of[r].begin(), recs_of[r].end());
+    general.insert(general.end(), general_of[r].begin(), general_of[r].end());
+    n_pairs += pairs_of[r];
+    n_quads += quads_of[r];
   }
   h->n_res_halo = H;
   h->n_res_segs = static_cast<int64_t>(segs.size());
