@@ -511,11 +511,13 @@ def secondary(hx_main, coords, forces, w_main, dev, peak, flags):
 
 def overlap_probe(dev, flags, names=("C2", "C4"), reps=40):
     """Exchange latency while a local kernel fills the GPU (the pages'
-    section "SM occupancy and kernel scheduling"): a stream of short-block
-    elementwise kernels runs on a low-priority stream, one step (coordinates
-    + forces) is issued on a high-priority stream, and its event-timed
-    latency is compared for the fused path (one launch per direction) and
-    the per-pulse unfused path (one launch per pulse and direction)."""
+    section "SM occupancy and kernel scheduling"): a local workload runs on a
+    low-priority stream, one step (coordinates + forces) is issued on a
+    high-priority stream, and its event-timed latency is compared for the
+    fused path (one launch per direction) and the per-pulse unfused path (one
+    launch per pulse and direction). Two local workloads: memory-bound
+    (`_loaded`: short-block elementwise kernels over 256 MB) and
+    compute-bound (`_loaded_compute`: bf16 8192^3 matrix products)."""
     import torch
 
     from domain_decomposition_halo_gb300 import HaloExchange
@@ -523,6 +525,9 @@ def overlap_probe(dev, flags, names=("C2", "C4"), reps=40):
     lo = torch.cuda.Stream(device=dev, priority=0)
     hi = torch.cuda.Stream(device=dev, priority=-5)
     filler = torch.ones(64 * 2 ** 20, device=dev)   # 256 MB: every launch is thousands of short blocks
+    ga = torch.randn(8192, 8192, device=dev, dtype=torch.bfloat16)
+    gb = torch.randn(8192, 8192, device=dev, dtype=torch.bfloat16)
+    gc = torch.empty(8192, 8192, device=dev, dtype=torch.bfloat16)
     out = {}
     for name in names:
         w = W.WORKLOADS[name]
@@ -541,15 +546,19 @@ def overlap_probe(dev, flags, names=("C2", "C4"), reps=40):
                 else:
                     hx.exchange_coords_unfused(x, stream=hi)
                     hx.exchange_forces_unfused(f, stream=hi)
-            for loaded in (False, True):
+            for loaded in ("", "_loaded", "_loaded_compute"):
                 ts = []
                 for _ in range(reps):
                     torch.cuda.synchronize()
                     if loaded:
                         with torch.cuda.stream(lo):
-                            for _ in range(8):
-                                filler.mul_(1.0000001)
-                        time.sleep(50e-6)   # let the filler occupy the SMs
+                            if loaded == "_loaded":
+                                for _ in range(8):
+                                    filler.mul_(1.0000001)
+                            else:
+                                for _ in range(2):
+                                    torch.mm(ga, gb, out=gc)
+                        time.sleep(50e-6)   # let the local work occupy the SMs
                     a = torch.cuda.Event(enable_timing=True)
                     b = torch.cuda.Event(enable_timing=True)
                     a.record(hi)
@@ -557,7 +566,7 @@ def overlap_probe(dev, flags, names=("C2", "C4"), reps=40):
                     b.record(hi)
                     torch.cuda.synchronize()
                     ts.append(a.elapsed_time(b) * 1e3)
-                res[("fused" if fused else "unfused") + ("_loaded" if loaded else "_idle")] = round(statistics.median(ts), 2)
+                res[("fused" if fused else "unfused") + (loaded or "_idle")] = round(statistics.median(ts), 2)
         res["launches_per_step"] = {"fused": 2, "unfused": 2 * hx.counts()[1]}
         out[name] = res
         del hx
