@@ -462,3 +462,32 @@ def test_host_buffer_rules():
         assert np.array_equal(_bits(pageable.numpy()), _bits(ref))
     except HX.HXError as e:
         assert e.code == HX.HX_ERR_ARG
+
+
+def test_host_buffer_misaligned():
+    """A host buffer one float off the device buffer's 16-byte phase: the
+    range copies take their word-by-word path; results stay bit-exact."""
+    w = W.WORKLOADS["C2"]
+    c = Case(w, flags=HX.HX_FLAG_FINE_WAITS)
+    o = c.o
+    hm = c.home_mask()
+    ref = o.coords().copy()
+    o.exchange_coords(ref)
+    store = torch.empty(3 * c.slots + 1, dtype=torch.float32).pin_memory()
+    host = store[1:].view(c.slots, 3)               # 4 bytes past a 16-byte boundary
+    assert host.data_ptr() % 16 == 4
+    host.copy_(torch.from_numpy(o.coords()))
+    host.numpy()[~hm] = np.nan
+    dev = torch.full((c.slots, 3), float("nan"), device="cuda")
+    c.hx.exchange_coords_host(host, dev)
+    torch.cuda.synchronize()
+    assert np.array_equal(_bits(host.numpy()), _bits(ref))
+    f0 = W.forces(w, c.slots)
+    fref = f0.copy()
+    o.exchange_forces(fref)
+    fstore = torch.empty(3 * c.slots + 1, dtype=torch.float32).pin_memory()
+    fh = fstore[1:].view(c.slots, 3)
+    fh.copy_(torch.from_numpy(f0))
+    c.hx.exchange_forces_host(fh, torch.empty_like(dev))
+    torch.cuda.synchronize()
+    assert np.array_equal(_bits(fh.numpy()[hm]), _bits(fref[hm]))
