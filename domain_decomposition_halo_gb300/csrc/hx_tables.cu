@@ -1,0 +1,891 @@
+// Work tables of libhx, built on the host from the maps at map-build time:
+// the fused kernels' chunk and unit lists with their waits, the per-pulse
+// chunk lists of the unfused baseline, the resolved-mode tables and the
+// range pieces of the host-buffer calls.
+#include "hx_runtime.h"
+
+namespace hx_rt {
+
+// ---------------------------------------------------------------- work tables
+//
+// Every (sender, pulse) item is cut into warp chunks of up to kChunk entries
+// (a coordinate item into its independent prefix and its forwarded tail).
+// Each chunk gets the list of what it must wait for:
+//   coarse (the pages' rule): a forwarded coordinate chunk waits for every
+//     earlier pulse into its sender; a force chunk of pulse p waits for every
+//     later pulse of its receiver (the slots it reads) and of its sender (the
+//     targets it adds into) - per-item signals;
+//   fine: the exact producer chunks - the chunks that stored the slots a
+//     forwarded coordinate chunk reads, the later-pulse chunks that add into
+//     the slots a force chunk reads or into the targets it adds into - each
+//     with its own signal.
+// Chunks are then listed in a topological order of those waits (Kahn's
+// algorithm, so a warp only ever waits for chunks handed out before its own)
+// that follows a priority: domains in a folded order where the neighbours a
+// pulse depends on sit close together, a domain's pulses together, and a
+// consumer one resident-warp window behind its producers. A domain's slots
+// are then fetched into L2 about once per launch, and a waiting chunk finds
+// its producers mostly done.
+
+// Runs body(i) for i in [0, n) on the host's cores (iterations must be
+// independent).
+template <class Body>
+void parallel_for(size_t n, Body body, size_t grain = 256) {
+  const size_t hw = std::max<size_t>(1, std::min<size_t>(16, std::thread::hardware_concurrency()));
+  const size_t workers = std::min(hw, std::max<size_t>(1, n / grain));
+  if (workers <= 1) {
+    for (size_t i = 0; i < n; ++i) body(i);
+    return;
+  }
+  std::vector<std::thread> pool;
+  pool.reserve(workers);
+  for (size_t w = 0; w < workers; ++w)
+    pool.emplace_back([&, w] {
+      for (size_t i = w; i < n; i += workers) body(i);
+    });
+  for (auto& t : pool) t.join();
+}
+
+struct ItemInfo {
+  int r, p, q;           // sender, pulse, receiver
+  int64_t src, dst, map; // slot of sender base, slot of receive-range start, first map entry
+  int size, split, dim, shift_flag;
+};
+
+struct Rec {             // one chunk before ordering
+  int item;
+  int begin, end;        // entry range within the item's map
+  int halo_src;
+  int stage;             // position of the chunk's pulse in the launch's dependency order
+  long long key;         // priority (smaller first)
+  std::vector<int> deps;   // chunk records that must be listed earlier
+  std::vector<int> wait;   // coarse: items to wait for; fine: chunk records to wait for
+};
+
+// Position of cell c in the folded ring order 0, n-1, 1, n-2, ...: cells that
+// are neighbours on the periodic ring are at most two positions apart.
+int fold(int c, int n) { return (2 * c < n) ? 2 * c : 2 * (n - 1 - c) + 1; }
+
+int64_t domain_rank(const Plan& pl, int r) {
+  int c[3];
+  cell_of(pl, r, c);
+  // the first-communicating dimension (Z) varies fastest, X slowest
+  return fold(c[2], pl.dims[2]) + static_cast<int64_t>(pl.dims[2]) *
+                                      (fold(c[1], pl.dims[1]) + static_cast<int64_t>(pl.dims[1]) * fold(c[0], pl.dims[0]));
+}
+
+// Kahn's algorithm over chunk records by ascending key.
+// Kahn's algorithm: a topological order of n records whose dependency lists
+// deps(i) name earlier-done records, taking among the ready ones the smallest
+// key(i) (ties by index). Users are kept in one flat list.
+template <class Deps, class Key>
+std::vector<int> kahn_order(int n, Deps deps, Key key) {
+  std::vector<int> first(n + 1, 0), unmet(n, 0);
+  for (int i = 0; i < n; ++i) {
+    const auto& d = deps(i);
+    unmet[i] = static_cast<int>(d.size());
+    for (int x : d) ++first[x + 1];
+  }
+  for (int i = 0; i < n; ++i) first[i + 1] += first[i];
+  std::vector<int> users(first[n]), fill(first.begin(), first.end() - 1);
+  for (int i = 0; i < n; ++i)
+    for (int x : deps(i)) users[fill[x]++] = i;
+  auto cmp = [&](int a, int b) {
+    const long long ka = key(a), kb = key(b);
+    return ka != kb ? ka > kb : a > b;
+  };
+  std::vector<int> heap;
+  for (int i = 0; i < n; ++i)
+    if (unmet[i] == 0) heap.push_back(i);
+  std::make_heap(heap.begin(), heap.end(), cmp);
+  std::vector<int> order;
+  order.reserve(n);
+  while (!heap.empty()) {
+    std::pop_heap(heap.begin(), heap.end(), cmp);
+    const int i = heap.back();
+    heap.pop_back();
+    order.push_back(i);
+    for (int k = first[i]; k < first[i + 1]; ++k)
+      if (--unmet[users[k]] == 0) {
+        heap.push_back(users[k]);
+        std::push_heap(heap.begin(), heap.end(), cmp);
+      }
+  }
+  return order;   // shorter than n only if the waits had a cycle (they cannot)
+}
+
+std::vector<int> order_chunks(const std::vector<Rec>& recs) {
+  return kahn_order(
+      static_cast<int>(recs.size()), [&](int i) -> const std::vector<int>& { return recs[i].deps; },
+      [&](int i) { return recs[i].key; });
+}
+
+// ---------------------------------------------------------------- tile tables
+//
+// Each domain's array is cut into ranges (home, then the slots received in
+// each pulse) and each range into tiles of up to kTile slots. A tile gets
+// one segment per (sender, pulse) map that has entries inside it: for
+// coordinates the maps it is a source of, for forces the maps it is a target
+// of (segments last pulse first). Dependencies:
+//   coordinates: a tile of received slots waits for the tiles of the sending
+//     domain that stored those slots;
+//   forces: a tile waits for the tiles of its receivers that hold the slots
+//     it reads, when those tiles are themselves targets of later pulses.
+// Tiles are listed by Kahn's algorithm with the same priority as the chunk
+// lists (folded domain order, dependency depth, a lag of one resident window
+// per depth).
+
+struct TRec {
+  int r;              // domain
+  int range;          // -1 home, else the pulse whose received slots the tile holds
+  int a, n;           // local index of the first slot, slot count
+  std::vector<TileSeg> segs;
+  std::vector<int> seg_pulse;
+  std::vector<int> deps;   // TRec indices
+  int stage = 0;
+  long long key = 0;
+};
+
+int build_tile_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::vector<int32_t>& maps,
+                      const std::vector<int64_t>& rank, int max_slots, int max_entries, long long lag,
+                      int tile_bytes, int map_bytes, int src_bytes, int dir) {
+  const Plan& pl = h->pl;
+  const int P = pl.n_pulses, nd = pl.ndom;
+  auto upper = [&](int r, int q) { return neighbour(pl, r, pl.pulse_dim[q], +1); };
+  {
+    // tiles of each domain, cut on all host cores, then listed domain after domain;
+    // by_range: per (domain, range) the tiles' indices in slot order
+    std::vector<std::vector<TRec>> per(nd);
+    std::vector<std::vector<std::vector<int>>> by_range(nd, std::vector<std::vector<int>>(P + 1));
+    parallel_for(nd, [&](size_t ri) {
+      const int r = static_cast<int>(ri);
+      for (int rg = -1; rg < P; ++rg) {
+        int lo, len;
+        if (rg < 0) {
+          lo = 0;
+          len = h->home[r];
+        } else {
+          const int tu = rg * nd + upper(r, rg);
+          lo = h->t_off[tu];
+          len = h->t_size[tu];
+        }
+        // entries of every map of r that fall in slots [a, b)
+        auto entries_in = [&](int a, int b) {
+          int e = 0;
+          for (int p = 0; p < P; ++p) {
+            const ItemInfo& it = items[p * nd + r];
+            if (it.size == 0) continue;
+            const int32_t* m = maps.data() + it.map;
+            e += static_cast<int>(std::lower_bound(m, m + it.size, b) - std::lower_bound(m, m + it.size, a));
+          }
+          return e;
+        };
+        for (int a = lo, b = lo; a < lo + len; a = b) {
+          // at most kTile slots and kTileEntries entries (a slot has at most one entry per pulse)
+          b = std::min(lo + len, a + max_slots);
+          if (entries_in(a, b) > max_entries) {
+            int good = a + 1, bad = b;
+            while (bad - good > 1) {
+              const int mid = good + (bad - good) / 2;
+              if (entries_in(a, mid) <= max_entries) good = mid;
+              else bad = mid;
+            }
+            b = good;
+          }
+          TRec t;
+          t.r = r;
+          t.range = rg;
+          t.a = a;
+          t.n = b - a;
+          for (int k = 0; k < P; ++k) {
+            const int p = dir == 0 ? k : P - 1 - k;
+            const ItemInfo& it = items[p * nd + r];
+            if (it.size == 0) continue;
+            const int32_t* m = maps.data() + it.map;
+            const int i1 = static_cast<int>(std::lower_bound(m, m + it.size, t.a) - m);
+            const int i2 = static_cast<int>(std::lower_bound(m, m + it.size, t.a + t.n) - m);
+            if (i2 <= i1) continue;
+            TileSeg sg;
+            std::memset(&sg, 0, sizeof(sg));
+            sg.map = it.map + i1;
+            sg.other = it.dst + i1;
+            sg.n = i2 - i1;
+            sg.dim = it.dim;
+            sg.shift = pl.boxf[it.dim];
+            sg.do_shift = (dir == 0) ? it.shift_flag : 0;
+            t.segs.push_back(sg);
+            t.seg_pulse.push_back(p);
+          }
+          if (t.segs.empty()) continue;
+          by_range[r][rg + 1].push_back(static_cast<int>(per[r].size()));
+          per[r].push_back(std::move(t));
+        }
+      }
+    }, 1);
+    std::vector<TRec> recs;
+    for (int r = 0; r < nd; ++r) {
+      const int base = static_cast<int>(recs.size());
+      for (auto& lst : by_range[r])
+        for (int& i : lst) i += base;
+      for (TRec& t : per[r]) recs.push_back(std::move(t));
+    }
+    per.clear();
+    // dependencies, one unit per task
+    parallel_for(recs.size(), [&](size_t i) {
+      TRec& t = recs[i];
+      if (dir == 0) {
+        if (t.range < 0) return;
+        // slots [a, a+n) of r's range `p0` are entries [a - off, a - off + n) of the map (u, p0)
+        const int p0 = t.range, u = upper(t.r, p0);
+        const int64_t e0 = t.a - h->t_off[p0 * nd + u], e1 = e0 + t.n;
+        for (int rg = 0; rg <= P; ++rg)
+          for (int j : by_range[u][rg]) {
+            const TRec& s = recs[j];
+            for (size_t k = 0; k < s.segs.size(); ++k) {
+              if (s.seg_pulse[k] != p0) continue;
+              const int64_t b0 = s.segs[k].map - items[p0 * nd + u].map, b1 = b0 + s.segs[k].n;
+              if (b0 < e1 && e0 < b1) t.deps.push_back(j);
+            }
+          }
+      } else {
+        // the slots read by segment (r, p) are q's slots [other, other + n) in q's range p
+        for (size_t k = 0; k < t.segs.size(); ++k) {
+          const int p = t.seg_pulse[k];
+          const int q = items[p * nd + t.r].q;
+          const int64_t s0 = t.segs[k].other - h->dom_offset[q], s1 = s0 + t.segs[k].n;
+          for (int j : by_range[q][p + 1]) {
+            const TRec& s = recs[j];
+            if (s.a < s1 && s0 < s.a + s.n) t.deps.push_back(j);
+          }
+        }
+      }
+      std::sort(t.deps.begin(), t.deps.end());
+      t.deps.erase(std::unique(t.deps.begin(), t.deps.end()), t.deps.end());
+    }, 64);
+    // dependency depth, then priority: base order + one resident window per depth
+    {
+      const int n = static_cast<int>(recs.size());
+      auto deps_of = [&](int i) -> const std::vector<int>& { return recs[i].deps; };
+      std::vector<int> topo = kahn_order(n, deps_of, [](int) { return 0ll; });   // any topological order
+      if (topo.size() != recs.size()) return HX_ERR_STATE;
+      for (int i : topo)
+        for (int d : recs[i].deps) recs[i].stage = std::max(recs[i].stage, recs[d].stage + 1);
+      std::vector<int> base(recs.size());
+      for (size_t i = 0; i < recs.size(); ++i) base[i] = static_cast<int>(i);
+      std::sort(base.begin(), base.end(), [&](int x, int y) {
+        const TRec& a = recs[x];
+        const TRec& b = recs[y];
+        if (rank[a.r] != rank[b.r]) return rank[a.r] < rank[b.r];
+        if (a.stage != b.stage) return a.stage < b.stage;
+        if (a.range != b.range) return a.range < b.range;
+        return a.a < b.a;
+      });
+      for (size_t k = 0; k < base.size(); ++k)
+        recs[base[k]].key = static_cast<long long>(k) + lag * recs[base[k]].stage;
+      std::vector<int> order = kahn_order(n, deps_of, [&](int i) { return recs[i].key; });
+      if (order.size() != recs.size()) return HX_ERR_STATE;
+      std::vector<int> pos(recs.size());
+      for (size_t k = 0; k < order.size(); ++k) pos[order[k]] = static_cast<int>(k);
+      std::vector<char> waited(recs.size(), 0);
+      for (auto& t : recs)
+        for (int d : t.deps) waited[d] = 1;
+      std::vector<TileUnit> units;
+      std::vector<TileSeg> segs;   // segments past kInlineSegs
+      std::vector<Wait> waits;
+      for (int i : order) {
+        const TRec& t = recs[i];
+        TileUnit u;
+        std::memset(&u, 0, sizeof(u));
+        u.base = h->dom_offset[t.r] + t.a;
+        u.n = t.n;
+        u.local_a = t.a;
+        u.seg_cnt = static_cast<int32_t>(t.segs.size());
+        u.extra_off = static_cast<int32_t>(segs.size());
+        // stage regions: each run's region starts on a 16-byte boundary and is 16 bytes longer than the run
+        int moff = tile_bytes, soff = tile_bytes + map_bytes;
+        for (size_t k = 0; k < t.segs.size(); ++k) {
+          TileSeg sg = t.segs[k];
+          sg.map_off = moff;
+          sg.src_off = dir == 1 ? soff : 0;
+          moff += ((4 * sg.n + 15) & ~15) + 16;
+          soff += ((12 * sg.n + 15) & ~15) + 16;
+          if (static_cast<int>(k) < kInlineSegs) u.seg[k] = sg;
+          else segs.push_back(sg);
+        }
+        // the stage regions must fit the kernel's buffer
+        if (moff > tile_bytes + map_bytes || (dir == 1 && soff > tile_bytes + map_bytes + src_bytes))
+          return HX_ERR_STATE;
+        u.wait_off = static_cast<int32_t>(waits.size());
+        u.wait_cnt = static_cast<int32_t>(t.deps.size());
+        for (int d : t.deps) waits.push_back({pos[d], 1});
+        u.flags = (waited[i] ? kSignal : 0) | (dir == 0 && t.range >= 0 ? kHaloSrc : 0);
+        u.item = t.seg_pulse[0] * nd + t.r;
+        for (const TileSeg& sg : t.segs) u.entries += sg.n;
+        units.push_back(u);
+      }
+      h->n_units[dir] = static_cast<int>(units.size());
+      HX_CUDA(dev_alloc(&h->d_units[dir], units.size()));
+      HX_CUDA(dev_alloc(&h->d_segs[dir], segs.size()));
+      HX_CUDA(dev_alloc(&h->d_twaits[dir], waits.size()));
+      if (!units.empty())
+        HX_CUDA(cudaMemcpy(h->d_units[dir], units.data(), sizeof(TileUnit) * units.size(), cudaMemcpyHostToDevice));
+      if (!segs.empty())
+        HX_CUDA(cudaMemcpy(h->d_segs[dir], segs.data(), sizeof(TileSeg) * segs.size(), cudaMemcpyHostToDevice));
+      if (!waits.empty())
+        HX_CUDA(cudaMemcpy(h->d_twaits[dir], waits.data(), sizeof(Wait) * waits.size(), cudaMemcpyHostToDevice));
+    }
+  }
+  return HX_OK;
+}
+
+// Resolved tables: every halo slot's origin and shift mask (pulses in order,
+// each received slot inheriting from the slot it was sent from), in halo
+// order (domain after domain) with one segment record per block; and one
+// tree per home atom that has copies, its adds sorted by descending pulse,
+// numbered in home-slot order: pairs and quads as 16-byte records, the
+// other trees as general records, each list in root order.
+int build_resolved_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::vector<int32_t>& maps,
+                          cudaStream_t s) {
+  const Plan& pl = h->pl;
+  const int P = pl.n_pulses, nd = pl.ndom;
+  // origins share a word with the shift mask; other slots are int32 in the records
+  if (h->total_slots >= (int64_t{1} << kResOriginBits)) return HX_ERR_CAPACITY;
+  std::vector<int64_t> hbase(nd + 1, 0), home_base(nd + 1, 0);
+  for (int r = 0; r < nd; ++r) {
+    hbase[r + 1] = hbase[r] + h->halo[r];
+    home_base[r + 1] = home_base[r] + h->home[r];
+  }
+  const int64_t H = hbase[nd];
+  std::vector<int32_t> origin_home(H), origin_slot(H), parent_h(H), root_dom(H);
+  std::vector<uint8_t> mask(H), pulse(H);
+  for (int p = 0; p < P; ++p)   // senders of one pulse write disjoint slots and read earlier pulses
+    parallel_for(nd, [&](size_t ri) {
+      const int r = static_cast<int>(ri);
+      const ItemInfo& it = items[p * nd + r];
+      const int64_t d0 = hbase[it.q] + (it.dst - h->dom_offset[it.q] - h->home[it.q]);
+      for (int i = 0; i < it.size; ++i) {
+        const int32_t mv = maps[it.map + i];
+        const int64_t k = d0 + i;
+        if (mv < h->home[r]) {
+          origin_home[k] = static_cast<int32_t>(home_base[r] + mv);
+          origin_slot[k] = static_cast<int32_t>(it.src + mv);
+          root_dom[k] = r;
+          mask[k] = 0;
+          parent_h[k] = -1;
+        } else {
+          const int64_t sh = hbase[r] + (mv - h->home[r]);
+          origin_home[k] = origin_home[sh];
+          origin_slot[k] = origin_slot[sh];
+          root_dom[k] = root_dom[sh];
+          mask[k] = mask[sh];
+          parent_h[k] = static_cast<int32_t>(sh);
+        }
+        if (it.shift_flag) mask[k] = static_cast<uint8_t>(mask[k] | (1 << it.dim));
+        pulse[k] = static_cast<uint8_t>(p);
+      }
+    }, 1);
+  // coordinates: origin and shift mask packed per halo slot, segments per domain
+  std::vector<uint32_t> om(H);
+  for (int64_t k = 0; k < H; ++k)
+    om[k] = static_cast<uint32_t>(origin_slot[k]) | (static_cast<uint32_t>(mask[k]) << kResOriginBits);
+  std::vector<ResSeg> segs;
+  const int64_t seg_len = int64_t{kResThreads} * resolved_per_thread(h, H, kResSlotsPerThread);
+  for (int r = 0; r < nd; ++r)
+    for (int64_t k = hbase[r]; k < hbase[r + 1]; k += seg_len) {
+      ResSeg sg;
+      sg.k = static_cast<int32_t>(k);
+      sg.slot = static_cast<int32_t>(h->dom_offset[r] + h->home[r] + (k - hbase[r]));
+      sg.n = static_cast<int32_t>(std::min<int64_t>(seg_len, hbase[r + 1] - k));
+      sg.pad = 0;
+      segs.push_back(sg);
+    }
+  // trees: one per home atom that has copies, numbered in home-slot order.
+  // A tree lies in its root's domain (every copy descends from the root), so
+  // the halo slots are grouped by root domain (stably: halo order kept) and
+  // each root domain's trees are built by one task, in a local array.
+  std::vector<int64_t> by_root_begin(nd + 1, 0);
+  for (int64_t k = 0; k < H; ++k) ++by_root_begin[root_dom[k] + 1];
+  for (int r = 0; r < nd; ++r) by_root_begin[r + 1] += by_root_begin[r];
+  std::vector<int32_t> by_root(H);
+  {
+    std::vector<int64_t> fill(by_root_begin.begin(), by_root_begin.end() - 1);
+    for (int64_t k = 0; k < H; ++k) by_root[fill[root_dom[k]]++] = static_cast<int32_t>(k);
+  }
+  std::vector<uint8_t> node_idx(H);
+  std::vector<std::vector<int4>> recs_of(nd);
+  std::vector<std::vector<TreeRec>> general_of(nd);
+  std::vector<int64_t> pairs_of(nd, 0), quads_of(nd, 0);
+  std::vector<char> overflow(nd, 0);
+  auto slot_of_halo = [&](int64_t k) {   // the global slot of halo index k
+    const int r = static_cast<int>(std::upper_bound(hbase.begin(), hbase.end(), k) - hbase.begin()) - 1;
+    return static_cast<int32_t>(h->dom_offset[r] + h->home[r] + (k - hbase[r]));
+  };
+  parallel_for(nd, [&](size_t ri) {
+    const int r0 = static_cast<int>(ri);
+    const int32_t* ks = by_root.data() + by_root_begin[r0];
+    const int64_t nk = by_root_begin[r0 + 1] - by_root_begin[r0];
+    std::vector<int32_t> tree_of(h->home[r0], -1);   // per home atom of r0
+    for (int64_t i = 0; i < nk; ++i) tree_of[origin_home[ks[i]] - home_base[r0]] = 0;   // marks the roots
+    int32_t n_trees = 0;
+    for (auto& t : tree_of)
+      if (t == 0) t = n_trees++;
+    std::vector<TreeRec> trees(static_cast<size_t>(n_trees));   // zero-filled
+    std::vector<uint8_t> add_pulse(trees.size() * kTreeNodes, 0);
+    for (int64_t i = 0; i < nk; ++i) {   // nodes: the root, then its copies in halo order
+      const int64_t k = ks[i];
+      TreeRec& rec = trees[tree_of[origin_home[k] - home_base[r0]]];
+      if (rec.n_nodes == 0) {
+        rec.node[0] = origin_slot[k];
+        rec.n_nodes = 1;
+      }
+      if (rec.n_nodes >= kTreeNodes) {   // more copies than a tree record holds
+        overflow[r0] = 1;
+        return;
+      }
+      node_idx[k] = static_cast<uint8_t>(rec.n_nodes);
+      rec.node[rec.n_nodes++] = slot_of_halo(k);
+    }
+    for (int64_t i = 0; i < nk; ++i) {   // adds: copy j (node j > 0) into its parent (same tree)
+      const int64_t k = ks[i];
+      const size_t t = static_cast<size_t>(tree_of[origin_home[k] - home_base[r0]]);
+      const int j = node_idx[k];
+      const int tg = parent_h[k] < 0 ? 0 : node_idx[parent_h[k]];
+      trees[t].ev[j - 1] = static_cast<uint8_t>(tg | (j << 4));
+      add_pulse[t * kTreeNodes + j - 1] = pulse[k];
+    }
+    std::vector<int4>& recs = recs_of[r0];
+    std::vector<TreeRec>& general = general_of[r0];
+    recs.reserve(trees.size());
+    for (size_t t = 0; t < trees.size(); ++t) {
+      TreeRec& rec = trees[t];
+      uint8_t* pu = add_pulse.data() + t * kTreeNodes;
+      const int m = rec.n_nodes - 1;
+      for (int a = 1; a < m; ++a)   // stable insertion sort by descending pulse
+        for (int b = a; b > 0 && pu[b] > pu[b - 1]; --b) {
+          std::swap(pu[b], pu[b - 1]);
+          std::swap(rec.ev[b], rec.ev[b - 1]);
+        }
+      // records in root order. A four-node tree is a quad when its last add
+      // (lowest pulse) is some copy u into the root and the two adds before
+      // it are one copy into the root and one copy into u: then the fixed
+      // order root += c, u += d, root += u is the staged order.
+      if (rec.n_nodes == 2) {
+        recs.push_back(make_int4(rec.node[0], rec.node[1], -1, -1));
+        ++pairs_of[r0];
+        continue;
+      }
+      if (rec.n_nodes == 4) {
+        const int tg2 = rec.ev[2] & 15, u = rec.ev[2] >> 4;
+        const int tg0 = rec.ev[0] & 15, s0 = rec.ev[0] >> 4, tg1 = rec.ev[1] & 15, s1 = rec.ev[1] >> 4;
+        if (tg2 == 0 && u != 0 && ((tg0 == 0 && tg1 == u) || (tg0 == u && tg1 == 0))) {
+          const int c = tg0 == 0 ? s0 : s1, d = tg0 == 0 ? s1 : s0;
+          recs.push_back(make_int4(rec.node[0], rec.node[u], rec.node[c], rec.node[d]));
+          ++quads_of[r0];
+          continue;
+        }
+      }
+      general.push_back(rec);
+    }
+  }, 1);
+  for (int r = 0; r < nd; ++r)
+    if (overflow[r]) return HX_ERR_PULSES;
+  std::vector<int4> recs;
+  std::vector<TreeRec> general;
+  int64_t n_pairs = 0, n_quads = 0;
+  for (int r = 0; r < nd; ++r) {   // domain after domain: root order overall
+    recs.insert(recs.end(), recs_of[r].begin(), recs_of[r].end());
+    general.insert(general.end(), general_of[r].begin(), general_of[r].end());
+    n_pairs += pairs_of[r];
+    n_quads += quads_of[r];
+  }
+  h->n_res_halo = H;
+  h->n_res_segs = static_cast<int64_t>(segs.size());
+  h->n_res_pairs = n_pairs;
+  h->n_res_quads = n_quads;
+  h->n_res_trees = static_cast<int64_t>(general.size());
+  HX_CUDA(dev_alloc(&h->d_res_om, om.size()));
+  HX_CUDA(dev_alloc(&h->d_res_segs, segs.size()));
+  HX_CUDA(dev_alloc(&h->d_res_recs, recs.size()));
+  HX_CUDA(dev_alloc(&h->d_res_trees, general.size()));
+  if (H > 0) {
+    HX_CUDA(cudaMemcpyAsync(h->d_res_om, om.data(), sizeof(uint32_t) * om.size(), cudaMemcpyHostToDevice, s));
+    HX_CUDA(cudaMemcpyAsync(h->d_res_segs, segs.data(), sizeof(ResSeg) * segs.size(), cudaMemcpyHostToDevice, s));
+  }
+  if (!recs.empty())
+    HX_CUDA(cudaMemcpyAsync(h->d_res_recs, recs.data(), sizeof(int4) * recs.size(), cudaMemcpyHostToDevice, s));
+  if (!general.empty())
+    HX_CUDA(cudaMemcpyAsync(h->d_res_trees, general.data(), sizeof(TreeRec) * general.size(),
+                            cudaMemcpyHostToDevice, s));
+  HX_CUDA(cudaStreamSynchronize(s));   // the host vectors go out of scope
+  return HX_OK;
+}
+
+// Range pieces of the host-buffer calls: every domain's home slots and halo
+// slots, cut into pieces of at most kCopyChunkWords words.
+int build_copy_chunks(hx_ctx* h) {
+  std::vector<CopyChunk> home, halo;
+  auto cut = [](std::vector<CopyChunk>& out, int64_t first_slot, int64_t slots) {
+    for (int64_t w = 0; w < 3 * slots; w += kCopyChunkWords) {
+      CopyChunk c;
+      c.word = 3 * first_slot + w;
+      c.n = static_cast<int32_t>(std::min<int64_t>(kCopyChunkWords, 3 * slots - w));
+      c.pad = 0;
+      out.push_back(c);
+    }
+  };
+  for (int r = 0; r < h->pl.ndom; ++r) {
+    cut(home, h->dom_offset[r], h->home[r]);
+    cut(halo, h->dom_offset[r] + h->home[r], h->halo[r]);
+  }
+  h->n_home_chunks = static_cast<int>(home.size());
+  h->n_halo_chunks = static_cast<int>(halo.size());
+  HX_CUDA(dev_alloc(&h->d_home_chunks, home.size()));
+  HX_CUDA(dev_alloc(&h->d_halo_chunks, halo.size()));
+  if (!home.empty())
+    HX_CUDA(cudaMemcpy(h->d_home_chunks, home.data(), sizeof(CopyChunk) * home.size(), cudaMemcpyHostToDevice));
+  if (!halo.empty())
+    HX_CUDA(cudaMemcpy(h->d_halo_chunks, halo.data(), sizeof(CopyChunk) * halo.size(), cudaMemcpyHostToDevice));
+  return HX_OK;
+}
+
+// Work tables of the fused and unfused kernels from the host copy of the plan.
+int build_tables(hx_ctx* h, cudaStream_t s) {
+  const Plan& pl = h->pl;
+  const int P = pl.n_pulses, nd = pl.ndom;
+  const int n_items = P * nd;
+  if (const int rc = build_copy_chunks(h); rc != HX_OK) return rc;
+  const bool fine = (h->flags & HX_FLAG_FINE_WAITS) != 0;
+  const bool ordered = !(h->flags & HX_FLAG_UNORDERED_FORCES);
+  std::vector<ItemInfo> items(std::max(n_items, 1));
+  for (int p = 0; p < P; ++p)
+    for (int r = 0; r < nd; ++r) {
+      const int t = p * nd + r;
+      ItemInfo& it = items[t];
+      it.r = r;
+      it.p = p;
+      it.q = h->t_recv[t];
+      it.src = h->dom_offset[r];
+      it.dst = h->dom_offset[it.q] + h->t_off[t];
+      it.map = h->t_map_off[t];
+      it.size = h->t_size[t];
+      it.split = h->t_split[t];
+      it.dim = pl.pulse_dim[p];
+      it.shift_flag = h->t_shift[t];
+    }
+  std::vector<int32_t> maps;
+  if ((fine || (h->flags & (HX_FLAG_TILES | HX_FLAG_SWEEP | HX_FLAG_SWEEP_FORCES | HX_FLAG_RESOLVED))) &&
+      h->total_entries > 0) {   // fine waits, units and resolved tables read the maps
+    maps.resize(h->total_entries);
+    // the maps were assembled on `s`, which need not synchronise with the legacy stream
+    HX_CUDA(cudaMemcpyAsync(maps.data(), h->d_maps, sizeof(int32_t) * h->total_entries, cudaMemcpyDeviceToHost, s));
+    HX_CUDA(cudaStreamSynchronize(s));
+  }
+  std::vector<int> upper_tab(static_cast<size_t>(nd) * std::max(P, 1));
+  for (int r = 0; r < nd; ++r)
+    for (int q = 0; q < P; ++q) upper_tab[static_cast<size_t>(r) * P + q] = neighbour(pl, r, pl.pulse_dim[q], +1);
+  auto upper = [&](int r, int q) { return upper_tab[static_cast<size_t>(r) * P + q]; };
+  std::vector<int64_t> rank(nd);
+  for (int r = 0; r < nd; ++r) rank[r] = domain_rank(pl, r);
+  h->family[0] = (h->flags & HX_FLAG_TILES)     ? kFamTiles
+                 : (h->flags & HX_FLAG_SWEEP)   ? kFamSweep
+                 : (h->flags & HX_FLAG_CLUSTER) ? kFamCluster
+                 : (h->flags & HX_FLAG_RESOLVED) ? kFamResolved
+                                                : kFamChunks;
+  h->family[1] = (h->flags & (HX_FLAG_SWEEP | HX_FLAG_SWEEP_FORCES)) ? kFamSweep : h->family[0];
+  for (int k = 0; k < 2; ++k) {
+    const int per_sm = std::max(1, h->family[k] == kFamTiles     ? tiles_blocks_per_sm(k)
+                                   : h->family[k] == kFamSweep   ? sweep_blocks_per_sm(k)
+                                   : h->family[k] == kFamCluster ? 1
+                                   : h->family[k] == kFamResolved ? 1
+                                                                 : max_blocks_per_sm(kernel_for(h, k)));
+    h->grid[k] = per_sm * h->sm_count;   // upper bound; trimmed to the work count below
+  }
+  // Unit lists. A dependent unit is placed a few resident windows after the
+  // units it waits for: tile mode three stages per block, sweep eight units
+  // per resident warp (measured on the 12M-atom workload: lags of 2, 3, 4, 6
+  // and 10 windows gave forces in 112.6, 100.5, 94.2, 92.2 and 92.2 us).
+  for (int dir = 0; dir < 2; ++dir) {
+    int rc = HX_OK;
+    if (h->family[dir] == kFamTiles) {
+      rc = build_tile_tables(h, items, maps, rank, kTile, kTileEntries, 3ll * h->grid[dir], kTile * 12 + 16,
+                             kTileEntries * 4 + 32 * kTileSegs, kTileEntries * 12 + 32 * kTileSegs, dir);
+    } else if (h->family[dir] == kFamSweep) {
+      if (P > kSweepSegs) return HX_ERR_PULSES;   // a unit's runs must fit one warp's stage
+      rc = build_tile_tables(h, items, maps, rank, kSweepSlots, kSweepEntries, 8ll * h->grid[dir] * kWarps,
+                             kSweepTileBytes, kSweepMapBytes, kSweepSrcBytes, dir);
+    }
+    if (rc != HX_OK) return rc;
+  }
+
+  for (int dir = 0; dir < 2; ++dir) {
+    if (h->family[dir] != kFamChunks) continue;
+    std::vector<Rec> recs;
+    std::vector<std::vector<int>> item_recs(std::max(n_items, 1));   // chunk records of each item, in entry order
+    auto add_part = [&](int t, int begin, int end, int halo_src, int stage, bool keep_empty) {
+      if (end <= begin && !keep_empty) return;
+      for (int b = begin;; b += kChunk) {
+        Rec rc;
+        rc.item = t;
+        rc.begin = b;
+        rc.end = std::min(end, b + kChunk);
+        rc.halo_src = halo_src;
+        rc.stage = stage;
+        rc.key = 0;
+        item_recs[t].push_back(static_cast<int>(recs.size()));
+        recs.push_back(std::move(rc));
+        if (b + kChunk >= end) break;
+      }
+    };
+    // chunk record of item t holding entry e (item_recs are in entry order)
+    auto rec_of_entry = [&](int t, int e) {
+      const std::vector<int>& v = item_recs[t];
+      int lo = 0, hi = static_cast<int>(v.size()) - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) / 2;
+        if (recs[v[mid]].begin <= e) lo = mid;
+        else hi = mid - 1;
+      }
+      return v[lo];
+    };
+    // Coarse waits may name empty items: those keep one empty chunk to signal.
+    std::vector<char> coarse_waited(std::max(n_items, 1), 0);
+    if (!fine) {
+      if (dir == 0) {
+        for (int p = 0; p < P; ++p)
+          for (int r = 0; r < nd; ++r)
+            if (items[p * nd + r].split < items[p * nd + r].size)
+              for (int q = 0; q < p; ++q) coarse_waited[q * nd + upper(r, q)] = 1;
+      } else {
+        for (int p = 0; p < P; ++p)
+          for (int r = 0; r < nd; ++r)
+            for (int pp = p + 1; pp < P; ++pp) {
+              coarse_waited[pp * nd + items[p * nd + r].q] = 1;
+              if (ordered) coarse_waited[pp * nd + r] = 1;
+            }
+      }
+    }
+    for (int p = 0; p < P; ++p)
+      for (int r = 0; r < nd; ++r) {
+        const int t = p * nd + r;
+        const ItemInfo& it = items[t];
+        if (dir == 0) {
+          add_part(t, 0, it.split, 0, 0, it.size == 0 && coarse_waited[t]);
+          add_part(t, it.split, it.size, 1, p, false);
+        } else {
+          add_part(t, 0, it.size, 1, P - 1 - p, it.size == 0 && coarse_waited[t]);
+        }
+      }
+    // waits (records are independent: spread over the host's cores)
+    parallel_for(recs.size(), [&](size_t ci) {
+      Rec& rc = recs[ci];
+      const ItemInfo& it = items[rc.item];
+      const int r = it.r, p = it.p;
+      if (dir == 0) {
+        if (!rc.halo_src) return;
+        if (!fine) {
+          for (int q = 0; q < p; ++q) rc.wait.push_back(q * nd + upper(r, q));
+          return;
+        }
+        // producers: chunks of (upper(r, q), q) that stored the slots read
+        // here. The entries ascend, r's receive ranges follow pulse order, and
+        // an item's records follow entry order, so both cursors only move on.
+        const int32_t* m = maps.data() + it.map;
+        int q = 0, k = 0;
+        for (int i = rc.begin; i < rc.end; ++i) {
+          while (q < p) {
+            const int tq = q * nd + upper(r, q);
+            if (m[i] < h->t_off[tq] + items[tq].size) break;
+            ++q;
+            k = 0;
+          }
+          if (q >= p) break;
+          const int tq = q * nd + upper(r, q);
+          const int64_t e = m[i] - h->t_off[tq];
+          if (e < 0) continue;   // a home slot (cannot occur in a forwarded tail)
+          const std::vector<int>& v = item_recs[tq];
+          while (k + 1 < static_cast<int>(v.size()) && recs[v[k + 1]].begin <= e) ++k;
+          if (rc.wait.empty() || rc.wait.back() != v[k]) rc.wait.push_back(v[k]);
+        }
+      } else {
+        if (!fine) {
+          for (int pp = p + 1; pp < P; ++pp) {
+            rc.wait.push_back(pp * nd + it.q);
+            if (ordered && it.q != r) rc.wait.push_back(pp * nd + r);
+          }
+          std::sort(rc.wait.begin(), rc.wait.end());
+          rc.wait.erase(std::unique(rc.wait.begin(), rc.wait.end()), rc.wait.end());
+          return;
+        }
+        if (rc.end <= rc.begin) return;
+        const int32_t* m = maps.data() + it.map;
+        const int64_t slot_lo = h->t_off[rc.item] + rc.begin, slot_hi = h->t_off[rc.item] + rc.end;
+        for (int pp = p + 1; pp < P; ++pp) {
+          // later-pulse chunks of the receiver that add into the slots read here
+          const int tq = pp * nd + it.q;
+          const int32_t* mq = maps.data() + items[tq].map;
+          const int nq = items[tq].size;
+          const int i1 = static_cast<int>(std::lower_bound(mq, mq + nq, static_cast<int32_t>(slot_lo)) - mq);
+          const int i2 = static_cast<int>(std::lower_bound(mq, mq + nq, static_cast<int32_t>(slot_hi)) - mq);
+          if (i1 < i2) {
+            const int c1 = rec_of_entry(tq, i1), c2 = rec_of_entry(tq, i2 - 1);
+            for (int c = c1; c <= c2; ++c) rc.wait.push_back(c);   // records of one item are consecutive
+          }
+          if (!ordered) continue;
+          // later-pulse chunks of the sender that add into the same targets
+          const int tr = pp * nd + r;
+          const int32_t* mr = maps.data() + items[tr].map;
+          const int nr = items[tr].size;
+          int k = static_cast<int>(std::lower_bound(mr, mr + nr, m[rc.begin]) - mr);
+          if (k >= nr) continue;
+          const std::vector<int>& v = item_recs[tr];
+          int rec = 0;
+          const int first = rec_of_entry(tr, k);
+          while (v[rec] != first) ++rec;
+          for (int i = rc.begin; i < rc.end && k < nr; ++i) {
+            while (k < nr && mr[k] < m[i]) ++k;
+            if (k < nr && mr[k] == m[i]) {
+              while (rec + 1 < static_cast<int>(v.size()) && recs[v[rec + 1]].begin <= k) ++rec;
+              if (rc.wait.empty() || rc.wait.back() != v[rec]) rc.wait.push_back(v[rec]);
+            }
+          }
+        }
+      }
+      std::sort(rc.wait.begin(), rc.wait.end());
+      rc.wait.erase(std::unique(rc.wait.begin(), rc.wait.end()), rc.wait.end());
+    });
+    // listing dependencies (chunk records) and who gets signalled
+    std::vector<char> rec_waited(recs.size(), 0), item_waited(std::max(n_items, 1), 0);
+    for (auto& rc : recs) {
+      if (fine) {
+        rc.deps = rc.wait;
+        for (int d : rc.wait) rec_waited[d] = 1;
+      } else {
+        for (int t : rc.wait) {
+          item_waited[t] = 1;
+          rc.deps.insert(rc.deps.end(), item_recs[t].begin(), item_recs[t].end());
+        }
+      }
+    }
+    // priority: base order (domain rank, stage, pulse, entry), then a lag of
+    // one resident-warp window per stage
+    {
+      std::vector<int> base(recs.size());
+      for (size_t i = 0; i < recs.size(); ++i) base[i] = static_cast<int>(i);
+      std::sort(base.begin(), base.end(), [&](int a, int b) {
+        const Rec& x = recs[a];
+        const Rec& y = recs[b];
+        const ItemInfo& ix = items[x.item];
+        const ItemInfo& iy = items[y.item];
+        if (rank[ix.r] != rank[iy.r]) return rank[ix.r] < rank[iy.r];
+        if (x.stage != y.stage) return x.stage < y.stage;
+        if (ix.p != iy.p) return ix.p < iy.p;
+        return x.begin < y.begin;
+      });
+      const long long window = static_cast<long long>(h->grid[dir]) * kWarps;
+      for (size_t k = 0; k < base.size(); ++k)
+        recs[base[k]].key = static_cast<long long>(k) + window * recs[base[k]].stage;
+    }
+    std::vector<int> order = order_chunks(recs);
+    if (order.size() != recs.size()) return HX_ERR_STATE;
+    std::vector<int> pos(recs.size());
+    for (size_t k = 0; k < order.size(); ++k) pos[order[k]] = static_cast<int>(k);
+    std::vector<int> item_chunks(std::max(n_items, 1), 0);
+    for (auto& rc : recs) item_chunks[rc.item] += 1;
+    std::vector<Chunk> chunks;
+    std::vector<Wait> waits;
+    chunks.reserve(order.size());
+    for (int ri : order) {
+      const Rec& rc = recs[ri];
+      const ItemInfo& it = items[rc.item];
+      Chunk ch;
+      std::memset(&ch, 0, sizeof(ch));
+      ch.src = it.src;
+      ch.dst = it.dst + rc.begin;
+      ch.map = it.map + rc.begin;
+      ch.n = rc.end - rc.begin;
+      ch.item = rc.item;
+      ch.item_chunks = item_chunks[rc.item];
+      ch.wait_off = static_cast<int32_t>(waits.size());
+      ch.wait_cnt = static_cast<int32_t>(rc.wait.size());
+      for (int w : rc.wait) waits.push_back(fine ? Wait{pos[w], 1} : Wait{w, 0});
+      const bool sig = fine ? rec_waited[ri] != 0 : item_waited[rc.item] != 0;
+      ch.flags = (rc.halo_src ? kHaloSrc : 0) | (sig ? kSignal : 0) | (dir == 0 && it.shift_flag ? kShift : 0);
+      ch.dim = it.dim;
+      ch.shift = pl.boxf[it.dim];
+      chunks.push_back(ch);
+    }
+    if (!fine)
+      for (auto& w : waits) w.chunks = item_chunks[w.item];
+    h->n_chunks[dir] = static_cast<int>(chunks.size());
+    HX_CUDA(dev_alloc(&h->d_chunks[dir], chunks.size()));
+    HX_CUDA(dev_alloc(&h->d_waits[dir], waits.size()));
+    if (!chunks.empty())
+      HX_CUDA(cudaMemcpy(h->d_chunks[dir], chunks.data(), sizeof(Chunk) * chunks.size(), cudaMemcpyHostToDevice));
+    if (!waits.empty())
+      HX_CUDA(cudaMemcpy(h->d_waits[dir], waits.data(), sizeof(Wait) * waits.size(), cudaMemcpyHostToDevice));
+  }
+
+  if (h->family[0] == kFamResolved) {
+    const int rc = build_resolved_tables(h, items, maps, s);
+    if (rc != HX_OK) return rc;
+  }
+
+  // Unfused: per pulse, every item's entries in sender order, no waits or signals.
+  std::vector<Chunk> uch;
+  h->u_begin.assign(P + 1, 0);
+  for (int p = 0; p < P; ++p) {
+    h->u_begin[p] = static_cast<int>(uch.size());
+    for (int r = 0; r < nd; ++r) {
+      const ItemInfo& it = items[p * nd + r];
+      for (int cb = 0; cb < it.size; cb += kChunk) {
+        Chunk ch;
+        std::memset(&ch, 0, sizeof(ch));
+        ch.src = it.src;
+        ch.dst = it.dst + cb;
+        ch.map = it.map + cb;
+        ch.n = std::min(it.size - cb, kChunk);
+        ch.item = p * nd + r;
+        ch.flags = kHaloSrc | (it.shift_flag ? kShift : 0);
+        ch.dim = it.dim;
+        ch.shift = pl.boxf[it.dim];
+        uch.push_back(ch);
+      }
+    }
+  }
+  h->u_begin[P] = static_cast<int>(uch.size());
+  HX_CUDA(dev_alloc(&h->d_uchunks, uch.size()));
+  if (!uch.empty())
+    HX_CUDA(cudaMemcpy(h->d_uchunks, uch.data(), sizeof(Chunk) * uch.size(), cudaMemcpyHostToDevice));
+
+  // one flag (and one election counter) per item or per chunk, per direction
+  h->n_flags = std::max<size_t>({static_cast<size_t>(std::max(n_items, 1)), static_cast<size_t>(h->n_chunks[0]),
+                                 static_cast<size_t>(h->n_chunks[1]), static_cast<size_t>(h->n_units[0]),
+                                 static_cast<size_t>(h->n_units[1])});
+  HX_CUDA(dev_alloc(&h->d_flags, 2 * h->n_flags));
+  HX_CUDA(dev_alloc(&h->d_blk, 2 * h->n_flags));
+  HX_CUDA(dev_alloc(&h->d_ctrl, 2));
+  // Persistent grid: every warp (tile mode: every block) co-resident, and no
+  // more of them than there is work.
+  for (int k = 0; k < 2; ++k) {
+    if (h->family[k] == kFamResolved) {
+      // coordinates: one block per halo segment; forces: general blocks, then record blocks
+      const int64_t n = h->n_res_pairs + h->n_res_quads;
+      const int64_t fb = resolved_blocks(n, resolved_per_thread(h, n, kResTreesPerThread)) +
+                         resolved_blocks(h->n_res_trees, 1);
+      h->grid[k] = static_cast<int>(std::max<int64_t>(1, k == 0 ? h->n_res_segs : fb));
+    } else if (h->family[k] == kFamCluster) {
+      h->grid[k] = kClusterCtas;   // exactly one cluster
+    } else if (h->family[k] == kFamTiles) {
+      h->grid[k] = std::max(1, std::min(h->n_units[k], h->grid[k]));
+    } else if (h->family[k] == kFamSweep) {   // one warp per batch of units
+      const int warps = std::max(1, std::min((h->n_units[k] + kSweepBatch - 1) / kSweepBatch, h->grid[k] * kWarps));
+      h->grid[k] = (warps + kWarps - 1) / kWarps;
+    } else {
+      const int warps = std::max(1, std::min(h->n_chunks[k], h->grid[k] * kWarps));
+      h->grid[k] = (warps + kWarps - 1) / kWarps;
+    }
+  }
+  return reset_signals(h, s);
+}
+
+}  // namespace hx_rt
