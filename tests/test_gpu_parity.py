@@ -491,3 +491,37 @@ def test_host_buffer_misaligned():
     c.hx.exchange_forces_host(fh, torch.empty_like(dev))
     torch.cuda.synchronize()
     assert np.array_equal(_bits(fh.numpy()[hm]), _bits(fref[hm]))
+
+
+def _random_shape(seed):
+    """A seeded random decomposition: 1-4 slabs per dimension, slab widths
+    0.4-3 nm, a cutoff below (n_d - 1) slab widths wherever n_d > 1, and
+    0-20000 atoms."""
+    rng = np.random.default_rng(1000 + seed)
+    dims = [int(v) for v in rng.integers(1, 5, 3)]
+    width = [float(v) for v in rng.uniform(0.4, 3.0, 3)]
+    box = tuple(round(dims[d] * width[d], 3) for d in range(3))
+    cutoff = float(rng.uniform(0.3, 1.5))
+    limits = [box[d] / dims[d] * (dims[d] - 1) for d in range(3) if dims[d] > 1]
+    if limits:
+        cutoff = min(cutoff, 0.95 * min(limits))
+    n = int(rng.integers(0, 20000))
+    return W.custom(f"random{seed}", n, box, tuple(dims), cutoff, seed=2000 + seed,
+                    forces_law="normal" if seed % 2 else "uniform")
+
+
+@pytest.mark.parametrize("seed", range(32))
+@pytest.mark.parametrize("flags", [0, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE | HX.HX_FLAG_SWEEP_FORCES,
+                                   HX.HX_FLAG_RESOLVED | HX.HX_FLAG_PDL, HX.HX_FLAG_FINE_WAITS])
+def test_random_shapes(seed, flags):
+    w = _random_shape(seed)
+    pulse_dims, _ = HX.query_plan(w.box, w.dims, w.cutoff)
+    copies_bound = int(np.prod([1 + int(np.sum(pulse_dims == d)) for d in range(3)]))
+    try:
+        c = Case(w, flags=flags)
+    except HX.HXError as e:   # resolved tables hold at most 7 copies per atom
+        assert flags & HX.HX_FLAG_RESOLVED and copies_bound > 8 and e.code == HX.HX_ERR_PULSES
+        return
+    check_build(c)
+    check_coord_steps(c)
+    check_force_steps(c)
