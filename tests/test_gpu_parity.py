@@ -511,8 +511,7 @@ def _random_shape(seed):
 
 
 @pytest.mark.parametrize("seed", range(32))
-@pytest.mark.parametrize("flags", [0, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE | HX.HX_FLAG_SWEEP_FORCES,
-                                   HX.HX_FLAG_RESOLVED | HX.HX_FLAG_PDL, HX.HX_FLAG_FINE_WAITS])
+@pytest.mark.parametrize("flags", ALL_MODES + [HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE | HX.HX_FLAG_SWEEP_FORCES])
 def test_random_shapes(seed, flags):
     w = _random_shape(seed)
     pulse_dims, _ = HX.query_plan(w.box, w.dims, w.cutoff)
