@@ -665,6 +665,14 @@ def run_reference(args):
         o.exchange_forces(f)
     el = time.perf_counter() - t0
     us_step = el / args.steps * 1e6 * scale
+    # the same loops with each pulse's senders on every host core (reported
+    # beside the one-core value; bit-identical results)
+    threads = min(os.cpu_count() or 1, o.max_threads())
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        o.exchange_coords_par(x, threads)
+        o.exchange_forces_par(f, threads)
+    us_all = (time.perf_counter() - t0) / args.steps * 1e6 * scale
     sample = (f"full {w.name} each step" if sw is w else
               f"{sw.describe()} each step ({o.total_entries} of {full_entries} map entries, same per-domain "
               f"geometry), scaled by the entry ratio {scale:.3f}")
@@ -675,7 +683,8 @@ def run_reference(args):
         "config": {"workload": workload_label(w), "map_entries": full_entries},
         "impl": "reference",
         "cpu_baseline": {"value": round(us_step, 1), "unit": "us/step", "kind": "oracle", "cores": 1,
-                         "sample": sample},
+                         "sample": sample,
+                         "all_cores": {"value": round(us_all, 1), "unit": "us/step", "cores": threads}},
         "e2e": {"value": round(us_step, 1), "unit": "us/step", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(out), flush=True)
