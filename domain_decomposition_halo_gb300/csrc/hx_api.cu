@@ -296,9 +296,12 @@ int launch(hx_ctx* h, int kind, float* buf, cudaStream_t s) {
     args = args2;
     grid = dim3(static_cast<unsigned>(h->grid[kind]));
   }
-  if (kind != 2 && h->family[kind] == kFamResolved && (h->flags & HX_FLAG_PDL)) {
+  if (kind != 2 && (h->family[kind] == kFamResolved || h->family[kind] == kFamChunks) && (h->flags & HX_FLAG_PDL)) {
     // direct launch that may start while the stream's previous kernel finishes;
-    // the resolved kernels wait for it (griddepcontrol.wait) before touching data
+    // the resolved and chunk kernels wait for it (griddepcontrol.wait) before
+    // touching data. Not the slot sweep: on the 12M-atom workload its
+    // persistent grid timed out under programmatic launch (a producer unit's
+    // signal never came), so it keeps plain stream order.
     cudaLaunchAttribute attr[1];
     std::memset(attr, 0, sizeof(attr));
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -70,6 +70,13 @@ __device__ __forceinline__ unsigned atom_inc_acq_rel(unsigned* p, unsigned mod) 
   return old;
 }
 
+// Programmatic dependent launch (HX_FLAG_PDL): let the stream's next kernel
+// be scheduled now, and wait for the previous kernel to complete before
+// reading or claiming anything. Both are no-ops in a launch without the
+// programmatic-serialization attribute.
+__device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void wait_prerequisites() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ unsigned long long global_timer_ns() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -357,6 +364,8 @@ __device__ __forceinline__ void run_warps(float* __restrict__ buf, const DirPara
   const unsigned long long W = static_cast<unsigned long long>(gridDim.x) * kWarps;
   const unsigned long long N = P.n_chunks;
   unsigned long long c = static_cast<unsigned long long>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+  allow_dependents();
+  wait_prerequisites();   // before the first ticket, flag or buffer access
   if (c >= N) return;
   const int drop_item = *reinterpret_cast<const volatile int*>(&P.ctrl->drop_item);
   unsigned long long base = ~0ull;   // first ticket of this launch: (epoch - 1) * N

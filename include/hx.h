@@ -115,11 +115,14 @@ typedef struct hx_ctx* hx_handle;
                                           "Optimizing for efficient transfers across NVIDIA
                                           NVLink-connected GPUs"); same results bit for bit. Applies
                                           where the chunk kernels run the coordinates */
-#define HX_FLAG_PDL 0x400u             /* with HX_FLAG_RESOLVED: launch the exchanges directly with
-                                          programmatic dependent launch, so a resolved exchange may be
+#define HX_FLAG_PDL 0x400u             /* launch the resolved and chunk kernels directly with
+                                          programmatic dependent launch, so an exchange may be
                                           scheduled while the stream's previous kernel finishes (it
-                                          reads its build-time tables, then waits for that kernel before
-                                          touching coordinates or forces); ignored by other modes */
+                                          waits for that kernel before claiming work or touching
+                                          coordinates, forces or flags; resolved kernels read their
+                                          build-time tables first). The slot sweep, tile and cluster
+                                          kernels keep plain stream order: the sweep's persistent grid
+                                          timed out under programmatic launch on a 12M-atom workload */
 #define HX_FLAG_RESOLVED 0x100u        /* the forwarding unrolled at build time: every halo slot is
                                           gathered straight from its origin home atom (plus the
                                           shifts its path added), and every home atom's force tree

@@ -24,7 +24,10 @@ ALL_MODES = [0, HX.HX_FLAG_COUNTER_SIGNAL, HX.HX_FLAG_NO_GRAPH,
              HX.HX_FLAG_CLUSTER | HX.HX_FLAG_NO_GRAPH, HX.HX_FLAG_RESOLVED,
              HX.HX_FLAG_RESOLVED | HX.HX_FLAG_NO_GRAPH, HX.HX_FLAG_RESOLVED | HX.HX_FLAG_SWEEP_FORCES,
              HX.HX_FLAG_BULK_STORE, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE,
-             HX.HX_FLAG_COUNTER_SIGNAL | HX.HX_FLAG_BULK_STORE, HX.HX_FLAG_RESOLVED | HX.HX_FLAG_PDL]
+             HX.HX_FLAG_COUNTER_SIGNAL | HX.HX_FLAG_BULK_STORE, HX.HX_FLAG_RESOLVED | HX.HX_FLAG_PDL,
+             HX.HX_FLAG_PDL, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_PDL,
+             HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE | HX.HX_FLAG_PDL,
+             HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE | HX.HX_FLAG_SWEEP_FORCES | HX.HX_FLAG_PDL]
 
 
 def _bits(a):
@@ -387,23 +390,27 @@ def test_dropped_signal_times_out_and_recovers(direction, flags):
 
 @pytest.mark.parametrize("name", ["C4", "C5"])
 @pytest.mark.parametrize("flags", [HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE | HX.HX_FLAG_SWEEP_FORCES,
-                                   HX.HX_FLAG_RESOLVED | HX.HX_FLAG_PDL])
+                                   HX.HX_FLAG_RESOLVED | HX.HX_FLAG_PDL,
+                                   HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE | HX.HX_FLAG_PDL,
+                                   HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_PDL, HX.HX_FLAG_PDL,
+                                   HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE | HX.HX_FLAG_SWEEP_FORCES |
+                                   HX.HX_FLAG_PDL])
 def test_back_to_back_steps(name, flags):
-    """Twenty coordinate + force exchanges queued back to back on one stream
+    """Forty coordinate + force exchanges queued back to back on one stream
     (no synchronisation between them, so consecutive launches may overlap
-    their start-up) give the oracle's result of the same twenty steps, bit
+    their start-up) give the oracle's result of the same forty steps, bit
     for bit: coordinates are idempotent, forces accumulate every step."""
     c = Case(W.WORKLOADS[name], flags=flags)
     x = c.o.coords().copy()
     f = W.forces(c.w, c.o.total_slots)
     xt = torch.from_numpy(x).cuda()
     ft = torch.from_numpy(f).cuda()
-    for _ in range(20):
+    for _ in range(40):
         c.hx.exchange_coords(xt)
         c.hx.exchange_forces(ft)
     torch.cuda.synchronize()
     assert c.hx.status()[0] == 0
-    for _ in range(20):
+    for _ in range(40):
         c.o.exchange_coords(x)
         c.o.exchange_forces(f)
     assert np.array_equal(_bits(xt.cpu().numpy()), _bits(x))
