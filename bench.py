@@ -50,7 +50,7 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU baseline budget")
     ap.add_argument("--flags", default="fine,bulkstore,sweepf",
                     help="comma list of libhx modes: fine, bulkstore (coordinates packed by bulk stores), sweepf "
-                         "(forces by the slot sweep), sweep, tiles, cluster, resolved, counter, nograph, unordered, "
+                         "(forces by the slot sweep), sweep, cluster, resolved, counter, nograph, unordered, "
                          "pages (= none)")
     return ap.parse_args()
 
@@ -58,7 +58,7 @@ def parse_args():
 def hx_flags(spec: str) -> int:
     from domain_decomposition_halo_gb300 import hx as HX
     table = {"fine": HX.HX_FLAG_FINE_WAITS, "counter": HX.HX_FLAG_COUNTER_SIGNAL, "nograph": HX.HX_FLAG_NO_GRAPH,
-             "unordered": HX.HX_FLAG_UNORDERED_FORCES, "tiles": HX.HX_FLAG_TILES, "sweep": HX.HX_FLAG_SWEEP,
+             "unordered": HX.HX_FLAG_UNORDERED_FORCES, "sweep": HX.HX_FLAG_SWEEP,
              "sweepf": HX.HX_FLAG_SWEEP_FORCES, "cluster": HX.HX_FLAG_CLUSTER,
              "resolved": HX.HX_FLAG_RESOLVED, "bulkstore": HX.HX_FLAG_BULK_STORE,
              "pdl": HX.HX_FLAG_PDL, "pages": 0, "": 0}
@@ -126,8 +126,6 @@ def kernel_source_digest():
 def kernel_impl(flags: int, direction: int) -> str:
     """The device function that runs a direction's fused exchange under `flags`."""
     from domain_decomposition_halo_gb300 import hx as HX
-    if flags & HX.HX_FLAG_TILES:
-        return f"k_tiles<{direction}> (tile pipeline)"
     if flags & HX.HX_FLAG_SWEEP or (direction == 1 and flags & HX.HX_FLAG_SWEEP_FORCES):
         return f"k_sweep<{direction}> (slot sweep)"
     if flags & HX.HX_FLAG_CLUSTER:
@@ -450,7 +448,7 @@ def secondary(hx_main, coords, forces, w_main, dev, peak, flags):
 
     # the probe in the run's modes, and with both directions on the chunk kernels
     from domain_decomposition_halo_gb300 import hx as HX
-    chunk_flags = flags & ~(HX.HX_FLAG_SWEEP | HX.HX_FLAG_SWEEP_FORCES | HX.HX_FLAG_TILES)
+    chunk_flags = flags & ~(HX.HX_FLAG_SWEEP | HX.HX_FLAG_SWEEP_FORCES)
     res = {"overlap_with_local_kernel_us": {"run_modes": overlap_probe(dev, flags)}}
     if chunk_flags != flags:
         res["overlap_with_local_kernel_us"]["chunk_kernels"] = overlap_probe(dev, chunk_flags)

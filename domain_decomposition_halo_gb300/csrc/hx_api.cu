@@ -175,8 +175,8 @@ const void* kernel_for(hx_ctx* h, int kind) {
 
 // Launch a fused exchange (kind 0/1) or the no-op (kind 2): directly, or via
 // a cached single-node graph keyed by (kind, buffer pointer).
-TileParams tile_params(hx_ctx* h, int dir) {
-  TileParams P;
+UnitParams unit_params(hx_ctx* h, int dir) {
+  UnitParams P;
   std::memset(&P, 0, sizeof(P));
   P.units = h->d_units[dir];
   P.extra = h->d_segs[dir];
@@ -200,7 +200,6 @@ int work_items(const hx_ctx* h, int dir) {
 
 // Launch shape of a direction's fused kernel.
 const void* fused_kernel(hx_ctx* h, int dir) {
-  if (h->family[dir] == kFamTiles) return tiles_kernel(dir);
   if (h->family[dir] == kFamSweep) return sweep_kernel(dir);
   if (h->family[dir] == kFamCluster) return cluster_kernel(dir);
   if (h->family[dir] == kFamResolved) return resolved_kernel(dir);
@@ -209,7 +208,7 @@ const void* fused_kernel(hx_ctx* h, int dir) {
 unsigned fused_threads(const hx_ctx* h, int dir) {
   if (h->family[dir] == kFamCluster) return kClusterThreads;
   if (h->family[dir] == kFamResolved) return kResThreads;
-  return h->family[dir] == kFamTiles ? kTileThreads : kThreads;
+  return kThreads;
 }
 
 // Blocks of kResThreads threads that hold n items at `per` items a thread.
@@ -249,14 +248,14 @@ ClusterParams cluster_params(hx_ctx* h) {
   return P;
 }
 size_t fused_smem(const hx_ctx* h, int dir) {
-  if (h->family[dir] == kFamTiles) return tiles_smem_bytes(dir);
   if (h->family[dir] == kFamSweep) return sweep_smem_bytes(dir);
+  if (h->family[dir] == kFamChunks) return chunk_smem_bytes(dir, dir == 0 && (h->flags & HX_FLAG_BULK_STORE));
   return 0;
 }
 
 int launch(hx_ctx* h, int kind, float* buf, cudaStream_t s) {
   DirParams P;
-  TileParams TP;
+  UnitParams TP;
   ClusterParams CP;
   ResolvedParams RP;
   void* args2[2];
@@ -281,7 +280,7 @@ int launch(hx_ctx* h, int kind, float* buf, cudaStream_t s) {
     block = dim3(kClusterThreads);
     fn = cluster_kernel(kind);
   } else if (kind != 2 && h->family[kind] != kFamChunks) {
-    TP = tile_params(h, kind);
+    TP = unit_params(h, kind);
     args2[0] = &buf;
     args2[1] = &TP;
     args = args2;
@@ -295,6 +294,7 @@ int launch(hx_ctx* h, int kind, float* buf, cudaStream_t s) {
     args2[1] = &P;
     args = args2;
     grid = dim3(static_cast<unsigned>(h->grid[kind]));
+    smem = fused_smem(h, kind);
   }
   if (kind != 2 && (h->family[kind] == kFamResolved || h->family[kind] == kFamChunks) && (h->flags & HX_FLAG_PDL)) {
     // direct launch that may start while the stream's previous kernel finishes;
@@ -579,7 +579,13 @@ int build(hx_ctx* h, const float* pos, int64_t n, float* coords, int64_t capacit
 
 // ------------------------------------------------------------------ scratch-free launch
 
-int hx::handle_device(const hx_ctx* h) { return h->device; }
+const void* hx::static_kernel(const hx_ctx* h) {
+  if (!h->built || h->pl.n_pulses == 0) return nullptr;
+  hx_ctx* m = const_cast<hx_ctx*>(h);
+  if (h->family[0] == kFamResolved) return resolved_kernel(0);
+  if (h->family[0] == kFamCluster) return cluster_kernel(0);
+  return h->family[0] != kFamChunks ? fused_kernel(m, 0) : kernel_for(m, 0);
+}
 
 int hx::launch_coords_with_scratch(hx_ctx* h, float* coords, cudaStream_t s, Ctrl* ctrl,
                                    unsigned long long* flags, unsigned int* arrivals, size_t max_flags) {
@@ -602,17 +608,18 @@ int hx::launch_coords_with_scratch(hx_ctx* h, float* coords, cudaStream_t s, Ctr
   const size_t need = std::max<size_t>(static_cast<size_t>(h->pl.n_pulses) * h->pl.ndom, static_cast<size_t>(work));
   if (need > max_flags) return HX_ERR_CAPACITY;
   HX_CUDA(cudaMemsetAsync(ctrl, 0, sizeof(Ctrl), s));
-  HX_CUDA(cudaMemsetAsync(&ctrl->drop_item, 0xff, sizeof(int), s));   // -1: no fault injection
+  // the handle's fault-injection item (hx_debug_drop_signal; -1: none), device to device
+  HX_CUDA(cudaMemcpyAsync(&ctrl->drop_item, &h->d_ctrl[0].drop_item, sizeof(int), cudaMemcpyDeviceToDevice, s));
   HX_CUDA(cudaMemsetAsync(flags, 0, sizeof(unsigned long long) * need, s));
   HX_CUDA(cudaMemsetAsync(arrivals, 0, sizeof(unsigned int) * need, s));
   void* args[2];
   DirParams P;
-  TileParams TP;
+  UnitParams TP;
   const void* fn;
   size_t smem = 0;
   args[0] = &coords;
   if (h->family[0] != kFamChunks) {
-    TP = tile_params(h, 0);
+    TP = unit_params(h, 0);
     TP.flags = flags;
     TP.ctrl = ctrl;
     args[1] = &TP;
@@ -625,6 +632,7 @@ int hx::launch_coords_with_scratch(hx_ctx* h, float* coords, cudaStream_t s, Ctr
     P.ctrl = ctrl;
     args[1] = &P;
     fn = kernel_for(h, 0);
+    smem = fused_smem(h, 0);
   }
   return to_err(cudaLaunchKernel(fn, dim3(static_cast<unsigned>(h->grid[0])), dim3(fused_threads(h, 0)),
                                 args, smem, s));
@@ -666,21 +674,23 @@ int hx_init(hx_handle* out, const double box[3], const int dims[3], double cutof
             unsigned timeout_us) {
   if (!out) return HX_ERR_ARG;
   *out = nullptr;
+  if (flags & ~HX_FLAGS_ALL) return HX_ERR_ARG;
   Plan pl;
   int rc = make_plan(box, dims, cutoff, &pl);
   if (rc != HX_OK) return rc;
   int ndev = 0;
   if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) return HX_ERR_CUDA;
-  if (cudaSetDevice(device) != cudaSuccess) return HX_ERR_CUDA;
+  DeviceGuard guard(device);
+  if (!guard.ok()) return HX_ERR_CUDA;
   hx_ctx* h = new (std::nothrow) hx_ctx();
   if (!h) return HX_ERR_NOMEM;
   h->pl = pl;
   h->device = device;
   // at most one kernel family for the coordinates (forces follow it), and
   // HX_FLAG_SWEEP_FORCES only over the chunk or resolved coordinate kernels
-  const unsigned families = flags & (HX_FLAG_TILES | HX_FLAG_SWEEP | HX_FLAG_CLUSTER | HX_FLAG_RESOLVED);
+  const unsigned families = flags & (HX_FLAG_SWEEP | HX_FLAG_CLUSTER | HX_FLAG_RESOLVED);
   const bool sweep_forces_clash =
-      (flags & HX_FLAG_SWEEP_FORCES) && (flags & (HX_FLAG_TILES | HX_FLAG_SWEEP | HX_FLAG_CLUSTER));
+      (flags & HX_FLAG_SWEEP_FORCES) && (flags & (HX_FLAG_SWEEP | HX_FLAG_CLUSTER));
   if ((families & (families - 1)) || sweep_forces_clash) {
     delete h;
     return HX_ERR_ARG;
@@ -698,12 +708,14 @@ int hx_init(hx_handle* out, const double box[3], const int dims[3], double cutof
 int hx_build_maps(hx_handle h, const float* pos_in, int64_t n_atoms, float* coords, int64_t capacity,
                   int64_t* needed, void* stream) {
   if (!h || n_atoms < 0 || n_atoms > INT32_MAX || (n_atoms > 0 && !pos_in)) return HX_ERR_ARG;
-  if (cudaSetDevice(h->device) != cudaSuccess) return HX_ERR_CUDA;
+  DeviceGuard guard(h->device);
+  if (!guard.ok()) return HX_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   free_tables(h);
   const int rc = build(h, pos_in, n_atoms, coords, capacity, s);
   if (rc == HX_OK || rc == HX_ERR_CAPACITY) {
     if (needed) *needed = h->total_slots;
+    static_prepare(h);   // on failure the static call reports HX_ERR_CUDA; the regular path is unaffected
     return rc;
   }
   free_tables(h);
@@ -712,20 +724,13 @@ int hx_build_maps(hx_handle h, const float* pos_in, int64_t n_atoms, float* coor
 
 namespace {
 
-int ensure_device(hx_ctx* h) {
-  int cur = -1;
-  if (cudaGetDevice(&cur) != cudaSuccess) return HX_ERR_CUDA;
-  if (cur != h->device && cudaSetDevice(h->device) != cudaSuccess) return HX_ERR_CUDA;
-  return HX_OK;
-}
-
 int exchange(hx_handle h, float* buf, void* stream, int kind) {
   if (!h) return HX_ERR_ARG;
   if (!h->built) return HX_ERR_STATE;
   if (!buf && h->total_slots > 0) return HX_ERR_ARG;   // an empty layout touches no memory
   if (h->pl.n_pulses == 0 || work_items(h, kind) == 0) return HX_OK;   // nothing moves
-  const int rc = ensure_device(h);
-  if (rc != HX_OK) return rc;
+  DeviceGuard guard(h->device);
+  if (!guard.ok()) return HX_ERR_CUDA;
   return launch(h, kind, buf, static_cast<cudaStream_t>(stream));
 }
 
@@ -753,8 +758,9 @@ int exchange_host(hx_handle h, float* host, float* dev, void* stream, int kind) 
   if (!h->built) return HX_ERR_STATE;
   if (h->total_slots == 0) return HX_OK;
   if (!host || !dev) return HX_ERR_ARG;
-  int rc = ensure_device(h);
-  if (rc != HX_OK) return rc;
+  DeviceGuard guard(h->device);
+  if (!guard.ok()) return HX_ERR_CUDA;
+  int rc = HX_OK;
   float* hv = nullptr;
   if ((rc = device_view(host, &hv)) != HX_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -784,8 +790,9 @@ int hx_exchange_coords_unfused(hx_handle h, float* coords, void* stream) {
   if (!h) return HX_ERR_ARG;
   if (!h->built) return HX_ERR_STATE;
   if (!coords && h->total_slots > 0) return HX_ERR_ARG;
-  int rc = ensure_device(h);
-  if (rc != HX_OK) return rc;
+  DeviceGuard guard(h->device);
+  if (!guard.ok()) return HX_ERR_CUDA;
+  int rc = HX_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   for (int p = 0; p < h->pl.n_pulses; ++p) {
     PulseParams pp{h->d_uchunks, h->d_maps, h->u_begin[p], h->u_begin[p + 1] - h->u_begin[p]};
@@ -799,8 +806,9 @@ int hx_exchange_forces_unfused(hx_handle h, float* forces, void* stream) {
   if (!h) return HX_ERR_ARG;
   if (!h->built) return HX_ERR_STATE;
   if (!forces && h->total_slots > 0) return HX_ERR_ARG;
-  int rc = ensure_device(h);
-  if (rc != HX_OK) return rc;
+  DeviceGuard guard(h->device);
+  if (!guard.ok()) return HX_ERR_CUDA;
+  int rc = HX_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   for (int p = h->pl.n_pulses - 1; p >= 0; --p) {
     PulseParams pp{h->d_uchunks, h->d_maps, h->u_begin[p], h->u_begin[p + 1] - h->u_begin[p]};
@@ -812,8 +820,8 @@ int hx_exchange_forces_unfused(hx_handle h, float* forces, void* stream) {
 
 int hx_noop(hx_handle h, void* stream) {
   if (!h) return HX_ERR_ARG;
-  const int rc = ensure_device(h);
-  if (rc != HX_OK) return rc;
+  DeviceGuard guard(h->device);
+  if (!guard.ok()) return HX_ERR_CUDA;
   return launch(h, 2, nullptr, static_cast<cudaStream_t>(stream));
 }
 
@@ -851,8 +859,8 @@ int hx_get_home_ids(hx_handle h, int32_t* home_ids, void* stream) {
   if (!h || (!home_ids && h->n_atoms > 0)) return HX_ERR_ARG;
   if (!h->built) return HX_ERR_STATE;
   if (h->n_atoms == 0) return HX_OK;
-  int rc = ensure_device(h);
-  if (rc != HX_OK) return rc;
+  DeviceGuard guard(h->device);
+  if (!guard.ok()) return HX_ERR_CUDA;
   return to_err(cudaMemcpyAsync(home_ids, h->d_home_ids, sizeof(int32_t) * h->n_atoms, cudaMemcpyDeviceToDevice,
                                 static_cast<cudaStream_t>(stream)));
 }
@@ -860,8 +868,8 @@ int hx_get_home_ids(hx_handle h, int32_t* home_ids, void* stream) {
 int hx_get_maps(hx_handle h, int32_t* maps_host, int64_t cap, int64_t* table_host) {
   if (!h) return HX_ERR_ARG;
   if (!h->built) return HX_ERR_STATE;
-  int rc = ensure_device(h);
-  if (rc != HX_OK) return rc;
+  DeviceGuard guard(h->device);
+  if (!guard.ok()) return HX_ERR_CUDA;
   if (maps_host) {
     if (cap < h->total_entries) return HX_ERR_CAPACITY;
     if (h->total_entries > 0 &&
@@ -886,8 +894,8 @@ int hx_status(hx_handle h, void* stream, int* detail) {
   if (detail) *detail = -1;
   if (!h) return HX_ERR_ARG;
   if (!h->built) return HX_OK;
-  int rc = ensure_device(h);
-  if (rc != HX_OK) return rc;
+  DeviceGuard guard(h->device);
+  if (!guard.ok()) return HX_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return HX_ERR_CUDA;
   Ctrl c[2];
@@ -898,16 +906,20 @@ int hx_status(hx_handle h, void* stream, int* detail) {
       return c[k].status;
     }
   }
-  return HX_OK;
+  int st = 0, det = -1;   // the handle's last call of hx_exchange_coords_static, if it is the device's last
+  if (static_status(h, &st, &det) != HX_OK) return HX_ERR_CUDA;
+  if (st != 0 && detail) *detail = det;
+  return st;
 }
 
 int hx_clear_status(hx_handle h, void* stream) {
   if (!h) return HX_ERR_ARG;
   if (!h->built) return HX_OK;
-  int rc = ensure_device(h);
-  if (rc != HX_OK) return rc;
+  DeviceGuard guard(h->device);
+  if (!guard.ok()) return HX_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return HX_ERR_CUDA;
+  if (static_clear(h, s) != HX_OK) return HX_ERR_CUDA;
   return reset_signals(h, s);
 }
 
@@ -919,8 +931,8 @@ int hx_debug_drop_signal(hx_handle h, int direction, int domain, int pulse) {
     if (domain >= h->pl.ndom || pulse < 0 || pulse >= h->pl.n_pulses) return HX_ERR_ARG;
     item = pulse * h->pl.ndom + domain;
   }
-  int rc = ensure_device(h);
-  if (rc != HX_OK) return rc;
+  DeviceGuard guard(h->device);
+  if (!guard.ok()) return HX_ERR_CUDA;
   if (cudaDeviceSynchronize() != cudaSuccess) return HX_ERR_CUDA;
   Ctrl* c = h->d_ctrl + direction;
   if (cudaMemcpy(&c->drop_item, &item, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return HX_ERR_CUDA;
@@ -929,7 +941,9 @@ int hx_debug_drop_signal(hx_handle h, int direction, int domain, int pulse) {
 
 void hx_destroy(hx_handle h) {
   if (!h) return;
-  if (ensure_device(h) == HX_OK) cudaDeviceSynchronize();
+  DeviceGuard guard(h->device);
+  if (guard.ok()) cudaDeviceSynchronize();
+  static_forget(h);
   free_tables(h);
   delete h;
 }

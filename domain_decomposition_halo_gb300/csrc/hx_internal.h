@@ -16,6 +16,15 @@ namespace hx {
 #ifndef HX_MIN_BLOCKS
 #define HX_MIN_BLOCKS 3
 #endif
+#ifndef HX_POLL_NAP_MIN_NS
+#define HX_POLL_NAP_MIN_NS 32
+#endif
+#ifndef HX_POLL_NAP_MAX_NS
+#define HX_POLL_NAP_MAX_NS 256
+#endif
+#ifndef HX_POLL_ACQUIRE
+#define HX_POLL_ACQUIRE 0
+#endif
 
 constexpr int kThreads = 256;                 // threads per block of the exchange kernels
 constexpr int kWarps = kThreads / 32;         // independent warps per block
@@ -55,21 +64,34 @@ struct Wait {
   int32_t chunks;
 };
 
+// A chunk of the fused lists as one self-contained record: its descriptor,
+// its map run and its first waits, so that a warp fetches everything it
+// needs for a chunk with one set of 16-byte copies and no dependent load
+// (waits past kWaitSlots stay in the direction's wait list).
+constexpr int kWaitSlots = 32;
+struct alignas(16) ChunkSlot {
+  Chunk rec;
+  int32_t map[kChunk];
+  Wait waits[kWaitSlots];
+};
+static_assert(sizeof(ChunkSlot) % 16 == 0, "chunk slots are copied in 16-byte pieces");
+
 // Per-direction control block (device memory; zeroed at build and by
 // hx_clear_status, never reset between launches).
 struct Ctrl {
-  unsigned long long ticket;  // work tickets handed out since the last reset; every
-                              // launch draws the same number (fixed by its work list
-                              // and grid), so ticket / that number numbers the launch
-                              // (its epoch is that + 1)
+  unsigned long long epoch;   // launches of this direction completed since the last
+                              // reset: a launch reads it at its start (its own epoch is
+                              // that + 1) and its last block to finish stores its epoch
   int status;                 // 0 or an HX_ERR_* code (sticky)
   int detail;                 // item of the first wait that gave up
   int drop_item;              // debug: item whose signals are dropped, or -1
-  int pad[3];
+  unsigned exits;             // blocks of the running launch that have finished
+  int pad[2];
 };
+static_assert(sizeof(Ctrl) == 32, "control block must stay 32 bytes");
 
 struct DirParams {
-  const Chunk* chunks;
+  const ChunkSlot* chunks;
   const Wait* waits;
   const int32_t* maps;
   unsigned long long* flags;  // per item (epoch flag or arrival counter) or per chunk (epoch flag)
@@ -97,8 +119,9 @@ enum SignalMode { kLastArrival = 0, kCounter = 1, kChunkFlag = 2 };
 // ---- exchange kernels (hx_kernels.cu) ----
 const void* coords_kernel(int signal_mode, bool bulk_store);   // bulk_store: gather to shared memory, bulk copy out
 const void* forces_kernel(int signal_mode, bool ordered);
+size_t chunk_smem_bytes(int dir, bool bulk_store);              // dynamic shared memory of a fused chunk kernel's block
 const void* noop_kernel();
-int max_blocks_per_sm(const void* fn);
+int max_blocks_per_sm(const void* fn, size_t smem);            // sets the kernel's dynamic shared memory limit first
 cudaError_t launch_pack_pulse(float* x, const PulseParams& p, cudaStream_t s);
 
 // ---- cluster kernels (hx_kernels.cu): one thread-block cluster walks the pulses ----
@@ -160,20 +183,18 @@ struct ResolvedParams {
 const void* resolved_kernel(int kind);    // 0 coordinates, 1 forces (ordered)
 cudaError_t launch_unpack_pulse(float* f, const PulseParams& p, cudaStream_t s);
 
-// ---- tile kernels (hx_tiles.cu) ----
+// ---- unit records of the slot-sweep kernels (hx_sweep.cu) ----
 //
-// A tile is up to kTile consecutive slots of one domain's array, inside one
-// range (home, or the slots received in one pulse). Coordinates: a tile is a
-// source - the block loads it into shared memory once and serves the gathers
-// of every pulse that selects from it. Forces: a tile is a target - the block
-// loads it, adds every pulse's contributions in reverse pulse order in shared
-// memory, and writes it back.
-constexpr int kTile = 1024;          // slots per tile at most
-constexpr int kTileEntries = 1024;   // map entries per tile at most (all segments together)
-constexpr int kTileSegs = 32;        // segments per tile at most (one per pulse)
-constexpr int kInlineSegs = 4;       // segments carried inside the tile record
+// A unit is up to kSweepSlots consecutive slots of one domain's array, inside
+// one range (home, or the slots received in one pulse), with one segment per
+// (sender, pulse) map that has entries inside it. Coordinates: a unit is a
+// source - its warp stages it in shared memory once and serves the gathers of
+// every pulse that selects from it. Forces: a unit is a target - its warp
+// stages it, adds every pulse's contributions in reverse pulse order in
+// shared memory, and writes it back.
+constexpr int kInlineSegs = 4;       // segments carried inside the unit record
 
-struct alignas(16) TileSeg {   // entries [map, map + n) of one (sender, pulse) map that fall in the tile
+struct alignas(16) UnitSeg {   // entries [map, map + n) of one (sender, pulse) map that fall in the unit
   int64_t map;        // first entry in the maps array
   int64_t other;      // receiver-side slot of that entry (coordinates: destination, forces: source)
   int32_t n;
@@ -184,30 +205,30 @@ struct alignas(16) TileSeg {   // entries [map, map + n) of one (sender, pulse) 
   int32_t src_off;    // stage byte offset of the region the received-force run is copied to
   int32_t pad[2];
 };
-static_assert(sizeof(TileSeg) == 48, "segment record must stay 48 bytes");
+static_assert(sizeof(UnitSeg) == 48, "segment record must stay 48 bytes");
 
-struct alignas(16) TileUnit {  // one 256-byte record, read by 16 threads in one round trip
-  int64_t base;       // caller-array slot of the tile's first slot
-  int32_t n;          // slots in the tile
+struct alignas(16) Unit {  // one 256-byte record, read by 16 threads in one round trip
+  int64_t base;       // caller-array slot of the unit's first slot
+  int32_t n;          // slots in the unit
   int32_t local_a;    // local index of the first slot within its domain
   int32_t seg_cnt;
   int32_t extra_off;  // segments past kInlineSegs in the direction's overflow list
-  int32_t wait_off;   // producer tiles to wait for (positions in the list)
+  int32_t wait_off;   // producer units to wait for (positions in the list)
   int32_t wait_cnt;
   int32_t flags;      // kSignal; kHaloSrc = slots written earlier in the same launch
   int32_t item;       // pulse * n_domains + domain of its first segment (status, fault injection)
   int32_t entries;    // entries of all segments
   int32_t pad[5];
-  TileSeg seg[kInlineSegs];
+  UnitSeg seg[kInlineSegs];
 };
-static_assert(sizeof(TileUnit) == 256, "tile record must stay 256 bytes");
+static_assert(sizeof(Unit) == 256, "unit record must stay 256 bytes");
 
-struct TileParams {
-  const TileUnit* units;
-  const TileSeg* extra;       // segments past kInlineSegs
+struct UnitParams {
+  const Unit* units;
+  const UnitSeg* extra;       // segments past kInlineSegs
   const Wait* waits;
   const int32_t* maps;
-  unsigned long long* flags;  // per tile: epoch flag
+  unsigned long long* flags;  // per unit: epoch flag
   Ctrl* ctrl;
   unsigned long long n_units;
   int direction;
@@ -215,15 +236,8 @@ struct TileParams {
   unsigned long long timeout_ns;
 };
 
-constexpr int kTileConsumerWarps = 8;                         // warps that process staged tiles
-constexpr int kTileThreads = (kTileConsumerWarps + 1) * 32;   // plus one producer warp
-
-const void* tiles_kernel(int kind);   // 0 coordinates, 1 forces
-size_t tiles_smem_bytes(int kind);
-int tiles_blocks_per_sm(int kind);
-
 // Kernel family of one direction's fused exchange.
-enum Family : int { kFamChunks = 0, kFamTiles = 1, kFamSweep = 2, kFamCluster = 3, kFamResolved = 4 };
+enum Family : int { kFamChunks = 0, kFamSweep = 2, kFamCluster = 3, kFamResolved = 4 };
 
 // ---- slot-sweep kernels (hx_sweep.cu): one warp per unit, same unit records ----
 #ifndef HX_SWEEP_SLOTS
@@ -237,16 +251,16 @@ constexpr int kSweepEntries = HX_SWEEP_ENTRIES;   // map entries of one unit at 
 #ifndef HX_SWEEP_BATCH
 #define HX_SWEEP_BATCH 2
 #endif
-constexpr int kSweepBatch = HX_SWEEP_BATCH;       // consecutive units claimed by one ticket
+constexpr int kSweepBatch = HX_SWEEP_BATCH;       // consecutive units a warp takes in one claim
 constexpr int kSweepSegs = 8;                     // segments (pulses) of one unit at most
 static_assert(1 + 2 * kSweepSegs <= 32, "a sweep unit stages one run per lane");
 // Stage layout of one warp: slots, then map runs, then (forces) received
 // runs; every run has a 16-byte-aligned region 16 bytes longer than itself.
-constexpr int kSweepTileBytes = kSweepSlots * 12 + 16;
+constexpr int kSweepSlotBytes = kSweepSlots * 12 + 16;
 constexpr int kSweepMapBytes = kSweepEntries * 4 + 32 * kSweepSegs;
 constexpr int kSweepSrcBytes = kSweepEntries * 12 + 32 * kSweepSegs;
 constexpr int sweep_stage_bytes(int kind) {
-  return kSweepTileBytes + kSweepMapBytes + (kind == 1 ? kSweepSrcBytes : 0);
+  return kSweepSlotBytes + kSweepMapBytes + (kind == 1 ? kSweepSrcBytes : 0);
 }
 const void* sweep_kernel(int kind);              // 0 coordinates, 1 forces
 size_t sweep_smem_bytes(int kind);               // dynamic shared memory of a block
@@ -259,7 +273,13 @@ int sweep_blocks_per_sm(int kind);
 // the handle's work list needs more than `max_flags` flags.
 int launch_coords_with_scratch(hx_ctx* h, float* coords, cudaStream_t s, Ctrl* ctrl, unsigned long long* flags,
                                unsigned int* arrivals, size_t max_flags);
-int handle_device(const hx_ctx* h);
+const void* static_kernel(const hx_ctx* h);   // the kernel launch_coords_with_scratch launches (NULL: none)
+// hx_noalloc.cu: the static path's set-up at build time, its status for
+// hx_status / hx_clear_status, and its bookkeeping at hx_destroy.
+int static_prepare(hx_ctx* h);
+int static_status(const hx_ctx* h, int* status, int* detail);
+int static_clear(const hx_ctx* h, cudaStream_t s);
+void static_forget(const hx_ctx* h);
 
 // ---- map builder (hx_build.cu) ----
 struct BuildTile {          // candidates [local_begin, local_begin + n) of one sender

@@ -4,9 +4,9 @@
 // across pulses through kernel fusion"; fusedPulsesPackAndSendKernel). The
 // work is cut into warp chunks of up to 256 entries of one (sender, pulse)
 // map, listed in a topological order (a chunk only waits for items listed
-// before it) chosen for L2 locality. A warp takes its first chunk by its
-// global warp index and every further one by an atomic ticket, so a waiting
-// chunk can only wait for chunks that running warps already own. Warps never
+// before it) chosen for L2 locality. Warp w of the persistent grid takes the
+// list positions w, w + W, w + 2W, ... in order, so a waiting chunk only
+// waits for chunks that running warps own and reach first. Warps never
 // synchronise with each other inside a block: like the pages' per-warp TMA
 // variant ("NVLink path: TMA-based direct stores"), each warp gathers,
 // stores and signals on its own.
@@ -14,8 +14,8 @@
 // A chunk gathers x[src + map[i]], applies the periodic shift, and stores
 // straight into the receiver's slots (the NVLink-path "pack directly into
 // the peer's coordinate array": here the same HBM). A chunk of forwarded
-// entries loads its map entries, then lane 0 waits with acquire loads at gpu
-// scope until the items that filled those slots have signalled
+// entries has its map entries at hand, then its lanes wait with acquire
+// loads at gpu scope until the items that filled those slots have signalled
 // (packHaloCoords). After its stores a chunk signals its item, when anybody
 // waits for it: either the pages' hierarchical scheme (signalPeerOnLastBlock:
 // a counting atomic with release semantics elects the last chunk, which
@@ -40,11 +40,23 @@ namespace {
 
 constexpr int kErrTimeout = -6;
 constexpr unsigned kFull = 0xffffffffu;
+constexpr unsigned kPollNapMinNs = HX_POLL_NAP_MIN_NS;   // back-off between flag polls: first nap
+constexpr unsigned kPollNapMaxNs = HX_POLL_NAP_MAX_NS;   // ... doubling up to this
 
 __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
   unsigned long long v;
   asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
+}
+
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
 __device__ __forceinline__ int ld_relaxed_s32(const int* p) {
@@ -96,36 +108,51 @@ __device__ __forceinline__ Chunk load_chunk(const Chunk* p) {
   return u.c;
 }
 
-// Lane 0 only. Returns false when a wait gave up (timeout, or another wait
-// already failed), in which case the chunk proceeds without the guarantee.
+// Whole warp: wait until every producer in the chunk's wait list has
+// signalled at this epoch. The lanes take the list in strides of 32 (the
+// first kWaitSlots entries from the copy in shared memory), so a chunk with
+// several producers pays about one flag round trip, not one per producer.
+// Each lane polls with acquire loads at gpu scope and a short back-off
+// between polls; the closing __syncwarp orders every lane's acquire before
+// the warp's loads. A wait that gives up (timeout, or another wait already
+// failed) records the status and lets the chunk proceed without the
+// guarantee.
 template <int MODE>
-__device__ bool wait_chunk(const DirParams& P, const Chunk& ch, unsigned long long epoch) {
-  for (int w = 0; w < ch.wait_cnt; ++w) {
-    const Wait wt = P.waits[ch.wait_off + w];
+__device__ __forceinline__ bool flag_ready(unsigned long long v, unsigned long long target) {
+  // epoch flags (per item or per chunk) are compared for equality, as the
+  // pages' signal wait does; arrival counters only grow
+  return (MODE == kCounter) ? (v >= target) : (v == target);
+}
+
+template <int MODE>
+__device__ void wait_chunk(const DirParams& P, const Chunk& ch, const Wait* waits, unsigned long long epoch) {
+  const int lane = threadIdx.x & 31;
+  for (int w = lane; w < ch.wait_cnt; w += 32) {
+    const Wait wt = w < kWaitSlots ? waits[w] : P.waits[ch.wait_off + w];
     const unsigned long long* flag = P.flags + wt.item;
     const unsigned long long target =
         (MODE == kCounter) ? epoch * static_cast<unsigned long long>(wt.chunks) : epoch;
     unsigned long long t0 = 0;
-    unsigned iter = 0;
-    // epoch flags (per item or per chunk) are compared for equality, as the
-    // pages' signal wait does; arrival counters only grow
-    while ((MODE == kCounter) ? (ld_acquire_u64(flag) < target) : (ld_acquire_u64(flag) != target)) {
-      if ((iter++ & 31u) == 0u) {
+    unsigned iter = 0, nap = 0;
+    while (!flag_ready<MODE>(ld_acquire_u64(flag), target)) {
+      if ((iter++ & 15u) == 0u) {
         const unsigned long long now = global_timer_ns();
         if (t0 == 0) t0 = now;
-        if (ld_relaxed_s32(&P.ctrl->status) != 0) return false;
+        if (ld_relaxed_s32(&P.ctrl->status) != 0) break;
         if (now - t0 > P.timeout_ns) {
           if (atomicCAS(&P.ctrl->status, 0, kErrTimeout) == 0) {
             // report the (sender, pulse) item, also when the wait was on one chunk of it
-            const int item = (MODE == kChunkFlag) ? P.chunks[wt.item].item : wt.item;
+            const int item = (MODE == kChunkFlag) ? P.chunks[wt.item].rec.item : wt.item;
             atomicExch(&P.ctrl->detail, P.direction * 65536 + item);
           }
-          return false;
+          break;
         }
       }
+      nap = nap ? min(2u * nap, kPollNapMaxNs) : kPollNapMinNs;
+      __nanosleep(nap);
     }
   }
-  return true;
+  __syncwarp();
 }
 
 // Lane 0 only, after the warp's stores (ordered by the preceding __syncwarp).
@@ -175,10 +202,9 @@ __device__ __forceinline__ void store_round(float* __restrict__ dst, int n_round
 // Coordinates of one chunk: gather (+shift) and store into the receiver.
 // Home slots are never written by the coordinate kernel, so independent
 // chunks read them through the read-only path.
-__device__ __forceinline__ void coords_chunk(float* __restrict__ x, const Chunk& ch, const int (&j)[kRounds],
-                                             float* stage) {
+__device__ __forceinline__ void gather_chunk(const float* __restrict__ x, const Chunk& ch, const int (&j)[kRounds],
+                                             float (&v)[kRounds][3]) {
   const float* src = x + 3 * ch.src;
-  float v[kRounds][3];
   const bool halo = (ch.flags & kHaloSrc) != 0;
 #pragma unroll
   for (int u = 0; u < kRounds; ++u) {
@@ -195,6 +221,12 @@ __device__ __forceinline__ void coords_chunk(float* __restrict__ x, const Chunk&
       }
     }
   }
+}
+
+__device__ __forceinline__ void coords_chunk(float* __restrict__ x, const Chunk& ch, const int (&j)[kRounds],
+                                             float* stage) {
+  float v[kRounds][3];
+  gather_chunk(x, ch, j, v);
   if (ch.flags & kShift) {   // no add otherwise: unshifted values keep every bit (-0.0 included)
 #pragma unroll
     for (int u = 0; u < kRounds; ++u) {
@@ -212,7 +244,8 @@ __device__ __forceinline__ void coords_chunk(float* __restrict__ x, const Chunk&
   }
 }
 
-// Forces of one chunk: targets[map[i]] += received[i], x then y then z.
+// Forces of one chunk: targets[map[i]] += received[i], x then y then z
+// (the unfused and cluster kernels; the fused loop stages the received run).
 template <bool ORDERED>
 __device__ __forceinline__ void forces_chunk(float* __restrict__ f, const Chunk& ch, const int (&j)[kRounds]) {
   const int lane = threadIdx.x & 31;
@@ -279,6 +312,16 @@ __device__ __forceinline__ void forces_chunk(float* __restrict__ f, const Chunk&
 // signal follows only once the copy is complete and ordered before the
 // release (bulk_store_done).
 constexpr int kBulkStageBytes = kChunk * 12 + 16;
+constexpr int kPipe = 2;         // chunks in a warp's pipeline: in use, next one in flight
+
+// A warp's shared memory in the fused chunk kernels: the chunk pipeline and
+// the stage (coordinates: a 32-entry transposed round, or the whole chunk for
+// the bulk store; forces: the chunk's received run).
+template <int KIND>
+struct alignas(16) ChunkWarpSmem {
+  ChunkSlot slot[kPipe];
+  alignas(16) unsigned char stage[KIND == 0 ? 96 * 4 : kBulkStageBytes];
+};
 
 __device__ __forceinline__ unsigned smem_u32(const void* p) {
   return static_cast<unsigned>(__cvta_generic_to_shared(p));
@@ -287,24 +330,8 @@ __device__ __forceinline__ unsigned smem_u32(const void* p) {
 __device__ __forceinline__ void coords_chunk_bulk(float* __restrict__ x, const Chunk& ch, const int (&j)[kRounds],
                                                   unsigned char* stage) {
   const int lane = threadIdx.x & 31;
-  const float* src = x + 3 * ch.src;
   float v[kRounds][3];
-  const bool halo = (ch.flags & kHaloSrc) != 0;
-#pragma unroll
-  for (int u = 0; u < kRounds; ++u) {
-    if (j[u] >= 0) {
-      const float* s = src + 3 * static_cast<int64_t>(j[u]);
-      if (halo) {
-        v[u][0] = s[0];
-        v[u][1] = s[1];
-        v[u][2] = s[2];
-      } else {
-        v[u][0] = __ldg(s);
-        v[u][1] = __ldg(s + 1);
-        v[u][2] = __ldg(s + 2);
-      }
-    }
-  }
+  gather_chunk(x, ch, j, v);
   if (ch.flags & kShift) {   // no add otherwise: unshifted values keep every bit (-0.0 included)
 #pragma unroll
     for (int u = 0; u < kRounds; ++u) {
@@ -356,65 +383,182 @@ __device__ __forceinline__ void bulk_store_done() {
   asm volatile("cp.async.bulk.wait_group 0;\n\tfence.proxy.async.global;" ::: "memory");
 }
 
+// Chunk pipeline of one warp in shared memory. While the warp works on its
+// chunk k, the whole record of chunk k+1 (descriptor, map run, first waits)
+// is copied in with cp.async: a warp's claims are static (below), so it
+// knows its next chunk ahead, and a chunk starts with everything at hand.
+__device__ __forceinline__ void cp_async_4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// All but the `n` most recently committed groups of this thread have landed.
+template <int n>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(n) : "memory"); }
+
+// Whole warp: one chunk record, in 16-byte pieces (committed as one group).
+__device__ __forceinline__ void fetch_chunk(ChunkSlot& s, const ChunkSlot* src) {
+  const int lane = threadIdx.x & 31;
+  constexpr int kPieces = static_cast<int>(sizeof(ChunkSlot) / 16);
+  const int4* g = reinterpret_cast<const int4*>(src);
+  int4* d = reinterpret_cast<int4*>(&s);
+#pragma unroll
+  for (int k = lane; k < kPieces; k += 32) cp_async_16(d + k, g + k);
+  cp_async_commit();
+}
+
+// Forces of one chunk: targets[map[i]] += received[i], x then y then z. The
+// received run (contiguous slots) is copied into the warp's stage with
+// cp.async (16-byte pieces for its aligned middle, words for the ragged ends;
+// the stage keeps the run's address mod 16) while the targets are loaded
+// into registers, so a chunk costs one round trip before its adds. The
+// stage's copy is committed as the newest group; the caller has committed
+// its other copies before.
+template <bool ORDERED>
+__device__ __forceinline__ void forces_chunk_staged(float* __restrict__ f, const Chunk& ch, const int (&j)[kRounds],
+                                                    unsigned char* stage) {
+  const int lane = threadIdx.x & 31;
+  const unsigned long long g = reinterpret_cast<unsigned long long>(f + 3 * ch.dst);
+  const unsigned bytes = 12u * static_cast<unsigned>(ch.n);
+  unsigned char* base = stage + (g & 15ull);   // base[k] holds the byte at g + k
+  const unsigned long long a0 = (g + 15ull) & ~15ull, a1 = (g + bytes) & ~15ull;
+  if (a1 > a0) {
+    const int pieces = static_cast<int>((a1 - a0) / 16);
+    for (int k = lane; k < pieces; k += 32)
+      cp_async_16(base + (a0 - g) + 16 * k, reinterpret_cast<const void*>(a0 + 16ull * k));
+    const int head = static_cast<int>((a0 - g) / 4), tail = static_cast<int>((g + bytes - a1) / 4);
+    if (lane < head) cp_async_4(base + 4 * lane, reinterpret_cast<const void*>(g + 4ull * lane));
+    else if (lane >= 4 && lane < 4 + tail)
+      cp_async_4(base + (a1 - g) + 4 * (lane - 4), reinterpret_cast<const void*>(a1 + 4ull * (lane - 4)));
+  } else {
+    for (int k = lane; k < static_cast<int>(bytes / 4); k += 32)
+      cp_async_4(base + 4 * k, reinterpret_cast<const void*>(g + 4ull * k));
+  }
+  cp_async_commit();
+  float* tgt = f + 3 * ch.src;
+  float t[kRounds][3];
+  if (ORDERED) {
+#pragma unroll
+    for (int u = 0; u < kRounds; ++u) {
+      if (j[u] >= 0) {
+        const float* p = tgt + 3 * static_cast<int64_t>(j[u]);
+        t[u][0] = p[0];
+        t[u][1] = p[1];
+        t[u][2] = p[2];
+      }
+    }
+  }
+  cp_async_wait<0>();   // this lane's copies of the run (and anything committed before)
+  __syncwarp();         // ... and every other lane's
+  const float* rcv = reinterpret_cast<const float*>(base);
+#pragma unroll
+  for (int u = 0; u < kRounds; ++u) {
+    const int jj = j[u];
+    if (jj >= 0) {
+      const int e = u * 32 + lane;
+      float* p = tgt + 3 * static_cast<int64_t>(jj);
+      if (ORDERED) {
+        p[0] = __fadd_rn(t[u][0], rcv[3 * e + 0]);
+        p[1] = __fadd_rn(t[u][1], rcv[3 * e + 1]);
+        p[2] = __fadd_rn(t[u][2], rcv[3 * e + 2]);
+      } else {
+        atomicAdd(p, rcv[3 * e + 0]);
+        atomicAdd(p + 1, rcv[3 * e + 1]);
+        atomicAdd(p + 2, rcv[3 * e + 2]);
+      }
+    }
+  }
+  __syncwarp();   // the stage is read before the next chunk's copy into it
+}
+
 // Persistent warp loop shared by both directions. KIND 0 = coordinates,
 // 1 = forces ordered, 2 = forces unordered, 3 = coordinates by bulk stores.
+//
+// Claims are static: warp w of the launch takes list positions w, w + W,
+// w + 2W, ... (W warps), in that order. The list is in a topological order
+// of the waits and every warp is resident, so the smallest unfinished
+// position always belongs to a warp that has finished all its earlier
+// positions and whose producers all sit at smaller positions: the launch
+// always progresses. No atomic ticket is drawn (thousands of warps drawing
+// from one counter at launch serialise for microseconds). The launch's epoch
+// is read from the control block at the start; the launch's last block to
+// finish stores it there for the next launch.
 template <int MODE, int KIND>
-__device__ __forceinline__ void run_warps(float* __restrict__ buf, const DirParams& P, float* stage) {
+__device__ __forceinline__ void run_warps(float* __restrict__ buf, const DirParams& P, ChunkWarpSmem<KIND>& S) {
   const int lane = threadIdx.x & 31;
   const unsigned long long W = static_cast<unsigned long long>(gridDim.x) * kWarps;
   const unsigned long long N = P.n_chunks;
   unsigned long long c = static_cast<unsigned long long>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
   allow_dependents();
-  wait_prerequisites();   // before the first ticket, flag or buffer access
-  if (c >= N) return;
-  const int drop_item = *reinterpret_cast<const volatile int*>(&P.ctrl->drop_item);
-  unsigned long long base = ~0ull;   // first ticket of this launch: (epoch - 1) * N
-  unsigned long long epoch = 0;
-  while (c < N) {
-    unsigned long long t = 0;
-    if (lane == 0) t = atomicAdd(&P.ctrl->ticket, 1ull);
-    const Chunk ch = load_chunk(P.chunks + c);
-    int j[kRounds];
-    load_map(P.maps + ch.map, ch.n, j);
-    t = __shfl_sync(kFull, t, 0);
-    if (base == ~0ull) {   // every ticket of one launch lies in [base, base + N)
-      base = t - t % N;
-      epoch = base / N + 1ull;
-    }
-    if (ch.wait_cnt > 0) {
-      if (lane == 0) wait_chunk<MODE>(P, ch, epoch);
-      __syncwarp();
-    }
-    if (KIND == 0) coords_chunk(buf, ch, j, stage);
-    else if (KIND == 3) coords_chunk_bulk(buf, ch, j, reinterpret_cast<unsigned char*>(stage));
-    else forces_chunk<KIND == 1>(buf, ch, j);
-    if (ch.flags & kSignal) {
-      __syncwarp();
-      if (lane == 0) {
-        if (KIND == 3) bulk_store_done();
-        signal_chunk<MODE>(P, ch, c, epoch, drop_item);
+  wait_prerequisites();   // before the first flag, table or buffer access
+  const unsigned long long epoch = ld_relaxed_u64(&P.ctrl->epoch) + 1ull;
+  if (c < N) {
+    const int drop_item = ld_relaxed_s32(&P.ctrl->drop_item);
+    fetch_chunk(S.slot[0], P.chunks + c);
+    cp_async_wait<0>();
+    __syncwarp();
+    int b = 0;
+    while (true) {
+      const ChunkSlot& cur = S.slot[b];
+      const Chunk ch = cur.rec;
+      int j[kRounds];
+#pragma unroll
+      for (int u = 0; u < kRounds; ++u) {
+        const int e = u * 32 + lane;
+        j[u] = (e < ch.n) ? cur.map[e] : -1;
       }
+      const unsigned long long c1 = c + W;
+      if (c1 < N) fetch_chunk(S.slot[b ^ 1], P.chunks + c1);
+      if (ch.wait_cnt > 0) wait_chunk<MODE>(P, ch, cur.waits, epoch);
+      if (KIND == 0) coords_chunk(buf, ch, j, reinterpret_cast<float*>(S.stage));
+      else if (KIND == 3) coords_chunk_bulk(buf, ch, j, S.stage);
+      else forces_chunk_staged<KIND == 1>(buf, ch, j, S.stage);
+      if (ch.flags & kSignal) {
+        __syncwarp();
+        if (lane == 0) {
+          if (KIND == 3) bulk_store_done();
+          signal_chunk<MODE>(P, ch, c, epoch, drop_item);
+        }
+      }
+      if (c1 >= N) break;
+      c = c1;
+      b ^= 1;
+      cp_async_wait<0>();   // the next chunk's record
+      __syncwarp();
     }
-    c = (t - base) + W;
+    if (KIND == 3 && lane == 0) bulk_store_done();   // nothing in flight when the warp exits
   }
-  if (KIND == 3 && lane == 0) bulk_store_done();   // nothing in flight when the warp exits
+  // The launch's last block to finish publishes its epoch for the next launch
+  // of this direction (which reads it after this grid has completed).
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned done = atomicAdd(&P.ctrl->exits, 1u);
+    if (done == gridDim.x - 1) {
+      P.ctrl->exits = 0u;
+      st_relaxed_u64(&P.ctrl->epoch, epoch);
+    }
+  }
 }
 
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) k_coords_fused(float* __restrict__ x, DirParams P) {
-  __shared__ float s_stage[kWarps][96];
-  run_warps<MODE, 0>(x, P, s_stage[threadIdx.x >> 5]);
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  run_warps<MODE, 0>(x, P, reinterpret_cast<ChunkWarpSmem<0>*>(smem_raw)[threadIdx.x >> 5]);
 }
 
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) k_coords_bulk(float* __restrict__ x, DirParams P) {
-  __shared__ __align__(16) float s_stage[kWarps][kBulkStageBytes / 4];
-  run_warps<MODE, 3>(x, P, s_stage[threadIdx.x >> 5]);
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  run_warps<MODE, 3>(x, P, reinterpret_cast<ChunkWarpSmem<3>*>(smem_raw)[threadIdx.x >> 5]);
 }
 
 template <int MODE, bool ORDERED>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) k_forces_fused(float* __restrict__ f, DirParams P) {
-  run_warps<MODE, ORDERED ? 1 : 2>(f, P, nullptr);
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  constexpr int K = ORDERED ? 1 : 2;
+  run_warps<MODE, K>(f, P, reinterpret_cast<ChunkWarpSmem<K>*>(smem_raw)[threadIdx.x >> 5]);
 }
 
 // Unfused baseline: one warp per chunk of one pulse, stream order between pulses.
@@ -503,9 +647,17 @@ const void* cluster_kernel(int kind) {
   return kind == 0 ? reinterpret_cast<const void*>(&k_cluster<0>) : reinterpret_cast<const void*>(&k_cluster<1>);
 }
 
-int max_blocks_per_sm(const void* fn) {
+size_t chunk_smem_bytes(int dir, bool bulk_store) {
+  if (dir == 1) return kWarps * sizeof(ChunkWarpSmem<1>);
+  return kWarps * (bulk_store ? sizeof(ChunkWarpSmem<3>) : sizeof(ChunkWarpSmem<0>));
+}
+
+int max_blocks_per_sm(const void* fn, size_t smem) {
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
+    return 0;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kThreads, 0) != cudaSuccess) return 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kThreads, smem) != cudaSuccess) return 0;
   return n;
 }
 

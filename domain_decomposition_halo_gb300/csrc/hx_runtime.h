@@ -28,6 +28,34 @@ struct GraphEntry {
   cudaGraphExec_t exec;
 };
 
+// Makes `device` current for the life of the guard and gives the caller's
+// current device back at the end, so that an entry point leaves the calling
+// thread's device as it found it. ok() is false when the switch failed.
+class DeviceGuard {
+ public:
+  explicit DeviceGuard(int device) {
+    if (cudaGetDevice(&prev_) != cudaSuccess) {
+      ok_ = false;
+      return;
+    }
+    if (prev_ != device) {
+      ok_ = cudaSetDevice(device) == cudaSuccess;
+      switched_ = ok_;
+    }
+  }
+  ~DeviceGuard() {
+    if (switched_) cudaSetDevice(prev_);
+  }
+  DeviceGuard(const DeviceGuard&) = delete;
+  DeviceGuard& operator=(const DeviceGuard&) = delete;
+  bool ok() const { return ok_; }
+
+ private:
+  int prev_ = -1;
+  bool ok_ = true;
+  bool switched_ = false;
+};
+
 template <class T>
 cudaError_t dev_alloc(T** p, size_t count) {
   *p = nullptr;
@@ -85,7 +113,7 @@ struct hx_ctx {
 
   int32_t* d_maps = nullptr;
   int32_t* d_home_ids = nullptr;
-  Chunk* d_chunks[2] = {nullptr, nullptr};   // fused coordinate / force chunk lists
+  ChunkSlot* d_chunks[2] = {nullptr, nullptr};   // fused coordinate / force chunk lists (self-contained records)
   Wait* d_waits[2] = {nullptr, nullptr};
   Chunk* d_uchunks = nullptr;                // unfused per-pulse chunk list
   unsigned long long* d_flags = nullptr;     // [2][n_items]
@@ -95,8 +123,8 @@ struct hx_ctx {
   int grid[2] = {0, 0};
   size_t n_flags = 1;                        // flags (and election counters) per direction
   int family[2] = {0, 0};                    // kernel family of each direction's fused path (Family)
-  TileUnit* d_units[2] = {nullptr, nullptr};
-  TileSeg* d_segs[2] = {nullptr, nullptr};
+  Unit* d_units[2] = {nullptr, nullptr};
+  UnitSeg* d_segs[2] = {nullptr, nullptr};
   Wait* d_twaits[2] = {nullptr, nullptr};
   int n_units[2] = {0, 0};
   std::vector<int> u_begin;                  // per pulse, first unfused chunk (P + 1 entries)
@@ -109,6 +137,7 @@ struct hx_ctx {
   CopyChunk* d_home_chunks = nullptr;        // host-buffer calls: every domain's home range
   CopyChunk* d_halo_chunks = nullptr;        // ... and halo range, in pieces of one block each
   int n_home_chunks = 0, n_halo_chunks = 0;
+  void* static_scratch = nullptr;            // hx_exchange_coords_static: device address of its scratch array
 };
 
 namespace hx_rt {
@@ -117,6 +146,7 @@ namespace hx_rt {
 void cell_of(const Plan& pl, int r, int c[3]);
 int neighbour(const Plan& pl, int r, int d, int step);
 const void* kernel_for(hx_ctx* h, int kind);
+size_t fused_smem(const hx_ctx* h, int dir);   // dynamic shared memory of a direction's fused kernel
 int reset_signals(hx_ctx* h, cudaStream_t s);
 int64_t resolved_blocks(int64_t n, int per);
 int resolved_per_thread(const hx_ctx* h, int64_t n, int most);

@@ -29,9 +29,9 @@
 // ("Enabling parallelism across pulses through kernel fusion"): a unit of
 // received slots waits for the units that stored them (coordinates), and a
 // unit waits for the receivers' units that still add into the slots it reads
-// (forces). Each warp is independent. It draws units by ticket, in a
-// topological order, and so never waits on a unit that no running warp has
-// claimed.
+// (forces). Each warp is independent. Its claims are static batches of
+// units in a topological order (warp w of W takes batches w, w + W, ...), so
+// it never waits on a unit that no running warp owns.
 #include <cstdint>
 
 #include "hx_internal.h"
@@ -41,6 +41,8 @@ namespace {
 
 constexpr int kErrTimeout = -6;
 constexpr unsigned kFull = 0xffffffffu;
+constexpr unsigned kPollNapMinNs = HX_POLL_NAP_MIN_NS;   // back-off between flag polls: first nap
+constexpr unsigned kPollNapMaxNs = HX_POLL_NAP_MAX_NS;   // ... doubling up to this
 
 // A warp's stage buffer: the unit's slots, its map runs and (forces) its
 // received runs, each in its own 16-byte-aligned region at the run's global
@@ -48,7 +50,7 @@ constexpr unsigned kFull = 0xffffffffu;
 template <int KIND>
 struct alignas(16) WarpSmem {
   alignas(16) unsigned char stage[sweep_stage_bytes(KIND)];
-  TileUnit desc[2];              // the current unit's record and the next one's
+  Unit desc[2];              // the current unit's record and the next one's
   float out[KIND == 0 ? 96 : 4];  // coordinates: one 32-entry round, transposed for coalesced stores
   unsigned long long bar;        // completion of the unit's bulk copies
 };
@@ -57,6 +59,16 @@ __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long
   unsigned long long v;
   asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
+}
+
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
 __device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
@@ -124,27 +136,28 @@ __device__ __forceinline__ void bulk_load(void* dst, unsigned long long src, uns
       : "memory");
 }
 
-__device__ __forceinline__ void record_timeout(const TileParams& P, int item) {
+__device__ __forceinline__ void record_timeout(const UnitParams& P, int item) {
   if (atomicCAS(&P.ctrl->status, 0, kErrTimeout) == 0) atomicExch(&P.ctrl->detail, P.direction * 65536 + item);
 }
 
-__device__ __forceinline__ TileSeg seg_at(const TileParams& P, const TileUnit& d, int s) {
+__device__ __forceinline__ UnitSeg seg_at(const UnitParams& P, const Unit& d, int s) {
   return s < kInlineSegs ? d.seg[s] : P.extra[d.extra_off + s - kInlineSegs];
 }
 
 // Whole warp: wait until every unit that d depends on has been signalled at
-// this epoch. Lanes take the wait list in strides of 32; a wait that runs
-// out records a timeout and gives up. The closing __syncwarp orders every
-// lane's acquire before the warp's loads.
-__device__ void wait_units(const TileParams& P, const TileUnit& d, unsigned long long epoch) {
+// this epoch. Lanes take the wait list in strides of 32 and poll with
+// acquire loads at gpu scope and a short back-off; the closing __syncwarp
+// orders every lane's acquire before the warp's loads. A wait that runs out
+// records a timeout and gives up.
+__device__ void wait_units(const UnitParams& P, const Unit& d, unsigned long long epoch) {
   const int lane = threadIdx.x & 31;
   for (int w = lane; w < d.wait_cnt; w += 32) {
     const Wait wt = P.waits[d.wait_off + w];
     const unsigned long long* flag = P.flags + wt.item;
     unsigned long long t0 = 0;
-    unsigned iter = 0;
+    unsigned iter = 0, nap = 0;
     while (ld_acquire_u64(flag) != epoch) {
-      if ((iter++ & 31u) == 0u) {
+      if ((iter++ & 15u) == 0u) {
         const unsigned long long now = global_timer_ns();
         if (t0 == 0) t0 = now;
         if (ld_relaxed_s32(&P.ctrl->status) != 0) break;
@@ -153,6 +166,8 @@ __device__ void wait_units(const TileParams& P, const TileUnit& d, unsigned long
           break;
         }
       }
+      nap = nap ? min(2u * nap, kPollNapMaxNs) : kPollNapMinNs;
+      __nanosleep(nap);
     }
   }
   __syncwarp();
@@ -161,7 +176,7 @@ __device__ void wait_units(const TileParams& P, const TileUnit& d, unsigned long
 // Run k of a unit: 0 = its slots, then per segment its map run and (forces)
 // its received-force run: global address, bytes, stage region offset.
 template <int KIND>
-__device__ __forceinline__ void run_of(const float* x, const TileParams& P, const TileUnit& d, int k,
+__device__ __forceinline__ void run_of(const float* x, const UnitParams& P, const Unit& d, int k,
                                        unsigned long long& g, unsigned& bytes, unsigned& region) {
   if (k == 0) {
     g = reinterpret_cast<unsigned long long>(x + 3 * d.base);
@@ -170,7 +185,7 @@ __device__ __forceinline__ void run_of(const float* x, const TileParams& P, cons
     return;
   }
   const int per = KIND == 1 ? 2 : 1;
-  const TileSeg sg = seg_at(P, d, (k - 1) / per);
+  const UnitSeg sg = seg_at(P, d, (k - 1) / per);
   if ((k - 1) % per == 0) {
     g = reinterpret_cast<unsigned long long>(P.maps + sg.map);
     bytes = 4u * static_cast<unsigned>(sg.n);
@@ -190,7 +205,7 @@ __device__ __forceinline__ void run_of(const float* x, const TileParams& P, cons
 // bytes each) with plain loads. Runs of under 32 bytes go entirely by plain
 // loads. The caller waits on the mbarrier and then on the warp (__syncwarp).
 template <int KIND>
-__device__ void stage_unit(const float* x, const TileParams& P, const TileUnit& d, unsigned char* st,
+__device__ void stage_unit(const float* x, const UnitParams& P, const Unit& d, unsigned char* st,
                            unsigned long long* bar) {
   const int lane = threadIdx.x & 31;
   const int n_runs = 1 + (KIND == 1 ? 2 : 1) * d.seg_cnt;
@@ -235,7 +250,7 @@ __device__ void stage_unit(const float* x, const TileParams& P, const TileUnit& 
 // whose producers have not signalled yet may be fetched early: L2 is where
 // later stores land, so the unit's own bulk copies still read the final data.
 template <int KIND>
-__device__ void prefetch_unit(const float* x, const TileParams& P, const TileUnit& d) {
+__device__ void prefetch_unit(const float* x, const UnitParams& P, const Unit& d) {
   const int lane = threadIdx.x & 31;
   const int n_runs = 1 + (KIND == 1 ? 2 : 1) * d.seg_cnt;
   if (lane < n_runs) {
@@ -277,13 +292,13 @@ __device__ __forceinline__ void store_round(float* __restrict__ dst, int n_round
 }
 
 // Coordinates of one staged unit: every pulse's gathers.
-__device__ __forceinline__ void coords_unit(float* __restrict__ x, const TileParams& P, const TileUnit& d,
+__device__ __forceinline__ void coords_unit(float* __restrict__ x, const UnitParams& P, const Unit& d,
                                             WarpSmem<0>& S) {
   const int lane = threadIdx.x & 31;
   const float* tile = reinterpret_cast<const float*>(
       S.stage + (reinterpret_cast<unsigned long long>(x + 3 * d.base) & 15ull));
   for (int s = 0; s < d.seg_cnt; ++s) {
-    const TileSeg sg = seg_at(P, d, s);
+    const UnitSeg sg = seg_at(P, d, s);
     const int32_t* smap = reinterpret_cast<const int32_t*>(
         S.stage + sg.map_off + (reinterpret_cast<unsigned long long>(P.maps + sg.map) & 15ull));
     float* dst = x + 3 * sg.other;
@@ -320,13 +335,13 @@ __device__ __forceinline__ void bulk_stores_done() {
 // segment have distinct targets. Then the slots are written back: one bulk
 // store for the 16-byte-aligned middle (the stage keeps the global address
 // mod 16), plain stores for the words around it.
-__device__ __forceinline__ void forces_unit(float* __restrict__ f, const TileParams& P, const TileUnit& d,
+__device__ __forceinline__ void forces_unit(float* __restrict__ f, const UnitParams& P, const Unit& d,
                                             WarpSmem<1>& S) {
   const int lane = threadIdx.x & 31;
   const unsigned long long gt = reinterpret_cast<unsigned long long>(f + 3 * d.base);
   float* tile = reinterpret_cast<float*>(S.stage + (gt & 15ull));
   for (int s = 0; s < d.seg_cnt; ++s) {
-    const TileSeg sg = seg_at(P, d, s);
+    const UnitSeg sg = seg_at(P, d, s);
     const int32_t* smap = reinterpret_cast<const int32_t*>(
         S.stage + sg.map_off + (reinterpret_cast<unsigned long long>(P.maps + sg.map) & 15ull));
     const float* src = reinterpret_cast<const float*>(
@@ -362,7 +377,7 @@ __device__ __forceinline__ void forces_unit(float* __restrict__ f, const TilePar
 
 // KIND 0 = coordinates, 1 = forces (ordered).
 template <int KIND>
-__global__ void __launch_bounds__(kThreads) k_sweep(float* __restrict__ buf, TileParams P) {
+__global__ void __launch_bounds__(kThreads) k_sweep(float* __restrict__ buf, UnitParams P) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const int lane = threadIdx.x & 31;
   WarpSmem<KIND>& S = reinterpret_cast<WarpSmem<KIND>*>(smem_raw)[threadIdx.x >> 5];
@@ -370,79 +385,82 @@ __global__ void __launch_bounds__(kThreads) k_sweep(float* __restrict__ buf, Til
   const unsigned long long N = P.n_units;
   const unsigned long long NB = (N + kSweepBatch - 1) / kSweepBatch;   // batches of units per launch
   const unsigned long long b0 = static_cast<unsigned long long>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
-  if (b0 >= NB) return;
-  unsigned long long c = b0 * kSweepBatch;
-  const int drop_item = *reinterpret_cast<const volatile int*>(&P.ctrl->drop_item);
-  if (lane == 0) {
-    mbar_init(&S.bar, 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  __syncwarp();
-  unsigned parity = 0;
-  // Units are claimed in batches of kSweepBatch consecutive units. The
-  // warp's first batch is its global index; each ticket, drawn when the warp
-  // starts a batch, names its following batch (ticket t of the launch ->
-  // batch t - base + W), so a launch draws exactly NB tickets. The next
-  // unit's record is copied in while the current unit is staged and
-  // processed. A warp works through its claims in list order, which keeps
-  // the topological order deadlock-free.
-  unsigned long long t = 0;
-  if (lane == 0) t = atomicAdd(&P.ctrl->ticket, 1ull);
-  if (lane < 16) cp_async_16(reinterpret_cast<int4*>(&S.desc[0]) + lane, reinterpret_cast<const int4*>(P.units + c) + lane);
-  cp_async_wait_all();
-  __syncwarp();
-  t = __shfl_sync(kFull, t, 0);
-  const unsigned long long base = t - t % NB;   // every ticket of one launch lies in [base, base + NB)
-  const unsigned long long epoch = base / NB + 1ull;
-  int b = 0;
-  while (true) {
-    const bool same_batch = (c + 1) % kSweepBatch != 0;
-    const unsigned long long cn = same_batch ? c + 1 : ((t - base) + W) * kSweepBatch;   // this warp's next unit
-    const bool new_ticket = !same_batch && cn < N;
-    if (cn < N) {
-      if (new_ticket && lane == 0) t = atomicAdd(&P.ctrl->ticket, 1ull);
-      if (lane < 16)
+  // The launch's epoch; its last block to finish stores it for the next
+  // launch of this direction (which reads it after this grid has completed).
+  const unsigned long long epoch = ld_relaxed_u64(&P.ctrl->epoch) + 1ull;
+  if (b0 < NB) {
+    unsigned long long c = b0 * kSweepBatch;
+    const int drop_item = *reinterpret_cast<const volatile int*>(&P.ctrl->drop_item);
+    if (lane == 0) {
+      mbar_init(&S.bar, 1);
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncwarp();
+    unsigned parity = 0;
+    // Units are claimed in batches of kSweepBatch consecutive units, and the
+    // claims are static: warp w of the W warps takes batches w, w + W,
+    // w + 2W, ... in order, so a warp works through its claims in list order
+    // and the topological order keeps the launch deadlock-free (the smallest
+    // unfinished unit's warp has finished its earlier units, and its
+    // producers sit at smaller positions). The next unit's record is copied
+    // in while the current unit is staged and processed.
+    if (lane < 16)
+      cp_async_16(reinterpret_cast<int4*>(&S.desc[0]) + lane, reinterpret_cast<const int4*>(P.units + c) + lane);
+    cp_async_wait_all();
+    __syncwarp();
+    int b = 0;
+    while (true) {
+      const bool same_batch = (c + 1) % kSweepBatch != 0;
+      const unsigned long long cn = same_batch ? c + 1 : (c / kSweepBatch + W) * kSweepBatch;   // this warp's next unit
+      if (cn < N && lane < 16)
         cp_async_16(reinterpret_cast<int4*>(&S.desc[b ^ 1]) + lane, reinterpret_cast<const int4*>(P.units + cn) + lane);
-    }
-    const TileUnit& d = S.desc[b];
-    if (d.wait_cnt > 0) {
-      wait_units(P, d, epoch);
-      // bulk copies (async proxy) then read what other warps stored (generic proxy) before their signals
-      if (lane == 0) asm volatile("fence.proxy.async.global;" ::: "memory");
-      __syncwarp();
-    }
-    if (KIND == 1) {   // the previous unit's write-back has read the stage
-      if (lane == 0) bulk_stores_read();
-      __syncwarp();
-    }
-    stage_unit<KIND>(buf, P, d, S.stage, &S.bar);
-    if (cn < N) {   // the next record, then its runs into L2 while this unit's copies land
-      cp_async_wait_all();
-      __syncwarp();
-      prefetch_unit<KIND>(buf, P, S.desc[b ^ 1]);
-    }
-    if (!mbar_wait(&S.bar, parity, P.timeout_ns)) {
-      if (lane == 0) record_timeout(P, d.item);
-    }
-    parity ^= 1u;
-    __syncwarp();   // the lanes' edge words are in place
-    if constexpr (KIND == 0) coords_unit(buf, P, d, S);
-    else forces_unit(buf, P, d, S);
-    if (d.flags & kSignal) {
-      __syncwarp();   // every lane's stores precede lane 0's release
-      if (lane == 0) {
-        if (KIND == 1) bulk_stores_done();
-        if (d.item != drop_item) st_release_u64(P.flags + c, epoch);
+      const Unit& d = S.desc[b];
+      if (d.wait_cnt > 0) {
+        wait_units(P, d, epoch);
+        // bulk copies (async proxy) then read what other warps stored (generic proxy) before their signals
+        if (lane == 0) asm volatile("fence.proxy.async.global;" ::: "memory");
+        __syncwarp();
       }
+      if (KIND == 1) {   // the previous unit's write-back has read the stage
+        if (lane == 0) bulk_stores_read();
+        __syncwarp();
+      }
+      stage_unit<KIND>(buf, P, d, S.stage, &S.bar);
+      if (cn < N) {   // the next record, then its runs into L2 while this unit's copies land
+        cp_async_wait_all();
+        __syncwarp();
+        prefetch_unit<KIND>(buf, P, S.desc[b ^ 1]);
+      }
+      if (!mbar_wait(&S.bar, parity, P.timeout_ns)) {
+        if (lane == 0) record_timeout(P, d.item);
+      }
+      parity ^= 1u;
+      __syncwarp();   // the lanes' edge words are in place
+      if constexpr (KIND == 0) coords_unit(buf, P, d, S);
+      else forces_unit(buf, P, d, S);
+      if (d.flags & kSignal) {
+        __syncwarp();   // every lane's stores precede lane 0's release
+        if (lane == 0) {
+          if (KIND == 1) bulk_stores_done();
+          if (d.item != drop_item) st_release_u64(P.flags + c, epoch);
+        }
+      }
+      if (cn >= N) break;
+      cp_async_wait_all();   // the next record
+      __syncwarp();          // ... for every lane; the stage is rewritten for the next unit
+      c = cn;
+      b ^= 1;
     }
-    if (cn >= N) break;
-    cp_async_wait_all();   // the next record
-    __syncwarp();          // ... for every lane; the stage is rewritten for the next unit
-    if (new_ticket) t = __shfl_sync(kFull, t, 0);
-    c = cn;
-    b ^= 1;
+    if (KIND == 1 && lane == 0) bulk_stores_done();   // nothing in flight when the warp exits
   }
-  if (KIND == 1 && lane == 0) bulk_stores_done();   // nothing in flight when the warp exits
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned done = atomicAdd(&P.ctrl->exits, 1u);
+    if (done == gridDim.x - 1) {
+      P.ctrl->exits = 0u;
+      st_relaxed_u64(&P.ctrl->epoch, epoch);
+    }
+  }
 }
 
 }  // namespace

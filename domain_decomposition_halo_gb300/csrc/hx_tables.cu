@@ -120,41 +120,41 @@ std::vector<int> order_chunks(const std::vector<Rec>& recs) {
       [&](int i) { return recs[i].key; });
 }
 
-// ---------------------------------------------------------------- tile tables
+// ---------------------------------------------------------------- unit tables
 //
 // Each domain's array is cut into ranges (home, then the slots received in
-// each pulse) and each range into tiles of up to kTile slots. A tile gets
+// each pulse) and each range into units of up to max_slots slots. A unit gets
 // one segment per (sender, pulse) map that has entries inside it: for
 // coordinates the maps it is a source of, for forces the maps it is a target
 // of (segments last pulse first). Dependencies:
-//   coordinates: a tile of received slots waits for the tiles of the sending
+//   coordinates: a unit of received slots waits for the units of the sending
 //     domain that stored those slots;
-//   forces: a tile waits for the tiles of its receivers that hold the slots
-//     it reads, when those tiles are themselves targets of later pulses.
-// Tiles are listed by Kahn's algorithm with the same priority as the chunk
-// lists (folded domain order, dependency depth, a lag of one resident window
-// per depth).
+//   forces: a unit waits for the units of its receivers that hold the slots
+//     it reads, when those units are themselves targets of later pulses.
+// Units are listed by Kahn's algorithm with the same priority as the chunk
+// lists (folded domain order, dependency depth, a lag of `lag` list
+// positions per depth).
 
 struct TRec {
   int r;              // domain
-  int range;          // -1 home, else the pulse whose received slots the tile holds
+  int range;          // -1 home, else the pulse whose received slots the unit holds
   int a, n;           // local index of the first slot, slot count
-  std::vector<TileSeg> segs;
+  std::vector<UnitSeg> segs;
   std::vector<int> seg_pulse;
   std::vector<int> deps;   // TRec indices
   int stage = 0;
   long long key = 0;
 };
 
-int build_tile_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::vector<int32_t>& maps,
+int build_unit_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::vector<int32_t>& maps,
                       const std::vector<int64_t>& rank, int max_slots, int max_entries, long long lag,
-                      int tile_bytes, int map_bytes, int src_bytes, int dir) {
+                      int slot_bytes, int map_bytes, int src_bytes, int dir) {
   const Plan& pl = h->pl;
   const int P = pl.n_pulses, nd = pl.ndom;
   auto upper = [&](int r, int q) { return neighbour(pl, r, pl.pulse_dim[q], +1); };
   {
-    // tiles of each domain, cut on all host cores, then listed domain after domain;
-    // by_range: per (domain, range) the tiles' indices in slot order
+    // units of each domain, cut on all host cores, then listed domain after domain;
+    // by_range: per (domain, range) the units' indices in slot order
     std::vector<std::vector<TRec>> per(nd);
     std::vector<std::vector<std::vector<int>>> by_range(nd, std::vector<std::vector<int>>(P + 1));
     parallel_for(nd, [&](size_t ri) {
@@ -181,7 +181,7 @@ int build_tile_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::
           return e;
         };
         for (int a = lo, b = lo; a < lo + len; a = b) {
-          // at most kTile slots and kTileEntries entries (a slot has at most one entry per pulse)
+          // at most max_slots slots and max_entries entries (a slot has at most one entry per pulse)
           b = std::min(lo + len, a + max_slots);
           if (entries_in(a, b) > max_entries) {
             int good = a + 1, bad = b;
@@ -205,7 +205,7 @@ int build_tile_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::
             const int i1 = static_cast<int>(std::lower_bound(m, m + it.size, t.a) - m);
             const int i2 = static_cast<int>(std::lower_bound(m, m + it.size, t.a + t.n) - m);
             if (i2 <= i1) continue;
-            TileSeg sg;
+            UnitSeg sg;
             std::memset(&sg, 0, sizeof(sg));
             sg.map = it.map + i1;
             sg.other = it.dst + i1;
@@ -289,12 +289,12 @@ int build_tile_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::
       std::vector<char> waited(recs.size(), 0);
       for (auto& t : recs)
         for (int d : t.deps) waited[d] = 1;
-      std::vector<TileUnit> units;
-      std::vector<TileSeg> segs;   // segments past kInlineSegs
+      std::vector<Unit> units;
+      std::vector<UnitSeg> segs;   // segments past kInlineSegs
       std::vector<Wait> waits;
       for (int i : order) {
         const TRec& t = recs[i];
-        TileUnit u;
+        Unit u;
         std::memset(&u, 0, sizeof(u));
         u.base = h->dom_offset[t.r] + t.a;
         u.n = t.n;
@@ -302,9 +302,9 @@ int build_tile_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::
         u.seg_cnt = static_cast<int32_t>(t.segs.size());
         u.extra_off = static_cast<int32_t>(segs.size());
         // stage regions: each run's region starts on a 16-byte boundary and is 16 bytes longer than the run
-        int moff = tile_bytes, soff = tile_bytes + map_bytes;
+        int moff = slot_bytes, soff = slot_bytes + map_bytes;
         for (size_t k = 0; k < t.segs.size(); ++k) {
-          TileSeg sg = t.segs[k];
+          UnitSeg sg = t.segs[k];
           sg.map_off = moff;
           sg.src_off = dir == 1 ? soff : 0;
           moff += ((4 * sg.n + 15) & ~15) + 16;
@@ -313,14 +313,14 @@ int build_tile_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::
           else segs.push_back(sg);
         }
         // the stage regions must fit the kernel's buffer
-        if (moff > tile_bytes + map_bytes || (dir == 1 && soff > tile_bytes + map_bytes + src_bytes))
+        if (moff > slot_bytes + map_bytes || (dir == 1 && soff > slot_bytes + map_bytes + src_bytes))
           return HX_ERR_STATE;
         u.wait_off = static_cast<int32_t>(waits.size());
         u.wait_cnt = static_cast<int32_t>(t.deps.size());
         for (int d : t.deps) waits.push_back({pos[d], 1});
         u.flags = (waited[i] ? kSignal : 0) | (dir == 0 && t.range >= 0 ? kHaloSrc : 0);
         u.item = t.seg_pulse[0] * nd + t.r;
-        for (const TileSeg& sg : t.segs) u.entries += sg.n;
+        for (const UnitSeg& sg : t.segs) u.entries += sg.n;
         units.push_back(u);
       }
       h->n_units[dir] = static_cast<int>(units.size());
@@ -328,9 +328,9 @@ int build_tile_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::
       HX_CUDA(dev_alloc(&h->d_segs[dir], segs.size()));
       HX_CUDA(dev_alloc(&h->d_twaits[dir], waits.size()));
       if (!units.empty())
-        HX_CUDA(cudaMemcpy(h->d_units[dir], units.data(), sizeof(TileUnit) * units.size(), cudaMemcpyHostToDevice));
+        HX_CUDA(cudaMemcpy(h->d_units[dir], units.data(), sizeof(Unit) * units.size(), cudaMemcpyHostToDevice));
       if (!segs.empty())
-        HX_CUDA(cudaMemcpy(h->d_segs[dir], segs.data(), sizeof(TileSeg) * segs.size(), cudaMemcpyHostToDevice));
+        HX_CUDA(cudaMemcpy(h->d_segs[dir], segs.data(), sizeof(UnitSeg) * segs.size(), cudaMemcpyHostToDevice));
       if (!waits.empty())
         HX_CUDA(cudaMemcpy(h->d_twaits[dir], waits.data(), sizeof(Wait) * waits.size(), cudaMemcpyHostToDevice));
     }
@@ -573,8 +573,7 @@ int build_tables(hx_ctx* h, cudaStream_t s) {
       it.shift_flag = h->t_shift[t];
     }
   std::vector<int32_t> maps;
-  if ((fine || (h->flags & (HX_FLAG_TILES | HX_FLAG_SWEEP | HX_FLAG_SWEEP_FORCES | HX_FLAG_RESOLVED))) &&
-      h->total_entries > 0) {   // fine waits, units and resolved tables read the maps
+  if (h->total_entries > 0) {   // chunk records carry their map runs; fine waits, units and resolved tables read them
     maps.resize(h->total_entries);
     // the maps were assembled on `s`, which need not synchronise with the legacy stream
     HX_CUDA(cudaMemcpyAsync(maps.data(), h->d_maps, sizeof(int32_t) * h->total_entries, cudaMemcpyDeviceToHost, s));
@@ -586,33 +585,28 @@ int build_tables(hx_ctx* h, cudaStream_t s) {
   auto upper = [&](int r, int q) { return upper_tab[static_cast<size_t>(r) * P + q]; };
   std::vector<int64_t> rank(nd);
   for (int r = 0; r < nd; ++r) rank[r] = domain_rank(pl, r);
-  h->family[0] = (h->flags & HX_FLAG_TILES)     ? kFamTiles
-                 : (h->flags & HX_FLAG_SWEEP)   ? kFamSweep
+  h->family[0] = (h->flags & HX_FLAG_SWEEP)   ? kFamSweep
                  : (h->flags & HX_FLAG_CLUSTER) ? kFamCluster
                  : (h->flags & HX_FLAG_RESOLVED) ? kFamResolved
                                                 : kFamChunks;
   h->family[1] = (h->flags & (HX_FLAG_SWEEP | HX_FLAG_SWEEP_FORCES)) ? kFamSweep : h->family[0];
   for (int k = 0; k < 2; ++k) {
-    const int per_sm = std::max(1, h->family[k] == kFamTiles     ? tiles_blocks_per_sm(k)
-                                   : h->family[k] == kFamSweep   ? sweep_blocks_per_sm(k)
+    const int per_sm = std::max(1, h->family[k] == kFamSweep   ? sweep_blocks_per_sm(k)
                                    : h->family[k] == kFamCluster ? 1
                                    : h->family[k] == kFamResolved ? 1
-                                                                 : max_blocks_per_sm(kernel_for(h, k)));
+                                                                 : max_blocks_per_sm(kernel_for(h, k), fused_smem(h, k)));
     h->grid[k] = per_sm * h->sm_count;   // upper bound; trimmed to the work count below
   }
   // Unit lists. A dependent unit is placed a few resident windows after the
-  // units it waits for: tile mode three stages per block, sweep eight units
-  // per resident warp (measured on the 12M-atom workload: lags of 2, 3, 4, 6
-  // and 10 windows gave forces in 112.6, 100.5, 94.2, 92.2 and 92.2 us).
+  // units it waits for: eight units per resident warp (measured on the
+  // 12M-atom workload: lags of 2, 3, 4, 6 and 10 windows gave forces in
+  // 112.6, 100.5, 94.2, 92.2 and 92.2 us).
   for (int dir = 0; dir < 2; ++dir) {
     int rc = HX_OK;
-    if (h->family[dir] == kFamTiles) {
-      rc = build_tile_tables(h, items, maps, rank, kTile, kTileEntries, 3ll * h->grid[dir], kTile * 12 + 16,
-                             kTileEntries * 4 + 32 * kTileSegs, kTileEntries * 12 + 32 * kTileSegs, dir);
-    } else if (h->family[dir] == kFamSweep) {
+    if (h->family[dir] == kFamSweep) {
       if (P > kSweepSegs) return HX_ERR_PULSES;   // a unit's runs must fit one warp's stage
-      rc = build_tile_tables(h, items, maps, rank, kSweepSlots, kSweepEntries, 8ll * h->grid[dir] * kWarps,
-                             kSweepTileBytes, kSweepMapBytes, kSweepSrcBytes, dir);
+      rc = build_unit_tables(h, items, maps, rank, kSweepSlots, kSweepEntries, 8ll * h->grid[dir] * kWarps,
+                             kSweepSlotBytes, kSweepMapBytes, kSweepSrcBytes, dir);
     }
     if (rc != HX_OK) return rc;
   }
@@ -791,14 +785,15 @@ int build_tables(hx_ctx* h, cudaStream_t s) {
     for (size_t k = 0; k < order.size(); ++k) pos[order[k]] = static_cast<int>(k);
     std::vector<int> item_chunks(std::max(n_items, 1), 0);
     for (auto& rc : recs) item_chunks[rc.item] += 1;
-    std::vector<Chunk> chunks;
+    std::vector<ChunkSlot> chunks(order.size());
     std::vector<Wait> waits;
-    chunks.reserve(order.size());
-    for (int ri : order) {
+    for (size_t k = 0; k < order.size(); ++k) {
+      const int ri = order[k];
       const Rec& rc = recs[ri];
       const ItemInfo& it = items[rc.item];
-      Chunk ch;
-      std::memset(&ch, 0, sizeof(ch));
+      ChunkSlot& slot = chunks[k];
+      std::memset(&slot, 0, sizeof(slot));
+      Chunk& ch = slot.rec;
       ch.src = it.src;
       ch.dst = it.dst + rc.begin;
       ch.map = it.map + rc.begin;
@@ -812,15 +807,17 @@ int build_tables(hx_ctx* h, cudaStream_t s) {
       ch.flags = (rc.halo_src ? kHaloSrc : 0) | (sig ? kSignal : 0) | (dir == 0 && it.shift_flag ? kShift : 0);
       ch.dim = it.dim;
       ch.shift = pl.boxf[it.dim];
-      chunks.push_back(ch);
+      if (ch.n > 0) std::memcpy(slot.map, maps.data() + ch.map, sizeof(int32_t) * ch.n);
     }
     if (!fine)
       for (auto& w : waits) w.chunks = item_chunks[w.item];
+    for (auto& slot : chunks)   // the first waits of each chunk inside its record
+      for (int w = 0; w < std::min(slot.rec.wait_cnt, kWaitSlots); ++w) slot.waits[w] = waits[slot.rec.wait_off + w];
     h->n_chunks[dir] = static_cast<int>(chunks.size());
     HX_CUDA(dev_alloc(&h->d_chunks[dir], chunks.size()));
     HX_CUDA(dev_alloc(&h->d_waits[dir], waits.size()));
     if (!chunks.empty())
-      HX_CUDA(cudaMemcpy(h->d_chunks[dir], chunks.data(), sizeof(Chunk) * chunks.size(), cudaMemcpyHostToDevice));
+      HX_CUDA(cudaMemcpy(h->d_chunks[dir], chunks.data(), sizeof(ChunkSlot) * chunks.size(), cudaMemcpyHostToDevice));
     if (!waits.empty())
       HX_CUDA(cudaMemcpy(h->d_waits[dir], waits.data(), sizeof(Wait) * waits.size(), cudaMemcpyHostToDevice));
   }
@@ -864,8 +861,8 @@ int build_tables(hx_ctx* h, cudaStream_t s) {
   HX_CUDA(dev_alloc(&h->d_flags, 2 * h->n_flags));
   HX_CUDA(dev_alloc(&h->d_blk, 2 * h->n_flags));
   HX_CUDA(dev_alloc(&h->d_ctrl, 2));
-  // Persistent grid: every warp (tile mode: every block) co-resident, and no
-  // more of them than there is work.
+  // Persistent grid: every warp co-resident, and no more of them than there
+  // is work.
   for (int k = 0; k < 2; ++k) {
     if (h->family[k] == kFamResolved) {
       // coordinates: one block per halo segment; forces: general blocks, then record blocks
@@ -875,8 +872,6 @@ int build_tables(hx_ctx* h, cudaStream_t s) {
       h->grid[k] = static_cast<int>(std::max<int64_t>(1, k == 0 ? h->n_res_segs : fb));
     } else if (h->family[k] == kFamCluster) {
       h->grid[k] = kClusterCtas;   // exactly one cluster
-    } else if (h->family[k] == kFamTiles) {
-      h->grid[k] = std::max(1, std::min(h->n_units[k], h->grid[k]));
     } else if (h->family[k] == kFamSweep) {   // one warp per batch of units
       const int warps = std::max(1, std::min((h->n_units[k] + kSweepBatch - 1) / kSweepBatch, h->grid[k] * kWarps));
       h->grid[k] = (warps + kWarps - 1) / kWarps;

@@ -29,7 +29,6 @@ HX_FLAG_UNORDERED_FORCES = 0x1
 HX_FLAG_NO_GRAPH = 0x2
 HX_FLAG_COUNTER_SIGNAL = 0x4
 HX_FLAG_FINE_WAITS = 0x8
-HX_FLAG_TILES = 0x10
 HX_FLAG_SWEEP = 0x20
 HX_FLAG_SWEEP_FORCES = 0x40
 HX_FLAG_CLUSTER = 0x80

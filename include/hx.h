@@ -42,6 +42,8 @@
  * Conventions: every pointer argument is a device pointer unless marked
  * "host". `stream` is a cudaStream_t passed as void* (NULL = legacy default
  * stream). Calls are asynchronous on `stream` unless marked "synchronises".
+ * A call that needs the handle's device makes it current for its duration
+ * and gives the calling thread's current device back before it returns.
  * Return value: HX_OK (0) or a negative HX_ERR_* code; no call throws, and
  * there is no CPU fallback: a handle exists only on a working CUDA device.
  * The library owns the maps, tables, flags and graphs of a handle until
@@ -84,23 +86,18 @@ typedef struct hx_ctx* hx_handle;
                                           chunks that wrote the slots it reads or, for forces, that
                                           add into its targets, each signalled by its own epoch flag
                                           (HX_FLAG_COUNTER_SIGNAL is then ignored) */
-#define HX_FLAG_TILES 0x10u            /* tile-staged kernels: a producer warp per block copies tiles of
-                                          up to 1024 consecutive slots of one sender into shared memory
-                                          (TMA bulk copies) and consumer warps serve every pulse's
-                                          gathers (coordinates) or reverse-ordered adds (forces) from
-                                          them; per-tile signals; same results bit for bit */
-#define HX_FLAG_SWEEP 0x20u            /* slot-sweep kernels: every warp takes units of up to 512
-                                          consecutive slots of one sender, copies them into its shared
-                                          memory with coalesced loads and serves every pulse's gathers
-                                          or reverse-ordered adds from them; per-unit signals; same
-                                          results bit for bit. Plans of more than 8 pulses get
-                                          HX_ERR_PULSES from hx_build_maps */
+#define HX_FLAG_SWEEP 0x20u            /* slot-sweep kernels: every warp takes units of up to 256
+                                          consecutive slots of one sender, stages them in its shared
+                                          memory with TMA bulk copies (cp.async.bulk) and serves every
+                                          pulse's gathers or reverse-ordered adds from them; per-unit
+                                          signals; same results bit for bit. Plans of more than 8
+                                          pulses get HX_ERR_PULSES from hx_build_maps */
 #define HX_FLAG_SWEEP_FORCES 0x40u     /* the force exchange by the slot-sweep kernel, the coordinate
                                           exchange by the chunk kernels (with HX_FLAG_FINE_WAITS or
                                           the other chunk flags) or, with HX_FLAG_RESOLVED, by the
-                                          resolved gather. At most one of HX_FLAG_TILES,
-                                          HX_FLAG_SWEEP, HX_FLAG_CLUSTER and HX_FLAG_RESOLVED, and
-                                          HX_FLAG_SWEEP_FORCES with none of the first three (else
+                                          resolved gather. At most one of HX_FLAG_SWEEP,
+                                          HX_FLAG_CLUSTER and HX_FLAG_RESOLVED, and
+                                          HX_FLAG_SWEEP_FORCES with neither of the first two (else
                                           HX_ERR_ARG) */
 #define HX_FLAG_CLUSTER 0x80u          /* both directions by one thread-block cluster of 8 CTAs that
                                           walks the pulses in order (forces in reverse), with a
@@ -135,6 +132,8 @@ typedef struct hx_ctx* hx_handle;
                                           HX_ERR_CAPACITY: a halo slot's origin and shifts share one
                                           32-bit word) */
 
+#define HX_FLAGS_ALL 0x7efu      /* every flag above */
+
 #define HX_MAX_PULSES 32
 #define HX_MAX_DOMAINS 4096
 
@@ -150,8 +149,12 @@ int hx_query_plan(const double box[3], const int dims[3], double cutoff,
 /* Creates a handle on CUDA device `device`. box (host, nm), dims (host),
  * cutoff (nm). timeout_us bounds every device-side wait for a pulse signal
  * (0 selects 1 s); a wait that runs out sets HX_ERR_TIMEOUT, read by
- * hx_status, and the kernel still finishes. Errors: HX_ERR_ARG,
- * HX_ERR_PULSES, HX_ERR_CUDA (no usable device), HX_ERR_NOMEM. */
+ * hx_status, and the kernel still finishes. flags: HX_FLAG_* above; a bit
+ * outside them is HX_ERR_ARG. Errors: HX_ERR_ARG, HX_ERR_PULSES, HX_ERR_CUDA
+ * (no usable device), HX_ERR_NOMEM.
+ * Pages: the pulse plan of "Dependency-aware packing" (Z -> Y -> X, one
+ * pulse per dimension when the cutoff fits one neighbour, more otherwise);
+ * the box, slab and cutoff geometry is not on the pages (readings above). */
 int hx_init(hx_handle* out, const double box[3], const int dims[3], double cutoff,
             int device, unsigned flags, unsigned timeout_us);
 
@@ -171,7 +174,10 @@ int hx_init(hx_handle* out, const double box[3], const int dims[3], double cutof
 int hx_build_maps(hx_handle h, const float* pos_in, int64_t n_atoms,
                   float* coords, int64_t capacity, int64_t* needed, void* stream);
 
-/* Sizes after a build (host outputs; any may be NULL). */
+/* Sizes after a build (host outputs; any may be NULL): domains, pulses,
+ * slots of the layout, map entries. Not on the pages (they take the maps'
+ * sizes as given: packSendBufKernel's `size`, the fused kernel's per-pulse
+ * send sizes); this reports what hx_build_maps derived. */
 int hx_get_counts(hx_handle h, int* n_domains, int* n_pulses, int64_t* total_slots,
                   int64_t* total_entries);
 
@@ -183,11 +189,16 @@ int hx_get_counts(hx_handle h, int* n_domains, int* n_pulses, int64_t* total_slo
 int hx_get_resolved_counts(hx_handle h, int64_t* n_pairs, int64_t* n_quads, int64_t* n_general);
 
 /* Per-domain layout (host arrays of n_domains entries; any may be NULL):
- * first slot, home-atom count, halo-slot count. */
+ * first slot, home-atom count, halo-slot count. Pages: "From MPI baseline to
+ * optimized GPU-native halo exchange" (received halo data lands in the
+ * coordinate buffer at its offset after the home atoms; the fused kernel's
+ * atomOffsetInPeer). */
 int hx_get_layout(hx_handle h, int64_t* dom_offset, int32_t* home_count, int32_t* halo_count);
 
 /* home_ids (device, int32 [n_atoms]): for the k-th home slot in layout order
- * (domain 0's home atoms, then domain 1's, ...) the input index of its atom. */
+ * (domain 0's home atoms, then domain 1's, ...) the input index of its atom.
+ * Not on the pages (their ranks own their atoms from the start); it maps the
+ * layout back to the caller's input order. */
 int hx_get_home_ids(hx_handle h, int32_t* home_ids, void* stream);
 
 /* Copies the maps to host for inspection (synchronises). maps_host (host,
@@ -261,32 +272,43 @@ int hx_exchange_forces_unfused(hx_handle h, float* forces, void* stream);
  * control block live in one fixed file-scope device array of
  * HX_STATIC_MAX_FLAGS flags (about 1.5 MB, held by every GPU that loads the
  * library until the process exits), cleared on `stream` at each call, and
- * the kernel is launched directly, without a CUDA graph. The first call on a
- * device looks up that array's device address (cudaGetSymbolAddress); make
- * that first call before any stream capture. All calls share the one array,
- * so calls whose work overlaps on the GPU (other streams, other handles on
- * the same device) race: serialise them. Device-side time-outs of this call
- * are recorded in that array, not in the handle (hx_status does not see
- * them). Errors: HX_ERR_ARG, HX_ERR_STATE, HX_ERR_CUDA, and HX_ERR_CAPACITY
- * when the handle's work list needs more than HX_STATIC_MAX_FLAGS signal
- * flags (its item count, chunk count or unit count, whichever it signals by);
+ * the kernel is launched directly, without a CUDA graph. hx_build_maps does
+ * the set-up, with the handle's device current: it looks up that array's
+ * device address (cudaGetSymbolAddress) and loads the kernel this call
+ * launches, so the call itself only reads the handle. All calls share the
+ * one array, which keeps the last call's contents, so calls whose work
+ * overlaps on the GPU (other streams, other handles on the same device)
+ * race: serialise them. A device-side time-out of this call is reported by
+ * hx_status of the calling handle (after the stream this call ran on has
+ * passed it) until another handle makes a static call on the same device or
+ * hx_clear_status clears it. Errors: HX_ERR_ARG, HX_ERR_STATE, HX_ERR_CUDA
+ * (also when the build could not do the set-up), and HX_ERR_CAPACITY when
+ * the handle's work list needs more than HX_STATIC_MAX_FLAGS signal flags
+ * (its item count, chunk count or unit count, whichever it signals by);
  * nothing is launched then. */
 #define HX_STATIC_MAX_FLAGS 131072
 int hx_exchange_coords_static(hx_handle h, float* coords, void* stream);
 
 /* Launches one empty kernel the way the fused exchanges are launched (graph
  * or direct, per the handle's flags): the launch floor for latency
- * measurements. */
+ * measurements. Not on the pages; it measures the per-launch cost that
+ * "Strategies in a nutshell" (six launches fused into one) removes. */
 int hx_noop(hx_handle h, void* stream);
 
 /* Synchronises `stream` and returns the sticky device status: HX_OK or
  * HX_ERR_TIMEOUT (a wait for a pulse signal ran out). *detail (host, may be
  * NULL) receives direction*65536 + item (item = pulse*n_domains + sender)
- * of the first wait that gave up, or -1. */
+ * of the first wait that gave up, or -1. The regular exchanges' status comes
+ * first; then that of the handle's last hx_exchange_coords_static call, if
+ * no other handle has made one on the device since. Not on the pages (their
+ * signal waits are unbounded); the bounded wait and its status are the
+ * failure detection of this library. */
 int hx_status(hx_handle h, void* stream, int* detail);
 
-/* Synchronises `stream`, clears the status and resets every pulse signal,
- * counter and epoch so that the next exchange starts clean. */
+/* Synchronises `stream`, clears the status (the handle's, and the static
+ * path's when hx_status would report it) and resets every pulse signal,
+ * counter and epoch so that the next exchange starts clean. Not on the
+ * pages: the recovery half of hx_status. */
 int hx_clear_status(hx_handle h, void* stream);
 
 /* Fault injection for tests (host side, no device fault): the chunks of
@@ -294,10 +316,11 @@ int hx_clear_status(hx_handle h, void* stream);
  * so its waiters run into the timeout. domain = -1 switches it off. */
 int hx_debug_drop_signal(hx_handle h, int direction, int domain, int pulse);
 
-/* Human-readable name of an HX_* code (static string). */
+/* Human-readable name of an HX_* code (static string). Not on the pages. */
 const char* hx_error_string(int code);
 
-/* Frees everything the handle owns (synchronises its device). NULL is a no-op. */
+/* Frees everything the handle owns (synchronises its device). NULL is a no-op.
+ * Not on the pages (resource lifetime of this library). */
 void hx_destroy(hx_handle h);
 
 #ifdef __cplusplus

@@ -71,6 +71,7 @@ def test_init_validates_before_touching_a_device():
     d = np.array([2, 1, 1], np.int32)
     assert lib.hx_init(ctypes.byref(h), b.ctypes.data, d.ctypes.data, -1.0, 0, 0, 0) == HX.HX_ERR_ARG
     assert lib.hx_init(None, b.ctypes.data, d.ctypes.data, 1.0, 0, 0, 0) == HX.HX_ERR_ARG
+    assert lib.hx_init(ctypes.byref(h), b.ctypes.data, d.ctypes.data, 1.0, 0, 0x10, 0) == HX.HX_ERR_ARG   # no such flag
     assert lib.hx_exchange_coords(None, None, None) == HX.HX_ERR_ARG
     assert lib.hx_status(None, None, None) == HX.HX_ERR_ARG
     assert lib.hx_exchange_coords_host(None, None, None, None) == HX.HX_ERR_ARG

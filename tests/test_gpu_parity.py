@@ -17,8 +17,7 @@ pytestmark = pytest.mark.gpu
 
 ALL_MODES = [0, HX.HX_FLAG_COUNTER_SIGNAL, HX.HX_FLAG_NO_GRAPH,
              HX.HX_FLAG_COUNTER_SIGNAL | HX.HX_FLAG_NO_GRAPH, HX.HX_FLAG_FINE_WAITS,
-             HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_COUNTER_SIGNAL, HX.HX_FLAG_TILES,
-             HX.HX_FLAG_TILES | HX.HX_FLAG_NO_GRAPH, HX.HX_FLAG_SWEEP,
+             HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_COUNTER_SIGNAL, HX.HX_FLAG_SWEEP,
              HX.HX_FLAG_SWEEP | HX.HX_FLAG_NO_GRAPH, HX.HX_FLAG_SWEEP_FORCES,
              HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES, HX.HX_FLAG_CLUSTER,
              HX.HX_FLAG_CLUSTER | HX.HX_FLAG_NO_GRAPH, HX.HX_FLAG_RESOLVED,
@@ -126,7 +125,7 @@ def test_parity_configs(name, flags):
     check_force_steps(c)
 
 
-@pytest.mark.parametrize("flags", [0, HX.HX_FLAG_FINE_WAITS, HX.HX_FLAG_TILES, HX.HX_FLAG_SWEEP,
+@pytest.mark.parametrize("flags", [0, HX.HX_FLAG_FINE_WAITS, HX.HX_FLAG_SWEEP,
                                    HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES, HX.HX_FLAG_RESOLVED,
                                    HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE | HX.HX_FLAG_SWEEP_FORCES])
 def test_parity_c5_full_size(flags):
@@ -162,7 +161,7 @@ def test_unfused_baseline(name):
     ((3.0, 3.0, 3.0), (3, 3, 3), 0.6, 2700),      # 27 domains
     ((40.0, 3.0, 3.0), (40, 1, 1), 1.0, 36000),   # many small domains along one dim
 ])
-@pytest.mark.parametrize("flags", [0, HX.HX_FLAG_COUNTER_SIGNAL, HX.HX_FLAG_FINE_WAITS, HX.HX_FLAG_TILES,
+@pytest.mark.parametrize("flags", [0, HX.HX_FLAG_COUNTER_SIGNAL, HX.HX_FLAG_FINE_WAITS,
                                    HX.HX_FLAG_SWEEP, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES,
                                    HX.HX_FLAG_CLUSTER, HX.HX_FLAG_RESOLVED, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE])
 def test_parity_shapes(box, dims, cutoff, n, flags):
@@ -224,7 +223,7 @@ def test_resolved_tree_classes(name):
         assert Case(W.WORKLOADS[name], flags=HX.HX_FLAG_FINE_WAITS).hx.resolved_counts() == (0, 0, 0)
 
 
-@pytest.mark.parametrize("flags", [0, HX.HX_FLAG_TILES, HX.HX_FLAG_SWEEP])
+@pytest.mark.parametrize("flags", [0, HX.HX_FLAG_SWEEP])
 def test_misaligned_buffers(flags):
     """Caller buffers that start 4 or 8 bytes past a 16-byte boundary (tile
     mode copies aligned middles in bulk and the edges with plain loads)."""
@@ -264,7 +263,7 @@ def test_boundary_atoms():
 
 def test_many_steps_reuse_signals():
     """Epoch-valued signals are never reset between launches: 200 steps."""
-    for flags in (0, HX.HX_FLAG_COUNTER_SIGNAL, HX.HX_FLAG_FINE_WAITS, HX.HX_FLAG_TILES, HX.HX_FLAG_SWEEP,
+    for flags in (0, HX.HX_FLAG_COUNTER_SIGNAL, HX.HX_FLAG_FINE_WAITS, HX.HX_FLAG_SWEEP,
                   HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES, HX.HX_FLAG_CLUSTER, HX.HX_FLAG_RESOLVED,
                   HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE, HX.HX_FLAG_RESOLVED | HX.HX_FLAG_PDL):
         c = Case(W.WORKLOADS["C2"], flags=flags)
@@ -337,8 +336,7 @@ def test_errors():
     with pytest.raises(HX.HXError) as ei:
         hx.build_maps(pos, small)
     assert ei.value.code == HX.HX_ERR_CAPACITY
-    for bad in (HX.HX_FLAG_TILES | HX.HX_FLAG_SWEEP, HX.HX_FLAG_SWEEP | HX.HX_FLAG_SWEEP_FORCES,
-                HX.HX_FLAG_TILES | HX.HX_FLAG_SWEEP_FORCES, HX.HX_FLAG_CLUSTER | HX.HX_FLAG_SWEEP_FORCES,
+    for bad in (HX.HX_FLAG_SWEEP | HX.HX_FLAG_SWEEP_FORCES, HX.HX_FLAG_CLUSTER | HX.HX_FLAG_SWEEP_FORCES,
                 HX.HX_FLAG_RESOLVED | HX.HX_FLAG_CLUSTER, HX.HX_FLAG_CLUSTER | HX.HX_FLAG_SWEEP):
         with pytest.raises(HX.HXError) as ei:   # the unit kernel families are alternatives
             HX.HaloExchange(w.box, w.dims, w.cutoff, flags=bad)
@@ -348,7 +346,7 @@ def test_errors():
 
 
 @pytest.mark.parametrize("direction", [0, 1])
-@pytest.mark.parametrize("flags", [0, HX.HX_FLAG_COUNTER_SIGNAL, HX.HX_FLAG_FINE_WAITS, HX.HX_FLAG_TILES,
+@pytest.mark.parametrize("flags", [0, HX.HX_FLAG_COUNTER_SIGNAL, HX.HX_FLAG_FINE_WAITS,
                                    HX.HX_FLAG_SWEEP, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES,
                                    HX.HX_FLAG_BULK_STORE, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE])
 def test_dropped_signal_times_out_and_recovers(direction, flags):
@@ -375,7 +373,7 @@ def test_dropped_signal_times_out_and_recovers(direction, flags):
     assert detail // 65536 == direction
     item = detail % 65536
     p_item = item // nd
-    if flags & (HX.HX_FLAG_TILES | HX.HX_FLAG_SWEEP) or (direction == 1 and flags & HX.HX_FLAG_SWEEP_FORCES):
+    if flags & HX.HX_FLAG_SWEEP or (direction == 1 and flags & HX.HX_FLAG_SWEEP_FORCES):
         # a unit is labelled by its first map's (pulse, domain); a cascade can
         # report any unit downstream of the dropped one
         assert 0 <= item < c.o.n_pulses * nd
