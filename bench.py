@@ -142,6 +142,52 @@ def kernel_impl(flags: int, direction: int) -> str:
     return f"k_forces_fused<{mode}, {order}> (chunks)"
 
 
+def traffic_floor(hx):
+    """DRAM bytes one launch of each direction must move at the least, from
+    the maps: every DRAM unit (32-byte sector, 64-byte granule) that holds a
+    byte the launch must read from or write to DRAM, counted once per
+    direction of transfer.
+
+    Coordinates read the home slots they gather (halo sources are written by
+    the same launch and may stay in L2) and the maps, and write every
+    received slot. Forces read every received slot (the halo forces) and
+    every target slot, and write every target slot, and read the maps."""
+    import numpy as np
+    maps, table = hx.maps()
+    off, home, _ = hx.layout()
+    n_p, nd, _ = table.shape
+    src, dst = [], []
+    home_end = {}
+    for p in range(n_p):
+        for r in range(nd):
+            m_off, size, q, r_off, _, _ = (int(v) for v in table[p, r])
+            if size == 0:
+                continue
+            src.append(int(off[r]) + maps[m_off:m_off + size].astype(np.int64))
+            dst.append(int(off[q]) + r_off + np.arange(size, dtype=np.int64))
+    if not src:
+        z = {"coords": 0, "forces": 0}
+        return {"sector_32B": z, "granule_64B": dict(z)}
+    src, dst = np.concatenate(src), np.concatenate(dst)
+    dom_of_slot = np.searchsorted(off, src, side="right") - 1
+    src_home = src[src < off[dom_of_slot] + home[dom_of_slot]]
+    entries = src.size
+    total_bytes = 12 * (int(max(dst.max(), src.max())) + 1)
+    out = {}
+    for g, name in ((32, "sector_32B"), (64, "granule_64B")):
+        def units(slots):   # bitmap of the g-byte units holding any byte of the slots
+            bm = np.zeros(total_bytes // g + 2, dtype=bool)
+            bm[(12 * slots) // g] = True
+            bm[(12 * slots + 11) // g] = True
+            return bm
+        n_map = -(-4 * entries // g)
+        u_dst, u_src = units(dst), units(src)
+        coords = g * (int(units(src_home).sum()) + n_map + int(u_dst.sum()))
+        forces = g * (int((u_dst | u_src).sum()) + n_map + int(u_src.sum()))
+        out[name] = {"coords": int(coords), "forces": int(forces)}
+    return out
+
+
 def profiled_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary of this kernel,
     if it was taken on the current kernel source; else None."""
@@ -255,13 +301,24 @@ def run_ours(args):
         hx.exchange_coords(coords)
         hx.exchange_forces(forces)
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     clocks = Clocks(local) if rank == 0 else None
+    # the timed region: K steps back to back, events only at its two ends
     start.record(stream)
+    for _ in range(K):
+        hx.exchange_coords(coords)
+        hx.exchange_forces(forces)
+    end.record(stream)
+    torch.cuda.synchronize()
+    total_ms = start.elapsed_time(end)
+    # the same K steps again with an event around every launch: the kernels'
+    # own durations (the roofline's achieved bytes per second) and the per-step
+    # distribution; the events between launches cost a few microseconds per
+    # step, so the main value comes from the pass above
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     for k in range(K):
         a, b, c = ev[k]
         a.record(stream)
@@ -269,10 +326,8 @@ def run_ours(args):
         b.record(stream)
         hx.exchange_forces(forces)
         c.record(stream)
-    end.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop() if clocks else None
-    total_ms = start.elapsed_time(end)
     coord_ms = statistics.fmean(e[0].elapsed_time(e[1]) for e in ev)
     force_ms = statistics.fmean(e[1].elapsed_time(e[2]) for e in ev)
     per_step_us = [e[0].elapsed_time(e[2]) * 1e3 for e in ev]
@@ -346,6 +401,20 @@ def run_ours(args):
     dom_ms = max(force_ms, coord_ms)
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
     step_gbs = (BYTES_COORD + BYTES_FORCE) * entries / (us_step * 1e-6) / 1e9
+    floors = traffic_floor(hx)
+    per_kernel = {}
+    for name, ms, per_entry, key in (("hx_coords_fused", coord_ms, BYTES_COORD, "coords"),
+                                     ("hx_forces_fused", force_ms, BYTES_FORCE, "forces")):
+        fb = floors["granule_64B"][key]
+        per_kernel[name] = {
+            "kernel_impl": kernel_impl(flags, 0 if key == "coords" else 1),
+            "us": round(ms * 1e3, 2), "algorithmic_bytes": per_entry * entries,
+            "achieved_gbs": round(per_entry * entries / (ms * 1e-3) / 1e9, 1),
+            "frac": round(per_entry * entries / (ms * 1e-3) / 1e9 / peak, 4),
+            "floor_bytes": fb, "floor_bytes_32B": floors["sector_32B"][key],
+            "frac_of_floor": round(fb / (ms * 1e-3) / 1e9 / peak, 4),
+            "frac_ceiling": round(per_entry * entries / fb, 4),
+            "traffic": profiled_traffic(name, w.name)}
     out = {
         "metric": METRIC,
         "value": round(us_step, 3),
@@ -374,9 +443,17 @@ def run_ours(args):
             "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
             "algorithmic_bytes_per_launch": dom_bytes,
             "traffic": profiled_traffic(dominant, w.name),
+            "floor_bytes": per_kernel[dominant]["floor_bytes"],
+            "frac_of_floor": per_kernel[dominant]["frac_of_floor"],
+            "floor_what": "distinct 64-byte DRAM granules a launch must read or write, from the maps "
+                          "(32-byte sectors beside it); frac_of_floor = floor bytes / launch time / peak; "
+                          "frac_ceiling = the algorithmic frac reached at that floor and the full peak",
+            "kernels": per_kernel,
         },
         "kernels_ms": {"hx_coords_fused": round(coord_ms, 5), "hx_forces_fused": round(force_ms, 5)},
         "step_us_distribution": step_distribution(per_step_us),
+        "step_us_distribution_what": "per-step event times of a second pass of the K steps with an event around "
+                                     "every launch (the kernels' durations come from it)",
         "clocks": clk,
         "e2e": {"value": round(e2e_us, 2), "unit": "us/step", "h2d_bytes_per_step": bytes_h2d,
                 "d2h_bytes_per_step": bytes_d2h,
@@ -384,6 +461,7 @@ def run_ours(args):
                         "buffers: home coordinates and every force in, halo coordinates and home forces out; "
                         "two handles on two streams take alternate steps"},
         "gpu_launches": 2 * K,
+        "gpu_launches_what": "libhx kernel launches in the timed region: one per direction per step",
         "build_maps_us": round(statistics.median(t_build), 1),
     }
     if rank == 0 and not args.no_extras:
@@ -434,17 +512,46 @@ def secondary(hx_main, coords, forces, w_main, dev, peak, flags):
             ts.append(a.elapsed_time(b) * 1e3)
         return step_distribution(ts) if dist else statistics.median(ts)
 
-    def floor(hx, reps=300):
-        ts = []
+    def floors(hx, reps=300):
+        """Launch floors measured like the steps: one empty launch alone, two
+        empty launches alone (a single step's shape), and two empty launches
+        back to back (a back-to-back step's shape)."""
+        one, two = [], []
         for _ in range(reps):
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
+            a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            torch.cuda.synchronize()
             a.record(stream)
             hx.noop()
             b.record(stream)
+            hx.noop()
+            c.record(stream)
             torch.cuda.synchronize()
-            ts.append(a.elapsed_time(b) * 1e3)
-        return statistics.median(ts)
+            one.append(a.elapsed_time(b) * 1e3)
+            two.append(a.elapsed_time(c) * 1e3)
+        n = 2000
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n):
+            hx.noop()
+            hx.noop()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return statistics.median(one), statistics.median(two), a.elapsed_time(b) * 1e3 / n
+
+    def per_direction(hx, x, f, reps=200):
+        cs, fs = [], []
+        for _ in range(reps):
+            a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            torch.cuda.synchronize()
+            a.record(stream)
+            hx.exchange_coords(x)
+            b.record(stream)
+            hx.exchange_forces(f)
+            c.record(stream)
+            torch.cuda.synchronize()
+            cs.append(a.elapsed_time(b) * 1e3)
+            fs.append(b.elapsed_time(c) * 1e3)
+        return statistics.median(cs), statistics.median(fs)
 
     # the probe in the run's modes, and with both directions on the chunk kernels
     from domain_decomposition_halo_gb300 import hx as HX
@@ -480,14 +587,21 @@ def secondary(hx_main, coords, forces, w_main, dev, peak, flags):
         torch.cuda.synchronize()
         back_to_back = a.elapsed_time(b) * 1e3 / n
         single = timed(hx, x, f, 300, name == "C4")
-        fl = floor(hx)
+        c_us, f_us = per_direction(hx, x, f)
+        one, two, two_b2b = floors(hx)
+        rc, _ = hx.status()
+        if rc != 0:
+            raise RuntimeError(f"{name}: device status {rc}")
         entry = {"us_step_back_to_back": round(back_to_back, 2), "us_step_single": round(single, 2),
-                 "launch_floor_us": round(fl, 2), "back_to_back_over_floor": round(back_to_back / fl, 2),
-                 "single_over_floor": round(single / fl, 2),
+                 "us_coords_single": round(c_us, 2), "us_forces_single": round(f_us, 2),
+                 "floor_one_launch_us": round(one, 2), "floor_two_launches_us": round(two, 2),
+                 "floor_two_launches_back_to_back_us": round(two_b2b, 2),
+                 "single_over_single_floor": round(single / two, 2),
+                 "back_to_back_over_back_to_back_floor": round(back_to_back / two_b2b, 2),
                  "map_entries": ent,
                  "frac_of_peak_back_to_back": round(68 * ent / (back_to_back * 1e-6) / 1e9 / peak, 4)}
         if name == "C4":
-            entry["cold_l2"] = True
+            entry["single_is_cold_l2"] = True
         del hx
         return entry
 
@@ -515,7 +629,11 @@ def overlap_probe(dev, flags, names=("C2", "C4"), reps=40):
     fused path (one launch per direction) and the per-pulse unfused path (one
     launch per pulse and direction). Two local workloads: memory-bound
     (`_loaded`: short-block elementwise kernels over 256 MB) and
-    compute-bound (`_loaded_compute`: bf16 8192^3 matrix products)."""
+    compute-bound (`_loaded_compute`: bf16 8192^3 matrix products). Every
+    step starts from the same inputs (halo coordinates poisoned with NaN) and
+    its results are compared bit for bit with an exchange on the idle GPU;
+    the device status is read after each step. A mismatch or a time-out
+    raises."""
     import torch
 
     from domain_decomposition_halo_gb300 import HaloExchange
@@ -534,7 +652,18 @@ def overlap_probe(dev, flags, names=("C2", "C4"), reps=40):
         slots = hx.build_maps(pos)
         x = torch.empty((slots, 3), device=dev)
         hx.build_maps(pos, x)
-        f = torch.from_numpy(W.forces(w, slots)).to(dev)
+        off, home_n, _ = hx.layout()
+        home = torch.zeros(slots, dtype=torch.bool, device=dev)
+        for r in range(len(off)):
+            home[int(off[r]): int(off[r]) + int(home_n[r])] = True
+        x0 = x.clone()
+        x0[~home] = float("nan")
+        f0 = torch.from_numpy(W.forces(w, slots)).to(dev)
+        x_ref, f_ref = x0.clone(), f0.clone()
+        hx.exchange_coords(x_ref)
+        hx.exchange_forces(f_ref)
+        f = f0.clone()
+        torch.cuda.synchronize()
         res = {}
         for fused in (True, False):
             def step():
@@ -547,6 +676,8 @@ def overlap_probe(dev, flags, names=("C2", "C4"), reps=40):
             for loaded in ("", "_loaded", "_loaded_compute"):
                 ts = []
                 for _ in range(reps):
+                    x.copy_(x0)
+                    f.copy_(f0)
                     torch.cuda.synchronize()
                     if loaded:
                         with torch.cuda.stream(lo):
@@ -564,8 +695,15 @@ def overlap_probe(dev, flags, names=("C2", "C4"), reps=40):
                     b.record(hi)
                     torch.cuda.synchronize()
                     ts.append(a.elapsed_time(b) * 1e3)
+                    rc, detail = hx.status(stream=hi)
+                    if rc != 0:
+                        raise RuntimeError(f"overlap probe {name}: device status {rc} (detail {detail})")
+                    if not (torch.equal(x.view(torch.int32), x_ref.view(torch.int32)) and
+                            torch.equal(f.view(torch.int32), f_ref.view(torch.int32))):
+                        raise RuntimeError(f"overlap probe {name}: results differ from the idle exchange")
                 res[("fused" if fused else "unfused") + (loaded or "_idle")] = round(statistics.median(ts), 2)
         res["launches_per_step"] = {"fused": 2, "unfused": 2 * hx.counts()[1]}
+        res["checked"] = "every step bit-exact against the idle exchange, status OK"
         out[name] = res
         del hx
     return out

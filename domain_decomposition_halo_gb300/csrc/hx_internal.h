@@ -249,7 +249,7 @@ enum Family : int { kFamChunks = 0, kFamSweep = 2, kFamCluster = 3, kFamResolved
 constexpr int kSweepSlots = HX_SWEEP_SLOTS;       // slots of one unit: a warp's staged tile
 constexpr int kSweepEntries = HX_SWEEP_ENTRIES;   // map entries of one unit at most
 #ifndef HX_SWEEP_BATCH
-#define HX_SWEEP_BATCH 2
+#define HX_SWEEP_BATCH 1
 #endif
 constexpr int kSweepBatch = HX_SWEEP_BATCH;       // consecutive units a warp takes in one claim
 constexpr int kSweepSegs = 8;                     // segments (pulses) of one unit at most
