@@ -50,7 +50,7 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU baseline budget")
     ap.add_argument("--flags", default="fine,bulkstore,sweepf",
                     help="comma list of libhx modes: fine, bulkstore (coordinates packed by bulk stores), sweepf "
-                         "(forces by the slot sweep), sweep, cluster, resolved, counter, nograph, unordered, "
+                         "(forces by the slot sweep), sweep, resolved, counter, nograph, unordered, "
                          "pages (= none)")
     return ap.parse_args()
 
@@ -59,7 +59,7 @@ def hx_flags(spec: str) -> int:
     from domain_decomposition_halo_gb300 import hx as HX
     table = {"fine": HX.HX_FLAG_FINE_WAITS, "counter": HX.HX_FLAG_COUNTER_SIGNAL, "nograph": HX.HX_FLAG_NO_GRAPH,
              "unordered": HX.HX_FLAG_UNORDERED_FORCES, "sweep": HX.HX_FLAG_SWEEP,
-             "sweepf": HX.HX_FLAG_SWEEP_FORCES, "cluster": HX.HX_FLAG_CLUSTER,
+             "sweepf": HX.HX_FLAG_SWEEP_FORCES,
              "resolved": HX.HX_FLAG_RESOLVED, "bulkstore": HX.HX_FLAG_BULK_STORE,
              "pdl": HX.HX_FLAG_PDL, "pages": 0, "": 0}
     flags = 0
@@ -128,8 +128,6 @@ def kernel_impl(flags: int, direction: int) -> str:
     from domain_decomposition_halo_gb300 import hx as HX
     if flags & HX.HX_FLAG_SWEEP or (direction == 1 and flags & HX.HX_FLAG_SWEEP_FORCES):
         return f"k_sweep<{direction}> (slot sweep)"
-    if flags & HX.HX_FLAG_CLUSTER:
-        return f"k_cluster<{direction}> (one cluster)"
     if flags & HX.HX_FLAG_RESOLVED:
         return "k_resolved_coords (resolved)" if direction == 0 else "k_resolved_forces (resolved)"
     mode = ("chunk flags" if flags & HX.HX_FLAG_FINE_WAITS else

@@ -192,7 +192,6 @@ UnitParams unit_params(hx_ctx* h, int dir) {
 
 // Work items of the fused list of direction `dir`: units or chunks.
 int work_items(const hx_ctx* h, int dir) {
-  if (h->family[dir] == kFamCluster) return h->u_begin.empty() ? 0 : h->u_begin.back();
   if (h->family[dir] == kFamResolved)
     return static_cast<int>(dir == 0 ? h->n_res_halo : h->n_res_pairs + h->n_res_quads + h->n_res_trees);
   return h->family[dir] == kFamChunks ? h->n_chunks[dir] : h->n_units[dir];
@@ -201,12 +200,10 @@ int work_items(const hx_ctx* h, int dir) {
 // Launch shape of a direction's fused kernel.
 const void* fused_kernel(hx_ctx* h, int dir) {
   if (h->family[dir] == kFamSweep) return sweep_kernel(dir);
-  if (h->family[dir] == kFamCluster) return cluster_kernel(dir);
   if (h->family[dir] == kFamResolved) return resolved_kernel(dir);
   return kernel_for(h, dir);
 }
 unsigned fused_threads(const hx_ctx* h, int dir) {
-  if (h->family[dir] == kFamCluster) return kClusterThreads;
   if (h->family[dir] == kFamResolved) return kResThreads;
   return kThreads;
 }
@@ -238,15 +235,6 @@ ResolvedParams resolved_params(hx_ctx* h) {
   return P;
 }
 
-ClusterParams cluster_params(hx_ctx* h) {
-  ClusterParams P;
-  std::memset(&P, 0, sizeof(P));
-  P.chunks = h->d_uchunks;
-  P.maps = h->d_maps;
-  P.n_pulses = h->pl.n_pulses;
-  for (int p = 0; p <= h->pl.n_pulses; ++p) P.begin[p] = h->u_begin[p];
-  return P;
-}
 size_t fused_smem(const hx_ctx* h, int dir) {
   if (h->family[dir] == kFamSweep) return sweep_smem_bytes(dir);
   if (h->family[dir] == kFamChunks) return chunk_smem_bytes(dir, dir == 0 && (h->flags & HX_FLAG_BULK_STORE));
@@ -256,7 +244,6 @@ size_t fused_smem(const hx_ctx* h, int dir) {
 int launch(hx_ctx* h, int kind, float* buf, cudaStream_t s) {
   DirParams P;
   UnitParams TP;
-  ClusterParams CP;
   ResolvedParams RP;
   void* args2[2];
   void** args = nullptr;
@@ -271,14 +258,6 @@ int launch(hx_ctx* h, int kind, float* buf, cudaStream_t s) {
     grid = dim3(static_cast<unsigned>(h->grid[kind]));
     block = dim3(kResThreads);
     fn = resolved_kernel(kind);
-  } else if (kind != 2 && h->family[kind] == kFamCluster) {
-    CP = cluster_params(h);
-    args2[0] = &buf;
-    args2[1] = &CP;
-    args = args2;
-    grid = dim3(kClusterCtas);
-    block = dim3(kClusterThreads);
-    fn = cluster_kernel(kind);
   } else if (kind != 2 && h->family[kind] != kFamChunks) {
     TP = unit_params(h, kind);
     args2[0] = &buf;
@@ -583,7 +562,6 @@ const void* hx::static_kernel(const hx_ctx* h) {
   if (!h->built || h->pl.n_pulses == 0) return nullptr;
   hx_ctx* m = const_cast<hx_ctx*>(h);
   if (h->family[0] == kFamResolved) return resolved_kernel(0);
-  if (h->family[0] == kFamCluster) return cluster_kernel(0);
   return h->family[0] != kFamChunks ? fused_kernel(m, 0) : kernel_for(m, 0);
 }
 
@@ -598,11 +576,6 @@ int hx::launch_coords_with_scratch(hx_ctx* h, float* coords, cudaStream_t s, Ctr
     void* rargs[2] = {&coords, &RP};
     return to_err(
         cudaLaunchKernel(resolved_kernel(0), dim3(static_cast<unsigned>(h->grid[0])), dim3(kResThreads), rargs, 0, s));
-  }
-  if (h->family[0] == kFamCluster) {   // cluster barriers, no scratch at all
-    ClusterParams CP = cluster_params(h);
-    void* cargs[2] = {&coords, &CP};
-    return to_err(cudaLaunchKernel(cluster_kernel(0), dim3(kClusterCtas), dim3(kClusterThreads), cargs, 0, s));
   }
   // flags are indexed by item (pulse signals) or by list position (chunk / tile signals)
   const size_t need = std::max<size_t>(static_cast<size_t>(h->pl.n_pulses) * h->pl.ndom, static_cast<size_t>(work));
@@ -688,9 +661,9 @@ int hx_init(hx_handle* out, const double box[3], const int dims[3], double cutof
   h->device = device;
   // at most one kernel family for the coordinates (forces follow it), and
   // HX_FLAG_SWEEP_FORCES only over the chunk or resolved coordinate kernels
-  const unsigned families = flags & (HX_FLAG_SWEEP | HX_FLAG_CLUSTER | HX_FLAG_RESOLVED);
+  const unsigned families = flags & (HX_FLAG_SWEEP | HX_FLAG_RESOLVED);
   const bool sweep_forces_clash =
-      (flags & HX_FLAG_SWEEP_FORCES) && (flags & (HX_FLAG_SWEEP | HX_FLAG_CLUSTER));
+      (flags & HX_FLAG_SWEEP_FORCES) && (flags & HX_FLAG_SWEEP);
   if ((families & (families - 1)) || sweep_forces_clash) {
     delete h;
     return HX_ERR_ARG;

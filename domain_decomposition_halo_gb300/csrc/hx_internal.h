@@ -124,18 +124,6 @@ const void* noop_kernel();
 int max_blocks_per_sm(const void* fn, size_t smem);            // sets the kernel's dynamic shared memory limit first
 cudaError_t launch_pack_pulse(float* x, const PulseParams& p, cudaStream_t s);
 
-// ---- cluster kernels (hx_kernels.cu): one thread-block cluster walks the pulses ----
-constexpr int kClusterCtas = 8;           // CTAs of the one cluster (portable cluster size)
-constexpr int kClusterThreads = 512;      // threads per CTA
-struct ClusterParams {
-  const Chunk* chunks;                    // the per-pulse chunk list, pulse after pulse
-  const int32_t* maps;
-  int begin[HX_MAX_PULSES + 1];           // first chunk of each pulse; begin[n_pulses] = end
-  int n_pulses;
-  int pad;
-};
-const void* cluster_kernel(int kind);     // 0 coordinates, 1 forces (ordered)
-
 // ---- resolved kernels (hx_resolved.cu): the forwarding unrolled at build time ----
 constexpr int kTreeNodes = 8;             // a home atom and at most 7 copies
 struct alignas(16) TreeRec {
@@ -237,7 +225,7 @@ struct UnitParams {
 };
 
 // Kernel family of one direction's fused exchange.
-enum Family : int { kFamChunks = 0, kFamSweep = 2, kFamCluster = 3, kFamResolved = 4 };
+enum Family : int { kFamChunks = 0, kFamSweep = 2, kFamResolved = 4 };
 
 // ---- slot-sweep kernels (hx_sweep.cu): one warp per unit, same unit records ----
 #ifndef HX_SWEEP_SLOTS

@@ -255,7 +255,7 @@ __device__ __forceinline__ void coords_chunk(float* __restrict__ x, const Chunk&
 }
 
 // Forces of one chunk: targets[map[i]] += received[i], x then y then z
-// (the unfused and cluster kernels; the fused loop stages the received run).
+// (the unfused kernels; the fused loop stages the received run).
 template <bool ORDERED>
 __device__ __forceinline__ void forces_chunk(float* __restrict__ f, const Chunk& ch, const int (&j)[kRounds]) {
   const int lane = threadIdx.x & 31;
@@ -583,39 +583,6 @@ __global__ void __launch_bounds__(kThreads) k_unpack_pulse(float* __restrict__ f
   forces_chunk<true>(f, ch, j);
 }
 
-// Cluster path: the whole exchange in one thread-block cluster. Pulse after
-// pulse (forces last pulse first), the cluster's warps take the pulse's
-// chunks; a cluster barrier with release/acquire semantics separates the
-// pulses, so a pulse reads every slot that earlier pulses stored (forwarding)
-// or added into (forces). No flags, tickets or spin waits: the pages' "each
-// waits for all preceding pulse signals", with the cluster barrier as the
-// signal. Meant for decompositions small enough that the dependency chain
-// and the launch, not bandwidth, set the step time.
-__device__ __forceinline__ void cluster_sync_release_acquire() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-template <int KIND>
-__global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kClusterThreads, 1)
-    k_cluster(float* __restrict__ buf, ClusterParams P) {
-  constexpr int kCtaWarps = kClusterThreads / 32;
-  __shared__ float s_stage[kCtaWarps][96];
-  const int warp = threadIdx.x >> 5;
-  const int gw = blockIdx.x * kCtaWarps + warp;   // the grid is the one cluster
-  const int W = kClusterCtas * kCtaWarps;
-  for (int k = 0; k < P.n_pulses; ++k) {
-    const int p = KIND == 0 ? k : P.n_pulses - 1 - k;
-    for (int c = P.begin[p] + gw; c < P.begin[p + 1]; c += W) {
-      const Chunk ch = load_chunk(P.chunks + c);   // flags carry kHaloSrc: halo sources by plain loads
-      int j[kRounds];
-      load_map(P.maps + ch.map, ch.n, j);
-      if (KIND == 0) coords_chunk(buf, ch, j, s_stage[warp]);
-      else forces_chunk<true>(buf, ch, j);
-    }
-    if (k + 1 < P.n_pulses) cluster_sync_release_acquire();
-  }
-}
-
 __global__ void k_noop() {}
 
 }  // namespace
@@ -643,10 +610,6 @@ const void* forces_kernel(int signal_mode, bool ordered) {
 }
 
 const void* noop_kernel() { return reinterpret_cast<const void*>(&k_noop); }
-
-const void* cluster_kernel(int kind) {
-  return kind == 0 ? reinterpret_cast<const void*>(&k_cluster<0>) : reinterpret_cast<const void*>(&k_cluster<1>);
-}
 
 size_t chunk_smem_bytes(int dir, bool bulk_store) {
   if (dir == 1) return kWarps * sizeof(ChunkWarpSmem<1>);

@@ -586,13 +586,11 @@ int build_tables(hx_ctx* h, cudaStream_t s) {
   std::vector<int64_t> rank(nd);
   for (int r = 0; r < nd; ++r) rank[r] = domain_rank(pl, r);
   h->family[0] = (h->flags & HX_FLAG_SWEEP)   ? kFamSweep
-                 : (h->flags & HX_FLAG_CLUSTER) ? kFamCluster
                  : (h->flags & HX_FLAG_RESOLVED) ? kFamResolved
                                                 : kFamChunks;
   h->family[1] = (h->flags & (HX_FLAG_SWEEP | HX_FLAG_SWEEP_FORCES)) ? kFamSweep : h->family[0];
   for (int k = 0; k < 2; ++k) {
     const int per_sm = std::max(1, h->family[k] == kFamSweep   ? sweep_blocks_per_sm(k)
-                                   : h->family[k] == kFamCluster ? 1
                                    : h->family[k] == kFamResolved ? 1
                                                                  : max_blocks_per_sm(kernel_for(h, k), fused_smem(h, k)));
     h->grid[k] = per_sm * h->sm_count;   // upper bound; trimmed to the work count below
@@ -870,8 +868,6 @@ int build_tables(hx_ctx* h, cudaStream_t s) {
       const int64_t fb = resolved_blocks(n, resolved_per_thread(h, n, kResTreesPerThread)) +
                          resolved_blocks(h->n_res_trees, 1);
       h->grid[k] = static_cast<int>(std::max<int64_t>(1, k == 0 ? h->n_res_segs : fb));
-    } else if (h->family[k] == kFamCluster) {
-      h->grid[k] = kClusterCtas;   // exactly one cluster
     } else if (h->family[k] == kFamSweep) {   // one warp per batch of units
       const int warps = std::max(1, std::min((h->n_units[k] + kSweepBatch - 1) / kSweepBatch, h->grid[k] * kWarps));
       h->grid[k] = (warps + kWarps - 1) / kWarps;

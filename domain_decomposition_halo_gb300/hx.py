@@ -31,7 +31,6 @@ HX_FLAG_COUNTER_SIGNAL = 0x4
 HX_FLAG_FINE_WAITS = 0x8
 HX_FLAG_SWEEP = 0x20
 HX_FLAG_SWEEP_FORCES = 0x40
-HX_FLAG_CLUSTER = 0x80
 HX_FLAG_RESOLVED = 0x100
 HX_FLAG_BULK_STORE = 0x200
 HX_FLAG_PDL = 0x400

@@ -95,17 +95,9 @@ typedef struct hx_ctx* hx_handle;
 #define HX_FLAG_SWEEP_FORCES 0x40u     /* the force exchange by the slot-sweep kernel, the coordinate
                                           exchange by the chunk kernels (with HX_FLAG_FINE_WAITS or
                                           the other chunk flags) or, with HX_FLAG_RESOLVED, by the
-                                          resolved gather. At most one of HX_FLAG_SWEEP,
-                                          HX_FLAG_CLUSTER and HX_FLAG_RESOLVED, and
-                                          HX_FLAG_SWEEP_FORCES with neither of the first two (else
-                                          HX_ERR_ARG) */
-#define HX_FLAG_CLUSTER 0x80u          /* both directions by one thread-block cluster of 8 CTAs that
-                                          walks the pulses in order (forces in reverse), with a
-                                          cluster barrier (release/acquire) between pulses instead of
-                                          flags: for small decompositions, where the launch and the
-                                          dependency chain set the step time. Forces are ordered
-                                          (HX_FLAG_UNORDERED_FORCES is ignored); there are no
-                                          device waits, so no time-outs and no signal to drop */
+                                          resolved gather. At most one of HX_FLAG_SWEEP and
+                                          HX_FLAG_RESOLVED, and HX_FLAG_SWEEP_FORCES not with
+                                          HX_FLAG_SWEEP (else HX_ERR_ARG) */
 #define HX_FLAG_BULK_STORE 0x200u      /* chunk coordinate kernels pack by bulk store: each warp gathers
                                           its chunk into shared memory and stores it to the receiver's
                                           slots with one cp.async.bulk (the pages' TMA variant, section
@@ -117,9 +109,9 @@ typedef struct hx_ctx* hx_handle;
                                           scheduled while the stream's previous kernel finishes (it
                                           waits for that kernel before claiming work or touching
                                           coordinates, forces or flags; resolved kernels read their
-                                          build-time tables first). The slot sweep, tile and cluster
-                                          kernels keep plain stream order: the sweep's persistent grid
-                                          timed out under programmatic launch on a 12M-atom workload */
+                                          build-time tables first). The slot sweep keeps plain stream
+                                          order (an earlier version of its persistent grid timed out
+                                          under programmatic launch on a 12M-atom workload) */
 #define HX_FLAG_RESOLVED 0x100u        /* the forwarding unrolled at build time: every halo slot is
                                           gathered straight from its origin home atom (plus the
                                           shifts its path added), and every home atom's force tree
@@ -132,7 +124,7 @@ typedef struct hx_ctx* hx_handle;
                                           HX_ERR_CAPACITY: a halo slot's origin and shifts share one
                                           32-bit word) */
 
-#define HX_FLAGS_ALL 0x7efu      /* every flag above */
+#define HX_FLAGS_ALL 0x76fu      /* every flag above */
 
 #define HX_MAX_PULSES 32
 #define HX_MAX_DOMAINS 4096

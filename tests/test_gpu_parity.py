@@ -19,8 +19,7 @@ ALL_MODES = [0, HX.HX_FLAG_COUNTER_SIGNAL, HX.HX_FLAG_NO_GRAPH,
              HX.HX_FLAG_COUNTER_SIGNAL | HX.HX_FLAG_NO_GRAPH, HX.HX_FLAG_FINE_WAITS,
              HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_COUNTER_SIGNAL, HX.HX_FLAG_SWEEP,
              HX.HX_FLAG_SWEEP | HX.HX_FLAG_NO_GRAPH, HX.HX_FLAG_SWEEP_FORCES,
-             HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES, HX.HX_FLAG_CLUSTER,
-             HX.HX_FLAG_CLUSTER | HX.HX_FLAG_NO_GRAPH, HX.HX_FLAG_RESOLVED,
+             HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES, HX.HX_FLAG_RESOLVED,
              HX.HX_FLAG_RESOLVED | HX.HX_FLAG_NO_GRAPH, HX.HX_FLAG_RESOLVED | HX.HX_FLAG_SWEEP_FORCES,
              HX.HX_FLAG_BULK_STORE, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE,
              HX.HX_FLAG_COUNTER_SIGNAL | HX.HX_FLAG_BULK_STORE, HX.HX_FLAG_RESOLVED | HX.HX_FLAG_PDL,
@@ -163,7 +162,7 @@ def test_unfused_baseline(name):
 ])
 @pytest.mark.parametrize("flags", [0, HX.HX_FLAG_COUNTER_SIGNAL, HX.HX_FLAG_FINE_WAITS,
                                    HX.HX_FLAG_SWEEP, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES,
-                                   HX.HX_FLAG_CLUSTER, HX.HX_FLAG_RESOLVED, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE])
+                                   HX.HX_FLAG_RESOLVED, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE])
 def test_parity_shapes(box, dims, cutoff, n, flags):
     w = W.custom("shape", n, box, dims, cutoff, seed=7 + n)
     pulse_dims, _ = HX.query_plan(box, dims, cutoff)
@@ -264,7 +263,7 @@ def test_boundary_atoms():
 def test_many_steps_reuse_signals():
     """Epoch-valued signals are never reset between launches: 200 steps."""
     for flags in (0, HX.HX_FLAG_COUNTER_SIGNAL, HX.HX_FLAG_FINE_WAITS, HX.HX_FLAG_SWEEP,
-                  HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES, HX.HX_FLAG_CLUSTER, HX.HX_FLAG_RESOLVED,
+                  HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES, HX.HX_FLAG_RESOLVED,
                   HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE, HX.HX_FLAG_RESOLVED | HX.HX_FLAG_PDL):
         c = Case(W.WORKLOADS["C2"], flags=flags)
         x = c.o.coords().copy()
@@ -336,8 +335,7 @@ def test_errors():
     with pytest.raises(HX.HXError) as ei:
         hx.build_maps(pos, small)
     assert ei.value.code == HX.HX_ERR_CAPACITY
-    for bad in (HX.HX_FLAG_SWEEP | HX.HX_FLAG_SWEEP_FORCES, HX.HX_FLAG_CLUSTER | HX.HX_FLAG_SWEEP_FORCES,
-                HX.HX_FLAG_RESOLVED | HX.HX_FLAG_CLUSTER, HX.HX_FLAG_CLUSTER | HX.HX_FLAG_SWEEP):
+    for bad in (HX.HX_FLAG_SWEEP | HX.HX_FLAG_SWEEP_FORCES, HX.HX_FLAG_RESOLVED | HX.HX_FLAG_SWEEP, 0x80):
         with pytest.raises(HX.HXError) as ei:   # the unit kernel families are alternatives
             HX.HaloExchange(w.box, w.dims, w.cutoff, flags=bad)
         assert ei.value.code == HX.HX_ERR_ARG

@@ -24,7 +24,7 @@ pytestmark = pytest.mark.gpu
 
 @pytest.mark.parametrize("name", ["C2", "C5"])
 @pytest.mark.parametrize("flags", [0, HX.HX_FLAG_FINE_WAITS, HX.HX_FLAG_SWEEP,
-                                   HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES, HX.HX_FLAG_CLUSTER,
+                                   HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES,
                                    HX.HX_FLAG_RESOLVED, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE])
 def test_static_scratch_matches_regular_exchange(name, flags):
     w = W.WORKLOADS[name]
@@ -70,7 +70,7 @@ def _static(hx, x, stream=None):
 
 
 @pytest.mark.parametrize("flags", [0, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE, HX.HX_FLAG_SWEEP,
-                                   HX.HX_FLAG_RESOLVED, HX.HX_FLAG_CLUSTER])
+                                   HX.HX_FLAG_RESOLVED])
 def test_static_call_allocates_no_device_memory(flags):
     """The set-up (symbol address, kernel module) happens in hx_build_maps,
     so from the first static call on the device's free memory stays put."""
