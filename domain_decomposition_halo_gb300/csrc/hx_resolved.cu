@@ -88,11 +88,13 @@ __device__ __forceinline__ void load3(const float* f, int slot, float (&v)[3]) {
   v[1] = p[1];
   v[2] = p[2];
 }
+// A scattered slot written as an 8-byte and a 4-byte store (one L2 write
+// request fewer than three words).
 __device__ __forceinline__ void store3(float* f, int slot, const float (&v)[3]) {
   float* p = f + 3 * static_cast<int64_t>(slot);
-  p[0] = v[0];
-  p[1] = v[1];
-  p[2] = v[2];
+  const bool lo8 = (reinterpret_cast<uintptr_t>(p) & 7u) == 0u;
+  *reinterpret_cast<float2*>(lo8 ? p : p + 1) = lo8 ? make_float2(v[0], v[1]) : make_float2(v[1], v[2]);
+  *(lo8 ? p + 2 : p) = lo8 ? v[2] : v[0];
 }
 __device__ __forceinline__ void add3(float (&a)[3], const float (&b)[3]) {
   a[0] = __fadd_rn(a[0], b[0]);
