@@ -603,13 +603,18 @@ def secondary(hx_main, coords, forces, w_main, dev, peak, flags):
         del hx
         return entry
 
-    # the small configurations in the run's modes, and with the forwarding
+    # the small configurations in the run's modes, with the forwarding
     # resolved at build time and launched with programmatic dependent launch
-    # (HX_FLAG_RESOLVED | HX_FLAG_PDL), the mode made for them
+    # (HX_FLAG_RESOLVED | HX_FLAG_PDL), the mode made for them,
+    # and the staged path with both directions on the chunk kernels launched
+    # with programmatic dependent launch (the sweep keeps plain stream order)
+    staged_pdl = HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE | HX.HX_FLAG_PDL
     for name in ("C1", "C2", "C3", "C4"):
         if name == w_main.name:
             continue
         res[name] = small(name, flags)
+        if flags != staged_pdl:
+            res[name]["staged_chunks_pdl"] = small(name, staged_pdl)
         if not flags & HX.HX_FLAG_RESOLVED:
             res[name]["resolved_pdl"] = small(name, HX.HX_FLAG_RESOLVED | HX.HX_FLAG_PDL)
     # the headline workload with the forwarding resolved at build time (not the
