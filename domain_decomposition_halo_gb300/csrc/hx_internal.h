@@ -22,9 +22,6 @@ namespace hx {
 #ifndef HX_POLL_NAP_MAX_NS
 #define HX_POLL_NAP_MAX_NS 256
 #endif
-#ifndef HX_POLL_ACQUIRE
-#define HX_POLL_ACQUIRE 0
-#endif
 
 constexpr int kThreads = 256;                 // threads per block of the exchange kernels
 constexpr int kWarps = kThreads / 32;         // independent warps per block
@@ -181,6 +178,7 @@ cudaError_t launch_unpack_pulse(float* f, const PulseParams& p, cudaStream_t s);
 // stages it, adds every pulse's contributions in reverse pulse order in
 // shared memory, and writes it back.
 constexpr int kInlineSegs = 4;       // segments carried inside the unit record
+constexpr int kInlineWaits = 2;      // waits carried inside the unit record
 
 struct alignas(16) UnitSeg {   // entries [map, map + n) of one (sender, pulse) map that fall in the unit
   int64_t map;        // first entry in the maps array
@@ -206,7 +204,8 @@ struct alignas(16) Unit {  // one 256-byte record, read by 16 threads in one rou
   int32_t flags;      // kSignal; kHaloSrc = slots written earlier in the same launch
   int32_t item;       // pulse * n_domains + domain of its first segment (status, fault injection)
   int32_t entries;    // entries of all segments
-  int32_t pad[5];
+  Wait wait_inline[kInlineWaits];   // the first waits (also in the wait list), read with the record
+  int32_t pad;
   UnitSeg seg[kInlineSegs];
 };
 static_assert(sizeof(Unit) == 256, "unit record must stay 256 bytes");

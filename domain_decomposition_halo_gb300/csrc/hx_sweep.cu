@@ -145,14 +145,15 @@ __device__ __forceinline__ UnitSeg seg_at(const UnitParams& P, const Unit& d, in
 }
 
 // Whole warp: wait until every unit that d depends on has been signalled at
-// this epoch. Lanes take the wait list in strides of 32 and poll with
+// this epoch (the first waits come with the unit's record, the rest from the
+// direction's wait list). Lanes take the wait list in strides of 32 and poll with
 // acquire loads at gpu scope and a short back-off; the closing __syncwarp
 // orders every lane's acquire before the warp's loads. A wait that runs out
 // records a timeout and gives up.
 __device__ void wait_units(const UnitParams& P, const Unit& d, unsigned long long epoch) {
   const int lane = threadIdx.x & 31;
   for (int w = lane; w < d.wait_cnt; w += 32) {
-    const Wait wt = P.waits[d.wait_off + w];
+    const Wait wt = w < kInlineWaits ? d.wait_inline[w] : P.waits[d.wait_off + w];
     const unsigned long long* flag = P.flags + wt.item;
     unsigned long long t0 = 0;
     unsigned iter = 0, nap = 0;
@@ -409,6 +410,7 @@ __global__ void __launch_bounds__(kThreads) k_sweep(float* __restrict__ buf, Uni
     cp_async_wait_all();
     __syncwarp();
     int b = 0;
+    bool next_ready = false;   // the next unit's waits were seen satisfied ahead of time
     while (true) {
       const bool same_batch = (c + 1) % kSweepBatch != 0;
       const unsigned long long cn = same_batch ? c + 1 : (c / kSweepBatch + W) * kSweepBatch;   // this warp's next unit
@@ -416,7 +418,7 @@ __global__ void __launch_bounds__(kThreads) k_sweep(float* __restrict__ buf, Uni
         cp_async_16(reinterpret_cast<int4*>(&S.desc[b ^ 1]) + lane, reinterpret_cast<const int4*>(P.units + cn) + lane);
       const Unit& d = S.desc[b];
       if (d.wait_cnt > 0) {
-        wait_units(P, d, epoch);
+        if (!next_ready) wait_units(P, d, epoch);
         // bulk copies (async proxy) then read what other warps stored (generic proxy) before their signals
         if (lane == 0) asm volatile("fence.proxy.async.global;" ::: "memory");
         __syncwarp();
@@ -438,6 +440,16 @@ __global__ void __launch_bounds__(kThreads) k_sweep(float* __restrict__ buf, Uni
       __syncwarp();   // the lanes' edge words are in place
       if constexpr (KIND == 0) coords_unit(buf, P, d, S);
       else forces_unit(buf, P, d, S);
+      // One acquire poll of the next unit's waits (when they all come with
+      // its record), issued before this unit's signal so that the two round
+      // trips overlap; if it finds them set, the next unit skips its wait.
+      unsigned long long pv = epoch;
+      bool poll_next = false;
+      if (cn < N) {
+        const Unit& dn = S.desc[b ^ 1];
+        poll_next = dn.wait_cnt > 0 && dn.wait_cnt <= kInlineWaits;
+        if (poll_next && lane < dn.wait_cnt) pv = ld_acquire_u64(P.flags + dn.wait_inline[lane].item);
+      }
       if (d.flags & kSignal) {
         __syncwarp();   // every lane's stores precede lane 0's release
         if (lane == 0) {
@@ -445,6 +457,7 @@ __global__ void __launch_bounds__(kThreads) k_sweep(float* __restrict__ buf, Uni
           if (d.item != drop_item) st_release_u64(P.flags + c, epoch);
         }
       }
+      next_ready = __all_sync(kFull, pv == epoch) && poll_next;   // every lane's acquire precedes the next staging
       if (cn >= N) break;
       cp_async_wait_all();   // the next record
       __syncwarp();          // ... for every lane; the stage is rewritten for the next unit

@@ -318,6 +318,7 @@ int build_unit_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::
         u.wait_off = static_cast<int32_t>(waits.size());
         u.wait_cnt = static_cast<int32_t>(t.deps.size());
         for (int d : t.deps) waits.push_back({pos[d], 1});
+        for (int w = 0; w < std::min(u.wait_cnt, kInlineWaits); ++w) u.wait_inline[w] = waits[u.wait_off + w];
         u.flags = (waited[i] ? kSignal : 0) | (dir == 0 && t.range >= 0 ? kHaloSrc : 0);
         u.item = t.seg_pulse[0] * nd + t.r;
         for (const UnitSeg& sg : t.segs) u.entries += sg.n;
