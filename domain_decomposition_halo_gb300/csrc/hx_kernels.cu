@@ -216,25 +216,43 @@ __device__ __forceinline__ void store_round(float* __restrict__ dst, int n_round
   __syncwarp();
 }
 
+// Where a chunk's map entries come from: registers loaded up front (the
+// unfused kernels) or the chunk's record in shared memory, read as each
+// round is issued (the fused loop: no registers held for the map).
+struct RegMap {
+  const int (&j)[kRounds];
+  __device__ __forceinline__ int operator()(int u) const { return j[u]; }
+};
+struct SmemMap {
+  const int32_t* m;
+  int n;
+  __device__ __forceinline__ int operator()(int u) const {
+    const int e = u * 32 + static_cast<int>(threadIdx.x & 31);
+    return e < n ? m[e] : -1;
+  }
+};
+
 // Coordinates of one chunk: gather (+shift) and store into the receiver.
 // Home slots are never written by the coordinate kernel, so independent
 // chunks read them through the read-only path.
-__device__ __forceinline__ void gather_chunk(const float* __restrict__ x, const Chunk& ch, const int (&j)[kRounds],
+template <class Map>
+__device__ __forceinline__ void gather_chunk(const float* __restrict__ x, const Chunk& ch, const Map& j,
                                              float (&v)[kRounds][3]) {
   const float* src = x + 3 * ch.src;
   const bool halo = (ch.flags & kHaloSrc) != 0;
 #pragma unroll
   for (int u = 0; u < kRounds; ++u) {
-    if (j[u] >= 0) {
-      const float* s = src + 3 * static_cast<int64_t>(j[u]);
+    const int ju = j(u);
+    if (ju >= 0) {
+      const float* s = src + 3 * static_cast<int64_t>(ju);
       if (halo) load_slot<false>(s, v[u][0], v[u][1], v[u][2]);
       else load_slot<true>(s, v[u][0], v[u][1], v[u][2]);
     }
   }
 }
 
-__device__ __forceinline__ void coords_chunk(float* __restrict__ x, const Chunk& ch, const int (&j)[kRounds],
-                                             float* stage) {
+template <class Map>
+__device__ __forceinline__ void coords_chunk(float* __restrict__ x, const Chunk& ch, const Map& j, float* stage) {
   float v[kRounds][3];
   gather_chunk(x, ch, j, v);
   if (ch.flags & kShift) {   // no add otherwise: unshifted values keep every bit (-0.0 included)
@@ -334,7 +352,8 @@ __device__ __forceinline__ unsigned smem_u32(const void* p) {
   return static_cast<unsigned>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ void coords_chunk_bulk(float* __restrict__ x, const Chunk& ch, const int (&j)[kRounds],
+template <class Map>
+__device__ __forceinline__ void coords_chunk_bulk(float* __restrict__ x, const Chunk& ch, const Map& j,
                                                   unsigned char* stage) {
   const int lane = threadIdx.x & 31;
   float v[kRounds][3];
@@ -355,8 +374,8 @@ __device__ __forceinline__ void coords_chunk_bulk(float* __restrict__ x, const C
   __syncwarp();
 #pragma unroll
   for (int u = 0; u < kRounds; ++u) {
-    if (j[u] >= 0) {
-      const int e = u * 32 + lane;
+    const int e = u * 32 + lane;
+    if (e < ch.n) {
       sv[3 * e + 0] = v[u][0];
       sv[3 * e + 1] = v[u][1];
       sv[3 * e + 2] = v[u][2];
@@ -423,8 +442,8 @@ __device__ __forceinline__ void fetch_chunk(ChunkSlot& s, const ChunkSlot* src) 
 // into registers, so a chunk costs one round trip before its adds. The
 // stage's copy is committed as the newest group; the caller has committed
 // its other copies before.
-template <bool ORDERED>
-__device__ __forceinline__ void forces_chunk_staged(float* __restrict__ f, const Chunk& ch, const int (&j)[kRounds],
+template <bool ORDERED, class Map>
+__device__ __forceinline__ void forces_chunk_staged(float* __restrict__ f, const Chunk& ch, const Map& j,
                                                     unsigned char* stage) {
   const int lane = threadIdx.x & 31;
   const unsigned long long g = reinterpret_cast<unsigned long long>(f + 3 * ch.dst);
@@ -449,7 +468,8 @@ __device__ __forceinline__ void forces_chunk_staged(float* __restrict__ f, const
   if (ORDERED) {
 #pragma unroll
     for (int u = 0; u < kRounds; ++u) {
-      if (j[u] >= 0) load_slot<false>(tgt + 3 * static_cast<int64_t>(j[u]), t[u][0], t[u][1], t[u][2]);
+      const int ju = j(u);
+      if (ju >= 0) load_slot<false>(tgt + 3 * static_cast<int64_t>(ju), t[u][0], t[u][1], t[u][2]);
     }
   }
   cp_async_wait<0>();   // this lane's copies of the run (and anything committed before)
@@ -457,7 +477,7 @@ __device__ __forceinline__ void forces_chunk_staged(float* __restrict__ f, const
   const float* rcv = reinterpret_cast<const float*>(base);
 #pragma unroll
   for (int u = 0; u < kRounds; ++u) {
-    const int jj = j[u];
+    const int jj = j(u);
     if (jj >= 0) {
       const int e = u * 32 + lane;
       float* p = tgt + 3 * static_cast<int64_t>(jj);
@@ -504,12 +524,7 @@ __device__ __forceinline__ void run_warps(float* __restrict__ buf, const DirPara
     while (true) {
       const ChunkSlot& cur = S.slot[b];
       const Chunk ch = cur.rec;
-      int j[kRounds];
-#pragma unroll
-      for (int u = 0; u < kRounds; ++u) {
-        const int e = u * 32 + lane;
-        j[u] = (e < ch.n) ? cur.map[e] : -1;
-      }
+      const SmemMap j{cur.map, ch.n};
       const unsigned long long c1 = c + W;
       if (c1 < N) fetch_chunk(S.slot[b ^ 1], P.chunks + c1);
       if (ch.wait_cnt > 0) wait_chunk<MODE>(P, ch, cur.waits, epoch);
@@ -571,7 +586,7 @@ __global__ void __launch_bounds__(kThreads) k_pack_pulse(float* __restrict__ x, 
   ch.flags |= kHaloSrc;   // earlier pulses' slots were written by earlier launches: any load path works
   int j[kRounds];
   load_map(P.maps + ch.map, ch.n, j);
-  coords_chunk(x, ch, j, s_stage[threadIdx.x >> 5]);
+  coords_chunk(x, ch, RegMap{j}, s_stage[threadIdx.x >> 5]);
 }
 
 __global__ void __launch_bounds__(kThreads) k_unpack_pulse(float* __restrict__ f, PulseParams P) {
