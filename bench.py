@@ -50,16 +50,15 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU baseline budget")
     ap.add_argument("--flags", default="fine,bulkstore,sweepf",
                     help="comma list of libhx modes: fine, bulkstore (coordinates packed by bulk stores), sweepf "
-                         "(forces by the slot sweep), sweep, resolved, counter, nograph, unordered, "
+                         "(forces by the slot sweep), resolved, pdl, nograph, unordered, "
                          "pages (= none)")
     return ap.parse_args()
 
 
 def hx_flags(spec: str) -> int:
     from domain_decomposition_halo_gb300 import hx as HX
-    table = {"fine": HX.HX_FLAG_FINE_WAITS, "counter": HX.HX_FLAG_COUNTER_SIGNAL, "nograph": HX.HX_FLAG_NO_GRAPH,
-             "unordered": HX.HX_FLAG_UNORDERED_FORCES, "sweep": HX.HX_FLAG_SWEEP,
-             "sweepf": HX.HX_FLAG_SWEEP_FORCES,
+    table = {"fine": HX.HX_FLAG_FINE_WAITS, "nograph": HX.HX_FLAG_NO_GRAPH,
+             "unordered": HX.HX_FLAG_UNORDERED_FORCES, "sweepf": HX.HX_FLAG_SWEEP_FORCES,
              "resolved": HX.HX_FLAG_RESOLVED, "bulkstore": HX.HX_FLAG_BULK_STORE,
              "pdl": HX.HX_FLAG_PDL, "pages": 0, "": 0}
     flags = 0
@@ -126,12 +125,11 @@ def kernel_source_digest():
 def kernel_impl(flags: int, direction: int) -> str:
     """The device function that runs a direction's fused exchange under `flags`."""
     from domain_decomposition_halo_gb300 import hx as HX
-    if flags & HX.HX_FLAG_SWEEP or (direction == 1 and flags & HX.HX_FLAG_SWEEP_FORCES):
+    if direction == 1 and flags & HX.HX_FLAG_SWEEP_FORCES:
         return f"k_sweep<{direction}> (slot sweep)"
     if flags & HX.HX_FLAG_RESOLVED:
         return "k_resolved_coords (resolved)" if direction == 0 else "k_resolved_forces (resolved)"
-    mode = ("chunk flags" if flags & HX.HX_FLAG_FINE_WAITS else
-            "counter" if flags & HX.HX_FLAG_COUNTER_SIGNAL else "last arrival")
+    mode = "chunk flags" if flags & HX.HX_FLAG_FINE_WAITS else "last arrival"
     if direction == 0:
         if flags & HX.HX_FLAG_BULK_STORE:
             return f"k_coords_bulk<{mode}> (chunks, bulk-store pack)"
@@ -553,7 +551,7 @@ def secondary(hx_main, coords, forces, w_main, dev, peak, flags):
 
     # the probe in the run's modes, and with both directions on the chunk kernels
     from domain_decomposition_halo_gb300 import hx as HX
-    chunk_flags = flags & ~(HX.HX_FLAG_SWEEP | HX.HX_FLAG_SWEEP_FORCES)
+    chunk_flags = flags & ~HX.HX_FLAG_SWEEP_FORCES
     res = {"overlap_with_local_kernel_us": {"run_modes": overlap_probe(dev, flags)}}
     if chunk_flags != flags:
         res["overlap_with_local_kernel_us"]["chunk_kernels"] = overlap_probe(dev, chunk_flags)

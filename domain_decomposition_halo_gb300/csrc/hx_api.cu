@@ -166,8 +166,7 @@ DirParams dir_params(hx_ctx* h, int dir) {
 }
 
 const void* kernel_for(hx_ctx* h, int kind) {
-  const int mode = (h->flags & HX_FLAG_FINE_WAITS) ? kChunkFlag
-                   : (h->flags & HX_FLAG_COUNTER_SIGNAL) ? kCounter : kLastArrival;
+  const int mode = (h->flags & HX_FLAG_FINE_WAITS) ? kChunkFlag : kLastArrival;
   if (kind == 0) return coords_kernel(mode, (h->flags & HX_FLAG_BULK_STORE) != 0);
   if (kind == 1) return forces_kernel(mode, !(h->flags & HX_FLAG_UNORDERED_FORCES));
   return noop_kernel();
@@ -562,7 +561,7 @@ const void* hx::static_kernel(const hx_ctx* h) {
   if (!h->built || h->pl.n_pulses == 0) return nullptr;
   hx_ctx* m = const_cast<hx_ctx*>(h);
   if (h->family[0] == kFamResolved) return resolved_kernel(0);
-  return h->family[0] != kFamChunks ? fused_kernel(m, 0) : kernel_for(m, 0);
+  return kernel_for(m, 0);
 }
 
 int hx::launch_coords_with_scratch(hx_ctx* h, float* coords, cudaStream_t s, Ctrl* ctrl,
@@ -577,7 +576,7 @@ int hx::launch_coords_with_scratch(hx_ctx* h, float* coords, cudaStream_t s, Ctr
     return to_err(
         cudaLaunchKernel(resolved_kernel(0), dim3(static_cast<unsigned>(h->grid[0])), dim3(kResThreads), rargs, 0, s));
   }
-  // flags are indexed by item (pulse signals) or by list position (chunk / tile signals)
+  // flags are indexed by item (pulse signals) or by list position (chunk signals)
   const size_t need = std::max<size_t>(static_cast<size_t>(h->pl.n_pulses) * h->pl.ndom, static_cast<size_t>(work));
   if (need > max_flags) return HX_ERR_CAPACITY;
   HX_CUDA(cudaMemsetAsync(ctrl, 0, sizeof(Ctrl), s));
@@ -585,30 +584,13 @@ int hx::launch_coords_with_scratch(hx_ctx* h, float* coords, cudaStream_t s, Ctr
   HX_CUDA(cudaMemcpyAsync(&ctrl->drop_item, &h->d_ctrl[0].drop_item, sizeof(int), cudaMemcpyDeviceToDevice, s));
   HX_CUDA(cudaMemsetAsync(flags, 0, sizeof(unsigned long long) * need, s));
   HX_CUDA(cudaMemsetAsync(arrivals, 0, sizeof(unsigned int) * need, s));
-  void* args[2];
-  DirParams P;
-  UnitParams TP;
-  const void* fn;
-  size_t smem = 0;
-  args[0] = &coords;
-  if (h->family[0] != kFamChunks) {
-    TP = unit_params(h, 0);
-    TP.flags = flags;
-    TP.ctrl = ctrl;
-    args[1] = &TP;
-    fn = fused_kernel(h, 0);
-    smem = fused_smem(h, 0);
-  } else {
-    P = dir_params(h, 0);
-    P.flags = flags;
-    P.arrivals = arrivals;
-    P.ctrl = ctrl;
-    args[1] = &P;
-    fn = kernel_for(h, 0);
-    smem = fused_smem(h, 0);
-  }
-  return to_err(cudaLaunchKernel(fn, dim3(static_cast<unsigned>(h->grid[0])), dim3(fused_threads(h, 0)),
-                                args, smem, s));
+  DirParams P = dir_params(h, 0);   // the chunk kernel, on the given scratch
+  P.flags = flags;
+  P.arrivals = arrivals;
+  P.ctrl = ctrl;
+  void* args[2] = {&coords, &P};
+  return to_err(cudaLaunchKernel(kernel_for(h, 0), dim3(static_cast<unsigned>(h->grid[0])), dim3(kThreads), args,
+                                fused_smem(h, 0), s));
 }
 
 // ------------------------------------------------------------------ C ABI
@@ -659,12 +641,8 @@ int hx_init(hx_handle* out, const double box[3], const int dims[3], double cutof
   if (!h) return HX_ERR_NOMEM;
   h->pl = pl;
   h->device = device;
-  // at most one kernel family for the coordinates (forces follow it), and
-  // HX_FLAG_SWEEP_FORCES only over the chunk or resolved coordinate kernels
-  const unsigned families = flags & (HX_FLAG_SWEEP | HX_FLAG_RESOLVED);
-  const bool sweep_forces_clash =
-      (flags & HX_FLAG_SWEEP_FORCES) && (flags & HX_FLAG_SWEEP);
-  if ((families & (families - 1)) || sweep_forces_clash) {
+  // the slot sweep serves the forces of the chunk modes; resolved mode has its own force pass
+  if ((flags & HX_FLAG_SWEEP_FORCES) && (flags & HX_FLAG_RESOLVED)) {
     delete h;
     return HX_ERR_ARG;
   }

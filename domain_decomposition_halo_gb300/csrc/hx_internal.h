@@ -91,7 +91,7 @@ struct DirParams {
   const ChunkSlot* chunks;
   const Wait* waits;
   const int32_t* maps;
-  unsigned long long* flags;  // per item (epoch flag or arrival counter) or per chunk (epoch flag)
+  unsigned long long* flags;  // epoch flags: per item (last-arrival signals) or per chunk (fine waits)
   unsigned int* arrivals;     // per item: last-arrival election counters
   Ctrl* ctrl;
   unsigned long long n_chunks;
@@ -109,9 +109,9 @@ struct PulseParams {
 };
 
 // kLastArrival: per-item epoch flag stored by the item's last chunk (the
-// pages' last-block election); kCounter: per-item arrival counter; kChunkFlag:
-// one epoch flag per chunk, for chunk-granular waits.
-enum SignalMode { kLastArrival = 0, kCounter = 1, kChunkFlag = 2 };
+// pages' last-block election); kChunkFlag: one epoch flag per chunk, for
+// chunk-granular waits.
+enum SignalMode { kLastArrival = 0, kChunkFlag = 2 };
 
 // ---- exchange kernels (hx_kernels.cu) ----
 const void* coords_kernel(int signal_mode, bool bulk_store);   // bulk_store: gather to shared memory, bulk copy out

@@ -19,8 +19,8 @@
 // (packHaloCoords). After its stores a chunk signals its item, when anybody
 // waits for it: either the pages' hierarchical scheme (signalPeerOnLastBlock:
 // a counting atomic with release semantics elects the last chunk, which
-// stores the epoch flag with release) or one release-add per chunk to an
-// arrival counter.
+// stores the epoch flag with release) or, with chunk-granular waits, one
+// epoch flag per chunk.
 //
 // Forces: the same skeleton in reverse pulse order ("Force halo exchange:
 // Reversing the dependency chain"): a chunk of (sender r, pulse p) adds the
@@ -67,10 +67,6 @@ __device__ __forceinline__ int ld_relaxed_s32(const int* p) {
 
 __device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
   asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-
-__device__ __forceinline__ void red_release_add_u64(unsigned long long* p, unsigned long long v) {
-  asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
 // Counting increment (wraps to 0 after `mod`) with acquire-release at gpu
@@ -135,23 +131,16 @@ __device__ __forceinline__ Chunk load_chunk(const Chunk* p) {
 // failed) records the status and lets the chunk proceed without the
 // guarantee.
 template <int MODE>
-__device__ __forceinline__ bool flag_ready(unsigned long long v, unsigned long long target) {
-  // epoch flags (per item or per chunk) are compared for equality, as the
-  // pages' signal wait does; arrival counters only grow
-  return (MODE == kCounter) ? (v >= target) : (v == target);
-}
-
-template <int MODE>
 __device__ void wait_chunk(const DirParams& P, const Chunk& ch, const Wait* waits, unsigned long long epoch) {
   const int lane = threadIdx.x & 31;
   for (int w = lane; w < ch.wait_cnt; w += 32) {
     const Wait wt = w < kWaitSlots ? waits[w] : P.waits[ch.wait_off + w];
     const unsigned long long* flag = P.flags + wt.item;
-    const unsigned long long target =
-        (MODE == kCounter) ? epoch * static_cast<unsigned long long>(wt.chunks) : epoch;
     unsigned long long t0 = 0;
     unsigned iter = 0, nap = 0;
-    while (!flag_ready<MODE>(ld_acquire_u64(flag), target)) {
+    // epoch flags (per item or per chunk) are compared for equality, as the
+    // pages' signal wait does
+    while (ld_acquire_u64(flag) != epoch) {
       if ((iter++ & 15u) == 0u) {
         const unsigned long long now = global_timer_ns();
         if (t0 == 0) t0 = now;
@@ -179,8 +168,6 @@ __device__ __forceinline__ void signal_chunk(const DirParams& P, const Chunk& ch
   const bool drop = ch.item == drop_item;
   if (MODE == kChunkFlag) {
     if (!drop) st_release_u64(P.flags + c, epoch);
-  } else if (MODE == kCounter) {
-    if (!drop) red_release_add_u64(P.flags + ch.item, 1ull);
   } else {
     const unsigned last = static_cast<unsigned>(ch.item_chunks - 1);
     const unsigned old = atom_inc_acq_rel(P.arrivals + ch.item, last);
@@ -603,23 +590,17 @@ __global__ void k_noop() {}
 }  // namespace
 
 const void* coords_kernel(int signal_mode, bool bulk_store) {
-  if (bulk_store) {
-    if (signal_mode == kChunkFlag) return reinterpret_cast<const void*>(&k_coords_bulk<kChunkFlag>);
-    return signal_mode == kCounter ? reinterpret_cast<const void*>(&k_coords_bulk<kCounter>)
-                                   : reinterpret_cast<const void*>(&k_coords_bulk<kLastArrival>);
-  }
-  if (signal_mode == kChunkFlag) return reinterpret_cast<const void*>(&k_coords_fused<kChunkFlag>);
-  return signal_mode == kCounter ? reinterpret_cast<const void*>(&k_coords_fused<kCounter>)
-                                 : reinterpret_cast<const void*>(&k_coords_fused<kLastArrival>);
+  if (bulk_store)
+    return signal_mode == kChunkFlag ? reinterpret_cast<const void*>(&k_coords_bulk<kChunkFlag>)
+                                     : reinterpret_cast<const void*>(&k_coords_bulk<kLastArrival>);
+  return signal_mode == kChunkFlag ? reinterpret_cast<const void*>(&k_coords_fused<kChunkFlag>)
+                                   : reinterpret_cast<const void*>(&k_coords_fused<kLastArrival>);
 }
 
 const void* forces_kernel(int signal_mode, bool ordered) {
   if (signal_mode == kChunkFlag)
     return ordered ? reinterpret_cast<const void*>(&k_forces_fused<kChunkFlag, true>)
                    : reinterpret_cast<const void*>(&k_forces_fused<kChunkFlag, false>);
-  if (signal_mode == kCounter)
-    return ordered ? reinterpret_cast<const void*>(&k_forces_fused<kCounter, true>)
-                   : reinterpret_cast<const void*>(&k_forces_fused<kCounter, false>);
   return ordered ? reinterpret_cast<const void*>(&k_forces_fused<kLastArrival, true>)
                  : reinterpret_cast<const void*>(&k_forces_fused<kLastArrival, false>);
 }

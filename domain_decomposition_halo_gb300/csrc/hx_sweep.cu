@@ -1,24 +1,20 @@
-// Slot-sweep exchange kernels of libhx (sm_103a).
+// Slot-sweep force exchange kernel of libhx (sm_103a).
 //
-// Same operation as the chunk kernels of hx_kernels.cu. Coordinates use the
-// gather packed[i] = x[map[i]] of packSendBufKernel, with the periodic
-// shift. Forces use the accumulation forces[map[i]] += packed[i] of
-// unpackRecvBufKernel<accumulate>, last pulse first ("Force halo exchange:
-// Reversing the dependency chain").
+// Same operation as the force chunk kernel of hx_kernels.cu: the
+// accumulation forces[map[i]] += packed[i] of unpackRecvBufKernel<accumulate>,
+// last pulse first ("Force halo exchange: Reversing the dependency chain").
 //
 // The two differ only in the unit of work. A chunk is a run of one pulse's
-// map. A sweep unit is a run of up to kSweepSlots consecutive slots of one
-// sender's array, with every pulse's map entries that fall in it:
-//   - coordinates: the unit is a source. Its slots and its map runs are
-//     staged in shared memory; every pulse's gathers are served from there
-//     and each pulse's run is stored into the receiver, coalesced;
-//   - forces: the unit is a target. Its slots, its map runs and the received
-//     force runs are staged; the runs are added last pulse first and the
-//     slots are written back.
+// map. A sweep unit is a run of up to kSweepSlots consecutive target slots
+// of one sender's array, with every pulse's map entries that fall in it. Its
+// slots, its map runs and the received force runs are staged in shared
+// memory; the runs are added last pulse first and the slots are written
+// back. (A coordinate form, with the unit as a gather source, was measured
+// slower than the chunk kernels everywhere and is not built.)
 //
 // Why this pays on one GPU: with random in-domain order nearly every
-// 64-byte granule of a sender's slots holds some pulse's selected atom. The
-// chunk kernels therefore touch the whole home region once per pulse, in
+// 64-byte granule of a sender's slots holds some pulse's target. The chunk
+// kernel therefore reads and writes the whole home region once per pulse, in
 // scattered 12-byte accesses. A sweep touches it once in total, as
 // sequential streams, and every per-entry access stays in shared memory.
 // Each contiguous run is one TMA bulk copy (cp.async.bulk) issued by one lane
@@ -26,10 +22,9 @@
 // handful of instructions instead of one per 128 bytes per lane.
 //
 // Dependencies and signals are per unit, as in the chunk kernels' fine mode
-// ("Enabling parallelism across pulses through kernel fusion"): a unit of
-// received slots waits for the units that stored them (coordinates), and a
-// unit waits for the receivers' units that still add into the slots it reads
-// (forces). Each warp is independent. Its claims are static batches of
+// ("Enabling parallelism across pulses through kernel fusion"): a unit waits
+// for the receivers' units that still add into the slots it reads. Each warp
+// is independent. Its claims are static batches of
 // units in a topological order (warp w of W takes batches w, w + W, ...), so
 // it never waits on a unit that no running warp owns.
 #include <cstdint>
@@ -51,7 +46,6 @@ template <int KIND>
 struct alignas(16) WarpSmem {
   alignas(16) unsigned char stage[sweep_stage_bytes(KIND)];
   Unit desc[2];              // the current unit's record and the next one's
-  float out[KIND == 0 ? 96 : 4];  // coordinates: one 32-entry round, transposed for coalesced stores
   unsigned long long bar;        // completion of the unit's bulk copies
 };
 
@@ -273,56 +267,6 @@ __device__ __forceinline__ void cp_async_16(void* smem_dst, const void* gmem_src
 
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-// Store one round of up to 32 consecutive entries as contiguous floats with
-// coalesced stores (transposed through the warp's `out`).
-__device__ __forceinline__ void store_round(float* __restrict__ dst, int n_round, float v0, float v1, float v2,
-                                            float* out) {
-  const int lane = threadIdx.x & 31;
-  if (lane < n_round) {
-    out[3 * lane + 0] = v0;
-    out[3 * lane + 1] = v1;
-    out[3 * lane + 2] = v2;
-  }
-  __syncwarp();
-#pragma unroll
-  for (int k = 0; k < 3; ++k) {
-    const int idx = k * 32 + lane;
-    if (idx < 3 * n_round) dst[idx] = out[idx];
-  }
-  __syncwarp();
-}
-
-// Coordinates of one staged unit: every pulse's gathers.
-__device__ __forceinline__ void coords_unit(float* __restrict__ x, const UnitParams& P, const Unit& d,
-                                            WarpSmem<0>& S) {
-  const int lane = threadIdx.x & 31;
-  const float* tile = reinterpret_cast<const float*>(
-      S.stage + (reinterpret_cast<unsigned long long>(x + 3 * d.base) & 15ull));
-  for (int s = 0; s < d.seg_cnt; ++s) {
-    const UnitSeg sg = seg_at(P, d, s);
-    const int32_t* smap = reinterpret_cast<const int32_t*>(
-        S.stage + sg.map_off + (reinterpret_cast<unsigned long long>(P.maps + sg.map) & 15ull));
-    float* dst = x + 3 * sg.other;
-    for (int i0 = 0; i0 < sg.n; i0 += 32) {
-      const int i = i0 + lane;
-      const int n_round = sg.n - i0;
-      float v0 = 0.f, v1 = 0.f, v2 = 0.f;
-      if (i < sg.n) {
-        const int j = smap[i] - d.local_a;
-        v0 = tile[3 * j + 0];
-        v1 = tile[3 * j + 1];
-        v2 = tile[3 * j + 2];
-        if (sg.do_shift) {   // no add otherwise: unshifted values keep every bit (-0.0 included)
-          if (sg.dim == 0) v0 = __fadd_rn(v0, sg.shift);
-          else if (sg.dim == 1) v1 = __fadd_rn(v1, sg.shift);
-          else v2 = __fadd_rn(v2, sg.shift);
-        }
-      }
-      store_round(dst + 3 * i0, n_round < 32 ? n_round : 32, v0, v1, v2, S.out);
-    }
-  }
-}
-
 // Lane 0: this warp's bulk stores have read the stage / have completed and
 // are ordered before later generic accesses (before a release).
 __device__ __forceinline__ void bulk_stores_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
@@ -376,9 +320,10 @@ __device__ __forceinline__ void forces_unit(float* __restrict__ f, const UnitPar
   }
 }
 
-// KIND 0 = coordinates, 1 = forces (ordered).
+// KIND 1 = forces (ordered), the one direction the sweep serves.
 template <int KIND>
 __global__ void __launch_bounds__(kThreads) k_sweep(float* __restrict__ buf, UnitParams P) {
+  static_assert(KIND == 1, "the slot sweep serves the force exchange");
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const int lane = threadIdx.x & 31;
   WarpSmem<KIND>& S = reinterpret_cast<WarpSmem<KIND>*>(smem_raw)[threadIdx.x >> 5];
@@ -478,11 +423,9 @@ __global__ void __launch_bounds__(kThreads) k_sweep(float* __restrict__ buf, Uni
 
 }  // namespace
 
-const void* sweep_kernel(int kind) {
-  return kind == 0 ? reinterpret_cast<const void*>(&k_sweep<0>) : reinterpret_cast<const void*>(&k_sweep<1>);
-}
+const void* sweep_kernel(int) { return reinterpret_cast<const void*>(&k_sweep<1>); }
 
-size_t sweep_smem_bytes(int kind) { return kWarps * (kind == 0 ? sizeof(WarpSmem<0>) : sizeof(WarpSmem<1>)); }
+size_t sweep_smem_bytes(int) { return kWarps * sizeof(WarpSmem<1>); }
 
 int sweep_blocks_per_sm(int kind) {
   const void* fn = sweep_kernel(kind);

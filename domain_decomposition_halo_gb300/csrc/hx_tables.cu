@@ -586,10 +586,9 @@ int build_tables(hx_ctx* h, cudaStream_t s) {
   auto upper = [&](int r, int q) { return upper_tab[static_cast<size_t>(r) * P + q]; };
   std::vector<int64_t> rank(nd);
   for (int r = 0; r < nd; ++r) rank[r] = domain_rank(pl, r);
-  h->family[0] = (h->flags & HX_FLAG_SWEEP)   ? kFamSweep
-                 : (h->flags & HX_FLAG_RESOLVED) ? kFamResolved
+  h->family[0] = (h->flags & HX_FLAG_RESOLVED) ? kFamResolved
                                                 : kFamChunks;
-  h->family[1] = (h->flags & (HX_FLAG_SWEEP | HX_FLAG_SWEEP_FORCES)) ? kFamSweep : h->family[0];
+  h->family[1] = (h->flags & HX_FLAG_SWEEP_FORCES) ? kFamSweep : h->family[0];
   for (int k = 0; k < 2; ++k) {
     const int per_sm = std::max(1, h->family[k] == kFamSweep   ? sweep_blocks_per_sm(k)
                                    : h->family[k] == kFamResolved ? 1

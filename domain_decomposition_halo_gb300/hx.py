@@ -27,9 +27,7 @@ HX_ERR_NOMEM = -8
 
 HX_FLAG_UNORDERED_FORCES = 0x1
 HX_FLAG_NO_GRAPH = 0x2
-HX_FLAG_COUNTER_SIGNAL = 0x4
 HX_FLAG_FINE_WAITS = 0x8
-HX_FLAG_SWEEP = 0x20
 HX_FLAG_SWEEP_FORCES = 0x40
 HX_FLAG_RESOLVED = 0x100
 HX_FLAG_BULK_STORE = 0x200

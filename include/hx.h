@@ -67,7 +67,7 @@ typedef struct hx_ctx* hx_handle;
 #define HX_OK 0
 #define HX_ERR_ARG (-1)       /* null pointer, cutoff <= 0, dims < 1, box <= 0, bad index */
 #define HX_ERR_PULSES (-2)    /* np_d >= n_d in some dimension, or too many pulses; from
-                                 hx_build_maps also a plan beyond what the HX_FLAG_SWEEP
+                                 hx_build_maps also a plan beyond what the HX_FLAG_SWEEP_FORCES
                                  (8 pulses) or HX_FLAG_RESOLVED (7 copies per atom) tables hold */
 #define HX_ERR_RANGE (-3)     /* an input position outside [0, L) or NaN */
 #define HX_ERR_CAPACITY (-4)  /* caller buffer smaller than the layout needs */
@@ -78,26 +78,26 @@ typedef struct hx_ctx* hx_handle;
 
 /* hx_init flags */
 #define HX_FLAG_UNORDERED_FORCES 0x1u /* force adds by atomics: order-free, within 1e-6 relative
-                                          of the ordered result; default is ordered and bit-exact */
+                                          of the ordered result; default is ordered and bit-exact.
+                                          Applies to the chunk force kernel: the slot sweep
+                                          (HX_FLAG_SWEEP_FORCES) and resolved mode always add in
+                                          order and ignore it */
 #define HX_FLAG_NO_GRAPH 0x2u          /* launch the fused kernels directly, not through a CUDA graph */
-#define HX_FLAG_COUNTER_SIGNAL 0x4u    /* every chunk adds to its pulse's arrival counter (release)
-                                          instead of the last chunk storing an epoch flag */
 #define HX_FLAG_FINE_WAITS 0x8u        /* chunk-granular dependencies: a chunk waits only for the
                                           chunks that wrote the slots it reads or, for forces, that
-                                          add into its targets, each signalled by its own epoch flag
-                                          (HX_FLAG_COUNTER_SIGNAL is then ignored) */
-#define HX_FLAG_SWEEP 0x20u            /* slot-sweep kernels: every warp takes units of up to 256
-                                          consecutive slots of one sender, stages them in its shared
-                                          memory with TMA bulk copies (cp.async.bulk) and serves every
-                                          pulse's gathers or reverse-ordered adds from them; per-unit
-                                          signals; same results bit for bit. Plans of more than 8
-                                          pulses get HX_ERR_PULSES from hx_build_maps */
-#define HX_FLAG_SWEEP_FORCES 0x40u     /* the force exchange by the slot-sweep kernel, the coordinate
-                                          exchange by the chunk kernels (with HX_FLAG_FINE_WAITS or
-                                          the other chunk flags) or, with HX_FLAG_RESOLVED, by the
-                                          resolved gather. At most one of HX_FLAG_SWEEP and
-                                          HX_FLAG_RESOLVED, and HX_FLAG_SWEEP_FORCES not with
-                                          HX_FLAG_SWEEP (else HX_ERR_ARG) */
+                                          add into its targets, each signalled by its own epoch flag;
+                                          without it, the pages' per-pulse signals (the last chunk of
+                                          a (sender, pulse) stores its epoch flag) */
+#define HX_FLAG_SWEEP_FORCES 0x40u     /* the force exchange by the slot-sweep kernel: every warp
+                                          takes units of up to 256 consecutive target slots of one
+                                          sender, stages them, their map runs and their received
+                                          force runs in shared memory with TMA bulk copies
+                                          (cp.async.bulk), adds every pulse's contributions in
+                                          reverse pulse order there and writes the slots back; per-
+                                          unit signals; same results bit for bit. The coordinates
+                                          stay on the chunk kernels. Not with HX_FLAG_RESOLVED (else
+                                          HX_ERR_ARG); plans of more than 8 pulses get HX_ERR_PULSES
+                                          from hx_build_maps */
 #define HX_FLAG_BULK_STORE 0x200u      /* chunk coordinate kernels pack by bulk store: each warp gathers
                                           its chunk into shared memory and stores it to the receiver's
                                           slots with one cp.async.bulk (the pages' TMA variant, section
@@ -124,7 +124,7 @@ typedef struct hx_ctx* hx_handle;
                                           HX_ERR_CAPACITY: a halo slot's origin and shifts share one
                                           32-bit word) */
 
-#define HX_FLAGS_ALL 0x76fu      /* every flag above */
+#define HX_FLAGS_ALL 0x74bu      /* every flag above */
 
 #define HX_MAX_PULSES 32
 #define HX_MAX_DOMAINS 4096

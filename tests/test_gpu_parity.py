@@ -15,16 +15,14 @@ from oracle.oracle import Oracle
 
 pytestmark = pytest.mark.gpu
 
-ALL_MODES = [0, HX.HX_FLAG_COUNTER_SIGNAL, HX.HX_FLAG_NO_GRAPH,
-             HX.HX_FLAG_COUNTER_SIGNAL | HX.HX_FLAG_NO_GRAPH, HX.HX_FLAG_FINE_WAITS,
-             HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_COUNTER_SIGNAL, HX.HX_FLAG_SWEEP,
-             HX.HX_FLAG_SWEEP | HX.HX_FLAG_NO_GRAPH, HX.HX_FLAG_SWEEP_FORCES,
-             HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES, HX.HX_FLAG_RESOLVED,
-             HX.HX_FLAG_RESOLVED | HX.HX_FLAG_NO_GRAPH, HX.HX_FLAG_RESOLVED | HX.HX_FLAG_SWEEP_FORCES,
-             HX.HX_FLAG_BULK_STORE, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE,
-             HX.HX_FLAG_COUNTER_SIGNAL | HX.HX_FLAG_BULK_STORE, HX.HX_FLAG_RESOLVED | HX.HX_FLAG_PDL,
+ALL_MODES = [0, HX.HX_FLAG_NO_GRAPH, HX.HX_FLAG_FINE_WAITS, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_NO_GRAPH,
+             HX.HX_FLAG_SWEEP_FORCES, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES,
+             HX.HX_FLAG_SWEEP_FORCES | HX.HX_FLAG_NO_GRAPH, HX.HX_FLAG_RESOLVED,
+             HX.HX_FLAG_RESOLVED | HX.HX_FLAG_NO_GRAPH, HX.HX_FLAG_BULK_STORE,
+             HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE, HX.HX_FLAG_RESOLVED | HX.HX_FLAG_PDL,
              HX.HX_FLAG_PDL, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_PDL,
              HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE | HX.HX_FLAG_PDL,
+             HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE | HX.HX_FLAG_NO_GRAPH,
              HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE | HX.HX_FLAG_SWEEP_FORCES | HX.HX_FLAG_PDL]
 
 
@@ -124,8 +122,8 @@ def test_parity_configs(name, flags):
     check_force_steps(c)
 
 
-@pytest.mark.parametrize("flags", [0, HX.HX_FLAG_FINE_WAITS, HX.HX_FLAG_SWEEP,
-                                   HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES, HX.HX_FLAG_RESOLVED,
+@pytest.mark.parametrize("flags", [0, HX.HX_FLAG_FINE_WAITS, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES,
+                                   HX.HX_FLAG_RESOLVED,
                                    HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE | HX.HX_FLAG_SWEEP_FORCES])
 def test_parity_c5_full_size(flags):
     """12M atoms, 256 domains: the bench's configuration and launch path."""
@@ -136,7 +134,7 @@ def test_parity_c5_full_size(flags):
 
 
 @pytest.mark.parametrize("name", ["C2", "C3", "C4"])
-@pytest.mark.parametrize("extra", [0, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_COUNTER_SIGNAL])
+@pytest.mark.parametrize("extra", [0, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE])
 def test_unordered_forces(name, extra):
     c = Case(W.WORKLOADS[name], flags=HX.HX_FLAG_UNORDERED_FORCES | extra)
     check_force_steps(c, steps=2, ordered=False)
@@ -160,8 +158,7 @@ def test_unfused_baseline(name):
     ((3.0, 3.0, 3.0), (3, 3, 3), 0.6, 2700),      # 27 domains
     ((40.0, 3.0, 3.0), (40, 1, 1), 1.0, 36000),   # many small domains along one dim
 ])
-@pytest.mark.parametrize("flags", [0, HX.HX_FLAG_COUNTER_SIGNAL, HX.HX_FLAG_FINE_WAITS,
-                                   HX.HX_FLAG_SWEEP, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES,
+@pytest.mark.parametrize("flags", [0, HX.HX_FLAG_FINE_WAITS, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES,
                                    HX.HX_FLAG_RESOLVED, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE])
 def test_parity_shapes(box, dims, cutoff, n, flags):
     w = W.custom("shape", n, box, dims, cutoff, seed=7 + n)
@@ -222,10 +219,11 @@ def test_resolved_tree_classes(name):
         assert Case(W.WORKLOADS[name], flags=HX.HX_FLAG_FINE_WAITS).hx.resolved_counts() == (0, 0, 0)
 
 
-@pytest.mark.parametrize("flags", [0, HX.HX_FLAG_SWEEP])
+@pytest.mark.parametrize("flags", [0, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE | HX.HX_FLAG_SWEEP_FORCES])
 def test_misaligned_buffers(flags):
-    """Caller buffers that start 4 or 8 bytes past a 16-byte boundary (tile
-    mode copies aligned middles in bulk and the edges with plain loads)."""
+    """Caller buffers that start 4, 8 or 12 bytes past a 16-byte boundary (the
+    bulk-store pack and the slot sweep move 16-byte-aligned middles in bulk
+    and the edges with plain loads and stores)."""
     w = W.WORKLOADS["C2"]
     c = Case(w, flags=flags)
     for shift in (1, 2, 3):
@@ -262,8 +260,7 @@ def test_boundary_atoms():
 
 def test_many_steps_reuse_signals():
     """Epoch-valued signals are never reset between launches: 200 steps."""
-    for flags in (0, HX.HX_FLAG_COUNTER_SIGNAL, HX.HX_FLAG_FINE_WAITS, HX.HX_FLAG_SWEEP,
-                  HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES, HX.HX_FLAG_RESOLVED,
+    for flags in (0, HX.HX_FLAG_FINE_WAITS, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES, HX.HX_FLAG_RESOLVED,
                   HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE, HX.HX_FLAG_RESOLVED | HX.HX_FLAG_PDL):
         c = Case(W.WORKLOADS["C2"], flags=flags)
         x = c.o.coords().copy()
@@ -335,8 +332,10 @@ def test_errors():
     with pytest.raises(HX.HXError) as ei:
         hx.build_maps(pos, small)
     assert ei.value.code == HX.HX_ERR_CAPACITY
-    for bad in (HX.HX_FLAG_SWEEP | HX.HX_FLAG_SWEEP_FORCES, HX.HX_FLAG_RESOLVED | HX.HX_FLAG_SWEEP, 0x80):
-        with pytest.raises(HX.HXError) as ei:   # the unit kernel families are alternatives
+    # resolved coordinates with swept forces is not a mode; 0x4, 0x10, 0x20 and
+    # 0x80 are retired or unassigned bits
+    for bad in (HX.HX_FLAG_RESOLVED | HX.HX_FLAG_SWEEP_FORCES, 0x4, 0x10, 0x20, 0x80):
+        with pytest.raises(HX.HXError) as ei:
             HX.HaloExchange(w.box, w.dims, w.cutoff, flags=bad)
         assert ei.value.code == HX.HX_ERR_ARG
     with pytest.raises(HX.HXError):
@@ -344,8 +343,7 @@ def test_errors():
 
 
 @pytest.mark.parametrize("direction", [0, 1])
-@pytest.mark.parametrize("flags", [0, HX.HX_FLAG_COUNTER_SIGNAL, HX.HX_FLAG_FINE_WAITS,
-                                   HX.HX_FLAG_SWEEP, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES,
+@pytest.mark.parametrize("flags", [0, HX.HX_FLAG_FINE_WAITS, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES,
                                    HX.HX_FLAG_BULK_STORE, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE])
 def test_dropped_signal_times_out_and_recovers(direction, flags):
     """Failure detection without a device fault: a (domain, pulse) that never
@@ -371,7 +369,7 @@ def test_dropped_signal_times_out_and_recovers(direction, flags):
     assert detail // 65536 == direction
     item = detail % 65536
     p_item = item // nd
-    if flags & HX.HX_FLAG_SWEEP or (direction == 1 and flags & HX.HX_FLAG_SWEEP_FORCES):
+    if direction == 1 and flags & HX.HX_FLAG_SWEEP_FORCES:
         # a unit is labelled by its first map's (pulse, domain); a cascade can
         # report any unit downstream of the dropped one
         assert 0 <= item < c.o.n_pulses * nd

@@ -23,8 +23,7 @@ pytestmark = pytest.mark.gpu
 
 
 @pytest.mark.parametrize("name", ["C2", "C5"])
-@pytest.mark.parametrize("flags", [0, HX.HX_FLAG_FINE_WAITS, HX.HX_FLAG_SWEEP,
-                                   HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES,
+@pytest.mark.parametrize("flags", [0, HX.HX_FLAG_FINE_WAITS, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES,
                                    HX.HX_FLAG_RESOLVED, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE])
 def test_static_scratch_matches_regular_exchange(name, flags):
     w = W.WORKLOADS[name]
@@ -69,7 +68,8 @@ def _static(hx, x, stream=None):
     return lib.hx_exchange_coords_static(hx._h, x.data_ptr(), s)
 
 
-@pytest.mark.parametrize("flags", [0, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE, HX.HX_FLAG_SWEEP,
+@pytest.mark.parametrize("flags", [0, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE,
+                                   HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE | HX.HX_FLAG_SWEEP_FORCES,
                                    HX.HX_FLAG_RESOLVED])
 def test_static_call_allocates_no_device_memory(flags):
     """The set-up (symbol address, kernel module) happens in hx_build_maps,
