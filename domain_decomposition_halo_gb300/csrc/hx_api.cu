@@ -161,6 +161,13 @@ DirParams dir_params(hx_ctx* h, int dir) {
   P.ctrl = h->d_ctrl + dir;
   P.n_chunks = static_cast<unsigned long long>(h->n_chunks[dir]);
   P.direction = dir;
+  // The slot sweep's persistent grid must be wholly resident. Scheduled
+  // while the coordinate blocks still run, some SMs were measured to take
+  // only two of its three blocks per SM once those blocks had gone (18-22 of
+  // 456 blocks on the 12M-atom workload started only after other sweep
+  // blocks finished, and waits on their units ran out). Scheduled as the
+  // coordinate blocks exit, it lands on empty SMs.
+  P.late_dependents = (dir == 0 && h->family[1] == kFamSweep) ? 1 : 0;
   P.timeout_ns = h->timeout_ns;
   return P;
 }
@@ -172,8 +179,6 @@ const void* kernel_for(hx_ctx* h, int kind) {
   return noop_kernel();
 }
 
-// Launch a fused exchange (kind 0/1) or the no-op (kind 2): directly, or via
-// a cached single-node graph keyed by (kind, buffer pointer).
 UnitParams unit_params(hx_ctx* h, int dir) {
   UnitParams P;
   std::memset(&P, 0, sizeof(P));
@@ -240,6 +245,8 @@ size_t fused_smem(const hx_ctx* h, int dir) {
   return 0;
 }
 
+// Launch a fused exchange (kind 0/1) or the no-op (kind 2): directly, or via
+// a cached single-node graph keyed by (kind, buffer pointer).
 int launch(hx_ctx* h, int kind, float* buf, cudaStream_t s) {
   DirParams P;
   UnitParams TP;
@@ -274,16 +281,15 @@ int launch(hx_ctx* h, int kind, float* buf, cudaStream_t s) {
     grid = dim3(static_cast<unsigned>(h->grid[kind]));
     smem = fused_smem(h, kind);
   }
-  if (kind != 2 && (h->family[kind] == kFamResolved || h->family[kind] == kFamChunks) && (h->flags & HX_FLAG_PDL)) {
-    // direct launch that may start while the stream's previous kernel finishes;
-    // the resolved and chunk kernels wait for it (griddepcontrol.wait) before
-    // touching data. Not the slot sweep: on the 12M-atom workload its
-    // persistent grid timed out under programmatic launch (a producer unit's
-    // signal never came), so it keeps plain stream order.
+  if (kind != 2 && (h->flags & HX_FLAG_PDL)) {
+    // Direct launch that may start while the stream's previous kernel
+    // finishes; every exchange kernel waits for it (griddepcontrol.wait)
+    // before touching data.
     cudaLaunchAttribute attr[1];
     std::memset(attr, 0, sizeof(attr));
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    const unsigned n_attr = 1;
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof(cfg));
     cfg.gridDim = grid;
@@ -291,7 +297,7 @@ int launch(hx_ctx* h, int kind, float* buf, cudaStream_t s) {
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = n_attr;
     return to_err(cudaLaunchKernelExC(&cfg, fn, args));
   }
   if (h->flags & HX_FLAG_NO_GRAPH) return to_err(cudaLaunchKernel(fn, grid, block, args, smem, s));

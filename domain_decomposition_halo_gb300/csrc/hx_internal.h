@@ -96,7 +96,8 @@ struct DirParams {
   Ctrl* ctrl;
   unsigned long long n_chunks;
   int direction;              // 0 coordinates, 1 forces
-  int pad;
+  int late_dependents;        // 1: under programmatic launch, the next kernel is scheduled only
+                              // as this grid's blocks exit (not as they start)
   unsigned long long timeout_ns;
 };
 

@@ -499,7 +499,7 @@ __device__ __forceinline__ void run_warps(float* __restrict__ buf, const DirPara
   const unsigned long long W = static_cast<unsigned long long>(gridDim.x) * kWarps;
   const unsigned long long N = P.n_chunks;
   unsigned long long c = static_cast<unsigned long long>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
-  allow_dependents();
+  if (!P.late_dependents) allow_dependents();
   wait_prerequisites();   // before the first flag, table or buffer access
   const unsigned long long epoch = ld_relaxed_u64(&P.ctrl->epoch) + 1ull;
   if (c < N) {

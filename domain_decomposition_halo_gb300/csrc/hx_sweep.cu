@@ -331,6 +331,13 @@ __global__ void __launch_bounds__(kThreads) k_sweep(float* __restrict__ buf, Uni
   const unsigned long long N = P.n_units;
   const unsigned long long NB = (N + kSweepBatch - 1) / kSweepBatch;   // batches of units per launch
   const unsigned long long b0 = static_cast<unsigned long long>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+  // Under programmatic dependent launch the next kernel of the stream may be
+  // scheduled once every block of this grid has started (so this grid is
+  // wholly resident first, as the static claims need), and this grid waits
+  // for the previous kernel to complete before it touches any table, flag
+  // or force. Both instructions are no-ops in a plain stream-ordered launch.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // The launch's epoch; its last block to finish stores it for the next
   // launch of this direction (which reads it after this grid has completed).
   const unsigned long long epoch = ld_relaxed_u64(&P.ctrl->epoch) + 1ull;
@@ -383,8 +390,7 @@ __global__ void __launch_bounds__(kThreads) k_sweep(float* __restrict__ buf, Uni
       }
       parity ^= 1u;
       __syncwarp();   // the lanes' edge words are in place
-      if constexpr (KIND == 0) coords_unit(buf, P, d, S);
-      else forces_unit(buf, P, d, S);
+      forces_unit(buf, P, d, S);
       // One acquire poll of the next unit's waits (when they all come with
       // its record), issued before this unit's signal so that the two round
       // trips overlap; if it finds them set, the next unit skips its wait.

@@ -104,14 +104,16 @@ typedef struct hx_ctx* hx_handle;
                                           "Optimizing for efficient transfers across NVIDIA
                                           NVLink-connected GPUs"); same results bit for bit. Applies
                                           where the chunk kernels run the coordinates */
-#define HX_FLAG_PDL 0x400u             /* launch the resolved and chunk kernels directly with
-                                          programmatic dependent launch, so an exchange may be
-                                          scheduled while the stream's previous kernel finishes (it
-                                          waits for that kernel before claiming work or touching
-                                          coordinates, forces or flags; resolved kernels read their
-                                          build-time tables first). The slot sweep keeps plain stream
-                                          order (an earlier version of its persistent grid timed out
-                                          under programmatic launch on a 12M-atom workload) */
+#define HX_FLAG_PDL 0x400u             /* launch the exchange kernels directly with programmatic
+                                          dependent launch, so an exchange may be scheduled while
+                                          the stream's previous kernel finishes (it waits for that
+                                          kernel before claiming work or touching coordinates,
+                                          forces or flags; resolved kernels read their build-time
+                                          tables first). A persistent grid lets the next kernel be
+                                          scheduled only once all of its own blocks have started;
+                                          with HX_FLAG_SWEEP_FORCES, only as the coordinate
+                                          kernel's blocks exit, so that the sweep's grid lands on
+                                          empty SMs and is wholly resident */
 #define HX_FLAG_RESOLVED 0x100u        /* the forwarding unrolled at build time: every halo slot is
                                           gathered straight from its origin home atom (plus the
                                           shifts its path added), and every home atom's force tree

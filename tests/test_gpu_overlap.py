@@ -24,7 +24,8 @@ pytestmark = pytest.mark.gpu
 
 MODES = [0, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE,
          HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE | HX.HX_FLAG_SWEEP_FORCES,
-         HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE | HX.HX_FLAG_PDL, HX.HX_FLAG_RESOLVED]
+         HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE | HX.HX_FLAG_PDL,
+         HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE | HX.HX_FLAG_SWEEP_FORCES | HX.HX_FLAG_PDL, HX.HX_FLAG_RESOLVED]
 
 
 @pytest.mark.parametrize("name", ["C2", "C4"])

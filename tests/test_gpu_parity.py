@@ -261,7 +261,8 @@ def test_boundary_atoms():
 def test_many_steps_reuse_signals():
     """Epoch-valued signals are never reset between launches: 200 steps."""
     for flags in (0, HX.HX_FLAG_FINE_WAITS, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES, HX.HX_FLAG_RESOLVED,
-                  HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE, HX.HX_FLAG_RESOLVED | HX.HX_FLAG_PDL):
+                  HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE, HX.HX_FLAG_RESOLVED | HX.HX_FLAG_PDL,
+                  HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE | HX.HX_FLAG_SWEEP_FORCES | HX.HX_FLAG_PDL):
         c = Case(W.WORKLOADS["C2"], flags=flags)
         x = c.o.coords().copy()
         xt = torch.from_numpy(x).cuda()
@@ -344,7 +345,9 @@ def test_errors():
 
 @pytest.mark.parametrize("direction", [0, 1])
 @pytest.mark.parametrize("flags", [0, HX.HX_FLAG_FINE_WAITS, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES,
-                                   HX.HX_FLAG_BULK_STORE, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE])
+                                   HX.HX_FLAG_BULK_STORE, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE,
+                                   HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE | HX.HX_FLAG_SWEEP_FORCES |
+                                   HX.HX_FLAG_PDL])
 def test_dropped_signal_times_out_and_recovers(direction, flags):
     """Failure detection without a device fault: a (domain, pulse) that never
     signals makes its waiters give up after the bounded wait; the kernel
