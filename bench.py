@@ -48,7 +48,7 @@ def parse_args():
     ap.add_argument("--workload", default="C5", choices=sorted(W.WORKLOADS))
     ap.add_argument("--no-extras", action="store_true", help="skip the secondary measurements")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU baseline budget")
-    ap.add_argument("--flags", default="fine,bulkstore,sweepf",
+    ap.add_argument("--flags", default="fine,bulkstore,sweepf,pdl",
                     help="comma list of libhx modes: fine, bulkstore (coordinates packed by bulk stores), sweepf "
                          "(forces by the slot sweep), resolved, pdl, nograph, unordered, "
                          "pages (= none)")
@@ -429,7 +429,9 @@ def run_ours(args):
             "domains": n_dom, "pulses": n_pulses, "map_entries": entries, "slots": slots,
             "l2": f"inputs larger than L2: coords+forces {2 * slots * 12 / 2**20:.0f} MiB vs L2 129 MiB; no flush",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-            "launch": ("one direct launch" if flags & 0x2 else "one CUDA-graph launch") + " per direction per step",
+            "launch": ("one direct launch with programmatic dependent launch" if flags & HX.HX_FLAG_PDL
+                       else "one direct launch" if flags & HX.HX_FLAG_NO_GRAPH
+                       else "one CUDA-graph launch") + " per direction per step",
             "hx_flags": args.flags,
         },
         "effective_gbs": round(step_gbs, 1),
@@ -605,7 +607,7 @@ def secondary(hx_main, coords, forces, w_main, dev, peak, flags):
     # resolved at build time and launched with programmatic dependent launch
     # (HX_FLAG_RESOLVED | HX_FLAG_PDL), the mode made for them,
     # and the staged path with both directions on the chunk kernels launched
-    # with programmatic dependent launch (the sweep keeps plain stream order)
+    # with programmatic dependent launch
     staged_pdl = HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE | HX.HX_FLAG_PDL
     for name in ("C1", "C2", "C3", "C4"):
         if name == w_main.name:
