@@ -122,6 +122,18 @@ def kernel_source_digest():
     return h.hexdigest()[:16]
 
 
+def launch_label(flags: int) -> str:
+    """How a step launches its two fused exchanges under `flags`."""
+    from domain_decomposition_halo_gb300 import hx as HX
+    if flags & HX.HX_FLAG_PDL:
+        how = "one direct launch with programmatic dependent launch"
+    elif flags & HX.HX_FLAG_NO_GRAPH:
+        how = "one direct launch"
+    else:
+        how = "one CUDA-graph launch"
+    return how + " per direction per step"
+
+
 def kernel_impl(flags: int, direction: int) -> str:
     """The device function that runs a direction's fused exchange under `flags`."""
     from domain_decomposition_halo_gb300 import hx as HX
@@ -429,9 +441,7 @@ def run_ours(args):
             "domains": n_dom, "pulses": n_pulses, "map_entries": entries, "slots": slots,
             "l2": f"inputs larger than L2: coords+forces {2 * slots * 12 / 2**20:.0f} MiB vs L2 129 MiB; no flush",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-            "launch": ("one direct launch with programmatic dependent launch" if flags & HX.HX_FLAG_PDL
-                       else "one direct launch" if flags & HX.HX_FLAG_NO_GRAPH
-                       else "one CUDA-graph launch") + " per direction per step",
+            "launch": launch_label(flags),
             "hx_flags": args.flags,
         },
         "effective_gbs": round(step_gbs, 1),

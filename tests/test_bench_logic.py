@@ -47,6 +47,12 @@ def test_kernel_impl_names_the_launched_kernels():
     assert bench.kernel_impl(bench.hx_flags("resolved"), 1).startswith("k_resolved_forces")
 
 
+def test_launch_label_follows_the_flags():
+    assert bench.launch_label(bench.hx_flags("fine,bulkstore,sweepf,pdl")).startswith("one direct launch with programmatic")
+    assert bench.launch_label(bench.hx_flags("fine,nograph")) == "one direct launch per direction per step"
+    assert bench.launch_label(0) == "one CUDA-graph launch per direction per step"
+
+
 def test_step_distribution_nearest_rank_p90():
     d = bench.step_distribution([10.0 - k for k in range(10)])   # 1..10, unsorted
     assert d == {"median": 5.5, "p90": 9.0, "min": 1.0, "max": 10.0, "n": 10}
