@@ -324,6 +324,16 @@ __device__ __forceinline__ void forces_chunk(float* __restrict__ f, const Chunk&
 // signal follows only once the copy is complete and ordered before the
 // release (bulk_store_done).
 constexpr int kBulkStageBytes = kChunk * 12 + 16;
+#ifndef HX_BULK_MIN_ENTRIES
+#define HX_BULK_MIN_ENTRIES 96
+#endif
+// Chunks of fewer entries take the plain-store path even in the bulk-store
+// kernel: for a small chunk the bulk copy's completion round trip before the
+// release costs more than the lanes' own stores (one GB300, back to back with
+// programmatic launch: 32-entry chunks 14.9 us per step with plain stores and
+// 15.6 with bulk stores on 8 domains; 256-entry chunks 27.9 with bulk stores
+// and 28.7 with plain ones on 64 domains).
+constexpr int kBulkMinEntries = HX_BULK_MIN_ENTRIES;
 constexpr int kPipe = 2;         // chunks in a warp's pipeline: in use, next one in flight
 
 // A warp's shared memory in the fused chunk kernels: the chunk pipeline and
@@ -516,7 +526,15 @@ __device__ __forceinline__ void run_warps(float* __restrict__ buf, const DirPara
       if (c1 < N) fetch_chunk(S.slot[b ^ 1], P.chunks + c1);
       if (ch.wait_cnt > 0) wait_chunk<MODE>(P, ch, cur.waits, epoch);
       if (KIND == 0) coords_chunk(buf, ch, j, reinterpret_cast<float*>(S.stage));
-      else if (KIND == 3) coords_chunk_bulk(buf, ch, j, S.stage);
+      else if (KIND == 3) {
+        if (ch.n >= kBulkMinEntries) {
+          coords_chunk_bulk(buf, ch, j, S.stage);
+        } else {   // small chunk: plain stores, once the previous bulk store has read the stage
+          if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+          __syncwarp();
+          coords_chunk(buf, ch, j, reinterpret_cast<float*>(S.stage));
+        }
+      }
       else forces_chunk_staged<KIND == 1>(buf, ch, j, S.stage);
       if (ch.flags & kSignal) {
         __syncwarp();
