@@ -100,8 +100,13 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-# Sources of the fused exchange kernels that the profiles under profiles/ describe.
-KERNEL_SOURCES = ("hx_kernels.cu", "hx_sweep.cu", "hx_internal.h")
+# Sources of each family of fused exchange kernels that the profiles under
+# profiles/ describe: a profile stays valid while its family's sources do.
+KERNEL_SOURCES = {
+    "chunks": ("hx_kernels.cu", "hx_internal.h"),
+    "sweep": ("hx_sweep.cu", "hx_internal.h"),
+    "resolved": ("hx_resolved.cu", "hx_internal.h"),
+}
 
 
 _TOKENS = re.compile(r'"(?:\\.|[^"\\\n])*"|//[^\n]*|/\*.*?\*/', re.S)
@@ -114,9 +119,17 @@ def code_only(text: str) -> str:
     return " ".join(text.split())
 
 
-def kernel_source_digest():
+def kernel_family(flags: int, direction: int) -> str:
+    """Which family of fused kernels runs a direction under `flags`."""
+    from domain_decomposition_halo_gb300 import hx as HX
+    if direction == 1 and flags & HX.HX_FLAG_SWEEP_FORCES:
+        return "sweep"
+    return "resolved" if flags & HX.HX_FLAG_RESOLVED else "chunks"
+
+
+def kernel_source_digest(family: str = "chunks"):
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES:
+    for name in KERNEL_SOURCES[family]:
         with open(os.path.join(ROOT, "domain_decomposition_halo_gb300", "csrc", name), encoding="utf-8") as fh:
             h.update(code_only(fh.read()).encode())
     return h.hexdigest()[:16]
@@ -196,9 +209,10 @@ def traffic_floor(hx):
     return out
 
 
-def profiled_traffic(kernel: str, workload: str):
+def profiled_traffic(kernel: str, workload: str, family: str):
     """DRAM bytes per launch from the committed ncu summary of this kernel,
-    if it was taken on the current kernel source; else None."""
+    if it was taken on the current source of the kernel family that runs it;
+    else None."""
     path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     try:
         text = open(path).read()
@@ -206,7 +220,7 @@ def profiled_traffic(kernel: str, workload: str):
         return None
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
     s = re.search(r"kernel_source_digest:\s*([0-9a-f]+)", text)
-    if not m or not s or s.group(1) != kernel_source_digest():
+    if not m or not s or s.group(1) != kernel_source_digest(family):
         return None
     return float(m.group(1))
 
@@ -422,7 +436,7 @@ def run_ours(args):
             "floor_bytes": fb, "floor_bytes_32B": floors["sector_32B"][key],
             "frac_of_floor": round(fb / (ms * 1e-3) / 1e9 / peak, 4),
             "frac_ceiling": round(per_entry * entries / fb, 4),
-            "traffic": profiled_traffic(name, w.name)}
+            "traffic": profiled_traffic(name, w.name, kernel_family(flags, 0 if key == "coords" else 1))}
     out = {
         "metric": METRIC,
         "value": round(us_step, 3),
@@ -450,7 +464,7 @@ def run_ours(args):
             "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
             "algorithmic_bytes_per_launch": dom_bytes,
-            "traffic": profiled_traffic(dominant, w.name),
+            "traffic": per_kernel[dominant]["traffic"],
             "floor_bytes": per_kernel[dominant]["floor_bytes"],
             "frac_of_floor": per_kernel[dominant]["frac_of_floor"],
             "floor_what": "distinct 64-byte DRAM granules a launch must read or write, from the maps "

@@ -29,14 +29,14 @@ def test_flag_names():
 def test_traffic_needs_matching_digest(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     (tmp_path / "domain_decomposition_halo_gb300" / "csrc").mkdir(parents=True)
-    for name in bench.KERNEL_SOURCES:
+    for name in sorted({n for files in bench.KERNEL_SOURCES.values() for n in files}):
         (tmp_path / "domain_decomposition_halo_gb300" / "csrc" / name).write_text("x")
     (tmp_path / "profiles").mkdir()
-    digest = bench.kernel_source_digest()
+    digest = bench.kernel_source_digest("sweep")
     (tmp_path / "profiles" / "k_C5.md").write_text(f"traffic_bytes_per_launch: 123\nkernel_source_digest: {digest}\n")
-    assert bench.profiled_traffic("k", "C5") == 123.0
+    assert bench.profiled_traffic("k", "C5", "sweep") == 123.0
     (tmp_path / "profiles" / "k_C5.md").write_text("traffic_bytes_per_launch: 123\nkernel_source_digest: 0000\n")
-    assert bench.profiled_traffic("k", "C5") is None
+    assert bench.profiled_traffic("k", "C5", "sweep") is None
 
 
 def test_kernel_impl_names_the_launched_kernels():
@@ -65,13 +65,37 @@ def test_digest_ignores_comments_not_code(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     d = tmp_path / "domain_decomposition_halo_gb300" / "csrc"
     d.mkdir(parents=True)
-    for name in bench.KERNEL_SOURCES:
+    names = sorted({n for files in bench.KERNEL_SOURCES.values() for n in files})
+    for name in names:
         (d / name).write_text('int f(int a) { return a + 1; }  // add\nconst char* s = "a // b";\n')
-    first = bench.kernel_source_digest()
-    (d / bench.KERNEL_SOURCES[0]).write_text(
+    first = bench.kernel_source_digest("chunks")
+    (d / "hx_kernels.cu").write_text(
         '/* a block\n comment */ int f(int a) {\n  return a + 1;   // another\n}\nconst char* s = "a // b";\n')
-    assert bench.kernel_source_digest() == first
-    (d / bench.KERNEL_SOURCES[0]).write_text('int f(int a) { return a + 2; }\nconst char* s = "a // b";\n')
-    assert bench.kernel_source_digest() != first
-    (d / bench.KERNEL_SOURCES[0]).write_text('int f(int a) { return a + 1; }\nconst char* s = "a // c";\n')
-    assert bench.kernel_source_digest() != first   # text inside a string is code
+    assert bench.kernel_source_digest("chunks") == first
+    (d / "hx_kernels.cu").write_text('int f(int a) { return a + 2; }\nconst char* s = "a // b";\n')
+    assert bench.kernel_source_digest("chunks") != first
+    (d / "hx_kernels.cu").write_text('int f(int a) { return a + 1; }\nconst char* s = "a // c";\n')
+    assert bench.kernel_source_digest("chunks") != first   # text inside a string is code
+
+
+def test_digest_is_per_kernel_family(tmp_path, monkeypatch):
+    """A change to the chunk kernels leaves the sweep's profile valid, and a
+    change to the shared header voids both."""
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    d = tmp_path / "domain_decomposition_halo_gb300" / "csrc"
+    d.mkdir(parents=True)
+    for name in sorted({n for files in bench.KERNEL_SOURCES.values() for n in files}):
+        (d / name).write_text(f"int {name.split('.')[0]}_v = 1;\n")
+    chunks, sweep = bench.kernel_source_digest("chunks"), bench.kernel_source_digest("sweep")
+    (d / "hx_kernels.cu").write_text("int hx_kernels_v = 2;\n")
+    assert bench.kernel_source_digest("sweep") == sweep
+    assert bench.kernel_source_digest("chunks") != chunks
+    (d / "hx_internal.h").write_text("int hx_internal_v = 2;\n")
+    assert bench.kernel_source_digest("sweep") != sweep
+
+
+def test_kernel_family_follows_the_flags():
+    f = bench.hx_flags("fine,bulkstore,sweepf,pdl")
+    assert bench.kernel_family(f, 0) == "chunks" and bench.kernel_family(f, 1) == "sweep"
+    assert bench.kernel_family(bench.hx_flags("resolved"), 1) == "resolved"
+    assert bench.kernel_family(bench.hx_flags("fine"), 1) == "chunks"
