@@ -549,6 +549,14 @@ int build_copy_chunks(hx_ctx* h) {
   return HX_OK;
 }
 
+#ifndef HX_CHUNK_LAG_WINDOWS
+#define HX_CHUNK_LAG_WINDOWS 1
+#endif
+// Resident-warp windows by which a chunk of dependency stage s is placed
+// after stage s - 1 in the chunk list (its priority key grows by that many
+// windows per stage).
+constexpr long long kChunkLagWindows = HX_CHUNK_LAG_WINDOWS;
+
 #ifndef HX_FUSED_CHUNK
 #define HX_FUSED_CHUNK 0   // 0: chosen per direction from the work (below)
 #endif
@@ -795,7 +803,7 @@ int build_tables(hx_ctx* h, cudaStream_t s) {
         if (ix.p != iy.p) return ix.p < iy.p;
         return x.begin < y.begin;
       });
-      const long long window = static_cast<long long>(h->grid[dir]) * kWarps;
+      const long long window = static_cast<long long>(h->grid[dir]) * kWarps * kChunkLagWindows;
       for (size_t k = 0; k < base.size(); ++k)
         recs[base[k]].key = static_cast<long long>(k) + window * recs[base[k]].stage;
     }
