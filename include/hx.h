@@ -50,8 +50,10 @@
  * hx_destroy; the caller owns every buffer it passes in. A handle is not
  * thread-safe: calls on one handle must not run concurrently from several
  * host threads, and two exchanges of the same direction must not overlap on
- * the GPU (they share that direction's signal flags and tickets; successive
- * exchanges on one stream never overlap). Different handles are independent.
+ * the GPU (they share that direction's signal flags and epoch word). Successive
+ * exchanges on one stream never do: under HX_FLAG_PDL the next kernel may be
+ * scheduled early, but it waits for the previous one to complete before it
+ * touches a flag or a buffer. Different handles are independent.
  */
 #ifndef HX_H
 #define HX_H
@@ -278,8 +280,8 @@ int hx_exchange_forces_unfused(hx_handle h, float* forces, void* stream);
  * hx_clear_status clears it. Errors: HX_ERR_ARG, HX_ERR_STATE, HX_ERR_CUDA
  * (also when the build could not do the set-up), and HX_ERR_CAPACITY when
  * the handle's work list needs more than HX_STATIC_MAX_FLAGS signal flags
- * (its item count, chunk count or unit count, whichever it signals by);
- * nothing is launched then. */
+ * (its item count or chunk count, whichever it signals by); nothing is
+ * launched then. */
 #define HX_STATIC_MAX_FLAGS 131072
 int hx_exchange_coords_static(hx_handle h, float* coords, void* stream);
 
