@@ -639,6 +639,10 @@ def secondary(hx_main, coords, forces, w_main, dev, peak, flags):
         res[name] = small(name, flags)
         if flags != staged_pdl:
             res[name]["staged_chunks_pdl"] = small(name, staged_pdl)
+        if name != "C4":
+            # the same with forces by atomics (within 1e-6 of the ordered sums),
+            # the fastest staged mode where the ordering waits dominate
+            res[name]["staged_chunks_pdl_unordered"] = small(name, staged_pdl | HX.HX_FLAG_UNORDERED_FORCES)
         if not flags & HX.HX_FLAG_RESOLVED:
             res[name]["resolved_pdl"] = small(name, HX.HX_FLAG_RESOLVED | HX.HX_FLAG_PDL)
     # the headline workload with the forwarding resolved at build time (not the

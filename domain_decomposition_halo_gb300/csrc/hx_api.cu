@@ -281,10 +281,11 @@ int launch(hx_ctx* h, int kind, float* buf, cudaStream_t s) {
     grid = dim3(static_cast<unsigned>(h->grid[kind]));
     smem = fused_smem(h, kind);
   }
-  if (kind != 2 && (h->flags & HX_FLAG_PDL)) {
+  if (h->flags & HX_FLAG_PDL) {
     // Direct launch that may start while the stream's previous kernel
     // finishes; every exchange kernel waits for it (griddepcontrol.wait)
-    // before touching data.
+    // before touching data. The empty kernel (kind 2) is launched the same
+    // way, so that launch floors are measured like the exchanges.
     cudaLaunchAttribute attr[1];
     std::memset(attr, 0, sizeof(attr));
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

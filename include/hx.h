@@ -285,9 +285,9 @@ int hx_exchange_forces_unfused(hx_handle h, float* forces, void* stream);
 #define HX_STATIC_MAX_FLAGS 131072
 int hx_exchange_coords_static(hx_handle h, float* coords, void* stream);
 
-/* Launches one empty kernel the way the fused exchanges are launched (graph
- * or direct, per the handle's flags): the launch floor for latency
- * measurements. Not on the pages; it measures the per-launch cost that
+/* Launches one empty kernel the way the fused exchanges are launched (graph,
+ * direct, or direct with programmatic dependent launch, per the handle's
+ * flags): the launch floor for latency measurements. Not on the pages; it measures the per-launch cost that
  * "Strategies in a nutshell" (six launches fused into one) removes. */
 int hx_noop(hx_handle h, void* stream);
 
