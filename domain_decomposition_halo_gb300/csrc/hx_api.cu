@@ -190,6 +190,13 @@ UnitParams unit_params(hx_ctx* h, int dir) {
   P.ctrl = h->d_ctrl + dir;
   P.n_units = static_cast<unsigned long long>(h->n_units[dir]);
   P.direction = dir;
+  // Segment-by-segment waits where each warp has few units, so that the
+  // pulse chain bounds the launch; whole-unit waits where each warp has many
+  // and its producers are mostly done by the time it reaches a dependent unit.
+  // Measured on one GB300 (forces back to back): 8 domains 11.0 -> 9.2 us and
+  // 64 domains 18.1 -> 15.7 us with segment waits (about 1.6 units a warp);
+  // 256 domains (16 units a warp) 78.2 -> 79.2 us, so it keeps unit waits.
+  P.seg_waits = h->n_units[dir] <= kSegWaitUnitsPerWarp * h->grid[dir] * kWarps ? 1 : 0;
   P.timeout_ns = h->timeout_ns;
   return P;
 }

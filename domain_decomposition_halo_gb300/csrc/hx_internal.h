@@ -190,7 +190,9 @@ struct alignas(16) UnitSeg {   // entries [map, map + n) of one (sender, pulse) 
   int32_t do_shift;
   int32_t map_off;    // stage byte offset of the region the map run is copied to
   int32_t src_off;    // stage byte offset of the region the received-force run is copied to
-  int32_t pad[2];
+  int32_t dep;        // forces: how many of the unit's waits (listed segment by segment) are
+                      // for the units of the same launch that write this segment's received run
+  int32_t pad;
 };
 static_assert(sizeof(UnitSeg) == 48, "segment record must stay 48 bytes");
 
@@ -220,7 +222,7 @@ struct UnitParams {
   Ctrl* ctrl;
   unsigned long long n_units;
   int direction;
-  int pad;
+  int seg_waits;              // 1: dependent segments wait for their own producers (see k_sweep)
   unsigned long long timeout_ns;
 };
 
@@ -240,6 +242,11 @@ constexpr int kSweepEntries = HX_SWEEP_ENTRIES;   // map entries of one unit at 
 #define HX_SWEEP_BATCH 1
 #endif
 constexpr int kSweepBatch = HX_SWEEP_BATCH;       // consecutive units a warp takes in one claim
+#ifndef HX_SEG_WAIT_UNITS_PER_WARP
+#define HX_SEG_WAIT_UNITS_PER_WARP 4
+#endif
+constexpr int kSegWaitUnitsPerWarp = HX_SEG_WAIT_UNITS_PER_WARP;   // segment-by-segment waits up to this
+                                                                    // many units a warp
 constexpr int kSweepSegs = 8;                     // segments (pulses) of one unit at most
 static_assert(1 + 2 * kSweepSegs <= 32, "a sweep unit stages one run per lane");
 // Stage layout of one warp: slots, then map runs, then (forces) received

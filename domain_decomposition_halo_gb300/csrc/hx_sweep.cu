@@ -47,6 +47,7 @@ struct alignas(16) WarpSmem {
   alignas(16) unsigned char stage[sweep_stage_bytes(KIND)];
   Unit desc[2];              // the current unit's record and the next one's
   unsigned long long bar;        // completion of the unit's bulk copies
+  unsigned long long bar_late;   // completion of a late segment's received run
 };
 
 __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
@@ -138,15 +139,15 @@ __device__ __forceinline__ UnitSeg seg_at(const UnitParams& P, const Unit& d, in
   return s < kInlineSegs ? d.seg[s] : P.extra[d.extra_off + s - kInlineSegs];
 }
 
-// Whole warp: wait until every unit that d depends on has been signalled at
-// this epoch (the first waits come with the unit's record, the rest from the
+// Whole warp: wait until the units of d's waits [first, first + cnt) have
+// been signalled at this epoch (the first waits come with the unit's record, the rest from the
 // direction's wait list). Lanes take the wait list in strides of 32 and poll with
 // acquire loads at gpu scope and a short back-off; the closing __syncwarp
 // orders every lane's acquire before the warp's loads. A wait that runs out
 // records a timeout and gives up.
-__device__ void wait_units(const UnitParams& P, const Unit& d, unsigned long long epoch) {
+__device__ void wait_units(const UnitParams& P, const Unit& d, unsigned long long epoch, int first, int cnt) {
   const int lane = threadIdx.x & 31;
-  for (int w = lane; w < d.wait_cnt; w += 32) {
+  for (int w = first + lane; w < first + cnt; w += 32) {
     const Wait wt = w < kInlineWaits ? d.wait_inline[w] : P.waits[d.wait_off + w];
     const unsigned long long* flag = P.flags + wt.item;
     unsigned long long t0 = 0;
@@ -168,11 +169,37 @@ __device__ void wait_units(const UnitParams& P, const Unit& d, unsigned long lon
   __syncwarp();
 }
 
+// Whole warp, no blocking: one acquire poll of each of d's first 32 waits;
+// returns a bit per dependent segment whose producers have all signalled at
+// this epoch (a segment with a wait past the first 32 counts as not ready).
+__device__ unsigned poll_segments(const UnitParams& P, const Unit& d, unsigned long long epoch) {
+  const int lane = threadIdx.x & 31;
+  bool pending = false;
+  if (lane < d.wait_cnt) {
+    const Wait wt = lane < kInlineWaits ? d.wait_inline[lane] : P.waits[d.wait_off + lane];
+    pending = ld_acquire_u64(P.flags + wt.item) != epoch;
+  }
+  const unsigned pend = __ballot_sync(kFull, pending);
+  unsigned ready = 0u;
+  int wpos = 0;
+  for (int s = 0; s < d.seg_cnt; ++s) {
+    const int n = seg_at(P, d, s).dep;
+    if (n > 0 && wpos + n <= 32) {
+      const unsigned bits = (n == 32 ? kFull : ((1u << n) - 1u)) << wpos;
+      if ((pend & bits) == 0u) ready |= 1u << s;
+    }
+    wpos += n;
+  }
+  return ready;
+}
+
 // Run k of a unit: 0 = its slots, then per segment its map run and (forces)
 // its received-force run: global address, bytes, stage region offset.
+// `dep`: the run is a received run that units of the same launch write.
 template <int KIND>
 __device__ __forceinline__ void run_of(const float* x, const UnitParams& P, const Unit& d, int k,
-                                       unsigned long long& g, unsigned& bytes, unsigned& region) {
+                                       unsigned long long& g, unsigned& bytes, unsigned& region, bool& dep) {
+  dep = false;
   if (k == 0) {
     g = reinterpret_cast<unsigned long long>(x + 3 * d.base);
     bytes = 12u * static_cast<unsigned>(d.n);
@@ -189,6 +216,7 @@ __device__ __forceinline__ void run_of(const float* x, const UnitParams& P, cons
     g = reinterpret_cast<unsigned long long>(x + 3 * sg.other);
     bytes = 12u * static_cast<unsigned>(sg.n);
     region = static_cast<unsigned>(sg.src_off);
+    dep = sg.dep != 0;
   }
 }
 
@@ -199,26 +227,33 @@ __device__ __forceinline__ void run_of(const float* x, const UnitParams& P, cons
 // run's middle as one bulk copy and copies the head and tail words (under 16
 // bytes each) with plain loads. Runs of under 32 bytes go entirely by plain
 // loads. The caller waits on the mbarrier and then on the warp (__syncwarp).
+//
+// `ready` has a bit per segment: the received run of a dependent segment
+// (one that units of this launch write) is staged only when its bit is set,
+// i.e. its producers have been seen signalled; the other runs always are.
+// The mbarrier's arrival announces the bytes of the runs staged.
 template <int KIND>
 __device__ void stage_unit(const float* x, const UnitParams& P, const Unit& d, unsigned char* st,
-                           unsigned long long* bar) {
+                           unsigned long long* bar, unsigned ready = kFull) {
   const int lane = threadIdx.x & 31;
   const int n_runs = 1 + (KIND == 1 ? 2 : 1) * d.seg_cnt;
   unsigned long long g = 0, a0 = 0, a1 = 0;
   unsigned bytes = 0, region = 0, middle = 0;
+  bool dep = false;
   if (lane < n_runs) {
-    run_of<KIND>(x, P, d, lane, g, bytes, region);
+    run_of<KIND>(x, P, d, lane, g, bytes, region, dep);
     a0 = (g + 15ull) & ~15ull;
     a1 = (g + bytes) & ~15ull;
     if (a1 > a0) middle = static_cast<unsigned>(a1 - a0);
   }
-  const unsigned total = __reduce_add_sync(kFull, middle);
+  const bool mine = !dep || ((ready >> ((lane - 1) / 2)) & 1u) != 0u;
+  const unsigned total = __reduce_add_sync(kFull, mine ? middle : 0u);
   if (lane == 0) {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the stage's earlier generic use
     mbar_arrive_expect_tx(bar, total);
   }
   __syncwarp();
-  if (lane < n_runs) {
+  if (lane < n_runs && mine) {
     unsigned char* dst = st + region + (g & 15ull);
     // Plain words: up to 3 before and 3 after an aligned middle, or a whole
     // run of under 32 bytes (at most 7 words). All loads are issued before
@@ -251,7 +286,8 @@ __device__ void prefetch_unit(const float* x, const UnitParams& P, const Unit& d
   if (lane < n_runs) {
     unsigned long long g;
     unsigned bytes, region;
-    run_of<KIND>(x, P, d, lane, g, bytes, region);
+    bool dep;
+    run_of<KIND>(x, P, d, lane, g, bytes, region, dep);
     const unsigned long long a0 = (g + 15ull) & ~15ull, a1 = (g + bytes) & ~15ull;
     if (a1 > a0)
       asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a0), "r"(static_cast<unsigned>(a1 - a0))
@@ -274,31 +310,12 @@ __device__ __forceinline__ void bulk_stores_done() {
   asm volatile("cp.async.bulk.wait_group 0;\n\tfence.proxy.async.global;" ::: "memory");
 }
 
-// Forces of one staged unit: each segment's received run added into the
-// slots, segments in list order (last pulse first), a warp barrier between
-// segments since one slot can be a target in several pulses; entries of one
-// segment have distinct targets. Then the slots are written back: one bulk
-// store for the 16-byte-aligned middle (the stage keeps the global address
-// mod 16), plain stores for the words around it.
-__device__ __forceinline__ void forces_unit(float* __restrict__ f, const UnitParams& P, const Unit& d,
-                                            WarpSmem<1>& S) {
+// Write-back of a unit's staged slots: one bulk store for the 16-byte-aligned
+// middle (the stage keeps the global address mod 16), plain stores for the
+// words around it.
+__device__ __forceinline__ void write_back(float* __restrict__ f, const Unit& d, float* tile) {
   const int lane = threadIdx.x & 31;
   const unsigned long long gt = reinterpret_cast<unsigned long long>(f + 3 * d.base);
-  float* tile = reinterpret_cast<float*>(S.stage + (gt & 15ull));
-  for (int s = 0; s < d.seg_cnt; ++s) {
-    const UnitSeg sg = seg_at(P, d, s);
-    const int32_t* smap = reinterpret_cast<const int32_t*>(
-        S.stage + sg.map_off + (reinterpret_cast<unsigned long long>(P.maps + sg.map) & 15ull));
-    const float* src = reinterpret_cast<const float*>(
-        S.stage + sg.src_off + (reinterpret_cast<unsigned long long>(f + 3 * sg.other) & 15ull));
-    for (int i = lane; i < sg.n; i += 32) {
-      float* t = tile + 3 * (smap[i] - d.local_a);
-      t[0] = __fadd_rn(t[0], src[3 * i + 0]);
-      t[1] = __fadd_rn(t[1], src[3 * i + 1]);
-      t[2] = __fadd_rn(t[2], src[3 * i + 2]);
-    }
-    __syncwarp();   // the next (earlier) pulse adds after this one
-  }
   const unsigned bytes = 12u * static_cast<unsigned>(d.n);
   const unsigned long long a0 = (gt + 15ull) & ~15ull, a1 = (gt + bytes) & ~15ull;
   if (a1 > a0) {
@@ -320,9 +337,76 @@ __device__ __forceinline__ void forces_unit(float* __restrict__ f, const UnitPar
   }
 }
 
+// Forces of one staged unit: each segment's received run added into the
+// slots, segments in list order (last pulse first), a warp barrier between
+// segments since one slot can be a target in several pulses; entries of one
+// segment have distinct targets. Then the slots are written back.
+//
+// A dependent segment (one whose received run other units of this launch
+// write) whose bit in `ready` is clear was not staged: it waits here for
+// exactly its producers (its share of the unit's waits, which are listed
+// segment by segment), then stages its run with one bulk copy completing on
+// the warp's second mbarrier, so the unit adds its earlier segments while the
+// producers of its later ones are still working.
+__device__ __forceinline__ void forces_unit(float* __restrict__ f, const UnitParams& P, const Unit& d,
+                                            WarpSmem<1>& S, unsigned long long epoch, unsigned ready,
+                                            unsigned& parity_late) {
+  const int lane = threadIdx.x & 31;
+  const unsigned long long gt = reinterpret_cast<unsigned long long>(f + 3 * d.base);
+  float* tile = reinterpret_cast<float*>(S.stage + (gt & 15ull));
+  int wpos = 0;
+  for (int s = 0; s < d.seg_cnt; ++s) {
+    const UnitSeg sg = seg_at(P, d, s);
+    const int32_t* smap = reinterpret_cast<const int32_t*>(
+        S.stage + sg.map_off + (reinterpret_cast<unsigned long long>(P.maps + sg.map) & 15ull));
+    const bool late = sg.dep > 0 && ((ready >> s) & 1u) == 0u;   // its run was not staged
+    wpos += sg.dep;
+    if (late) {
+      wait_units(P, d, epoch, wpos - sg.dep, sg.dep);
+      // the run into its stage region: one bulk copy of its aligned middle on
+      // the late barrier, the words around it by lane 0's plain loads
+      if (lane == 0) {
+        const unsigned long long g = reinterpret_cast<unsigned long long>(f + 3 * sg.other);
+        const unsigned bytes = 12u * static_cast<unsigned>(sg.n);
+        const unsigned long long a0 = (g + 15ull) & ~15ull, a1 = (g + bytes) & ~15ull;
+        const unsigned middle = a1 > a0 ? static_cast<unsigned>(a1 - a0) : 0u;
+        unsigned char* dst = S.stage + sg.src_off + (g & 15ull);
+        asm volatile("fence.proxy.async.global;" ::: "memory");       // the producers' stores, to the copy
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the stage's earlier generic use
+        mbar_arrive_expect_tx(&S.bar_late, middle);
+        if (middle > 0) bulk_load(dst + (a0 - g), a0, middle, &S.bar_late);
+        const unsigned nh = middle > 0 ? static_cast<unsigned>(a0 - g) / 4 : bytes / 4;
+        const unsigned nt = middle > 0 ? static_cast<unsigned>(g + bytes - a1) / 4 : 0u;
+        for (unsigned k = 0; k < nh + nt; ++k) {
+          const unsigned off = k < nh ? 4u * k : static_cast<unsigned>(a1 - g) + 4u * (k - nh);
+          *reinterpret_cast<float*>(dst + off) = __ldcg(reinterpret_cast<const float*>(g + off));
+        }
+      }
+      if (!mbar_wait(&S.bar_late, parity_late, P.timeout_ns)) {
+        if (lane == 0) record_timeout(P, d.item);
+      }
+      parity_late ^= 1u;
+      __syncwarp();   // lane 0's words are in place
+    }
+    {
+      const float* src = reinterpret_cast<const float*>(
+          S.stage + sg.src_off + (reinterpret_cast<unsigned long long>(f + 3 * sg.other) & 15ull));
+      for (int i = lane; i < sg.n; i += 32) {
+        float* t = tile + 3 * (smap[i] - d.local_a);
+        t[0] = __fadd_rn(t[0], src[3 * i + 0]);
+        t[1] = __fadd_rn(t[1], src[3 * i + 1]);
+        t[2] = __fadd_rn(t[2], src[3 * i + 2]);
+      }
+    }
+    __syncwarp();   // the next (earlier) pulse adds after this one
+  }
+  write_back(f, d, tile);
+}
+
+
 // KIND 1 = forces (ordered), the one direction the sweep serves.
 template <int KIND>
-__global__ void __launch_bounds__(kThreads) k_sweep(float* __restrict__ buf, UnitParams P) {
+__global__ void __launch_bounds__(kThreads, 3) k_sweep(float* __restrict__ buf, UnitParams P) {
   static_assert(KIND == 1, "the slot sweep serves the force exchange");
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const int lane = threadIdx.x & 31;
@@ -346,10 +430,11 @@ __global__ void __launch_bounds__(kThreads) k_sweep(float* __restrict__ buf, Uni
     const int drop_item = *reinterpret_cast<const volatile int*>(&P.ctrl->drop_item);
     if (lane == 0) {
       mbar_init(&S.bar, 1);
+      mbar_init(&S.bar_late, 1);
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncwarp();
-    unsigned parity = 0;
+    unsigned parity = 0, parity_late = 0;
     // Units are claimed in batches of kSweepBatch consecutive units, and the
     // claims are static: warp w of the W warps takes batches w, w + W,
     // w + 2W, ... in order, so a warp works through its claims in list order
@@ -369,17 +454,25 @@ __global__ void __launch_bounds__(kThreads) k_sweep(float* __restrict__ buf, Uni
       if (cn < N && lane < 16)
         cp_async_16(reinterpret_cast<int4*>(&S.desc[b ^ 1]) + lane, reinterpret_cast<const int4*>(P.units + cn) + lane);
       const Unit& d = S.desc[b];
+      // The unit's waits. With segment waits (short lists, where the pulse
+      // chain bounds the launch), one poll decides which dependent runs are
+      // staged now; the others are read after their own segment's wait.
+      // Otherwise the warp waits for all its producers before staging.
+      unsigned ready = kFull;
       if (d.wait_cnt > 0) {
-        if (!next_ready) wait_units(P, d, epoch);
+        if (!next_ready) {
+          if (P.seg_waits) ready = poll_segments(P, d, epoch);
+          else wait_units(P, d, epoch, 0, d.wait_cnt);
+        }
         // bulk copies (async proxy) then read what other warps stored (generic proxy) before their signals
-        if (lane == 0) asm volatile("fence.proxy.async.global;" ::: "memory");
+        if (lane == 0 && ready) asm volatile("fence.proxy.async.global;" ::: "memory");
         __syncwarp();
       }
       if (KIND == 1) {   // the previous unit's write-back has read the stage
         if (lane == 0) bulk_stores_read();
         __syncwarp();
       }
-      stage_unit<KIND>(buf, P, d, S.stage, &S.bar);
+      stage_unit<KIND>(buf, P, d, S.stage, &S.bar, ready);
       if (cn < N) {   // the next record, then its runs into L2 while this unit's copies land
         cp_async_wait_all();
         __syncwarp();
@@ -390,7 +483,7 @@ __global__ void __launch_bounds__(kThreads) k_sweep(float* __restrict__ buf, Uni
       }
       parity ^= 1u;
       __syncwarp();   // the lanes' edge words are in place
-      forces_unit(buf, P, d, S);
+      forces_unit(buf, P, d, S, epoch, ready, parity_late);
       // One acquire poll of the next unit's waits (when they all come with
       // its record), issued before this unit's signal so that the two round
       // trips overlap; if it finds them set, the next unit skips its wait.

@@ -248,16 +248,22 @@ int build_unit_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::
             }
           }
       } else {
-        // the slots read by segment (r, p) are q's slots [other, other + n) in q's range p
+        // the slots read by segment (r, p) are q's slots [other, other + n) in q's range p.
+        // The waits are listed segment by segment (segments of one unit read
+        // different ranges, so their producers differ), and each segment
+        // records how many of them are its own.
         for (size_t k = 0; k < t.segs.size(); ++k) {
           const int p = t.seg_pulse[k];
           const int q = items[p * nd + t.r].q;
           const int64_t s0 = t.segs[k].other - h->dom_offset[q], s1 = s0 + t.segs[k].n;
+          const size_t first = t.deps.size();
           for (int j : by_range[q][p + 1]) {
             const TRec& s = recs[j];
             if (s.a < s1 && s0 < s.a + s.n) t.deps.push_back(j);
           }
+          t.segs[k].dep = static_cast<int32_t>(t.deps.size() - first);
         }
+        return;
       }
       std::sort(t.deps.begin(), t.deps.end());
       t.deps.erase(std::unique(t.deps.begin(), t.deps.end()), t.deps.end());
