@@ -421,68 +421,6 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int n>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(n) : "memory"); }
 
-#ifndef HX_CP_GATHER
-#define HX_CP_GATHER 0
-#endif
-#if HX_CP_GATHER
-// Bulk-store pack with the gathers copied straight into the stage by the
-// lanes' 4-byte cp.async: the gathered values never occupy registers, so a
-// warp keeps every gather of its chunk in flight with a small register
-// budget.
-template <class Map>
-__device__ __forceinline__ void coords_chunk_cp(float* __restrict__ x, const Chunk& ch, const Map& j,
-                                                unsigned char* stage) {
-  const int lane = threadIdx.x & 31;
-  float* dst = x + 3 * ch.dst;
-  const unsigned long long gd = reinterpret_cast<unsigned long long>(dst);
-  float* sv = reinterpret_cast<float*>(stage + (gd & 15ull));
-  // the previous chunk's bulk store has read the stage
-  if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-  __syncwarp();
-  const float* src = x + 3 * ch.src;
-#pragma unroll
-  for (int u = 0; u < kRounds; ++u) {
-    const int ju = j(u);
-    if (ju >= 0) {
-      const float* s = src + 3 * static_cast<int64_t>(ju);
-      float* t = sv + 3 * (u * 32 + lane);
-      cp_async_4(t, s);
-      cp_async_4(t + 1, s + 1);
-      cp_async_4(t + 2, s + 2);
-    }
-  }
-  cp_async_commit();
-  cp_async_wait<0>();
-  if (ch.flags & kShift) {   // no add otherwise: unshifted values keep every bit (-0.0 included)
-#pragma unroll
-    for (int u = 0; u < kRounds; ++u) {
-      const int e = u * 32 + lane;
-      if (e < ch.n) sv[3 * e + ch.dim] = __fadd_rn(sv[3 * e + ch.dim], ch.shift);
-    }
-  }
-  __syncwarp();
-  const unsigned bytes = 12u * static_cast<unsigned>(ch.n);
-  const unsigned long long a0 = (gd + 15ull) & ~15ull, a1 = (gd + bytes) & ~15ull;
-  if (a1 > a0) {
-    if (lane == 0) {
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the lanes' stage writes, to the copy
-      asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n\tcp.async.bulk.commit_group;" ::"l"(
-                       a0),
-                   "r"(smem_u32(stage + (gd & 15ull) + (a0 - gd))), "r"(static_cast<unsigned>(a1 - a0))
-                   : "memory");
-    }
-    const int head = static_cast<int>((a0 - gd) / 4), tail = static_cast<int>((gd + bytes - a1) / 4);
-    if (lane < head) dst[lane] = sv[lane];
-    else if (lane >= 4 && lane < 4 + tail) {
-      const int k = static_cast<int>((a1 - gd) / 4) + (lane - 4);
-      dst[k] = sv[k];
-    }
-  } else {
-    for (int k = lane; k < 3 * ch.n; k += 32) dst[k] = sv[k];
-  }
-}
-#endif
-
 // Whole warp: one chunk record, in 16-byte pieces (committed as one group).
 __device__ __forceinline__ void fetch_chunk(ChunkSlot& s, const ChunkSlot* src) {
   const int lane = threadIdx.x & 31;
@@ -590,11 +528,7 @@ __device__ __forceinline__ void run_warps(float* __restrict__ buf, const DirPara
       if (KIND == 0) coords_chunk(buf, ch, j, reinterpret_cast<float*>(S.stage));
       else if (KIND == 3) {
         if (ch.n >= kBulkMinEntries) {
-#if HX_CP_GATHER
-          coords_chunk_cp(buf, ch, j, S.stage);
-#else
           coords_chunk_bulk(buf, ch, j, S.stage);
-#endif
         } else {   // small chunk: plain stores, once the previous bulk store has read the stage
           if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
           __syncwarp();
@@ -635,11 +569,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_coords_fused(float* __
   run_warps<MODE, 0>(x, P, reinterpret_cast<ChunkWarpSmem<0>*>(smem_raw)[threadIdx.x >> 5]);
 }
 
-#ifndef HX_COORD_MIN_BLOCKS
-#define HX_COORD_MIN_BLOCKS HX_MIN_BLOCKS
-#endif
 template <int MODE>
-__global__ void __launch_bounds__(kThreads, HX_COORD_MIN_BLOCKS) k_coords_bulk(float* __restrict__ x, DirParams P) {
+__global__ void __launch_bounds__(kThreads, kMinBlocks) k_coords_bulk(float* __restrict__ x, DirParams P) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   run_warps<MODE, 3>(x, P, reinterpret_cast<ChunkWarpSmem<3>*>(smem_raw)[threadIdx.x >> 5]);
 }
