@@ -350,8 +350,8 @@ def run_ours(args):
         c.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop() if clocks else None
-    coord_ms = statistics.fmean(e[0].elapsed_time(e[1]) for e in ev)
-    force_ms = statistics.fmean(e[1].elapsed_time(e[2]) for e in ev)
+    coord_ms, coord_dropped = launch_mean([e[0].elapsed_time(e[1]) for e in ev])
+    force_ms, force_dropped = launch_mean([e[1].elapsed_time(e[2]) for e in ev])
     per_step_us = [e[0].elapsed_time(e[2]) * 1e3 for e in ev]
     if world > 1:
         total_ms = max_over_ranks(total_ms, dev)
@@ -473,6 +473,9 @@ def run_ours(args):
             "kernels": per_kernel,
         },
         "kernels_ms": {"hx_coords_fused": round(coord_ms, 5), "hx_forces_fused": round(force_ms, 5)},
+        "kernels_ms_what": "mean of per-launch event times over the second pass, launches over 3x the median "
+                           "(host stalls) left out",
+        "kernels_launches_left_out": {"hx_coords_fused": coord_dropped, "hx_forces_fused": force_dropped},
         "step_us_distribution": step_distribution(per_step_us),
         "step_us_distribution_what": "per-step event times of a second pass of the K steps with an event around "
                                      "every launch (the kernels' durations come from it)",
@@ -494,6 +497,16 @@ def run_ours(args):
         print(json.dumps(out), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def launch_mean(ts, limit=3.0):
+    """Mean of per-launch event times without the launches that took more
+    than `limit` times the median: those intervals hold a host stall (the
+    queue ran dry while the host was away), not kernel time. Returns the
+    mean and how many launches were left out."""
+    med = statistics.median(ts)
+    kept = [t for t in ts if t <= limit * med]
+    return statistics.fmean(kept), len(ts) - len(kept)
 
 
 def step_distribution(ts):

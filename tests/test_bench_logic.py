@@ -99,3 +99,11 @@ def test_kernel_family_follows_the_flags():
     assert bench.kernel_family(f, 0) == "chunks" and bench.kernel_family(f, 1) == "sweep"
     assert bench.kernel_family(bench.hx_flags("resolved"), 1) == "resolved"
     assert bench.kernel_family(bench.hx_flags("fine"), 1) == "chunks"
+
+def test_launch_mean_leaves_out_host_stalls():
+    # one interval that holds a host stall (the queue ran dry) must not move the kernel's duration
+    ts = [80.0] * 999 + [33000.0]
+    mean, dropped = bench.launch_mean(ts)
+    assert dropped == 1 and mean == 80.0
+    mean, dropped = bench.launch_mean([1.0, 2.0, 3.0])
+    assert dropped == 0 and mean == 2.0
