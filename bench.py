@@ -37,6 +37,7 @@ BYTES_FORCE = 40   # map 4 + halo-slot read 12 + target read 12 + target write 1
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 2 ** 20
 METRIC = "halo exchange μs/step (coords+forces) and effective GB/s vs GB300 HBM peak"
+E2E_HANDLES = 3    # handles (each with its own stream and buffers) that take turns in the end-to-end steps
 
 
 def parse_args():
@@ -361,61 +362,91 @@ def run_ours(args):
         raise RuntimeError(f"device status {rc} (detail {detail}) after the timed region")
     us_step = total_ms * 1e3 / K
 
-    # end to end through the C-ABI with host buffers: each step calls
-    # hx_exchange_coords_host (home coordinates in, halo coordinates out) and
-    # hx_exchange_forces_host (every force in, home forces out) on page-locked
-    # host buffers. Two handles with the same maps, each with its own buffers
-    # and stream, take alternate steps, so one step's copies out overlap the
-    # next step's copies in (a handle runs one exchange per direction at a
-    # time).
-    hx_b = HaloExchange(w.box, w.dims, w.cutoff, device=local, flags=flags)
-    hx_b.build_maps(pos_t, torch.empty_like(coords))
-    handles = (hx, hx_b)
+    # end to end through the C-ABI with host buffers, packed: each step calls
+    # hx_exchange_coords_host_packed (home coordinates in, halo coordinates
+    # out) and hx_exchange_forces_host_packed (every force in, home forces
+    # out) on page-locked host buffers. Several handles with the same maps,
+    # each with its own buffers and stream, take turns, so one step's copies
+    # out overlap the next steps' copies in (a handle runs one exchange per
+    # direction at a time). The layout-shaped host calls are timed the same
+    # way beside it.
     off, home_n, _ = hx.layout()
     home_mask = torch.zeros(slots, dtype=torch.bool)
     for r in range(len(off)):
         home_mask[int(off[r]): int(off[r]) + int(home_n[r])] = True
+    n_home = int(home_mask.sum())
+    handles = [hx]
+    for _ in range(E2E_HANDLES - 1):
+        handles.append(HaloExchange(w.box, w.dims, w.cutoff, device=local, flags=flags))
+        handles[-1].build_maps(pos_t, torch.empty_like(coords))
     coords_h0 = coords.cpu()
-    coords_h0[~home_mask] = float("nan")   # halo slots come back from the device
     forces_h0 = forces.cpu()
-    host = [(coords_h0.clone().pin_memory(), forces_h0.clone().pin_memory()) for _ in range(2)]
-    devs = [(torch.empty_like(coords), torch.empty_like(forces)) for _ in range(2)]
-    streams = [torch.cuda.Stream(device=dev) for _ in range(2)]
+    streams = [torch.cuda.Stream(device=dev) for _ in handles]
+    devs = [(torch.empty_like(coords), torch.empty_like(forces)) for _ in handles]
     n_e2e = max(3, min(K, 30))
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    for i in range(2 + n_e2e):
-        if i == 2:   # two untimed steps, then the timed ones
-            torch.cuda.synchronize()
-            e0.record(streams[0])
-            streams[1].wait_event(e0)
-        k = i % 2
-        handles[k].exchange_coords_host(host[k][0], devs[k][0], stream=streams[k])
-        handles[k].exchange_forces_host(host[k][1], devs[k][1], stream=streams[k])
-    streams[0].wait_stream(streams[1])
-    e1.record(streams[0])
-    torch.cuda.synchronize()
-    e2e_us = e0.elapsed_time(e1) * 1e3 / n_e2e
-    # checks: the coordinates on each host buffer equal a device exchange of
-    # the same home coordinates; one fresh force step equals a device one
+
+    def e2e_time(step_fn):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        untimed = 2 * len(handles)
+        for i in range(untimed + n_e2e):
+            if i == untimed:   # every handle's buffers used twice, then the timed steps
+                torch.cuda.synchronize()
+                e0.record(streams[0])
+                for st in streams[1:]:
+                    st.wait_event(e0)
+            step_fn(i % len(handles))
+        for st in streams[1:]:
+            streams[0].wait_stream(st)
+        e1.record(streams[0])
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / n_e2e
+
+    packed = [dict(home=coords_h0[home_mask].clone().pin_memory(),
+                   halo=torch.empty((slots - n_home, 3)).pin_memory(),
+                   f=forces_h0.clone().pin_memory(),
+                   fhome=torch.empty((n_home, 3)).pin_memory()) for _ in handles]
+
+    def step_packed(k):
+        b = packed[k]
+        handles[k].exchange_coords_host_packed(b["home"], b["halo"], devs[k][0], stream=streams[k])
+        handles[k].exchange_forces_host_packed(b["f"], b["fhome"], devs[k][1], stream=streams[k])
+
+    e2e_us = e2e_time(step_packed)
+    layout_bufs = []
+    for _ in handles:
+        ch = coords_h0.clone()
+        ch[~home_mask] = float("nan")   # halo slots come back from the device
+        layout_bufs.append((ch.pin_memory(), forces_h0.clone().pin_memory()))
+
+    def step_layout(k):
+        handles[k].exchange_coords_host(layout_bufs[k][0], devs[k][0], stream=streams[k])
+        handles[k].exchange_forces_host(layout_bufs[k][1], devs[k][1], stream=streams[k])
+
+    e2e_layout_us = e2e_time(step_layout)
+    # checks: every handle's host outputs equal a device exchange of the same
+    # inputs, bit for bit, in both forms
     ref_c = coords.clone()
     hx.exchange_coords(ref_c)
     ref_f = forces_h0.to(dev)
     hx.exchange_forces(ref_f)
     torch.cuda.synchronize()
     ref_c, ref_f = ref_c.cpu(), ref_f.cpu()
-    host[0][1].copy_(forces_h0)
-    hx.exchange_forces_host(host[0][1], devs[0][1], stream=streams[0])
-    torch.cuda.synchronize()
-    for ch, _ in host:
-        if not torch.equal(ch.view(torch.int32), ref_c.view(torch.int32)):
+    for k, b in enumerate(packed):
+        if not torch.equal(b["halo"].view(torch.int32), ref_c[~home_mask].view(torch.int32)):
+            raise RuntimeError("end-to-end (packed) halo coordinates differ from a device exchange")
+        if not torch.equal(b["fhome"].view(torch.int32), ref_f[home_mask].view(torch.int32)):
+            raise RuntimeError("end-to-end (packed) home forces differ from a device exchange")
+        if not torch.equal(layout_bufs[k][0].view(torch.int32), ref_c.view(torch.int32)):
             raise RuntimeError("end-to-end coordinates differ from a device exchange")
-    if not torch.equal(host[0][1][home_mask].view(torch.int32), ref_f[home_mask].view(torch.int32)):
+    layout_bufs[0][1].copy_(forces_h0)
+    hx.exchange_forces_host(layout_bufs[0][1], devs[0][1], stream=streams[0])
+    torch.cuda.synchronize()
+    if not torch.equal(layout_bufs[0][1][home_mask].view(torch.int32), ref_f[home_mask].view(torch.int32)):
         raise RuntimeError("end-to-end forces differ from a device exchange")
-    n_home = int(home_mask.sum())
     bytes_h2d = 12 * n_home + 12 * slots              # home coordinates, every force
     bytes_d2h = 12 * (slots - n_home) + 12 * n_home   # halo coordinates, home forces
-    del hx_b
+    del handles, packed, layout_bufs, devs
 
     peak, peak_kind = measured_hbm_peak()
     dominant = "hx_forces_fused" if force_ms >= coord_ms else "hx_coords_fused"
@@ -482,9 +513,13 @@ def run_ours(args):
         "clocks": clk,
         "e2e": {"value": round(e2e_us, 2), "unit": "us/step", "h2d_bytes_per_step": bytes_h2d,
                 "d2h_bytes_per_step": bytes_d2h,
-                "what": "hx_exchange_coords_host + hx_exchange_forces_host every step on page-locked host "
-                        "buffers: home coordinates and every force in, halo coordinates and home forces out; "
-                        "two handles on two streams take alternate steps"},
+                "what": "hx_exchange_coords_host_packed + hx_exchange_forces_host_packed every step on "
+                        "page-locked host buffers: packed home coordinates and every force in, packed halo "
+                        f"coordinates and home forces out; {E2E_HANDLES} handles on {E2E_HANDLES} streams take "
+                        "turns",
+                "layout_buffers_us": round(e2e_layout_us, 2),
+                "layout_buffers_what": "the same steps through hx_exchange_coords_host + hx_exchange_forces_host "
+                                       "(host buffers shaped like the slot layout)"},
         "gpu_launches": 2 * K,
         "gpu_launches_what": "libhx kernel launches in the timed region: one per direction per step",
         "build_maps_us": round(statistics.median(t_build), 1),

@@ -130,6 +130,8 @@ void free_tables(hx_ctx* h) {
   dev_free(h->d_home_chunks);
   dev_free(h->d_halo_chunks);
   h->n_home_chunks = h->n_halo_chunks = 0;
+  dev_free(h->d_pack);
+  h->pack_slots = 0;
   for (int k = 0; k < 2; ++k) {
     dev_free(h->d_units[k]);
     dev_free(h->d_segs[k]);
@@ -730,13 +732,60 @@ int exchange_host(hx_handle h, float* host, float* dev, void* stream, int kind) 
   if ((rc = device_view(host, &hv)) != HX_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (kind == 0) {   // home coordinates in, halo coordinates out
-    HX_CUDA(launch_copy_chunks(hv, dev, h->d_home_chunks, h->n_home_chunks, s));
+    HX_CUDA(launch_copy_chunks(hv, dev, h->d_home_chunks, h->n_home_chunks, kCopySame, s));
     if ((rc = exchange(h, dev, stream, 0)) != HX_OK) return rc;
-    HX_CUDA(launch_copy_chunks(dev, hv, h->d_halo_chunks, h->n_halo_chunks, s));
+    HX_CUDA(launch_copy_chunks(dev, hv, h->d_halo_chunks, h->n_halo_chunks, kCopySame, s));
   } else {           // every slot's force in, home forces out
     HX_CUDA(cudaMemcpyAsync(dev, host, sizeof(float) * 3 * h->total_slots, cudaMemcpyHostToDevice, s));
     if ((rc = exchange(h, dev, stream, 1)) != HX_OK) return rc;
-    HX_CUDA(launch_copy_chunks(dev, hv, h->d_home_chunks, h->n_home_chunks, s));
+    HX_CUDA(launch_copy_chunks(dev, hv, h->d_home_chunks, h->n_home_chunks, kCopySame, s));
+  }
+  return HX_OK;
+}
+
+// The packed form: one copy-engine transfer each way over the host link, the
+// scatter into the layout and the gather out of it as range copies in HBM
+// through the handle's packing buffer.
+int exchange_host_packed(hx_handle h, const float* in, float* out, float* dev, void* stream, int kind) {
+  if (!h) return HX_ERR_ARG;
+  if (!h->built) return HX_ERR_STATE;
+  if (h->total_slots == 0) return HX_OK;
+  const int64_t n_home = h->n_atoms, n_halo = h->total_slots - h->n_atoms;
+  if (!dev || (!in && (kind == 1 || n_home > 0)) || (!out && (kind == 1 ? n_home > 0 : n_halo > 0)))
+    return HX_ERR_ARG;
+  DeviceGuard guard(h->device);
+  if (!guard.ok()) return HX_ERR_CUDA;
+  const int64_t need = std::max<int64_t>(1, std::max(n_home, n_halo));
+  if (h->pack_slots < need) {
+    // The first packed call after a build allocates the buffer; it is kept
+    // until the next build or hx_destroy.
+    dev_free(h->d_pack);
+    h->pack_slots = 0;
+    if (dev_alloc(&h->d_pack, 3 * need) != cudaSuccess) {
+      cudaGetLastError();
+      return HX_ERR_NOMEM;
+    }
+    h->pack_slots = need;
+  }
+  int rc = HX_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (kind == 0) {   // packed home coordinates in, packed halo coordinates out
+    if (n_home > 0) {
+      HX_CUDA(cudaMemcpyAsync(h->d_pack, in, sizeof(float) * 3 * n_home, cudaMemcpyHostToDevice, s));
+      HX_CUDA(launch_copy_chunks(h->d_pack, dev, h->d_home_chunks, h->n_home_chunks, kCopyUnpack, s));
+    }
+    if ((rc = exchange(h, dev, stream, 0)) != HX_OK) return rc;
+    if (n_halo > 0) {
+      HX_CUDA(launch_copy_chunks(dev, h->d_pack, h->d_halo_chunks, h->n_halo_chunks, kCopyPack, s));
+      HX_CUDA(cudaMemcpyAsync(out, h->d_pack, sizeof(float) * 3 * n_halo, cudaMemcpyDeviceToHost, s));
+    }
+  } else {           // every slot's force in (the layout), packed home forces out
+    HX_CUDA(cudaMemcpyAsync(dev, in, sizeof(float) * 3 * h->total_slots, cudaMemcpyHostToDevice, s));
+    if ((rc = exchange(h, dev, stream, 1)) != HX_OK) return rc;
+    if (n_home > 0) {
+      HX_CUDA(launch_copy_chunks(dev, h->d_pack, h->d_home_chunks, h->n_home_chunks, kCopyPack, s));
+      HX_CUDA(cudaMemcpyAsync(out, h->d_pack, sizeof(float) * 3 * n_home, cudaMemcpyDeviceToHost, s));
+    }
   }
   return HX_OK;
 }
@@ -749,6 +798,16 @@ int hx_exchange_coords_host(hx_handle h, float* coords_host, float* coords_dev, 
 
 int hx_exchange_forces_host(hx_handle h, float* forces_host, float* forces_dev, void* stream) {
   return exchange_host(h, forces_host, forces_dev, stream, 1);
+}
+
+int hx_exchange_coords_host_packed(hx_handle h, const float* home_host, float* halo_host, float* coords_dev,
+                                   void* stream) {
+  return exchange_host_packed(h, home_host, halo_host, coords_dev, stream, 0);
+}
+
+int hx_exchange_forces_host_packed(hx_handle h, const float* forces_host, float* home_forces_host, float* forces_dev,
+                                   void* stream) {
+  return exchange_host_packed(h, forces_host, home_forces_host, forces_dev, stream, 1);
 }
 
 int hx_exchange_coords_unfused(hx_handle h, float* coords, void* stream) {

@@ -15,10 +15,10 @@ constexpr int kCopyThreads = 256;
 // mod 16, the chunk's aligned middle moves in 16-byte words, four per thread
 // in flight; the few words around it, and every word otherwise, one by one.
 __global__ void __launch_bounds__(kCopyThreads) k_copy_chunks(const float* __restrict__ src, float* __restrict__ dst,
-                                                              const CopyChunk* __restrict__ chunks) {
+                                                              const CopyChunk* __restrict__ chunks, int mode) {
   const CopyChunk c = chunks[blockIdx.x];
-  const float* s = src + c.word;
-  float* d = dst + c.word;
+  const float* s = src + (mode == kCopyUnpack ? c.packed : c.word);
+  float* d = dst + (mode == kCopyPack ? c.packed : c.word);
   const int n = c.n;
   const int t = static_cast<int>(threadIdx.x);
   const uintptr_t sa = reinterpret_cast<uintptr_t>(s), da = reinterpret_cast<uintptr_t>(d);
@@ -47,9 +47,10 @@ __global__ void __launch_bounds__(kCopyThreads) k_copy_chunks(const float* __res
 
 }  // namespace
 
-cudaError_t launch_copy_chunks(const float* src, float* dst, const CopyChunk* chunks, int n_chunks, cudaStream_t s) {
+cudaError_t launch_copy_chunks(const float* src, float* dst, const CopyChunk* chunks, int n_chunks, int mode,
+                               cudaStream_t s) {
   if (n_chunks <= 0) return cudaSuccess;
-  k_copy_chunks<<<n_chunks, kCopyThreads, 0, s>>>(src, dst, chunks);
+  k_copy_chunks<<<n_chunks, kCopyThreads, 0, s>>>(src, dst, chunks, mode);
   return cudaGetLastError();
 }
 

@@ -531,18 +531,21 @@ int build_resolved_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const s
 // slots, cut into pieces of at most kCopyChunkWords words.
 int build_copy_chunks(hx_ctx* h) {
   std::vector<CopyChunk> home, halo;
-  auto cut = [](std::vector<CopyChunk>& out, int64_t first_slot, int64_t slots) {
+  int64_t packed_home = 0, packed_halo = 0;   // words of each table's ranges laid end to end so far
+  auto cut = [](std::vector<CopyChunk>& out, int64_t& packed, int64_t first_slot, int64_t slots) {
     for (int64_t w = 0; w < 3 * slots; w += kCopyChunkWords) {
       CopyChunk c;
       c.word = 3 * first_slot + w;
+      c.packed = packed + w;
       c.n = static_cast<int32_t>(std::min<int64_t>(kCopyChunkWords, 3 * slots - w));
       c.pad = 0;
       out.push_back(c);
     }
+    packed += 3 * slots;
   };
   for (int r = 0; r < h->pl.ndom; ++r) {
-    cut(home, h->dom_offset[r], h->home[r]);
-    cut(halo, h->dom_offset[r] + h->home[r], h->halo[r]);
+    cut(home, packed_home, h->dom_offset[r], h->home[r]);
+    cut(halo, packed_halo, h->dom_offset[r] + h->home[r], h->halo[r]);
   }
   h->n_home_chunks = static_cast<int>(home.size());
   h->n_halo_chunks = static_cast<int>(halo.size());

@@ -50,6 +50,8 @@ SIGNATURES = {
     "hx_exchange_forces": (_I, [_P, _P, _P]),
     "hx_exchange_coords_host": (_I, [_P, _P, _P, _P]),
     "hx_exchange_forces_host": (_I, [_P, _P, _P, _P]),
+    "hx_exchange_coords_host_packed": (_I, [_P, _P, _P, _P, _P]),
+    "hx_exchange_forces_host_packed": (_I, [_P, _P, _P, _P, _P]),
     "hx_exchange_coords_unfused": (_I, [_P, _P, _P]),
     "hx_exchange_forces_unfused": (_I, [_P, _P, _P]),
     "hx_exchange_coords_static": (_I, [_P, _P, _P]),
@@ -283,6 +285,36 @@ class HaloExchange:
         self._check_tensor(forces_dev, 3 * self.total_slots, "forces_dev")
         _check(self._lib.hx_exchange_forces_host(self._h, forces_host.data_ptr(), forces_dev.data_ptr(),
                                                  _stream_ptr(stream, self.device)), "hx_exchange_forces_host")
+
+    def _check_host_packed(self, t, n_slots: int, what: str) -> None:
+        if t.is_cuda or t.dtype.itemsize != 4 or not t.is_floating_point() or not t.is_contiguous():
+            raise ValueError(f"{what} must be a contiguous float32 host tensor (page-locked for asynchronous copies)")
+        if t.numel() < 3 * n_slots:
+            raise ValueError(f"{what} holds {t.numel()} elements, {3 * n_slots} needed")
+
+    def exchange_coords_host_packed(self, home_host, halo_host, coords_dev, stream=None) -> None:
+        """Packed home coordinates from ``home_host`` (CPU fp32 [n_atoms, 3], layout
+        order) into ``coords_dev``'s home slots, the coordinate exchange there,
+        and every halo slot packed into ``halo_host`` (CPU fp32 [halo slots, 3]);
+        queued on ``stream``."""
+        n_home = self.n_atoms
+        self._check_host_packed(home_host, n_home, "home_host")
+        self._check_host_packed(halo_host, self.total_slots - n_home, "halo_host")
+        self._check_tensor(coords_dev, 3 * self.total_slots, "coords_dev")
+        _check(self._lib.hx_exchange_coords_host_packed(self._h, home_host.data_ptr(), halo_host.data_ptr(),
+                                                        coords_dev.data_ptr(), _stream_ptr(stream, self.device)),
+               "hx_exchange_coords_host_packed")
+
+    def exchange_forces_host_packed(self, forces_host, home_forces_host, forces_dev, stream=None) -> None:
+        """Every slot's force from ``forces_host`` (CPU fp32 [slots, 3]) into
+        ``forces_dev``, the force exchange there, and the home forces packed
+        into ``home_forces_host`` (CPU fp32 [n_atoms, 3], layout order)."""
+        self._check_host_packed(forces_host, self.total_slots, "forces_host")
+        self._check_host_packed(home_forces_host, self.n_atoms, "home_forces_host")
+        self._check_tensor(forces_dev, 3 * self.total_slots, "forces_dev")
+        _check(self._lib.hx_exchange_forces_host_packed(self._h, forces_host.data_ptr(), home_forces_host.data_ptr(),
+                                                        forces_dev.data_ptr(), _stream_ptr(stream, self.device)),
+               "hx_exchange_forces_host_packed")
 
     def exchange_coords_unfused(self, coords, stream=None) -> None:
         self._check_tensor(coords, 3 * self.total_slots, "coords")

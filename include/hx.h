@@ -252,6 +252,43 @@ int hx_exchange_forces(hx_handle h, float* forces, void* stream);
 int hx_exchange_coords_host(hx_handle h, float* coords_host, float* coords_dev, void* stream);
 int hx_exchange_forces_host(hx_handle h, float* forces_host, float* forces_dev, void* stream);
 
+/* The same two exchanges with packed host buffers: a domain's atoms are
+ * contiguous in host memory, so each direction crosses the host link as one
+ * copy-engine transfer, and the scatter into the slot layout and the gather
+ * out of it run as range copies in HBM (like the pages' packSendBufKernel,
+ * which gathers a pulse's atoms into one contiguous buffer before it is sent;
+ * "From MPI baseline to optimized GPU-native halo exchange").
+ *   hx_exchange_coords_host_packed: home_host (host, float3 [n_atoms]) holds
+ *     the home coordinates in layout order (domain 0's home slots, then
+ *     domain 1's, ...: the order of hx_get_home_ids); they are copied into
+ *     coords_dev's home slots, hx_exchange_coords(coords_dev) runs, and every
+ *     halo slot is copied out to halo_host (host, float3 [total_slots -
+ *     n_atoms]) in layout order (domain 0's halo slots, then domain 1's, ...).
+ *   hx_exchange_forces_host_packed: forces_host (host, float3 slots of the
+ *     layout: every slot's force) is copied into forces_dev,
+ *     hx_exchange_forces(forces_dev) runs, and the home forces are copied out
+ *     to home_forces_host (host, float3 [n_atoms], layout order).
+ *   coords_dev / forces_dev: device float3 slots of the layout, owned by the
+ *     caller (as for the calls above).
+ * All copies are queued on `stream`; the output buffer holds the results once
+ * the stream has passed this point. Host buffers should be page-locked
+ * (cudaHostAlloc or cudaHostRegister) for the copies to be asynchronous;
+ * pageable memory gives the same results with synchronous copies. They are
+ * owned by the caller and must not be written (input) or read (output) until
+ * the stream has passed the call. Host traffic: 12 B per home slot in and
+ * 12 B per halo slot out (coordinates), 12 B per slot in and 12 B per home
+ * slot out (forces), as for the calls above. The first packed call after a
+ * build allocates the handle's packing buffer (12 B x the larger of the home
+ * and halo slot counts), kept until the next build or hx_destroy; make it
+ * before any stream capture. Calls on one handle share that buffer: calls
+ * whose work overlaps on the GPU (other streams) race, so use one handle per
+ * stream. Errors: those of the exchange; HX_ERR_ARG for a NULL buffer that
+ * would be read or written; HX_ERR_NOMEM if the buffer cannot be allocated. */
+int hx_exchange_coords_host_packed(hx_handle h, const float* home_host, float* halo_host, float* coords_dev,
+                                   void* stream);
+int hx_exchange_forces_host_packed(hx_handle h, const float* forces_host, float* home_forces_host,
+                                   float* forces_dev, void* stream);
+
 /* Unfused baseline of the same two exchanges: one stream-ordered kernel
  * launch per pulse (all senders of that pulse in one launch), no signals.
  * Same results bit for bit as the fused calls in ordered mode. Pages: the

@@ -448,6 +448,93 @@ def test_host_buffer_exchanges(name, flags):
     assert rc == 0, (rc, det)
 
 
+@pytest.mark.parametrize("name", ["C1", "C2", "C3", "C4"])
+@pytest.mark.parametrize("flags", [HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE | HX.HX_FLAG_SWEEP_FORCES | HX.HX_FLAG_PDL,
+                                   HX.HX_FLAG_RESOLVED | HX.HX_FLAG_PDL, 0])
+def test_host_packed_exchanges(name, flags):
+    """hx_exchange_coords_host_packed / hx_exchange_forces_host_packed: packed
+    home coordinates in, packed halo coordinates out (layout order); every
+    slot's force in, packed home forces out; bit-exact, twice on the same
+    buffers, inputs left as given."""
+    w = W.WORKLOADS[name]
+    c = Case(w, flags=flags)
+    o = c.o
+    hm = c.home_mask()
+    x0 = o.coords()
+    ref = x0.copy()
+    o.exchange_coords(ref)
+    home = torch.from_numpy(x0[hm].copy()).pin_memory()
+    halo = torch.full((int((~hm).sum()), 3), float("nan")).pin_memory()
+    dev = torch.full((c.slots, 3), float("nan"), device="cuda")
+    for _ in range(2):
+        c.hx.exchange_coords_host_packed(home, halo, dev)
+        torch.cuda.synchronize()
+        assert np.array_equal(_bits(halo.numpy()), _bits(ref[~hm]))
+        assert np.array_equal(_bits(dev.cpu().numpy()), _bits(ref))
+        assert np.array_equal(_bits(home.numpy()), _bits(x0[hm]))
+    f0 = W.forces(w, c.slots)
+    fref = f0.copy()
+    o.exchange_forces(fref)
+    fh = torch.from_numpy(f0.copy()).pin_memory()
+    hf = torch.full((int(hm.sum()), 3), float("nan")).pin_memory()
+    fd = torch.full((c.slots, 3), float("nan"), device="cuda")
+    for _ in range(2):
+        c.hx.exchange_forces_host_packed(fh, hf, fd)
+        torch.cuda.synchronize()
+        assert np.array_equal(_bits(hf.numpy()), _bits(fref[hm]))   # home forces: the reduced sums
+        assert np.array_equal(_bits(fh.numpy()), _bits(f0))         # the input is left as given
+    rc, det = c.hx.status()
+    assert rc == 0, (rc, det)
+
+
+def test_host_packed_misaligned_pageable_and_rebuild():
+    """Packed buffers 4 bytes off a 16-byte boundary and in pageable memory
+    (synchronous copies) give the same bits; a rebuild with more atoms grows
+    the packing buffer; undersized buffers are refused before any copy."""
+    w = W.WORKLOADS["C2"]
+    pos = W.positions(w)
+    c = Case(w, flags=HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES, pos=pos[: len(pos) // 2].copy())
+    for step, p in enumerate((pos[: len(pos) // 2].copy(), pos)):
+        if step:
+            c = Case(w, flags=HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_SWEEP_FORCES, pos=p)
+        o = c.o
+        hm = c.home_mask()
+        ref = o.coords().copy()
+        o.exchange_coords(ref)
+        nh, nl = int(hm.sum()), int((~hm).sum())
+        store = torch.empty(3 * nh + 1, dtype=torch.float32).pin_memory()
+        home = store[1:].view(nh, 3)                       # 4 bytes past a 16-byte boundary
+        home.copy_(torch.from_numpy(o.coords()[hm]))
+        halo = torch.from_numpy(np.full((nl, 3), np.nan, np.float32))   # pageable
+        dev = torch.empty((c.slots, 3), device="cuda")
+        c.hx.exchange_coords_host_packed(home, halo, dev)
+        torch.cuda.synchronize()
+        assert np.array_equal(_bits(halo.numpy()), _bits(ref[~hm]))
+        with pytest.raises(ValueError):
+            c.hx.exchange_coords_host_packed(home[:-1], halo, dev)
+        with pytest.raises(ValueError):
+            c.hx.exchange_forces_host_packed(torch.empty((c.slots - 1, 3)), torch.empty((nh, 3)), dev)
+    # the same handle rebuilt with more atoms: the packing buffer grows with it
+    hx = HX.HaloExchange(w.box, w.dims, w.cutoff, flags=HX.HX_FLAG_FINE_WAITS)
+    for p in (pos[: len(pos) // 3], pos):
+        o = Oracle(w.box, w.dims, w.cutoff)
+        o.build(p)
+        pt = torch.from_numpy(p.copy()).cuda()
+        n = hx.build_maps(pt)
+        dev = torch.empty((n, 3), device="cuda")
+        hx.build_maps(pt, dev)
+        hm = np.zeros(n, bool)
+        for r in range(o.n_domains):
+            hm[o.dom_offset[r]: o.dom_offset[r] + o.home[r]] = True
+        ref = o.coords().copy()
+        o.exchange_coords(ref)
+        halo = torch.empty((int((~hm).sum()), 3)).pin_memory()
+        hx.exchange_coords_host_packed(torch.from_numpy(o.coords()[hm].copy()).pin_memory(), halo, dev)
+        torch.cuda.synchronize()
+        assert np.array_equal(_bits(halo.numpy()), _bits(ref[~hm]))
+    hx.close()
+
+
 def test_host_buffer_rules():
     w = W.WORKLOADS["C2"]
     c = Case(w, flags=HX.HX_FLAG_FINE_WAITS)
