@@ -558,6 +558,11 @@ int build_copy_chunks(hx_ctx* h) {
   return HX_OK;
 }
 
+#ifndef HX_SWEEP_LAG_WINDOWS
+#define HX_SWEEP_LAG_WINDOWS 8
+#endif
+constexpr long long kSweepLagWindows = HX_SWEEP_LAG_WINDOWS;   // resident-warp windows per dependency stage
+
 #ifndef HX_CHUNK_LAG_WINDOWS
 #define HX_CHUNK_LAG_WINDOWS 1
 #endif
@@ -635,13 +640,15 @@ int build_tables(hx_ctx* h, cudaStream_t s) {
   }
   // Unit lists. A dependent unit is placed a few resident windows after the
   // units it waits for: eight units per resident warp (measured on the
-  // 12M-atom workload: lags of 2, 3, 4, 6 and 10 windows gave forces in
-  // 112.6, 100.5, 94.2, 92.2 and 92.2 us).
+  // 12M-atom workload with an earlier sweep: lags of 2, 3, 4, 6 and 10
+  // windows gave forces in 112.6, 100.5, 94.2, 92.2 and 92.2 us; with the
+  // current one, 2 and 4 windows 81.7 and 79.5 us against 78.5 at 8).
   for (int dir = 0; dir < 2; ++dir) {
     int rc = HX_OK;
     if (h->family[dir] == kFamSweep) {
       if (P > kSweepSegs) return HX_ERR_PULSES;   // a unit's runs must fit one warp's stage
-      rc = build_unit_tables(h, items, maps, rank, kSweepSlots, kSweepEntries, 8ll * h->grid[dir] * kWarps,
+      rc = build_unit_tables(h, items, maps, rank, kSweepSlots, kSweepEntries,
+                             kSweepLagWindows * h->grid[dir] * kWarps,
                              kSweepSlotBytes, kSweepMapBytes, kSweepSrcBytes, dir);
     }
     if (rc != HX_OK) return rc;
