@@ -4,6 +4,8 @@
 // range pieces of the host-buffer calls.
 #include "hx_runtime.h"
 
+#include <atomic>
+
 namespace hx_rt {
 
 // ---------------------------------------------------------------- work tables
@@ -114,10 +116,60 @@ std::vector<int> kahn_order(int n, Deps deps, Key key) {
   return order;   // shorter than n only if the waits had a cycle (they cannot)
 }
 
+// The records in ascending key (ties by index) when that order is
+// topological, else Kahn's order by the same keys (which then differs only
+// where a record's key is below one of its producers'). A key that grows by
+// a lag of whole resident windows per dependency stage makes the first case
+// the usual one, and the keys span a small range: a counting sort, then one
+// check of every dependency.
+template <class Deps, class Key>
+std::vector<int> key_order(int n, Deps deps, Key key) {
+  std::vector<int> order(n);
+  if (n == 0) return order;
+  long long lo = key(0), hi = key(0);
+  for (int i = 1; i < n; ++i) {
+    lo = std::min(lo, key(i));
+    hi = std::max(hi, key(i));
+  }
+  if (hi - lo > 4ll * n + (1ll << 20)) return kahn_order(n, deps, key);
+  std::vector<int> first(static_cast<size_t>(hi - lo) + 2, 0);
+  for (int i = 0; i < n; ++i) ++first[static_cast<size_t>(key(i) - lo) + 1];
+  for (size_t k = 1; k < first.size(); ++k) first[k] += first[k - 1];
+  for (int i = 0; i < n; ++i) order[first[static_cast<size_t>(key(i) - lo)]++] = i;   // stable: ties by index
+  std::vector<int> pos(n);
+  for (int k = 0; k < n; ++k) pos[order[k]] = k;
+  for (int i = 0; i < n; ++i)
+    for (int d : deps(i))
+      if (pos[d] >= pos[i]) return kahn_order(n, deps, key);
+  return order;
+}
+
 std::vector<int> order_chunks(const std::vector<Rec>& recs) {
-  return kahn_order(
+  return key_order(
       static_cast<int>(recs.size()), [&](int i) -> const std::vector<int>& { return recs[i].deps; },
       [&](int i) { return recs[i].key; });
+}
+
+// Dependency depth of every record: 0 without producers, else one more than
+// its deepest producer. Relaxation passes over all records: the depths settle
+// within as many passes as the longest chain has links. False if they still
+// change after `max_passes` (a cycle, which the waits cannot form).
+template <class Deps>
+bool dependency_depths(int n, Deps deps, std::vector<int>& depth, int max_passes) {
+  depth.assign(n, 0);
+  for (int pass = 0; pass <= max_passes; ++pass) {
+    bool changed = false;
+    for (int i = 0; i < n; ++i) {
+      int v = 0;
+      for (int d : deps(i)) v = std::max(v, depth[d] + 1);
+      if (v != depth[i]) {
+        depth[i] = v;
+        changed = true;
+      }
+    }
+    if (!changed) return true;
+  }
+  return false;
 }
 
 // ---------------------------------------------------------------- unit tables
@@ -257,10 +309,11 @@ int build_unit_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::
           const int q = items[p * nd + t.r].q;
           const int64_t s0 = t.segs[k].other - h->dom_offset[q], s1 = s0 + t.segs[k].n;
           const size_t first = t.deps.size();
-          for (int j : by_range[q][p + 1]) {
-            const TRec& s = recs[j];
-            if (s.a < s1 && s0 < s.a + s.n) t.deps.push_back(j);
-          }
+          // q's units of range p, in slot order: the first one that ends past s0, then on while they start before s1
+          const std::vector<int>& in_range = by_range[q][p + 1];
+          auto it_j = std::partition_point(in_range.begin(), in_range.end(),
+                                           [&](int j) { return recs[j].a + recs[j].n <= s0; });
+          for (; it_j != in_range.end() && recs[*it_j].a < s1; ++it_j) t.deps.push_back(*it_j);
           t.segs[k].dep = static_cast<int32_t>(t.deps.size() - first);
         }
         return;
@@ -272,64 +325,76 @@ int build_unit_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::
     {
       const int n = static_cast<int>(recs.size());
       auto deps_of = [&](int i) -> const std::vector<int>& { return recs[i].deps; };
-      std::vector<int> topo = kahn_order(n, deps_of, [](int) { return 0ll; });   // any topological order
-      if (topo.size() != recs.size()) return HX_ERR_STATE;
-      for (int i : topo)
-        for (int d : recs[i].deps) recs[i].stage = std::max(recs[i].stage, recs[d].stage + 1);
-      std::vector<int> base(recs.size());
-      for (size_t i = 0; i < recs.size(); ++i) base[i] = static_cast<int>(i);
-      std::sort(base.begin(), base.end(), [&](int x, int y) {
-        const TRec& a = recs[x];
-        const TRec& b = recs[y];
-        if (rank[a.r] != rank[b.r]) return rank[a.r] < rank[b.r];
-        if (a.stage != b.stage) return a.stage < b.stage;
-        if (a.range != b.range) return a.range < b.range;
-        return a.a < b.a;
-      });
-      for (size_t k = 0; k < base.size(); ++k)
-        recs[base[k]].key = static_cast<long long>(k) + lag * recs[base[k]].stage;
-      std::vector<int> order = kahn_order(n, deps_of, [&](int i) { return recs[i].key; });
+      std::vector<int> depth;
+      if (!dependency_depths(n, deps_of, depth, P + 1)) return HX_ERR_STATE;
+      for (int i = 0; i < n; ++i) recs[i].stage = depth[i];
+      // Base order: domains by rank, a domain's units by stage, then as they
+      // were cut (range, then first slot), which is their order in `recs`.
+      std::vector<int> doms(nd);
+      for (int r = 0; r < nd; ++r) doms[r] = r;
+      std::sort(doms.begin(), doms.end(), [&](int x, int y) { return rank[x] != rank[y] ? rank[x] < rank[y] : x < y; });
+      std::vector<int> dom_first(nd + 1, 0);
+      for (const TRec& t : recs) ++dom_first[t.r + 1];
+      for (int r = 0; r < nd; ++r) dom_first[r + 1] += dom_first[r];
+      long long k = 0;
+      int max_stage = 0;
+      for (const TRec& t : recs) max_stage = std::max(max_stage, t.stage);
+      for (int r : doms)
+        for (int st = 0; st <= max_stage; ++st)
+          for (int i = dom_first[r]; i < dom_first[r + 1]; ++i)
+            if (recs[i].stage == st) recs[i].key = k++ + lag * st;
+      std::vector<int> order = key_order(n, deps_of, [&](int i) { return recs[i].key; });
       if (order.size() != recs.size()) return HX_ERR_STATE;
       std::vector<int> pos(recs.size());
-      for (size_t k = 0; k < order.size(); ++k) pos[order[k]] = static_cast<int>(k);
+      for (size_t q = 0; q < order.size(); ++q) pos[order[q]] = static_cast<int>(q);
       std::vector<char> waited(recs.size(), 0);
       for (auto& t : recs)
         for (int d : t.deps) waited[d] = 1;
-      std::vector<Unit> units;
-      std::vector<UnitSeg> segs;   // segments past kInlineSegs
-      std::vector<Wait> waits;
-      for (int i : order) {
+      // records in list order, filled on the host's cores: each one's share of
+      // the overflow segments and of the wait list comes from prefix sums
+      std::vector<int64_t> seg_at(n + 1, 0), wait_at(n + 1, 0);
+      for (int q = 0; q < n; ++q) {
+        const TRec& t = recs[order[q]];
+        seg_at[q + 1] = seg_at[q] + std::max<int64_t>(0, static_cast<int64_t>(t.segs.size()) - kInlineSegs);
+        wait_at[q + 1] = wait_at[q] + static_cast<int64_t>(t.deps.size());
+      }
+      std::vector<Unit> units(n);
+      std::vector<UnitSeg> segs(seg_at[n]);   // segments past kInlineSegs
+      std::vector<Wait> waits(wait_at[n]);
+      std::atomic<bool> fits{true};
+      parallel_for(static_cast<size_t>(n), [&](size_t q) {
+        const int i = order[q];
         const TRec& t = recs[i];
-        Unit u;
+        Unit& u = units[q];
         std::memset(&u, 0, sizeof(u));
         u.base = h->dom_offset[t.r] + t.a;
         u.n = t.n;
         u.local_a = t.a;
         u.seg_cnt = static_cast<int32_t>(t.segs.size());
-        u.extra_off = static_cast<int32_t>(segs.size());
+        u.extra_off = static_cast<int32_t>(seg_at[q]);
         // stage regions: each run's region starts on a 16-byte boundary and is 16 bytes longer than the run
         int moff = slot_bytes, soff = slot_bytes + map_bytes;
-        for (size_t k = 0; k < t.segs.size(); ++k) {
-          UnitSeg sg = t.segs[k];
+        for (size_t g = 0; g < t.segs.size(); ++g) {
+          UnitSeg sg = t.segs[g];
           sg.map_off = moff;
           sg.src_off = dir == 1 ? soff : 0;
           moff += ((4 * sg.n + 15) & ~15) + 16;
           soff += ((12 * sg.n + 15) & ~15) + 16;
-          if (static_cast<int>(k) < kInlineSegs) u.seg[k] = sg;
-          else segs.push_back(sg);
+          if (static_cast<int>(g) < kInlineSegs) u.seg[g] = sg;
+          else segs[u.extra_off + g - kInlineSegs] = sg;
         }
         // the stage regions must fit the kernel's buffer
         if (moff > slot_bytes + map_bytes || (dir == 1 && soff > slot_bytes + map_bytes + src_bytes))
-          return HX_ERR_STATE;
-        u.wait_off = static_cast<int32_t>(waits.size());
+          fits.store(false, std::memory_order_relaxed);
+        u.wait_off = static_cast<int32_t>(wait_at[q]);
         u.wait_cnt = static_cast<int32_t>(t.deps.size());
-        for (int d : t.deps) waits.push_back({pos[d], 1});
+        for (int w = 0; w < u.wait_cnt; ++w) waits[u.wait_off + w] = {pos[t.deps[w]], 1};
         for (int w = 0; w < std::min(u.wait_cnt, kInlineWaits); ++w) u.wait_inline[w] = waits[u.wait_off + w];
         u.flags = (waited[i] ? kSignal : 0) | (dir == 0 && t.range >= 0 ? kHaloSrc : 0);
         u.item = t.seg_pulse[0] * nd + t.r;
         for (const UnitSeg& sg : t.segs) u.entries += sg.n;
-        units.push_back(u);
-      }
+      }, 64);
+      if (!fits.load()) return HX_ERR_STATE;
       h->n_units[dir] = static_cast<int>(units.size());
       HX_CUDA(dev_alloc(&h->d_units[dir], units.size()));
       HX_CUDA(dev_alloc(&h->d_segs[dir], segs.size()));
@@ -807,18 +872,25 @@ int build_tables(hx_ctx* h, cudaStream_t s) {
     // priority: base order (domain rank, stage, pulse, entry), then a lag of
     // one resident-warp window per stage
     {
+      // Records were cut pulse by pulse, each pulse domain by domain, so a
+      // domain's records of one stage are already in (pulse, entry) order: a
+      // counting sort by (domain rank, stage) keeps that order.
+      std::vector<int> dom_pos(nd);
+      {
+        std::vector<int> doms(nd);
+        for (int r = 0; r < nd; ++r) doms[r] = r;
+        std::sort(doms.begin(), doms.end(),
+                  [&](int x, int y) { return rank[x] != rank[y] ? rank[x] < rank[y] : x < y; });
+        for (int q = 0; q < nd; ++q) dom_pos[doms[q]] = q;
+      }
+      int n_stages = 1;
+      for (const Rec& rc : recs) n_stages = std::max(n_stages, rc.stage + 1);
+      std::vector<int> first(static_cast<size_t>(nd) * n_stages + 1, 0);
+      auto bucket = [&](const Rec& rc) { return static_cast<size_t>(dom_pos[items[rc.item].r]) * n_stages + rc.stage; };
+      for (const Rec& rc : recs) ++first[bucket(rc) + 1];
+      for (size_t q = 1; q < first.size(); ++q) first[q] += first[q - 1];
       std::vector<int> base(recs.size());
-      for (size_t i = 0; i < recs.size(); ++i) base[i] = static_cast<int>(i);
-      std::sort(base.begin(), base.end(), [&](int a, int b) {
-        const Rec& x = recs[a];
-        const Rec& y = recs[b];
-        const ItemInfo& ix = items[x.item];
-        const ItemInfo& iy = items[y.item];
-        if (rank[ix.r] != rank[iy.r]) return rank[ix.r] < rank[iy.r];
-        if (x.stage != y.stage) return x.stage < y.stage;
-        if (ix.p != iy.p) return ix.p < iy.p;
-        return x.begin < y.begin;
-      });
+      for (size_t i = 0; i < recs.size(); ++i) base[first[bucket(recs[i])]++] = static_cast<int>(i);
       const long long window = static_cast<long long>(h->grid[dir]) * kWarps * kChunkLagWindows;
       for (size_t k = 0; k < base.size(); ++k)
         recs[base[k]].key = static_cast<long long>(k) + window * recs[base[k]].stage;
@@ -829,9 +901,13 @@ int build_tables(hx_ctx* h, cudaStream_t s) {
     for (size_t k = 0; k < order.size(); ++k) pos[order[k]] = static_cast<int>(k);
     std::vector<int> item_chunks(std::max(n_items, 1), 0);
     for (auto& rc : recs) item_chunks[rc.item] += 1;
-    std::vector<ChunkSlot> chunks(order.size());
-    std::vector<Wait> waits;
-    for (size_t k = 0; k < order.size(); ++k) {
+    // records in list order, filled on the host's cores (wait-list offsets from a prefix sum)
+    const size_t nc = order.size();
+    std::vector<int64_t> wait_at(nc + 1, 0);
+    for (size_t k = 0; k < nc; ++k) wait_at[k + 1] = wait_at[k] + static_cast<int64_t>(recs[order[k]].wait.size());
+    std::vector<ChunkSlot> chunks(nc);
+    std::vector<Wait> waits(wait_at[nc]);
+    parallel_for(nc, [&](size_t k) {
       const int ri = order[k];
       const Rec& rc = recs[ri];
       const ItemInfo& it = items[rc.item];
@@ -844,19 +920,20 @@ int build_tables(hx_ctx* h, cudaStream_t s) {
       ch.n = rc.end - rc.begin;
       ch.item = rc.item;
       ch.item_chunks = item_chunks[rc.item];
-      ch.wait_off = static_cast<int32_t>(waits.size());
+      ch.wait_off = static_cast<int32_t>(wait_at[k]);
       ch.wait_cnt = static_cast<int32_t>(rc.wait.size());
-      for (int w : rc.wait) waits.push_back(fine ? Wait{pos[w], 1} : Wait{w, 0});
+      for (int w = 0; w < ch.wait_cnt; ++w) {
+        const int x = rc.wait[w];
+        waits[ch.wait_off + w] = fine ? Wait{pos[x], 1} : Wait{x, item_chunks[x]};
+      }
       const bool sig = fine ? rec_waited[ri] != 0 : item_waited[rc.item] != 0;
       ch.flags = (rc.halo_src ? kHaloSrc : 0) | (sig ? kSignal : 0) | (dir == 0 && it.shift_flag ? kShift : 0);
       ch.dim = it.dim;
       ch.shift = pl.boxf[it.dim];
       if (ch.n > 0) std::memcpy(slot.map, maps.data() + ch.map, sizeof(int32_t) * ch.n);
-    }
-    if (!fine)
-      for (auto& w : waits) w.chunks = item_chunks[w.item];
-    for (auto& slot : chunks)   // the first waits of each chunk inside its record
-      for (int w = 0; w < std::min(slot.rec.wait_cnt, kWaitSlots); ++w) slot.waits[w] = waits[slot.rec.wait_off + w];
+      // the first waits of the chunk inside its record
+      for (int w = 0; w < std::min(ch.wait_cnt, kWaitSlots); ++w) slot.waits[w] = waits[ch.wait_off + w];
+    }, 64);
     h->n_chunks[dir] = static_cast<int>(chunks.size());
     HX_CUDA(dev_alloc(&h->d_chunks[dir], chunks.size()));
     HX_CUDA(dev_alloc(&h->d_waits[dir], waits.size()));
