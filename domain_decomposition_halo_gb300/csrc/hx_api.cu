@@ -198,7 +198,9 @@ UnitParams unit_params(hx_ctx* h, int dir) {
   // Measured on one GB300 (forces back to back): 8 domains 11.0 -> 9.2 us and
   // 64 domains 18.1 -> 15.7 us with segment waits (about 1.6 units a warp);
   // 256 domains (16 units a warp) 78.2 -> 79.2 us, so it keeps unit waits.
-  P.seg_waits = h->n_units[dir] <= kSegWaitUnitsPerWarp * h->grid[dir] * kWarps ? 1 : 0;
+  P.seg_waits = h->sweep_waits == 1   ? 1
+                : h->sweep_waits == 2 ? 0
+                                      : (h->n_units[dir] <= kSegWaitUnitsPerWarp * h->grid[dir] * kWarps ? 1 : 0);
   P.timeout_ns = h->timeout_ns;
   return P;
 }
@@ -960,6 +962,16 @@ int hx_debug_drop_signal(hx_handle h, int direction, int domain, int pulse) {
   if (cudaDeviceSynchronize() != cudaSuccess) return HX_ERR_CUDA;
   Ctrl* c = h->d_ctrl + direction;
   if (cudaMemcpy(&c->drop_item, &item, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return HX_ERR_CUDA;
+  return HX_OK;
+}
+
+int hx_debug_sweep_waits(hx_handle h, int mode) {
+  if (!h || mode < 0 || mode > 2) return HX_ERR_ARG;
+  DeviceGuard guard(h->device);
+  if (!guard.ok()) return HX_ERR_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return HX_ERR_CUDA;
+  h->sweep_waits = mode;
+  drop_graphs(h);   // cached graphs hold the launch parameters of the previous choice
   return HX_OK;
 }
 

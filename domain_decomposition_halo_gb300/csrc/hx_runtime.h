@@ -137,6 +137,7 @@ struct hx_ctx {
   CopyChunk* d_home_chunks = nullptr;        // host-buffer calls: every domain's home range
   CopyChunk* d_halo_chunks = nullptr;        // ... and halo range, in pieces of one block each
   int n_home_chunks = 0, n_halo_chunks = 0;
+  int sweep_waits = 0;                      // force sweep: 0 by units per warp, 1 segment waits, 2 whole-unit waits
   float* d_pack = nullptr;                  // packed host-buffer calls: the home or halo ranges end to end
   int64_t pack_slots = 0;                   // its size in slots (allocated by the first packed call)
   void* static_scratch = nullptr;            // hx_exchange_coords_static: device address of its scratch array

@@ -59,6 +59,7 @@ SIGNATURES = {
     "hx_status": (_I, [_P, _P, _P]),
     "hx_clear_status": (_I, [_P, _P]),
     "hx_debug_drop_signal": (_I, [_P, _I, _I, _I]),
+    "hx_debug_sweep_waits": (_I, [_P, _I]),
     "hx_error_string": (ctypes.c_char_p, [_I]),
     "hx_destroy": (None, [_P]),
 }
@@ -350,3 +351,7 @@ class HaloExchange:
     def debug_drop_signal(self, direction: int, domain: int, pulse: int = 0) -> None:
         _check(self._lib.hx_debug_drop_signal(self._h, int(direction), int(domain), int(pulse)),
                "hx_debug_drop_signal")
+
+    def debug_sweep_waits(self, mode: int) -> None:
+        """Force sweep waits: 0 automatic, 1 segment by segment, 2 whole unit."""
+        _check(self._lib.hx_debug_sweep_waits(self._h, int(mode)), "hx_debug_sweep_waits")

@@ -349,6 +349,16 @@ int hx_clear_status(hx_handle h, void* stream);
  * so its waiters run into the timeout. domain = -1 switches it off. */
 int hx_debug_drop_signal(hx_handle h, int direction, int domain, int pulse);
 
+/* Test and tuning hook for the force sweep (HX_FLAG_SWEEP_FORCES): mode 1
+ * makes each dependent segment of a unit wait for its own producers (the
+ * default where a warp has at most four units), mode 2 makes a unit wait for
+ * all its producers before staging (the default otherwise), mode 0 restores
+ * the automatic choice. Results are bit-identical in every mode; only the
+ * timing differs. Synchronises the device and drops the handle's cached
+ * graphs. Not on the pages (their force kernel waits per pulse). Errors:
+ * HX_ERR_ARG, HX_ERR_CUDA. */
+int hx_debug_sweep_waits(hx_handle h, int mode);
+
 /* Human-readable name of an HX_* code (static string). Not on the pages. */
 const char* hx_error_string(int code);
 

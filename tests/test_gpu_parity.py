@@ -535,6 +535,55 @@ def test_host_packed_misaligned_pageable_and_rebuild():
     hx.close()
 
 
+SWEEP = HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE | HX.HX_FLAG_SWEEP_FORCES
+
+
+@pytest.mark.parametrize("name", ["C2", "C3", "C4"] + [f"rand{k}" for k in (9, 20, 25, 31)])
+@pytest.mark.parametrize("pdl", [0, HX.HX_FLAG_PDL])
+def test_sweep_wait_modes(name, pdl):
+    """The force sweep with its waits forced segment by segment and forced per
+    whole unit, on shapes with one and two pulses per dimension: ordered forces
+    bit-exact against the oracle in both, over several steps."""
+    w = _random_shape(int(name[4:])) if name.startswith("rand") else W.WORKLOADS[name]
+    try:
+        c = Case(w, flags=SWEEP | pdl)
+    except HX.HXError as e:   # the sweep serves at most 8 pulses
+        assert e.code == HX.HX_ERR_PULSES
+        pytest.skip("more pulses than the force sweep serves")
+    f0 = W.forces(w, c.slots)
+    ref = f0.copy()
+    c.o.exchange_forces(ref)
+    for mode in (1, 2, 0):
+        c.hx.debug_sweep_waits(mode)
+        for _ in range(3):
+            ft = torch.from_numpy(f0.copy()).cuda()
+            c.hx.exchange_forces(ft)
+            torch.cuda.synchronize()
+            assert np.array_equal(_bits(ft.cpu().numpy()), _bits(ref)), (name, mode)
+    rc, det = c.hx.status()
+    assert rc == 0, (rc, det)
+    with pytest.raises(HX.HXError):
+        c.hx.debug_sweep_waits(3)
+
+
+def test_sweep_segment_waits_full_size():
+    """The 12M-atom workload takes whole-unit waits by default: its forces with
+    segment waits forced are the same bits."""
+    w = W.WORKLOADS["C5"]
+    c = Case(w, flags=SWEEP | HX.HX_FLAG_PDL)
+    f0 = W.forces(w, c.slots)
+    ref = f0.copy()
+    c.o.exchange_forces(ref)
+    c.hx.debug_sweep_waits(1)
+    for _ in range(2):
+        ft = torch.from_numpy(f0.copy()).cuda()
+        c.hx.exchange_forces(ft)
+        torch.cuda.synchronize()
+        assert np.array_equal(_bits(ft.cpu().numpy()), _bits(ref))
+    rc, det = c.hx.status()
+    assert rc == 0, (rc, det)
+
+
 def test_host_buffer_rules():
     w = W.WORKLOADS["C2"]
     c = Case(w, flags=HX.HX_FLAG_FINE_WAITS)
