@@ -141,6 +141,7 @@ void free_tables(hx_ctx* h) {
   dev_free(h->d_flags);
   dev_free(h->d_blk);
   dev_free(h->d_ctrl);
+  dev_free(h->d_status);
   h->built = false;
 }
 
@@ -613,6 +614,23 @@ int hx::launch_coords_with_scratch(hx_ctx* h, float* coords, cudaStream_t s, Ctr
 
 // ------------------------------------------------------------------ C ABI
 
+namespace {
+
+// hx_status_async: the first direction's sticky status that is not HX_OK
+// (else HX_OK) and its detail, for one copy to the host in stream order.
+__global__ void k_status(const Ctrl* c, int* out) {
+  int st = 0, det = -1;
+  for (int k = 0; k < 2; ++k)
+    if (st == 0 && c[k].status != 0) {
+      st = c[k].status;
+      det = c[k].detail;
+    }
+  out[0] = st;
+  out[1] = det;
+}
+
+}  // namespace
+
 extern "C" {
 
 const char* hx_error_string(int code) {
@@ -936,6 +954,22 @@ int hx_status(hx_handle h, void* stream, int* detail) {
   if (static_status(h, &st, &det) != HX_OK) return HX_ERR_CUDA;
   if (st != 0 && detail) *detail = det;
   return st;
+}
+
+int hx_status_async(hx_handle h, int* status_host, void* stream) {
+  if (!h || !status_host) return HX_ERR_ARG;
+  if (!h->built) {
+    status_host[0] = HX_OK;
+    status_host[1] = -1;
+    return HX_OK;
+  }
+  DeviceGuard guard(h->device);
+  if (!guard.ok()) return HX_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  k_status<<<1, 1, 0, s>>>(h->d_ctrl, h->d_status);
+  HX_CUDA(cudaGetLastError());
+  HX_CUDA(cudaMemcpyAsync(status_host, h->d_status, 2 * sizeof(int), cudaMemcpyDeviceToHost, s));
+  return HX_OK;
 }
 
 int hx_clear_status(hx_handle h, void* stream) {

@@ -119,6 +119,7 @@ struct hx_ctx {
   unsigned long long* d_flags = nullptr;     // [2][n_items]
   unsigned int* d_blk = nullptr;             // [2][n_items]
   Ctrl* d_ctrl = nullptr;                    // [2]
+  int* d_status = nullptr;                   // [2]: hx_status_async's status and detail, on the device
   int n_chunks[2] = {0, 0};
   int grid[2] = {0, 0};
   size_t n_flags = 1;                        // flags (and election counters) per direction

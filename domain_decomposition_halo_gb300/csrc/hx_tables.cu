@@ -982,6 +982,7 @@ int build_tables(hx_ctx* h, cudaStream_t s) {
   HX_CUDA(dev_alloc(&h->d_flags, 2 * h->n_flags));
   HX_CUDA(dev_alloc(&h->d_blk, 2 * h->n_flags));
   HX_CUDA(dev_alloc(&h->d_ctrl, 2));
+  HX_CUDA(dev_alloc(&h->d_status, 2));
   // Persistent grid: every warp co-resident, and no more of them than there
   // is work.
   for (int k = 0; k < 2; ++k) {

@@ -57,6 +57,7 @@ SIGNATURES = {
     "hx_exchange_coords_static": (_I, [_P, _P, _P]),
     "hx_noop": (_I, [_P, _P]),
     "hx_status": (_I, [_P, _P, _P]),
+    "hx_status_async": (_I, [_P, _P, _P]),
     "hx_clear_status": (_I, [_P, _P]),
     "hx_debug_drop_signal": (_I, [_P, _I, _I, _I]),
     "hx_debug_sweep_waits": (_I, [_P, _I]),
@@ -344,6 +345,15 @@ class HaloExchange:
         detail = ctypes.c_int(-1)
         rc = self._lib.hx_status(self._h, _stream_ptr(stream, self.device), ctypes.byref(detail))
         return rc, detail.value
+
+    def status_async(self, out, stream=None) -> None:
+        """Queue the sticky status and detail into ``out`` (a CPU int32 tensor of
+        2 elements, page-locked for an asynchronous copy) without synchronising;
+        ``out`` holds them once ``stream`` has passed this call."""
+        import torch
+        if out.is_cuda or out.dtype != torch.int32 or out.numel() < 2 or not out.is_contiguous():
+            raise ValueError("out must be a contiguous int32 host tensor of 2 elements")
+        _check(self._lib.hx_status_async(self._h, out.data_ptr(), _stream_ptr(stream, self.device)), "hx_status_async")
 
     def clear_status(self, stream=None) -> None:
         _check(self._lib.hx_clear_status(self._h, _stream_ptr(stream, self.device)), "hx_clear_status")

@@ -338,6 +338,19 @@ int hx_noop(hx_handle h, void* stream);
  * failure detection of this library. */
 int hx_status(hx_handle h, void* stream, int* detail);
 
+/* The regular exchanges' sticky status without synchronising: queues on
+ * `stream` one small kernel that reads it and a copy of {status, detail}
+ * (as hx_status returns them; HX_OK and -1 when no wait gave up) into
+ * status_host[0] and status_host[1] (host memory owned by the caller;
+ * page-locked for the copy to be asynchronous). The values are there once
+ * the stream has passed this point, e.g. after an event recorded after the
+ * call, so a caller can check every step for a time-out without stalling the
+ * stream. A call between two exchanges on the stream sits between their
+ * launches (no programmatic overlap there). The static path's status is read
+ * by hx_status only. Not on the pages (their waits are unbounded). Errors:
+ * HX_ERR_ARG (NULL handle or buffer), HX_ERR_CUDA. */
+int hx_status_async(hx_handle h, int* status_host, void* stream);
+
 /* Synchronises `stream`, clears the status (the handle's, and the static
  * path's when hx_status would report it) and resets every pulse signal,
  * counter and epoch so that the next exchange starts clean. Not on the

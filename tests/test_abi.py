@@ -79,6 +79,7 @@ def test_init_validates_before_touching_a_device():
     assert lib.hx_exchange_coords_host_packed(None, None, None, None, None) == HX.HX_ERR_ARG
     assert lib.hx_exchange_forces_host_packed(None, None, None, None, None) == HX.HX_ERR_ARG
     assert lib.hx_debug_sweep_waits(None, 1) == HX.HX_ERR_ARG
+    assert lib.hx_status_async(None, None, None) == HX.HX_ERR_ARG
     assert lib.hx_get_resolved_counts(None, None, None, None) == HX.HX_ERR_ARG
     lib.hx_destroy(None)
     assert lib.hx_error_string(HX.HX_ERR_TIMEOUT)

@@ -385,6 +385,34 @@ def test_dropped_signal_times_out_and_recovers(direction, flags):
     check_force_steps(c, steps=1)
 
 
+@pytest.mark.parametrize("flags", [0, HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE | HX.HX_FLAG_SWEEP_FORCES | HX.HX_FLAG_PDL])
+def test_status_async_reports_without_synchronising(flags):
+    """hx_status_async queues the sticky status on the stream: OK after a clean
+    exchange, HX_ERR_TIMEOUT with the same detail as hx_status after a dropped
+    signal, and OK again once cleared."""
+    c = Case(W.WORKLOADS["C2"], flags=flags, timeout_us=20000)
+    out = torch.full((2,), 7, dtype=torch.int32).pin_memory()
+    xt = torch.from_numpy(c.o.coords().copy()).cuda()
+    c.hx.exchange_coords(xt)
+    c.hx.status_async(out)
+    torch.cuda.synchronize()
+    assert out.tolist() == [HX.HX_OK, -1]
+    c.hx.debug_drop_signal(0, 3, 0)
+    c.hx.exchange_coords(xt)
+    c.hx.status_async(out)
+    torch.cuda.synchronize()
+    rc, detail = c.hx.status()
+    assert rc == HX.HX_ERR_TIMEOUT and out.tolist() == [rc, detail]
+    c.hx.debug_drop_signal(0, -1)
+    c.hx.clear_status()
+    c.hx.exchange_coords(xt)
+    c.hx.status_async(out)
+    torch.cuda.synchronize()
+    assert out.tolist() == [HX.HX_OK, -1]
+    with pytest.raises(ValueError):
+        c.hx.status_async(torch.empty(2, dtype=torch.int32, device="cuda"))
+
+
 @pytest.mark.parametrize("name", ["C4", "C5"])
 @pytest.mark.parametrize("flags", [HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE | HX.HX_FLAG_SWEEP_FORCES,
                                    HX.HX_FLAG_RESOLVED | HX.HX_FLAG_PDL,
