@@ -515,6 +515,34 @@ def test_host_packed_exchanges(name, flags):
     assert rc == 0, (rc, det)
 
 
+def test_host_packed_full_size():
+    """The packed host-buffer calls on the 12M-atom workload in the bench's
+    modes: packed halo coordinates and home forces bit-exact against the
+    oracle."""
+    w = W.WORKLOADS["C5"]
+    c = Case(w, flags=HX.HX_FLAG_FINE_WAITS | HX.HX_FLAG_BULK_STORE | HX.HX_FLAG_SWEEP_FORCES | HX.HX_FLAG_PDL)
+    o = c.o
+    hm = c.home_mask()
+    x0 = o.coords()
+    ref = x0.copy()
+    o.exchange_coords(ref)
+    home = torch.from_numpy(x0[hm].copy()).pin_memory()
+    halo = torch.empty((int((~hm).sum()), 3)).pin_memory()
+    dev = torch.empty((c.slots, 3), device="cuda")
+    c.hx.exchange_coords_host_packed(home, halo, dev)
+    torch.cuda.synchronize()
+    assert np.array_equal(_bits(halo.numpy()), _bits(ref[~hm]))
+    f0 = W.forces(w, c.slots)
+    fref = f0.copy()
+    o.exchange_forces(fref)
+    hf = torch.empty((int(hm.sum()), 3)).pin_memory()
+    c.hx.exchange_forces_host_packed(torch.from_numpy(f0).pin_memory(), hf, dev)
+    torch.cuda.synchronize()
+    assert np.array_equal(_bits(hf.numpy()), _bits(fref[hm]))
+    rc, det = c.hx.status()
+    assert rc == 0, (rc, det)
+
+
 def test_host_packed_misaligned_pageable_and_rebuild():
     """Packed buffers 4 bytes off a 16-byte boundary and in pageable memory
     (synchronous copies) give the same bits; a rebuild with more atoms grows
