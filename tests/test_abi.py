@@ -89,3 +89,49 @@ def test_many_pulses_plan():
     # 2 pulses in each of three dims: Z0 Z1 Y0 Y1 X0 X1
     pd, pk = HX.query_plan((5.0, 5.0, 5.0), (5, 5, 5), 1.5)
     assert pd.tolist() == [2, 2, 1, 1, 0, 0] and pk.tolist() == [0, 1, 0, 1, 0, 1]
+
+
+C_PROGRAM = r"""
+#include <stdio.h>
+#include "hx.h"
+int main(void) {
+  double box[3] = {5.0, 5.0, 5.0};
+  int dims[3] = {5, 5, 5};
+  int np = 0;
+  int32_t pd[HX_MAX_PULSES], pk[HX_MAX_PULSES];
+  hx_handle h = NULL;
+  int rc = hx_query_plan(box, dims, 1.5, &np, pd, pk);
+  printf("%d %d", rc, np);
+  for (int i = 0; i < np; ++i) printf(" %d:%d", pd[i], pk[i]);
+  printf(" | %d", hx_init(&h, box, dims, -1.0, 0, 0, 0));
+  printf(" %d", hx_exchange_coords(NULL, NULL, NULL));
+  printf(" %d\n", hx_status_async(NULL, NULL, NULL));
+  hx_destroy(NULL);
+  return 0;
+}
+"""
+
+
+def test_boundary_is_plain_c(tmp_path):
+    """include/hx.h compiles as C99 (no C++ or torch types) and a C program
+    links libhx.so and calls it: the plan of three dimensions with two pulses
+    each, and argument errors returned as codes."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not found")
+    lib = HX.load_library()
+    libdir = os.path.dirname(HX.library_path())
+    src = tmp_path / "boundary.c"
+    src.write_text(C_PROGRAM)
+    exe = tmp_path / "boundary"
+    cmd = [gcc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", os.path.join(ROOT, "include"),
+           str(src), "-L", libdir, "-lhx", f"-Wl,-rpath,{libdir}", "-o", str(exe)]
+    done = subprocess.run(cmd, capture_output=True, text=True)
+    assert done.returncode == 0, done.stderr
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()
+    assert out[:2] == ["0", "6"]
+    assert out[2:8] == ["2:0", "2:1", "1:0", "1:1", "0:0", "0:1"]
+    assert out[8] == "|" and out[9:] == [str(HX.HX_ERR_ARG)] * 3
+    assert lib is not None
