@@ -191,8 +191,7 @@ struct TRec {
   int r;              // domain
   int range;          // -1 home, else the pulse whose received slots the unit holds
   int a, n;           // local index of the first slot, slot count
-  std::vector<UnitSeg> segs;
-  std::vector<int> seg_pulse;
+  int seg_begin, seg_cnt;   // its segments in the domain's segment pool (each with its pulse in `pad`)
   std::vector<int> deps;   // TRec indices
   int stage = 0;
   long long key = 0;
@@ -204,13 +203,26 @@ int build_unit_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::
   const Plan& pl = h->pl;
   const int P = pl.n_pulses, nd = pl.ndom;
   auto upper = [&](int r, int q) { return neighbour(pl, r, pl.pulse_dim[q], +1); };
+  std::vector<std::vector<UnitSeg>> seg_pool;
   {
     // units of each domain, cut on all host cores, then listed domain after domain;
     // by_range: per (domain, range) the units' indices in slot order
     std::vector<std::vector<TRec>> per(nd);
     std::vector<std::vector<std::vector<int>>> by_range(nd, std::vector<std::vector<int>>(P + 1));
+    // one pool of segments per domain (a unit refers to a run of its domain's
+    // pool), so that cutting tens of thousands of units allocates per domain
+    seg_pool.assign(nd, std::vector<UnitSeg>());
     parallel_for(nd, [&](size_t ri) {
       const int r = static_cast<int>(ri);
+      {
+        size_t est = 0;   // units before any split by entries
+        for (int rg = -1; rg < P; ++rg) {
+          const int len = rg < 0 ? h->home[r] : h->t_size[rg * nd + upper(r, rg)];
+          est += static_cast<size_t>((len + max_slots - 1) / max_slots);
+        }
+        per[r].reserve(est + 1);
+        seg_pool[r].reserve(est * static_cast<size_t>(P) + 1);
+      }
       for (int rg = -1; rg < P; ++rg) {
         int lo, len;
         if (rg < 0) {
@@ -249,6 +261,8 @@ int build_unit_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::
           t.range = rg;
           t.a = a;
           t.n = b - a;
+          t.seg_begin = static_cast<int>(seg_pool[r].size());
+          t.seg_cnt = 0;
           for (int k = 0; k < P; ++k) {
             const int p = dir == 0 ? k : P - 1 - k;
             const ItemInfo& it = items[p * nd + r];
@@ -265,16 +279,23 @@ int build_unit_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::
             sg.dim = it.dim;
             sg.shift = pl.boxf[it.dim];
             sg.do_shift = (dir == 0) ? it.shift_flag : 0;
-            t.segs.push_back(sg);
-            t.seg_pulse.push_back(p);
+            sg.pad = p;   // the segment's pulse while the tables are built (cleared in the records)
+            seg_pool[r].push_back(sg);
+            ++t.seg_cnt;
           }
-          if (t.segs.empty()) continue;
+          if (t.seg_cnt == 0) continue;
           by_range[r][rg + 1].push_back(static_cast<int>(per[r].size()));
           per[r].push_back(std::move(t));
         }
       }
     }, 1);
     std::vector<TRec> recs;
+    {
+      size_t total = 0;
+      for (int r = 0; r < nd; ++r) total += per[r].size();
+      recs.reserve(total);
+    }
+    auto seg = [&](const TRec& t, int k) -> UnitSeg& { return seg_pool[t.r][static_cast<size_t>(t.seg_begin + k)]; };
     for (int r = 0; r < nd; ++r) {
       const int base = static_cast<int>(recs.size());
       for (auto& lst : by_range[r])
@@ -293,9 +314,10 @@ int build_unit_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::
         for (int rg = 0; rg <= P; ++rg)
           for (int j : by_range[u][rg]) {
             const TRec& s = recs[j];
-            for (size_t k = 0; k < s.segs.size(); ++k) {
-              if (s.seg_pulse[k] != p0) continue;
-              const int64_t b0 = s.segs[k].map - items[p0 * nd + u].map, b1 = b0 + s.segs[k].n;
+            for (int k = 0; k < s.seg_cnt; ++k) {
+              const UnitSeg& sk = seg(s, k);
+              if (sk.pad != p0) continue;
+              const int64_t b0 = sk.map - items[p0 * nd + u].map, b1 = b0 + sk.n;
               if (b0 < e1 && e0 < b1) t.deps.push_back(j);
             }
           }
@@ -304,17 +326,19 @@ int build_unit_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::
         // The waits are listed segment by segment (segments of one unit read
         // different ranges, so their producers differ), and each segment
         // records how many of them are its own.
-        for (size_t k = 0; k < t.segs.size(); ++k) {
-          const int p = t.seg_pulse[k];
+        t.deps.reserve(static_cast<size_t>(2 * t.seg_cnt));
+        for (int k = 0; k < t.seg_cnt; ++k) {
+          UnitSeg& sk = seg(t, k);
+          const int p = sk.pad;
           const int q = items[p * nd + t.r].q;
-          const int64_t s0 = t.segs[k].other - h->dom_offset[q], s1 = s0 + t.segs[k].n;
+          const int64_t s0 = sk.other - h->dom_offset[q], s1 = s0 + sk.n;
           const size_t first = t.deps.size();
           // q's units of range p, in slot order: the first one that ends past s0, then on while they start before s1
           const std::vector<int>& in_range = by_range[q][p + 1];
           auto it_j = std::partition_point(in_range.begin(), in_range.end(),
                                            [&](int j) { return recs[j].a + recs[j].n <= s0; });
           for (; it_j != in_range.end() && recs[*it_j].a < s1; ++it_j) t.deps.push_back(*it_j);
-          t.segs[k].dep = static_cast<int32_t>(t.deps.size() - first);
+          sk.dep = static_cast<int32_t>(t.deps.size() - first);
         }
         return;
       }
@@ -355,7 +379,7 @@ int build_unit_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::
       std::vector<int64_t> seg_at(n + 1, 0), wait_at(n + 1, 0);
       for (int q = 0; q < n; ++q) {
         const TRec& t = recs[order[q]];
-        seg_at[q + 1] = seg_at[q] + std::max<int64_t>(0, static_cast<int64_t>(t.segs.size()) - kInlineSegs);
+        seg_at[q + 1] = seg_at[q] + std::max<int64_t>(0, static_cast<int64_t>(t.seg_cnt) - kInlineSegs);
         wait_at[q + 1] = wait_at[q] + static_cast<int64_t>(t.deps.size());
       }
       std::vector<Unit> units(n);
@@ -370,12 +394,13 @@ int build_unit_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::
         u.base = h->dom_offset[t.r] + t.a;
         u.n = t.n;
         u.local_a = t.a;
-        u.seg_cnt = static_cast<int32_t>(t.segs.size());
+        u.seg_cnt = static_cast<int32_t>(t.seg_cnt);
         u.extra_off = static_cast<int32_t>(seg_at[q]);
         // stage regions: each run's region starts on a 16-byte boundary and is 16 bytes longer than the run
         int moff = slot_bytes, soff = slot_bytes + map_bytes;
-        for (size_t g = 0; g < t.segs.size(); ++g) {
-          UnitSeg sg = t.segs[g];
+        for (int g = 0; g < t.seg_cnt; ++g) {
+          UnitSeg sg = seg(t, g);
+          sg.pad = 0;
           sg.map_off = moff;
           sg.src_off = dir == 1 ? soff : 0;
           moff += ((4 * sg.n + 15) & ~15) + 16;
@@ -391,8 +416,8 @@ int build_unit_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::
         for (int w = 0; w < u.wait_cnt; ++w) waits[u.wait_off + w] = {pos[t.deps[w]], 1};
         for (int w = 0; w < std::min(u.wait_cnt, kInlineWaits); ++w) u.wait_inline[w] = waits[u.wait_off + w];
         u.flags = (waited[i] ? kSignal : 0) | (dir == 0 && t.range >= 0 ? kHaloSrc : 0);
-        u.item = t.seg_pulse[0] * nd + t.r;
-        for (const UnitSeg& sg : t.segs) u.entries += sg.n;
+        u.item = seg(t, 0).pad * nd + t.r;
+        for (int g = 0; g < t.seg_cnt; ++g) u.entries += seg(t, g).n;
       }, 64);
       if (!fits.load()) return HX_ERR_STATE;
       h->n_units[dir] = static_cast<int>(units.size());
