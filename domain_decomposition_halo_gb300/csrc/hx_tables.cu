@@ -233,28 +233,38 @@ int build_unit_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::
           lo = h->t_off[tu];
           len = h->t_size[tu];
         }
-        // entries of every map of r that fall in slots [a, b)
-        auto entries_in = [&](int a, int b) {
+        // Per pulse, the first map entry at or past slot a: the units of a
+        // range advance through every map, so each unit costs one search per
+        // pulse (for its end) from where the previous one ended.
+        int cur[HX_MAX_PULSES], end[HX_MAX_PULSES];
+        for (int p = 0; p < P; ++p) {
+          const ItemInfo& it = items[p * nd + r];
+          const int32_t* m = maps.data() + it.map;
+          cur[p] = static_cast<int>(std::lower_bound(m, m + it.size, lo) - m);
+        }
+        // entries of every map of r in slots [a, b), with end[p] the first entry at or past b
+        auto entries_to = [&](int b) {
           int e = 0;
           for (int p = 0; p < P; ++p) {
             const ItemInfo& it = items[p * nd + r];
-            if (it.size == 0) continue;
             const int32_t* m = maps.data() + it.map;
-            e += static_cast<int>(std::lower_bound(m, m + it.size, b) - std::lower_bound(m, m + it.size, a));
+            end[p] = static_cast<int>(std::lower_bound(m + cur[p], m + it.size, b) - m);
+            e += end[p] - cur[p];
           }
           return e;
         };
         for (int a = lo, b = lo; a < lo + len; a = b) {
           // at most max_slots slots and max_entries entries (a slot has at most one entry per pulse)
           b = std::min(lo + len, a + max_slots);
-          if (entries_in(a, b) > max_entries) {
+          if (entries_to(b) > max_entries) {
             int good = a + 1, bad = b;
             while (bad - good > 1) {
               const int mid = good + (bad - good) / 2;
-              if (entries_in(a, mid) <= max_entries) good = mid;
+              if (entries_to(mid) <= max_entries) good = mid;
               else bad = mid;
             }
             b = good;
+            entries_to(b);
           }
           TRec t;
           t.r = r;
@@ -267,9 +277,7 @@ int build_unit_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::
             const int p = dir == 0 ? k : P - 1 - k;
             const ItemInfo& it = items[p * nd + r];
             if (it.size == 0) continue;
-            const int32_t* m = maps.data() + it.map;
-            const int i1 = static_cast<int>(std::lower_bound(m, m + it.size, t.a) - m);
-            const int i2 = static_cast<int>(std::lower_bound(m, m + it.size, t.a + t.n) - m);
+            const int i1 = cur[p], i2 = end[p];
             if (i2 <= i1) continue;
             UnitSeg sg;
             std::memset(&sg, 0, sizeof(sg));
@@ -283,6 +291,7 @@ int build_unit_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::
             seg_pool[r].push_back(sg);
             ++t.seg_cnt;
           }
+          for (int p = 0; p < P; ++p) cur[p] = end[p];
           if (t.seg_cnt == 0) continue;
           by_range[r][rg + 1].push_back(static_cast<int>(per[r].size()));
           per[r].push_back(std::move(t));
