@@ -5,6 +5,7 @@
 #include "hx_runtime.h"
 
 #include <atomic>
+#include <memory>
 
 namespace hx_rt {
 
@@ -149,6 +150,19 @@ std::vector<int> order_chunks(const std::vector<Rec>& recs) {
       static_cast<int>(recs.size()), [&](int i) -> const std::vector<int>& { return recs[i].deps; },
       [&](int i) { return recs[i].key; });
 }
+
+// An array of n records left uninitialised: the parallel fill that follows
+// writes every byte of each record, and is also its first touch.
+template <class T>
+struct RecordArray {
+  std::unique_ptr<T[]> p;
+  size_t n;
+  explicit RecordArray(size_t count) : p(new T[count ? count : 1]), n(count) {}
+  T& operator[](size_t i) { return p[i]; }
+  T* data() { return p.get(); }
+  size_t size() const { return n; }
+  bool empty() const { return n == 0; }
+};
 
 // Dependency depth of every record: 0 without producers, else one more than
 // its deepest producer. Relaxation passes over all records: the depths settle
@@ -391,7 +405,7 @@ int build_unit_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::
         seg_at[q + 1] = seg_at[q] + std::max<int64_t>(0, static_cast<int64_t>(t.seg_cnt) - kInlineSegs);
         wait_at[q + 1] = wait_at[q] + static_cast<int64_t>(t.deps.size());
       }
-      std::vector<Unit> units(n);
+      RecordArray<Unit> units(n);
       std::vector<UnitSeg> segs(seg_at[n]);   // segments past kInlineSegs
       std::vector<Wait> waits(wait_at[n]);
       std::atomic<bool> fits{true};
@@ -939,7 +953,7 @@ int build_tables(hx_ctx* h, cudaStream_t s) {
     const size_t nc = order.size();
     std::vector<int64_t> wait_at(nc + 1, 0);
     for (size_t k = 0; k < nc; ++k) wait_at[k + 1] = wait_at[k] + static_cast<int64_t>(recs[order[k]].wait.size());
-    std::vector<ChunkSlot> chunks(nc);
+    RecordArray<ChunkSlot> chunks(nc);
     std::vector<Wait> waits(wait_at[nc]);
     parallel_for(nc, [&](size_t k) {
       const int ri = order[k];
