@@ -204,7 +204,7 @@ struct alignas(16) Unit {  // one 256-byte record, read by 16 threads in one rou
   int32_t extra_off;  // segments past kInlineSegs in the direction's overflow list
   int32_t wait_off;   // producer units to wait for (positions in the list)
   int32_t wait_cnt;
-  int32_t flags;      // kSignal; kHaloSrc = slots written earlier in the same launch
+  int32_t flags;      // kSignal: other units of the launch wait for this one
   int32_t item;       // pulse * n_domains + domain of its first segment (status, fault injection)
   int32_t entries;    // entries of all segments
   Wait wait_inline[kInlineWaits];   // the first waits (also in the wait list), read with the record

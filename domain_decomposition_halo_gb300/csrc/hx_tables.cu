@@ -190,23 +190,28 @@ bool dependency_depths(int n, Deps deps, std::vector<int>& depth, int max_passes
 //
 // Each domain's array is cut into ranges (home, then the slots received in
 // each pulse) and each range into units of up to max_slots slots. A unit gets
-// one segment per (sender, pulse) map that has entries inside it: for
-// coordinates the maps it is a source of, for forces the maps it is a target
-// of (segments last pulse first). Dependencies:
-//   coordinates: a unit of received slots waits for the units of the sending
-//     domain that stored those slots;
-//   forces: a unit waits for the units of its receivers that hold the slots
-//     it reads, when those units are themselves targets of later pulses.
-// Units are listed by Kahn's algorithm with the same priority as the chunk
-// lists (folded domain order, dependency depth, a lag of `lag` list
-// positions per depth).
+// one segment per (sender, pulse) map whose targets fall inside it, last
+// pulse first. A unit waits for the units of its receivers that hold the
+// slots it reads, when those units are themselves targets of later pulses.
+// Units are listed with the same priority as the chunk lists (folded domain
+// order, dependency depth, a lag of `lag` list positions per depth).
+
+// The dependencies of a unit: a run of the unit list's dependency pool.
+struct IntSpan {
+  const int* b;
+  const int* e;
+  const int* begin() const { return b; }
+  const int* end() const { return e; }
+  size_t size() const { return static_cast<size_t>(e - b); }
+};
 
 struct TRec {
   int r;              // domain
   int range;          // -1 home, else the pulse whose received slots the unit holds
   int a, n;           // local index of the first slot, slot count
   int seg_begin, seg_cnt;   // its segments in the domain's segment pool (each with its pulse in `pad`)
-  std::vector<int> deps;   // TRec indices
+  int64_t dep_begin;  // its dependencies (unit indices) in the dependency pool, segment by segment
+  int dep_cnt;
   int stage = 0;
   long long key = 0;
 };
@@ -216,6 +221,7 @@ int build_unit_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::
                       int slot_bytes, int map_bytes, int src_bytes, int dir) {
   const Plan& pl = h->pl;
   const int P = pl.n_pulses, nd = pl.ndom;
+  if (dir != 1) return HX_ERR_STATE;   // the sweep serves the force exchange
   auto upper = [&](int r, int q) { return neighbour(pl, r, pl.pulse_dim[q], +1); };
   std::vector<std::vector<UnitSeg>> seg_pool;
   {
@@ -288,7 +294,7 @@ int build_unit_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::
           t.seg_begin = static_cast<int>(seg_pool[r].size());
           t.seg_cnt = 0;
           for (int k = 0; k < P; ++k) {
-            const int p = dir == 0 ? k : P - 1 - k;
+            const int p = P - 1 - k;
             const ItemInfo& it = items[p * nd + r];
             if (it.size == 0) continue;
             const int i1 = cur[p], i2 = end[p];
@@ -300,7 +306,7 @@ int build_unit_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::
             sg.n = i2 - i1;
             sg.dim = it.dim;
             sg.shift = pl.boxf[it.dim];
-            sg.do_shift = (dir == 0) ? it.shift_flag : 0;
+            sg.do_shift = 0;
             sg.pad = p;   // the segment's pulse while the tables are built (cleared in the records)
             seg_pool[r].push_back(sg);
             ++t.seg_cnt;
@@ -326,52 +332,57 @@ int build_unit_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::
       for (TRec& t : per[r]) recs.push_back(std::move(t));
     }
     per.clear();
-    // dependencies, one unit per task
+    // Dependencies. The slots read by segment (r, p) are q's slots [other,
+    // other + n) in q's range p; the units of q's range p that overlap them
+    // are its producers. They are listed segment by segment (segments of one
+    // unit read different ranges, so their producers differ), each segment
+    // records how many are its own, and all units' lists share one pool:
+    // counted on the host's cores, laid out by a prefix sum, then filled.
+    auto producers = [&](const TRec& t, const UnitSeg& sk) {
+      const int q = items[sk.pad * nd + t.r].q;
+      const int64_t s0 = sk.other - h->dom_offset[q], s1 = s0 + sk.n;
+      // q's units of range p, in slot order: the first one that ends past s0, then on while they start before s1
+      const std::vector<int>& in_range = by_range[q][sk.pad + 1];
+      auto lo_j = std::partition_point(in_range.begin(), in_range.end(),
+                                       [&](int j) { return recs[j].a + recs[j].n <= s0; });
+      auto hi_j = lo_j;
+      while (hi_j != in_range.end() && recs[*hi_j].a < s1) ++hi_j;
+      return std::make_pair(lo_j, hi_j);
+    };
     parallel_for(recs.size(), [&](size_t i) {
       TRec& t = recs[i];
-      if (dir == 0) {
-        if (t.range < 0) return;
-        // slots [a, a+n) of r's range `p0` are entries [a - off, a - off + n) of the map (u, p0)
-        const int p0 = t.range, u = upper(t.r, p0);
-        const int64_t e0 = t.a - h->t_off[p0 * nd + u], e1 = e0 + t.n;
-        for (int rg = 0; rg <= P; ++rg)
-          for (int j : by_range[u][rg]) {
-            const TRec& s = recs[j];
-            for (int k = 0; k < s.seg_cnt; ++k) {
-              const UnitSeg& sk = seg(s, k);
-              if (sk.pad != p0) continue;
-              const int64_t b0 = sk.map - items[p0 * nd + u].map, b1 = b0 + sk.n;
-              if (b0 < e1 && e0 < b1) t.deps.push_back(j);
-            }
-          }
-      } else {
-        // the slots read by segment (r, p) are q's slots [other, other + n) in q's range p.
-        // The waits are listed segment by segment (segments of one unit read
-        // different ranges, so their producers differ), and each segment
-        // records how many of them are its own.
-        t.deps.reserve(static_cast<size_t>(2 * t.seg_cnt));
-        for (int k = 0; k < t.seg_cnt; ++k) {
-          UnitSeg& sk = seg(t, k);
-          const int p = sk.pad;
-          const int q = items[p * nd + t.r].q;
-          const int64_t s0 = sk.other - h->dom_offset[q], s1 = s0 + sk.n;
-          const size_t first = t.deps.size();
-          // q's units of range p, in slot order: the first one that ends past s0, then on while they start before s1
-          const std::vector<int>& in_range = by_range[q][p + 1];
-          auto it_j = std::partition_point(in_range.begin(), in_range.end(),
-                                           [&](int j) { return recs[j].a + recs[j].n <= s0; });
-          for (; it_j != in_range.end() && recs[*it_j].a < s1; ++it_j) t.deps.push_back(*it_j);
-          sk.dep = static_cast<int32_t>(t.deps.size() - first);
-        }
-        return;
+      t.dep_cnt = 0;
+      for (int k = 0; k < t.seg_cnt; ++k) {
+        UnitSeg& sk = seg(t, k);
+        const auto range = producers(t, sk);
+        sk.dep = static_cast<int32_t>(range.second - range.first);
+        t.dep_cnt += sk.dep;
       }
-      std::sort(t.deps.begin(), t.deps.end());
-      t.deps.erase(std::unique(t.deps.begin(), t.deps.end()), t.deps.end());
+    }, 64);
+    std::vector<int> dep_pool;
+    {
+      int64_t total = 0;
+      for (TRec& t : recs) {
+        t.dep_begin = total;
+        total += t.dep_cnt;
+      }
+      dep_pool.resize(static_cast<size_t>(total));
+    }
+    parallel_for(recs.size(), [&](size_t i) {
+      const TRec& t = recs[i];
+      int64_t w = t.dep_begin;
+      for (int k = 0; k < t.seg_cnt; ++k) {
+        const auto range = producers(t, seg(t, k));
+        for (auto j = range.first; j != range.second; ++j) dep_pool[static_cast<size_t>(w++)] = *j;
+      }
     }, 64);
     // dependency depth, then priority: base order + one resident window per depth
     {
       const int n = static_cast<int>(recs.size());
-      auto deps_of = [&](int i) -> const std::vector<int>& { return recs[i].deps; };
+      auto deps_of = [&](int i) {
+        const int* b = dep_pool.data() + recs[i].dep_begin;
+        return IntSpan{b, b + recs[i].dep_cnt};
+      };
       std::vector<int> depth;
       if (!dependency_depths(n, deps_of, depth, P + 1)) return HX_ERR_STATE;
       for (int i = 0; i < n; ++i) recs[i].stage = depth[i];
@@ -395,15 +406,14 @@ int build_unit_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::
       std::vector<int> pos(recs.size());
       for (size_t q = 0; q < order.size(); ++q) pos[order[q]] = static_cast<int>(q);
       std::vector<char> waited(recs.size(), 0);
-      for (auto& t : recs)
-        for (int d : t.deps) waited[d] = 1;
+      for (int d : dep_pool) waited[d] = 1;
       // records in list order, filled on the host's cores: each one's share of
       // the overflow segments and of the wait list comes from prefix sums
       std::vector<int64_t> seg_at(n + 1, 0), wait_at(n + 1, 0);
       for (int q = 0; q < n; ++q) {
         const TRec& t = recs[order[q]];
         seg_at[q + 1] = seg_at[q] + std::max<int64_t>(0, static_cast<int64_t>(t.seg_cnt) - kInlineSegs);
-        wait_at[q + 1] = wait_at[q] + static_cast<int64_t>(t.deps.size());
+        wait_at[q + 1] = wait_at[q] + t.dep_cnt;
       }
       RecordArray<Unit> units(n);
       std::vector<UnitSeg> segs(seg_at[n]);   // segments past kInlineSegs
@@ -425,20 +435,21 @@ int build_unit_tables(hx_ctx* h, const std::vector<ItemInfo>& items, const std::
           UnitSeg sg = seg(t, g);
           sg.pad = 0;
           sg.map_off = moff;
-          sg.src_off = dir == 1 ? soff : 0;
+          sg.src_off = soff;
           moff += ((4 * sg.n + 15) & ~15) + 16;
           soff += ((12 * sg.n + 15) & ~15) + 16;
           if (static_cast<int>(g) < kInlineSegs) u.seg[g] = sg;
           else segs[u.extra_off + g - kInlineSegs] = sg;
         }
         // the stage regions must fit the kernel's buffer
-        if (moff > slot_bytes + map_bytes || (dir == 1 && soff > slot_bytes + map_bytes + src_bytes))
+        if (moff > slot_bytes + map_bytes || soff > slot_bytes + map_bytes + src_bytes)
           fits.store(false, std::memory_order_relaxed);
         u.wait_off = static_cast<int32_t>(wait_at[q]);
-        u.wait_cnt = static_cast<int32_t>(t.deps.size());
-        for (int w = 0; w < u.wait_cnt; ++w) waits[u.wait_off + w] = {pos[t.deps[w]], 1};
+        u.wait_cnt = static_cast<int32_t>(t.dep_cnt);
+        const int* deps = dep_pool.data() + t.dep_begin;
+        for (int w = 0; w < u.wait_cnt; ++w) waits[u.wait_off + w] = {pos[deps[w]], 1};
         for (int w = 0; w < std::min(u.wait_cnt, kInlineWaits); ++w) u.wait_inline[w] = waits[u.wait_off + w];
-        u.flags = (waited[i] ? kSignal : 0) | (dir == 0 && t.range >= 0 ? kHaloSrc : 0);
+        u.flags = waited[i] ? kSignal : 0;
         u.item = seg(t, 0).pad * nd + t.r;
         for (int g = 0; g < t.seg_cnt; ++g) u.entries += seg(t, g).n;
       }, 64);
